@@ -1,0 +1,371 @@
+"""Pins for the fp64 oracle: it is checked against things other than itself.
+
+Each test names what fixes the expected value: a number the pages print, a
+closed form, an invariant of the mathematics, a torch library routine, or a
+scalar brute-force restatement (tests/bruteforce.py) on tiny inputs.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import bruteforce as bf
+from oracle import oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+RNG = np.random.default_rng(1234)
+
+TINY = O.Config(hidden=8, n_heads=2, n_kv_heads=1, head_dim=4, intermediate=6, n_layers=2,
+                vocab=11, max_pos=64, rms_eps=1e-5, rope_theta=100.0)
+
+
+def tiny_weights(cfg, rng, std=0.4):
+    d, hd = cfg.hidden, cfg.head_dim
+    shapes = dict(wq=(cfg.n_heads * hd, d), wk=(cfg.n_kv_heads * hd, d), wv=(cfg.n_kv_heads * hd, d),
+                  wo=(d, cfg.n_heads * hd), wgate=(cfg.intermediate, d), wup=(cfg.intermediate, d),
+                  wdown=(d, cfg.intermediate))
+    w = {k: rng.normal(0, std, s) for k, s in shapes.items()}
+    w["attn_norm"] = 1 + rng.normal(0, 0.1, d)
+    w["mlp_norm"] = 1 + rng.normal(0, 0.1, d)
+    return w
+
+
+def as_block(w):
+    return O.BlockWeights(**{k: np.asarray(v) for k, v in w.items()})
+
+
+def nested(a):
+    return np.asarray(a).tolist()
+
+
+# ---------------------------------------------------------------- page facts
+
+def test_param_total_matches_page():
+    facts = json.load(open(os.path.join(GOLDEN, "smollm2_135m_facts.json")))
+    c = facts["config"]
+    cfg = O.Config(hidden=c["hidden_size"], n_heads=c["num_attention_heads"],
+                   n_kv_heads=c["num_key_value_heads"], head_dim=c["head_dim"],
+                   intermediate=c["intermediate_size"], n_layers=c["num_hidden_layers"],
+                   vocab=c["vocab_size"], max_pos=c["max_position_embeddings"],
+                   rms_eps=c["rms_norm_eps"], rope_theta=float(c["rope_theta"]))
+    assert cfg == O.SMOLLM2_135M
+    assert cfg.hidden == cfg.n_heads * cfg.head_dim
+    assert O.param_count(cfg, tied=c["tie_word_embeddings"]) == facts["param_total"]
+    # an untied head would add exactly one more V x d matrix
+    assert O.param_count(cfg, tied=False) == facts["param_total"] + cfg.vocab * cfg.hidden
+
+
+def test_logits_shapes_match_page():
+    facts = json.load(open(os.path.join(GOLDEN, "smollm2_135m_facts.json")))
+    rng = np.random.default_rng(0)
+    for (ids_shape, logits_shape) in facts["logits_shapes"]:
+        # same shapes with a tiny stand-in vocabulary/depth; the vocab axis is checked symbolically
+        cfg = TINY
+        layers = [as_block(tiny_weights(cfg, rng))]
+        embed = rng.normal(0, 0.3, (cfg.vocab, cfg.hidden))
+        ids = rng.integers(0, cfg.vocab, ids_shape)
+        out = O.model_forward(cfg, layers, embed, np.ones(cfg.hidden), ids)
+        assert out.shape == tuple(ids_shape) + (cfg.vocab,)
+        assert logits_shape[-1] == O.SMOLLM2_135M.vocab and list(logits_shape[:2]) == list(ids_shape)
+
+
+def test_max_position_guard():
+    cfg = O.Config(**{**TINY.__dict__, "max_pos": 4})
+    rng = np.random.default_rng(0)
+    layers = [as_block(tiny_weights(cfg, rng))]
+    embed = rng.normal(0, 0.3, (cfg.vocab, cfg.hidden))
+    with pytest.raises(ValueError):
+        O.model_forward(cfg, layers, embed, np.ones(cfg.hidden), np.zeros((1, 5), dtype=int))
+
+
+# ---------------------------------------------------------------- RMSNorm
+
+def test_rmsnorm_closed_forms():
+    # constant vector c: every output is w_i * c / sqrt(c^2 + eps)
+    c, eps = 3.0, 1e-5
+    w = np.array([1.0, 2.0, -0.5, 4.0])
+    y = O.rms_norm(np.full(4, c), w, eps)
+    np.testing.assert_allclose(y, w * c / math.sqrt(c * c + eps), rtol=1e-15)
+    # [1,2,3,4], w=1, eps=0: mean square 7.5
+    y = O.rms_norm(np.array([1.0, 2, 3, 4]), np.ones(4), 0.0)
+    np.testing.assert_allclose(y, np.array([1, 2, 3, 4]) / math.sqrt(7.5), rtol=1e-15)
+    # w = 1, eps = 0 gives unit root-mean-square output, scale-invariant input
+    x = RNG.normal(0, 5, (7, 33))
+    y = O.rms_norm(x, np.ones(33), 0.0)
+    np.testing.assert_allclose(np.sqrt(np.mean(y * y, axis=-1)), 1.0, rtol=1e-13)
+    np.testing.assert_allclose(O.rms_norm(10 * x, np.ones(33), 0.0), y, rtol=1e-13)
+
+
+def test_rmsnorm_vs_torch_library():
+    x = RNG.normal(0, 1, (5, 24))
+    w = 1 + RNG.normal(0, 0.1, 24)
+    ref = F.rms_norm(torch.tensor(x), (24,), torch.tensor(w), eps=1e-6).numpy()
+    np.testing.assert_allclose(O.rms_norm(x, w, 1e-6), ref, rtol=1e-13, atol=1e-15)
+
+
+# ---------------------------------------------------------------- RoPE
+
+def test_rope_inv_freq_closed_form():
+    f = O.rope_inv_freq(64, 1e4)
+    assert f[0] == 1.0
+    np.testing.assert_allclose(f[16], 1e4 ** -0.5, rtol=1e-15)   # i = hd/4 -> theta^(-1/2)
+    # the first model.py's form base^(-i/half) is the same number
+    half = 32
+    np.testing.assert_allclose(f, 1.0 / (1e4 ** (np.arange(half) / half)), rtol=1e-14)
+    assert np.all(np.diff(f) < 0)
+
+
+def test_rope_position_zero_is_identity():
+    x = RNG.normal(0, 1, (3, 5, 64))
+    np.testing.assert_array_equal(O.apply_rope(x, np.zeros((3, 5), dtype=int), 1e5), x)
+
+
+def test_rope_preserves_norm_of_each_pair():
+    x = RNG.normal(0, 1, (4, 64))
+    pos = np.array([0, 7, 300, 8191])
+    y = O.apply_rope(x, pos, 1e5)
+    pair = lambda a: a[..., :32] ** 2 + a[..., 32:] ** 2
+    np.testing.assert_allclose(pair(y), pair(x), rtol=1e-12)
+
+
+def test_rope_relative_position_invariance():
+    q = RNG.normal(0, 1, 64)
+    k = RNG.normal(0, 1, 64)
+    for m, n, delta in [(5, 2, 11), (100, 3, 1000), (0, 0, 4096)]:
+        a = O.apply_rope(q, np.array(m), 1e5) @ O.apply_rope(k, np.array(n), 1e5)
+        b = O.apply_rope(q, np.array(m + delta), 1e5) @ O.apply_rope(k, np.array(n + delta), 1e5)
+        assert abs(a - b) < 1e-11 * (1 + abs(a))
+
+
+def test_rope_equals_complex_rotation():
+    x = RNG.normal(0, 1, 8)
+    for pos in (1, 3, 250):
+        y = O.apply_rope(x, np.array(pos), 10.0)
+        ref = bf.rotate(list(x), pos, 10.0)
+        np.testing.assert_allclose(y, ref, rtol=1e-13, atol=1e-14)
+    # explicit 2x2 rotation of the first pair at pos 1, freq 1: angle = 1 rad
+    e = np.zeros(8); e[0] = 1.0
+    y = O.apply_rope(e, np.array(1), 10.0)
+    np.testing.assert_allclose([y[0], y[4]], [math.cos(1.0), math.sin(1.0)], rtol=1e-15)
+
+
+# ---------------------------------------------------------------- SiLU
+
+def test_silu_vs_torch_and_limits():
+    z = np.linspace(-30, 30, 121)
+    np.testing.assert_allclose(O.silu(z), F.silu(torch.tensor(z)).numpy(), rtol=1e-14, atol=1e-300)
+    assert O.silu(0.0) == 0.0
+    assert abs(O.silu(40.0) - 40.0) < 1e-15 * 40 * 10
+    assert abs(O.silu(-40.0)) < 1e-15
+
+
+# ---------------------------------------------------------------- attention
+
+def _rand_qkv(B, H, KV, T, hd, rng):
+    return (rng.normal(0, 1, (B, H, T, hd)), rng.normal(0, 1, (B, KV, T, hd)),
+            rng.normal(0, 1, (B, KV, T, hd)))
+
+
+def test_attention_vs_bruteforce_loops():
+    rng = np.random.default_rng(7)
+    B, H, KV, T, hd = 2, 6, 2, 7, 4
+    q, k, v = _rand_qkv(B, H, KV, T, hd, rng)
+    vs = [0, 3]
+    o = O.gqa_attention(q, k, v, vs)
+    for b in range(B):
+        for h in range(H):
+            kvh = h // (H // KV)
+            for t in range(T):
+                keys = [j for j in range(T) if vs[b] <= j <= t]
+                if not keys:
+                    np.testing.assert_array_equal(o[b, h, t], 0.0)
+                    continue
+                s = [sum(q[b, h, t, c] * k[b, kvh, j, c] for c in range(hd)) / math.sqrt(hd) for j in keys]
+                e = [math.exp(x) for x in s]
+                ref = [sum(e[a] * v[b, kvh, j, c] for a, j in enumerate(keys)) / sum(e) for c in range(hd)]
+                np.testing.assert_allclose(o[b, h, t], ref, rtol=1e-12, atol=1e-13)
+
+
+def test_attention_vs_torch_sdpa():
+    rng = np.random.default_rng(8)
+    B, H, KV, T, hd = 2, 9, 3, 33, 16
+    q, k, v = _rand_qkv(B, H, KV, T, hd, rng)
+    g = H // KV
+    kt = torch.tensor(k).repeat_interleave(g, dim=1)
+    vt = torch.tensor(v).repeat_interleave(g, dim=1)
+    ref = F.scaled_dot_product_attention(torch.tensor(q), kt, vt, is_causal=True).numpy()
+    np.testing.assert_allclose(O.gqa_attention(q, k, v), ref, rtol=1e-11, atol=1e-12)
+
+
+def test_attention_causality():
+    rng = np.random.default_rng(9)
+    B, H, KV, T, hd = 1, 4, 2, 12, 8
+    q, k, v = _rand_qkv(B, H, KV, T, hd, rng)
+    base = O.gqa_attention(q, k, v)
+    t = 6
+    k2, v2, q2 = k.copy(), v.copy(), q.copy()
+    k2[:, :, t + 1] += 3.0
+    v2[:, :, t + 1] -= 2.0
+    q2[:, :, t + 1] *= -1
+    pert = O.gqa_attention(q2, k2, v2)
+    np.testing.assert_array_equal(pert[:, :, :t + 1], base[:, :, :t + 1])
+    assert not np.allclose(pert[:, :, t + 1], base[:, :, t + 1])
+
+
+# ---------------------------------------------------------------- block / model
+
+def test_block_vs_bruteforce_loops():
+    rng = np.random.default_rng(11)
+    w = tiny_weights(TINY, rng)
+    x = rng.normal(0, 1, (2, 5, TINY.hidden))
+    for vs in (None, [0, 2]):
+        out = O.block_forward(TINY, as_block(w), x, vs)
+        ref = np.array(bf.block(TINY, {k: nested(a) for k, a in w.items()}, nested(x), vs))
+        rows = slice(None) if vs is None else None
+        if vs is None:
+            np.testing.assert_allclose(out, ref, rtol=1e-11, atol=1e-12)
+        else:
+            for b in range(2):
+                np.testing.assert_allclose(out[b, vs[b]:], ref[b, vs[b]:], rtol=1e-11, atol=1e-12)
+
+
+def test_block_gqa_with_groups_of_three():
+    cfg = O.Config(hidden=12, n_heads=6, n_kv_heads=2, head_dim=2, intermediate=5, n_layers=1,
+                   vocab=5, max_pos=64, rms_eps=1e-6, rope_theta=1e4)
+    rng = np.random.default_rng(12)
+    w = tiny_weights(cfg, rng)
+    x = rng.normal(0, 1, (1, 4, cfg.hidden))
+    out = O.block_forward(cfg, as_block(w), x)
+    ref = np.array(bf.block(cfg, {k: nested(a) for k, a in w.items()}, nested(x)))
+    np.testing.assert_allclose(out, ref, rtol=1e-11, atol=1e-12)
+
+
+def test_gqa_equals_mha_with_duplicated_kv_weights():
+    cfg = O.Config(hidden=24, n_heads=6, n_kv_heads=2, head_dim=4, intermediate=10, n_layers=1,
+                   vocab=5, max_pos=64, rms_eps=1e-5, rope_theta=1e4)
+    rng = np.random.default_rng(13)
+    w = tiny_weights(cfg, rng)
+    x = rng.normal(0, 1, (2, 9, cfg.hidden))
+    g = cfg.n_heads // cfg.n_kv_heads
+    hd = cfg.head_dim
+    dup = lambda m: np.concatenate([m[(h // g) * hd:(h // g + 1) * hd] for h in range(cfg.n_heads)])
+    w_mha = dict(w, wk=dup(w["wk"]), wv=dup(w["wv"]))
+    cfg_mha = O.Config(**{**cfg.__dict__, "n_kv_heads": cfg.n_heads})
+    np.testing.assert_allclose(O.block_forward(cfg, as_block(w), x),
+                               O.block_forward(cfg_mha, as_block(w_mha), x), rtol=1e-13, atol=1e-13)
+
+
+def test_block_decomposition_identity():
+    rng = np.random.default_rng(14)
+    w = tiny_weights(TINY, rng)
+    x = rng.normal(0, 1, (2, 6, TINY.hidden))
+    taps = {}
+    out = O.block_forward(TINY, as_block(w), x, taps=taps)
+    np.testing.assert_array_equal(taps["layer_input"] + taps["attention_output"] + taps["mlp_output"], out)
+    np.testing.assert_array_equal(taps["layer_mid"], taps["layer_input"] + taps["attention_output"])
+
+
+def test_block_causality():
+    rng = np.random.default_rng(15)
+    w = tiny_weights(TINY, rng)
+    x = rng.normal(0, 1, (1, 8, TINY.hidden))
+    base = O.block_forward(TINY, as_block(w), x)
+    x2 = x.copy()
+    x2[0, 5] += 1.0
+    pert = O.block_forward(TINY, as_block(w), x2)
+    np.testing.assert_array_equal(pert[0, :5], base[0, :5])
+    assert not np.allclose(pert[0, 5], base[0, 5])
+
+
+def test_left_padding_equals_unpadded_run():
+    cfg = O.Config(hidden=16, n_heads=4, n_kv_heads=2, head_dim=4, intermediate=12, n_layers=1,
+                   vocab=5, max_pos=64, rms_eps=1e-5, rope_theta=1e4)
+    rng = np.random.default_rng(16)
+    w = as_block(tiny_weights(cfg, rng))
+    T, lens = 10, [10, 4, 7]
+    x = rng.normal(0, 1, (3, T, cfg.hidden))
+    vs = [T - L for L in lens]
+    padded = O.block_forward(cfg, w, x, vs)
+    for b, L in enumerate(lens):
+        alone = O.block_forward(cfg, w, x[b:b + 1, T - L:])
+        np.testing.assert_allclose(padded[b, T - L:], alone[0], rtol=1e-13, atol=1e-13)
+        # padding rows keep their residual input plus the MLP of it: attention output is 0
+        taps = {}
+        O.block_forward(cfg, w, x[b:b + 1], [T - L], taps=taps)
+        np.testing.assert_array_equal(taps["attention_head_outputs"][0, :T - L], 0.0)
+
+
+def test_model_vs_bruteforce_loops():
+    rng = np.random.default_rng(17)
+    layers_raw = [tiny_weights(TINY, rng) for _ in range(2)]
+    embed = rng.normal(0, 0.5, (TINY.vocab, TINY.hidden))
+    fnorm = 1 + rng.normal(0, 0.1, TINY.hidden)
+    ids = rng.integers(0, TINY.vocab, (2, 4))
+    out = O.model_forward(TINY, [as_block(w) for w in layers_raw], embed, fnorm, ids)
+    ref = np.array(bf.model(TINY, [{k: nested(a) for k, a in w.items()} for w in layers_raw],
+                            nested(embed), nested(fnorm), nested(ids)))
+    np.testing.assert_allclose(out, ref, rtol=1e-11, atol=1e-12)
+
+
+def test_tied_head_uses_embedding_table():
+    rng = np.random.default_rng(18)
+    layers = [as_block(tiny_weights(TINY, rng))]
+    embed = rng.normal(0, 0.5, (TINY.vocab, TINY.hidden))
+    fnorm = 1 + rng.normal(0, 0.1, TINY.hidden)
+    ids = rng.integers(0, TINY.vocab, (1, 3))
+    taps = {}
+    logits = O.model_forward(TINY, layers, embed, fnorm, ids, taps=taps)
+    # scaling row r of the table scales column r of the logits of the last layer's output only via
+    # the head (the embedding of ids not equal to r is untouched)
+    r = [i for i in range(TINY.vocab) if i not in ids[0]][0]
+    embed2 = embed.copy(); embed2[r] *= 2.0
+    logits2 = O.model_forward(TINY, layers, embed2, fnorm, ids)
+    np.testing.assert_allclose(logits2[..., r], 2.0 * logits[..., r], rtol=1e-13)
+    others = [i for i in range(TINY.vocab) if i != r]
+    np.testing.assert_array_equal(logits2[..., others], logits[..., others])
+
+
+# ---------------------------------------------------------------- decode
+
+def _prefill_cache(cfg, layers, embed, ids):
+    """Post-RoPE K and V of every layer for a prefill of ids [B, T]."""
+    x = embed[ids]
+    ks, vs = [], []
+    for w in layers:
+        taps = {}
+        x = O.block_forward(cfg, w, x, taps=taps)
+        ks.append(taps["attention_keys"])
+        vs.append(taps["attention_values"])
+    return np.stack(ks), np.stack(vs)   # [L, B, KV, T, hd]
+
+
+def test_decode_matches_last_row_of_prefill():
+    cfg = O.Config(hidden=16, n_heads=4, n_kv_heads=2, head_dim=4, intermediate=12, n_layers=3,
+                   vocab=13, max_pos=64, rms_eps=1e-5, rope_theta=1e4)
+    rng = np.random.default_rng(19)
+    layers = [as_block(tiny_weights(cfg, rng)) for _ in range(cfg.n_layers)]
+    embed = rng.normal(0, 0.5, (cfg.vocab, cfg.hidden))
+    fnorm = 1 + rng.normal(0, 0.1, cfg.hidden)
+    lens = [5, 9]
+    S = 12
+    seqs = [rng.integers(0, cfg.vocab, L + 1) for L in lens]
+    k_cache = np.zeros((cfg.n_layers, 2, cfg.n_kv_heads, S, cfg.head_dim))
+    v_cache = np.zeros_like(k_cache)
+    for b, L in enumerate(lens):
+        k, v = _prefill_cache(cfg, layers, embed, seqs[b][None, :L])
+        k_cache[:, b, :, :L] = k[:, 0]
+        v_cache[:, b, :, :L] = v[:, 0]
+        k_cache[:, b, :, L:] = 99.0        # slots past the length must not be read
+        v_cache[:, b, :, L:] = -99.0
+    ids = np.array([s[-1] for s in seqs])
+    logits, k_new, v_new = O.decode_step(cfg, layers, embed, fnorm, ids, lens, k_cache, v_cache)
+    for b, L in enumerate(lens):
+        full = O.model_forward(cfg, layers, embed, fnorm, seqs[b][None])
+        np.testing.assert_allclose(logits[b], full[0, -1], rtol=1e-11, atol=1e-12)
+        k, v = _prefill_cache(cfg, layers, embed, seqs[b][None])
+        np.testing.assert_allclose(k_new[:, b], k[:, 0, :, L], rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(v_new[:, b], v[:, 0, :, L], rtol=1e-11, atol=1e-12)
