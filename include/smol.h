@@ -1,0 +1,209 @@
+/*
+ * smol.h - C ABI of libsmol, a GB300 (sm_103a) implementation of the forward
+ * pass of a pre-norm LLaMA-style decoder (SmolLM2-135M and relatives).
+ *
+ * Sources (web pages describing the method, cited by title and section):
+ *   [M1] "model.py", minimal SmolLM2-135M style model (Sualeh77 Space):
+ *        1 Config, 2 RMSNorm, 3 RoPE, 4 Attention, 5 MLP (SwiGLU),
+ *        6 Transformer Block, 7 Top-level SmolLM2-135M (forward, generate).
+ *   [M3] "SmolLM3" (nnterp encyclopedia): "The block, in order",
+ *        "Grouped-query attention", "The readout, the embeddings and the tokenizer".
+ *   [M4] "model.py", complete SmolLM2-135M implementation (abi96062):
+ *        SmolLM2Model.forward (position_ids).
+ *   [M5] "components.py" (abi96062): RMSNorm, RotaryEmbedding,
+ *        GroupedQueryAttention, SwiGLU_FFN, TransformerBlock.
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument marked "device" is a CUDA device pointer on the
+ *     current device; "host" pointers are ordinary host memory read before
+ *     the call returns.  Tensors are dense, row-major (last index fastest),
+ *     bf16 unless stated; weight matrices use the nn.Linear layout [out, in].
+ *   - Device buffers must be 16-byte aligned (SMOL_ERR_MISALIGNED otherwise).
+ *   - The caller owns every buffer and the stream.  No entry point allocates,
+ *     frees or synchronises: all work is enqueued asynchronously on `stream`
+ *     (a cudaStream_t passed as void*; NULL = the legacy default stream).
+ *   - Return value: SMOL_OK (0) or a negative smol_status.  On an argument
+ *     error nothing is launched.  SMOL_ERR_CUDA reports a launch error; the
+ *     text of the last one is available through smol_status_string.
+ *   - Kernels never spin without a bound.  A bounded wait that gives up
+ *     writes a nonzero code into the workspace's status word and the kernel
+ *     returns; smol_workspace_status reads that word.
+ *   - Supported shapes: head_dim in {64, 128}; hidden == n_heads * head_dim;
+ *     n_heads % n_kv_heads == 0 with a group of at most 8; hidden, intermediate
+ *     and vocab multiples of 64; T >= 1; rows (B*T) up to 2^31-1.
+ */
+#ifndef SMOL_H
+#define SMOL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Model dimensions ([M1] section 1 Config). */
+typedef struct smol_config {
+  int hidden;          /* d */
+  int n_heads;         /* H, query heads */
+  int n_kv_heads;      /* KV, key/value heads */
+  int head_dim;        /* hd */
+  int intermediate;    /* I, SwiGLU width */
+  int n_layers;        /* L */
+  int vocab;           /* V (0 if no embedding/head is used) */
+  int max_pos;         /* max_position_embeddings: RoPE table rows and length guard */
+  float rms_eps;       /* RMSNorm epsilon */
+  float rope_theta;    /* RoPE base */
+} smol_config;
+
+/* One block's weights, device pointers, bf16, nn.Linear layout [out, in]. */
+typedef struct smol_block_weights {
+  const void *attn_norm; /* [d]          RMSNorm before attention            */
+  const void *wq;        /* [H*hd, d]                                        */
+  const void *wk;        /* [KV*hd, d]                                       */
+  const void *wv;        /* [KV*hd, d]                                       */
+  const void *wo;        /* [d, H*hd]                                        */
+  const void *mlp_norm;  /* [d]          RMSNorm before the MLP              */
+  const void *wgate;     /* [I, d]                                           */
+  const void *wup;       /* [I, d]                                           */
+  const void *wdown;     /* [d, I]                                           */
+} smol_block_weights;
+
+/* Whole-model weights.  `layers` is a HOST array of n_layers structs holding
+ * device pointers.  `embed` [V, d] is also the tied lm_head ([M1] section 7,
+ * "tie weights"; [M3] "The readout").  embed/final_norm may be NULL when only
+ * blocks are packed. */
+typedef struct smol_model_weights {
+  const smol_block_weights *layers;
+  const void *embed;       /* [V, d] device, bf16 */
+  const void *final_norm;  /* [d]    device, bf16 */
+} smol_model_weights;
+
+typedef enum smol_status {
+  SMOL_OK = 0,
+  SMOL_ERR_INVALID_ARG = -1,       /* NULL pointer, non-positive size, bad layer index */
+  SMOL_ERR_UNSUPPORTED_SHAPE = -2, /* see "Supported shapes" above                   */
+  SMOL_ERR_MISALIGNED = -3,        /* a device buffer is not 16-byte aligned         */
+  SMOL_ERR_TOO_LONG = -4,          /* positions exceed max_pos ([M1] section 7 assert) */
+  SMOL_ERR_WORKSPACE = -5,         /* workspace or packed buffer too small           */
+  SMOL_ERR_CUDA = -6,              /* a CUDA runtime call or launch failed           */
+  SMOL_ERR_DEVICE = -7,            /* current device is not a compute-capability 10.3 GPU */
+  SMOL_ERR_TIMEOUT = -8            /* a kernel's bounded wait gave up (status word)  */
+} smol_status;
+
+/* Operation selector for smol_workspace_bytes. */
+enum { SMOL_OP_BLOCK = 1, SMOL_OP_MODEL = 2, SMOL_OP_DECODE = 3 };
+
+/* Element type of the residual stream (x and out) of smol_block_forward.
+ * SMOL_ACT_F32 keeps the residual stream in fp32 across block calls (the
+ * projections still read a bf16 copy as their tensor-core operand). */
+enum { SMOL_ACT_BF16 = 0, SMOL_ACT_F32 = 1 };
+
+/* ---------------------------------------------------------------------------
+ * Packed weights.
+ * smol_prepare_weights converts raw weights into the library's layout, once,
+ * on `stream`:
+ *   - the attention and MLP RMSNorm weights are folded into the columns of
+ *     the projections that consume them (W'[j,k] = W[j,k] * w_norm[k],
+ *     rounded to bf16), and the final-norm weight into a copy of the tied
+ *     head, so each norm reduces to a per-row scale rsqrt(mean(x^2)+eps)
+ *     ([M1] section 2; [M5] RMSNorm formula);
+ *   - Wq, Wk, Wv are stacked into one [(H+2KV)*hd, d] matrix;
+ *   - Wgate and Wup are interleaved in groups of 64 rows;
+ *   - a cos/sin table of the RoPE angles pos * theta^(-2i/hd) for
+ *     pos < max_pos is computed in double precision and stored as fp32
+ *     ([M1] section 3; [M5] RotaryEmbedding).
+ * n_layers <= cfg->n_layers layers are packed (layers[0..n_layers)).  With
+ * w->embed non-NULL the embedding and head are packed too (needs vocab > 0).
+ * `packed` (device) must hold smol_packed_bytes(cfg, n_layers, with_embed)
+ * bytes; it is written asynchronously and owned by the caller.
+ * ------------------------------------------------------------------------- */
+size_t smol_packed_bytes(const smol_config *cfg, int n_layers, int with_embed);
+int smol_prepare_weights(const smol_config *cfg, const smol_model_weights *w, int n_layers,
+                         void *packed, size_t packed_bytes, void *stream);
+
+/* Workspace bytes needed by one call of `op` with batch B and T tokens per
+ * sequence (decode: T is ignored).  0 for an unsupported configuration. */
+size_t smol_workspace_bytes(const smol_config *cfg, int op, int B, int T);
+
+/* ---------------------------------------------------------------------------
+ * smol_block_forward: one decoder block, layer `layer` of a packed set.
+ *   h   = x + O(GQA-attention(RoPE(Q), RoPE(K), V)),  Q,K,V = RMSNorm1(x) W^T
+ *   out = h + Down(SiLU(Gate(RMSNorm2(h))) * Up(RMSNorm2(h)))
+ * [M1] sections 4-6 (MultiHeadSelfAttention, SmolMLP, SmolBlock);
+ * [M3] "The block, in order"; [M5] TransformerBlock.
+ *   x            device [B, T, d] input (read only), bf16 or fp32 per act_dtype.
+ *   out          device [B, T, d] output of the same type; may equal x.
+ *   act_dtype    SMOL_ACT_BF16 or SMOL_ACT_F32.
+ *   valid_start  device int32 [B] or NULL.  Sequence b is left-padded: tokens
+ *                t < valid_start[b] are padding.  A key j is visible to query t
+ *                iff valid_start[b] <= j <= t (causal plus padding mask, [M1]
+ *                section 4), and the position id of token t is
+ *                t - valid_start[b] ([M4] position_ids).  Padding rows get an
+ *                attention output of 0; their `out` rows are finite but are
+ *                not defined by the method.  Each value must lie in [0, T].
+ *   k_out,v_out  device [B, KV, T, hd] bf16 or NULL: post-RoPE keys and the
+ *                values, the per-layer cache entries of [M1] section 4.
+ *   ws           device workspace of at least
+ *                smol_workspace_bytes(cfg, SMOL_OP_BLOCK, B, T) bytes.
+ * Positions must stay below cfg->max_pos (else SMOL_ERR_TOO_LONG).
+ * ------------------------------------------------------------------------- */
+int smol_block_forward(const smol_config *cfg, const void *packed, int layer,
+                       const void *x, void *out, int act_dtype, int B, int T,
+                       const int32_t *valid_start,
+                       void *k_out, void *v_out, void *ws, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * smol_model_forward: embedding -> cfg->n_layers blocks -> final RMSNorm ->
+ * tied lm_head ([M1] section 7 SmolLM2.forward; [M4] SmolLM2Model.forward).
+ *   ids          device int32 [B, T], each in [0, V) (out-of-range ids are
+ *                clamped into range by the gather).
+ *   valid_start  device int32 [B] or NULL (as in smol_block_forward).
+ *   logits       device [B, T, V] bf16.
+ *   ws           >= smol_workspace_bytes(cfg, SMOL_OP_MODEL, B, T) bytes.
+ * Needs a packed set with all cfg->n_layers layers and the embedding.
+ * ------------------------------------------------------------------------- */
+int smol_model_forward(const smol_config *cfg, const void *packed, const int32_t *ids,
+                       int B, int T, const int32_t *valid_start, void *logits,
+                       void *ws, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * smol_decode_step: one new token per sequence with a KV cache
+ * ([M1] section 4, the past_key_value branch, and section 7 generate).
+ *   ids        device int32 [B], the new tokens.
+ *   cache_len  device int32 [B]: sequence b has cache_len[b] cached entries
+ *              (slots [0, cache_len[b]) of its cache rows); its new token is
+ *              at position cache_len[b] and attends over those entries plus
+ *              its own key/value, with no other mask.  Each value must lie in
+ *              [0, S_max] and cache_len[b] < max_pos (not checked on the host:
+ *              values are clamped to [0, min(S_max, max_pos-1)] on the device).
+ *   k_cache,v_cache device [L, B, KV, S_max, hd] bf16, post-RoPE keys (stored
+ *              "after RoPE, before GQA expansion", [M1] section 4).  Read only.
+ *   k_new,v_new device [L, B, KV, hd] bf16 outputs: this token's post-RoPE key
+ *              and its value per layer.  The cache is not written; appending
+ *              them at slot cache_len[b] is left to the caller (the slot may
+ *              not exist when cache_len[b] == S_max).
+ *   logits     device [B, V] bf16, next-token logits.
+ *   ws         >= smol_workspace_bytes(cfg, SMOL_OP_DECODE, B, 1) bytes.
+ * ------------------------------------------------------------------------- */
+int smol_decode_step(const smol_config *cfg, const void *packed, const int32_t *ids,
+                     const int32_t *cache_len, int B, const void *k_cache, const void *v_cache,
+                     int S_max, void *k_new, void *v_new, void *logits,
+                     void *ws, size_t ws_bytes, void *stream);
+
+/* Reads (synchronising `stream`) and clears the workspace status word written
+ * by kernels whose bounded waits gave up.  Returns SMOL_OK, SMOL_ERR_TIMEOUT
+ * or SMOL_ERR_CUDA.  Not meant for the hot path. */
+int smol_workspace_status(void *ws, void *stream);
+
+/* Number of kernels the most recent forward/decode call on this thread
+ * launched (0 after an argument error). */
+int smol_last_launch_count(void);
+
+/* Static text for a status code; for SMOL_ERR_CUDA, the last CUDA error text. */
+const char *smol_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SMOL_H */

@@ -1,0 +1,92 @@
+// common.cuh - declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "smol.h"
+
+namespace smol {
+
+typedef __nv_bfloat16 bf16;
+typedef __half f16;
+
+__host__ __device__ constexpr long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
+
+// ------------------------------------------------------------------ GEMM
+// D[M, N] = A[M, K] * B[N, K]^T on tcgen05 with one of these epilogues.
+enum Epilogue : int {
+  kEpiQkvRope = 0,   // rstd row scale, RoPE on q/k heads, scatter to [B, heads, T, hd]
+  kEpiResidual = 1,  // out = resid + D (fp32 and/or bf16), accumulates row sum(out^2)
+  kEpiSwiglu = 2,    // rstd row scale, silu(gate) * up over 64-column gate/up groups
+  kEpiScale = 3,     // out = rstd * D (bf16); rstd = 1 without ssq_in
+};
+
+// Operands A and B are f16 (activations are kept as f16 tensor-core operands,
+// weights are converted to f16 when packed); accumulation is fp32.
+struct GemmParams {
+  int M, N, K;
+  void *out;              // 16-bit output rows, leading dimension ldo (elements); optional
+                          // for kEpiResidual when out_f32 is given
+  int out_is_f16;         // element type of `out`: 1 = f16, 0 = bf16
+  long long ldo;
+  const bf16 *resid;      // kEpiResidual: bf16 residual rows (leading dimension ldo), or
+  const float *resid_f32; //   fp32 residual rows (exactly one of the two is set)
+  float *out_f32;         // kEpiResidual: optional fp32 copy of the output rows
+  const float *ssq_in;    // per-row sum of squares feeding rstd (nullptr: scale 1)
+  float inv_dim;          // 1 / d for the mean of squares
+  float eps;
+  float *ssq_out;         // kEpiResidual: atomically accumulates sum(out^2) per row
+  float *ssq_zero;        // rows of this buffer are cleared by the n-block-0 tiles
+  // kEpiQkvRope
+  f16 *q, *k, *v;         // f16 [B, H, T, hd], [B, KV, T, hd], [B, KV, T, hd]; k, v optional
+  bf16 *k_bf, *v_bf;      // optional bf16 copies of k and v (cache entries), same layout
+  int T, H, KV, hd;
+  const float2 *rope;     // [max_pos][hd/2] (cos, sin)
+  const int *valid_start; // [B] or nullptr: position t - valid_start[b]
+  const int *pos_add;     // [B] or nullptr: adds clamp(pos_add[b], 0, pos_limit) (decode)
+  int pos_limit;
+  int max_pos;
+  int *status;            // device status word
+};
+
+// Encodes a 2-D f16 tensor map (rows x cols, row pitch in elements) with a
+// box of box_rows x 64 columns and 128-byte swizzle.  Returns false on error.
+bool make_tmap_f16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                    uint64_t row_pitch_elems, uint32_t box_rows);
+
+// Chooses the N tile for an epilogue and problem; 0 if unsupported.
+int gemm_pick_bn(int epi, int N, int hd);
+
+// Launches the persistent GEMM (A: M x K, B: N x K, both K-contiguous).
+cudaError_t launch_gemm(int epi, int bn, const void *A, const void *B, const GemmParams &p,
+                        int num_sms, cudaStream_t stream);
+
+// ------------------------------------------------------------------ attention
+struct AttnParams {
+  const f16 *q;           // [B, H, T, hd]
+  const f16 *k, *v;       // [B, KV, T, hd]
+  f16 *o;                 // [B, T, H * hd]
+  const int *valid_start; // [B] or nullptr
+  int B, T, H, KV, hd;
+  float scale_log2;       // log2(e) / sqrt(hd)
+};
+cudaError_t launch_flash_attention(const AttnParams &p, cudaStream_t stream);
+
+// ------------------------------------------------------------------ small kernels
+cudaError_t launch_embed_rows(const int *ids, const bf16 *embed, int vocab, int d, long long rows,
+                              f16 *x16, float *x_f32, float *ssq, cudaStream_t stream);
+cudaError_t launch_row_ssq(const bf16 *x, long long rows, int d, f16 *x16, float *ssq,
+                           cudaStream_t stream);
+cudaError_t launch_row_ssq_f32(const float *x, long long rows, int d, f16 *x16, float *ssq,
+                               cudaStream_t stream);
+cudaError_t launch_scale_cols_copy(const bf16 *src, const bf16 *norm_w, long long rows, int cols,
+                                   f16 *dst, cudaStream_t stream);
+cudaError_t launch_interleave_gate_up(const bf16 *wg, const bf16 *wu, const bf16 *norm_w, int I,
+                                      int d, f16 *dst, cudaStream_t stream);
+cudaError_t launch_rope_table(int max_pos, int hd, float theta, float2 *table, cudaStream_t stream);
+
+}  // namespace smol

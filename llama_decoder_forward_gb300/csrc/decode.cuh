@@ -1,0 +1,26 @@
+// decode.cuh - one KV-cache decode step (declarations).
+#pragma once
+
+#include "common.cuh"
+
+namespace smol {
+
+struct DecodeArgs {
+  smol_config cfg;
+  int B, S_max;
+  const int *ids;          // [B]
+  const int *cache_len;    // [B]
+  const bf16 *k_cache, *v_cache;   // [L, B, KV, S_max, hd]
+  bf16 *k_new, *v_new;     // [L, B, KV, hd]
+  bf16 *logits;            // [B, V]
+  const float2 *rope;      // [max_pos][hd/2]
+  const bf16 *embed;       // bf16 table for the gather
+  const f16 *head;         // f16 norm-folded tied head
+  const uint8_t *layer0;   // first packed layer
+  size_t layer_bytes, off_qkv, off_o, off_gu, off_down;
+};
+
+size_t decode_ws_bytes(const smol_config *cfg, int B);
+cudaError_t run_decode(const DecodeArgs &a, void *ws, int sms, cudaStream_t stream, int *launches);
+
+}  // namespace smol

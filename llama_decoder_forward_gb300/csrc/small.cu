@@ -1,0 +1,191 @@
+// small.cu - bandwidth-bound helper kernels: embedding gather with row
+// sum-of-squares, row sum-of-squares, one-time weight packing, RoPE table.
+#include <math.h>
+
+#include "common.cuh"
+#include "prims.cuh"
+
+namespace smol {
+
+// x[r, :] = E[ids[r], :] as an f16 operand copy (x16) and in fp32 (x_f32,
+// optional), and ssq[r] = sum_k x[r,k]^2 (feeds the first RMSNorm).
+// "model.py" (SmolLM2-135M) section 7: embed_tokens(input_ids).  One warp per
+// row, 16-byte loads.  d must be a multiple of 8.
+__global__ void embed_rows_kernel(const int *__restrict__ ids, const bf16 *__restrict__ E, int V,
+                                  int d, long long rows, f16 *__restrict__ x16,
+                                  float *__restrict__ x_f32, float *__restrict__ ssq) {
+  const long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  int id = ids[r];
+  id = id < 0 ? 0 : (id >= V ? V - 1 : id);
+  const uint4 *src = reinterpret_cast<const uint4 *>(E + (long long)id * d);
+  uint4 *dst = reinterpret_cast<uint4 *>(x16 + r * d);
+  float acc = 0.f;
+  for (int c = lane; c < d / 8; c += 32) {
+    const uint4 v = src[c];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float f[8];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 t = unpack_bf16x2(w[e]);
+      f[2 * e] = t.x;
+      f[2 * e + 1] = t.y;
+      acc += t.x * t.x + t.y * t.y;
+    }
+    dst[c] = make_uint4(pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]), pack_f16x2(f[4], f[5]),
+                        pack_f16x2(f[6], f[7]));
+    if (x_f32) {
+      float4 *d4 = reinterpret_cast<float4 *>(x_f32 + r * d) + 2 * c;
+      d4[0] = make_float4(f[0], f[1], f[2], f[3]);
+      d4[1] = make_float4(f[4], f[5], f[6], f[7]);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) ssq[r] = acc;
+}
+
+// ssq[r] = sum_k x[r,k]^2 for an fp32 row, plus its f16 copy (the tensor-core
+// operand of the next projection).
+__global__ void row_ssq_f32_kernel(const float *__restrict__ x, long long rows, int d,
+                                   f16 *__restrict__ x16, float *__restrict__ ssq) {
+  const long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  const float4 *src = reinterpret_cast<const float4 *>(x + r * d);
+  uint4 *dst = reinterpret_cast<uint4 *>(x16 + r * d);
+  float acc = 0.f;
+  for (int c = lane; c < d / 8; c += 32) {
+    const float4 a = src[2 * c], b = src[2 * c + 1];
+    acc += a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w + b.x * b.x + b.y * b.y + b.z * b.z + b.w * b.w;
+    dst[c] = make_uint4(pack_f16x2(a.x, a.y), pack_f16x2(a.z, a.w), pack_f16x2(b.x, b.y),
+                        pack_f16x2(b.z, b.w));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) ssq[r] = acc;
+}
+
+// The same for a bf16 row.
+__global__ void row_ssq_kernel(const bf16 *__restrict__ x, long long rows, int d,
+                               f16 *__restrict__ x16, float *__restrict__ ssq) {
+  const long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  const uint4 *src = reinterpret_cast<const uint4 *>(x + r * d);
+  uint4 *dst = reinterpret_cast<uint4 *>(x16 + r * d);
+  float acc = 0.f;
+  for (int c = lane; c < d / 8; c += 32) {
+    const uint4 v = src[c];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = unpack_bf16x2(w[e]);
+      acc += f.x * f.x + f.y * f.y;
+      o[e] = pack_f16x2(f.x, f.y);
+    }
+    dst[c] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) ssq[r] = acc;
+}
+
+// dst[r, c] = f16(src[r, c] * w[c]) (w == nullptr: plain conversion).  Folds
+// an RMSNorm weight into the columns of the matrix that consumes its output.
+__global__ void scale_cols_kernel(const bf16 *__restrict__ src, const bf16 *__restrict__ w,
+                                  long long rows, int cols, f16 *__restrict__ dst) {
+  const long long n = rows * cols;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int c = static_cast<int>(i % cols);
+    float v = __bfloat162float(src[i]);
+    if (w) v *= __bfloat162float(w[c]);
+    dst[i] = __float2half_rn(v);
+  }
+}
+
+// Packed gate/up matrix [2I, d]: rows 128j..128j+63 are gate rows 64j..64j+63,
+// rows 128j+64..128j+127 are the matching up rows; both scaled by the MLP
+// norm weight along d, stored as f16.
+__global__ void interleave_gate_up_kernel(const bf16 *__restrict__ wg, const bf16 *__restrict__ wu,
+                                          const bf16 *__restrict__ w, int I, int d,
+                                          f16 *__restrict__ dst) {
+  const long long n = 2LL * I * d;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long r = i / d;
+    const int c = static_cast<int>(i - r * d);
+    const long long grp = r / 128, within = r % 128;
+    const bf16 *src = within < 64 ? wg : wu;
+    const long long sr = grp * 64 + (within & 63);
+    float v = __bfloat162float(src[sr * d + c]);
+    if (w) v *= __bfloat162float(w[c]);
+    dst[i] = __float2half_rn(v);
+  }
+}
+
+// table[pos][i] = (cos, sin)(pos * theta^(-2i/hd)) computed in double and
+// stored as fp32 ("model.py" (SmolLM2-135M) section 3 rope_freqs /
+// build_rope_cache; "components.py" RotaryEmbedding).  Exact integer positions.
+__global__ void rope_table_kernel(int max_pos, int hd, double theta, float2 *__restrict__ table) {
+  const int half = hd / 2;
+  const long long n = (long long)max_pos * half;
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < n;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const long long pos = idx / half;
+    const int i = static_cast<int>(idx - pos * half);
+    const double inv_freq = pow(theta, -2.0 * i / hd);
+    const double ang = static_cast<double>(pos) * inv_freq;
+    table[idx] = make_float2(static_cast<float>(cos(ang)), static_cast<float>(sin(ang)));
+  }
+}
+
+static int grid_for(long long n, int threads) {
+  long long g = cdiv(n, threads);
+  return static_cast<int>(g > 65535LL * 8 ? 65535LL * 8 : (g < 1 ? 1 : g));
+}
+
+cudaError_t launch_embed_rows(const int *ids, const bf16 *embed, int vocab, int d, long long rows,
+                              f16 *x16, float *x_f32, float *ssq, cudaStream_t stream) {
+  const int wpb = 8;
+  embed_rows_kernel<<<(unsigned)cdiv(rows, wpb), wpb * 32, 0, stream>>>(ids, embed, vocab, d, rows,
+                                                                          x16, x_f32, ssq);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_row_ssq(const bf16 *x, long long rows, int d, f16 *x16, float *ssq,
+                           cudaStream_t stream) {
+  const int wpb = 8;
+  row_ssq_kernel<<<(unsigned)cdiv(rows, wpb), wpb * 32, 0, stream>>>(x, rows, d, x16, ssq);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_row_ssq_f32(const float *x, long long rows, int d, f16 *x16, float *ssq,
+                               cudaStream_t stream) {
+  const int wpb = 8;
+  row_ssq_f32_kernel<<<(unsigned)cdiv(rows, wpb), wpb * 32, 0, stream>>>(x, rows, d, x16, ssq);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scale_cols_copy(const bf16 *src, const bf16 *norm_w, long long rows, int cols,
+                                   f16 *dst, cudaStream_t stream) {
+  scale_cols_kernel<<<grid_for(rows * cols, 256), 256, 0, stream>>>(src, norm_w, rows, cols, dst);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_interleave_gate_up(const bf16 *wg, const bf16 *wu, const bf16 *norm_w, int I,
+                                      int d, f16 *dst, cudaStream_t stream) {
+  interleave_gate_up_kernel<<<grid_for(2LL * I * d, 256), 256, 0, stream>>>(wg, wu, norm_w, I, d, dst);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_table(int max_pos, int hd, float theta, float2 *table, cudaStream_t stream) {
+  rope_table_kernel<<<grid_for((long long)max_pos * (hd / 2), 256), 256, 0, stream>>>(
+      max_pos, hd, static_cast<double>(theta), table);
+  return cudaGetLastError();
+}
+
+}  // namespace smol

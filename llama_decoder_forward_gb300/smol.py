@@ -1,0 +1,205 @@
+"""ctypes binding of libsmol (include/smol.h): argument marshalling only.
+
+Every computation runs in the library's CUDA kernels.  Importing this module
+loads ``libsmol.so`` from this package directory and raises ImportError if it
+has not been built (``python -c "import __graft_entry__ as g; g.build()"``);
+there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from ctypes import POINTER, c_float, c_int, c_size_t, c_void_p
+from typing import Dict, List, Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsmol.so")
+HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "smol.h")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libsmol.so is not built ({LIB_PATH}); run __graft_entry__.build() first")
+_lib = ctypes.CDLL(LIB_PATH)
+
+OK = 0
+ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_MISALIGNED, ERR_TOO_LONG = -1, -2, -3, -4
+ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE, ERR_TIMEOUT = -5, -6, -7, -8
+OP_BLOCK, OP_MODEL, OP_DECODE = 1, 2, 3
+ACT_BF16, ACT_F32 = 0, 1
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("hidden", c_int), ("n_heads", c_int), ("n_kv_heads", c_int), ("head_dim", c_int),
+                ("intermediate", c_int), ("n_layers", c_int), ("vocab", c_int), ("max_pos", c_int),
+                ("rms_eps", c_float), ("rope_theta", c_float)]
+
+
+class BlockWeights(ctypes.Structure):
+    _fields_ = [(k, c_void_p) for k in ("attn_norm", "wq", "wk", "wv", "wo", "mlp_norm", "wgate",
+                                       "wup", "wdown")]
+
+
+class ModelWeights(ctypes.Structure):
+    _fields_ = [("layers", POINTER(BlockWeights)), ("embed", c_void_p), ("final_norm", c_void_p)]
+
+
+_CFG = POINTER(Config)
+_SIGS = {
+    "smol_packed_bytes": (c_size_t, [_CFG, c_int, c_int]),
+    "smol_prepare_weights": (c_int, [_CFG, POINTER(ModelWeights), c_int, c_void_p, c_size_t, c_void_p]),
+    "smol_workspace_bytes": (c_size_t, [_CFG, c_int, c_int, c_int]),
+    "smol_block_forward": (c_int, [_CFG, c_void_p, c_int, c_void_p, c_void_p, c_int, c_int, c_int, c_void_p,
+                                   c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "smol_model_forward": (c_int, [_CFG, c_void_p, c_void_p, c_int, c_int, c_void_p, c_void_p,
+                                   c_void_p, c_size_t, c_void_p]),
+    "smol_decode_step": (c_int, [_CFG, c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_int,
+                                 c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "smol_workspace_status": (c_int, [c_void_p, c_void_p]),
+    "smol_last_launch_count": (c_int, []),
+    "smol_status_string": (ctypes.c_char_p, [c_int]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+
+def declared_symbols() -> List[str]:
+    """Function names declared in include/smol.h."""
+    text = open(HEADER_PATH).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(smol_\w+)\s*\(", text, re.M)))
+
+
+class SmolError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {code} ({status_string(code)})")
+
+
+def status_string(code: int) -> str:
+    return _lib.smol_status_string(code).decode()
+
+
+def _check(code: int, where: str) -> None:
+    if code != OK:
+        raise SmolError(code, where)
+
+
+def make_config(hidden, n_heads, n_kv_heads, head_dim, intermediate, n_layers, vocab, max_pos,
+                rms_eps, rope_theta) -> Config:
+    return Config(hidden, n_heads, n_kv_heads, head_dim, intermediate, n_layers, vocab, max_pos,
+                  rms_eps, rope_theta)
+
+
+def config_of(wl) -> Config:
+    """Config from a synth.Workload (same field names)."""
+    return make_config(wl.hidden, wl.n_heads, wl.n_kv_heads, wl.head_dim, wl.intermediate,
+                       wl.n_layers, wl.vocab, wl.max_pos, wl.rms_eps, wl.rope_theta)
+
+
+def _p(t: Optional[torch.Tensor]):
+    return None if t is None else c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return c_void_p(s.cuda_stream)
+
+
+def _dev(t: torch.Tensor, dtype, name: str) -> torch.Tensor:
+    if not (t.is_cuda and t.dtype == dtype and t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
+    return t
+
+
+def packed_bytes(cfg: Config, n_layers: int, with_embed: bool) -> int:
+    return _lib.smol_packed_bytes(ctypes.byref(cfg), n_layers, int(with_embed))
+
+
+def workspace_bytes(cfg: Config, op: int, B: int, T: int) -> int:
+    return _lib.smol_workspace_bytes(ctypes.byref(cfg), op, B, T)
+
+
+def alloc_workspace(cfg: Config, op: int, B: int, T: int, device="cuda") -> torch.Tensor:
+    n = workspace_bytes(cfg, op, B, T)
+    if n == 0:
+        raise SmolError(ERR_UNSUPPORTED_SHAPE, "smol_workspace_bytes")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+_LAYER_KEYS = ("attn_norm", "wq", "wk", "wv", "wo", "mlp_norm", "wgate", "wup", "wdown")
+
+
+def prepare_weights(cfg: Config, layers: Sequence[Dict[str, torch.Tensor]], embed=None,
+                    final_norm=None, stream=None) -> torch.Tensor:
+    """Packs raw bf16 weights (device tensors) into a new device buffer."""
+    n_layers = len(layers)
+    arr = (BlockWeights * max(n_layers, 1))()
+    for i, lw in enumerate(layers):
+        arr[i] = BlockWeights(*[c_void_p(_dev(lw[k], torch.bfloat16, k).data_ptr()) for k in _LAYER_KEYS])
+    mw = ModelWeights(arr, _p(embed), _p(final_norm))
+    if embed is not None:
+        _dev(embed, torch.bfloat16, "embed")
+        _dev(final_norm, torch.bfloat16, "final_norm")
+    n = packed_bytes(cfg, n_layers, embed is not None)
+    if n == 0:
+        raise SmolError(ERR_UNSUPPORTED_SHAPE, "smol_packed_bytes")
+    device = embed.device if embed is not None else layers[0]["wq"].device
+    packed = torch.empty(n, dtype=torch.uint8, device=device)
+    _check(_lib.smol_prepare_weights(ctypes.byref(cfg), ctypes.byref(mw), n_layers, _p(packed), n,
+                                     _stream(stream)), "smol_prepare_weights")
+    return packed
+
+
+def block_forward(cfg: Config, packed: torch.Tensor, layer: int, x: torch.Tensor, out: torch.Tensor,
+                  ws: torch.Tensor, valid_start=None, k_out=None, v_out=None, stream=None) -> None:
+    B, T, _ = x.shape
+    if x.dtype not in (torch.bfloat16, torch.float32) or out.dtype != x.dtype:
+        raise ValueError("x and out must both be bf16 or both fp32")
+    _dev(x, x.dtype, "x")
+    _dev(out, x.dtype, "out")
+    act = ACT_F32 if x.dtype == torch.float32 else ACT_BF16
+    if valid_start is not None:
+        _dev(valid_start, torch.int32, "valid_start")
+    _check(_lib.smol_block_forward(ctypes.byref(cfg), _p(packed), layer, _p(x), _p(out), act, B, T,
+                                   _p(valid_start), _p(k_out), _p(v_out), _p(ws), ws.numel(),
+                                   _stream(stream)), "smol_block_forward")
+
+
+def model_forward(cfg: Config, packed: torch.Tensor, ids: torch.Tensor, logits: torch.Tensor,
+                  ws: torch.Tensor, valid_start=None, stream=None) -> None:
+    B, T = ids.shape
+    _dev(ids, torch.int32, "ids")
+    _dev(logits, torch.bfloat16, "logits")
+    _check(_lib.smol_model_forward(ctypes.byref(cfg), _p(packed), _p(ids), B, T, _p(valid_start),
+                                   _p(logits), _p(ws), ws.numel(), _stream(stream)),
+           "smol_model_forward")
+
+
+def decode_step(cfg: Config, packed: torch.Tensor, ids: torch.Tensor, cache_len: torch.Tensor,
+                k_cache: torch.Tensor, v_cache: torch.Tensor, k_new: torch.Tensor,
+                v_new: torch.Tensor, logits: torch.Tensor, ws: torch.Tensor, stream=None) -> None:
+    B = ids.shape[0]
+    S_max = k_cache.shape[3]
+    _dev(ids, torch.int32, "ids")
+    _dev(cache_len, torch.int32, "cache_len")
+    for name, t in (("k_cache", k_cache), ("v_cache", v_cache), ("k_new", k_new), ("v_new", v_new),
+                    ("logits", logits)):
+        _dev(t, torch.bfloat16, name)
+    _check(_lib.smol_decode_step(ctypes.byref(cfg), _p(packed), _p(ids), _p(cache_len), B,
+                                 _p(k_cache), _p(v_cache), S_max, _p(k_new), _p(v_new), _p(logits),
+                                 _p(ws), ws.numel(), _stream(stream)), "smol_decode_step")
+
+
+def workspace_status(ws: torch.Tensor, stream=None) -> int:
+    """Synchronising read (and reset) of the kernels' status word."""
+    return _lib.smol_workspace_status(_p(ws), _stream(stream))
+
+
+def last_launch_count() -> int:
+    return _lib.smol_last_launch_count()
+
+
+raw = _lib   # the C entry points themselves, for callers that marshal by hand

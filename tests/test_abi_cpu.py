@@ -1,0 +1,108 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds and loads,
+exports every function include/smol.h declares, and rejects bad arguments
+before touching the device."""
+import ctypes
+import re
+
+import pytest
+
+from llama_decoder_forward_gb300 import build as B
+
+
+@pytest.fixture(scope="module")
+def smol():
+    B.build()
+    from llama_decoder_forward_gb300 import smol as S
+    return S
+
+
+def test_exports_every_declared_symbol(smol):
+    names = smol.declared_symbols()
+    assert len(names) >= 9
+    for n in ("smol_block_forward", "smol_model_forward", "smol_decode_step", "smol_prepare_weights",
+              "smol_workspace_bytes", "smol_packed_bytes", "smol_status_string"):
+        assert n in names
+    lib = ctypes.CDLL(smol.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_no_unexpected_exports(smol):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", smol.LIB_PATH], capture_output=True, text=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    ours = {n for n in exported if n.startswith("smol_")}
+    assert ours == set(smol.declared_symbols())
+
+
+def _cfg(smol, **kw):
+    base = dict(hidden=576, n_heads=9, n_kv_heads=3, head_dim=64, intermediate=1536, n_layers=30,
+                vocab=49152, max_pos=8192, rms_eps=1e-5, rope_theta=1e5)
+    base.update(kw)
+    return smol.make_config(**base)
+
+
+def test_size_queries(smol):
+    cfg = _cfg(smol)
+    d, hd, H, KV, I, V = 576, 64, 9, 3, 1536, 49152
+    layer = (H + 2 * KV) * hd * d * 2 + d * H * hd * 2 + 2 * I * d * 2 + d * I * 2
+    rope = 8192 * (hd // 2) * 8
+    total = smol.packed_bytes(cfg, 30, True)
+    assert total >= rope + 30 * layer + 2 * V * d * 2
+    assert total < rope + 30 * layer + 2 * V * d * 2 + 64 * 1024
+    assert smol.packed_bytes(cfg, 1, False) < smol.packed_bytes(cfg, 2, False)
+    assert smol.packed_bytes(cfg, 31, False) == 0
+    ws = smol.workspace_bytes(cfg, smol.OP_MODEL, 8, 2048)
+    M = 8 * 2048
+    assert ws >= M * (2 * d + 2 * H * hd + 2 * KV * hd + I) * 2 + 2 * M * 4
+    assert smol.workspace_bytes(cfg, smol.OP_DECODE, 64, 1) > 0
+    assert smol.workspace_bytes(cfg, 99, 8, 2048) == 0
+    assert smol.workspace_bytes(_cfg(smol, head_dim=96, hidden=864), smol.OP_BLOCK, 1, 1) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(head_dim=96, hidden=864), -2),     # unsupported head_dim
+    (dict(n_kv_heads=4), -2),                # H % KV != 0
+    (dict(hidden=512), -2),                  # d != H * hd
+    (dict(n_kv_heads=1, n_heads=9), 0),      # group 9 > 8 is rejected below separately
+    (dict(intermediate=1500), -2),           # not a multiple of 64
+    (dict(rms_eps=-1.0), -1),
+    (dict(n_layers=0), -1),
+])
+def test_config_validation(smol, kw, code):
+    cfg = _cfg(smol, **kw)
+    fake = ctypes.c_void_p(0x10000)
+    rc = smol.raw.smol_block_forward(ctypes.byref(cfg), fake, 0, fake, fake, 0, 1, 8, None, None, None,
+                                     fake, 1 << 40, None)
+    if code == 0:
+        assert rc == -2   # group of 9 query heads per kv head exceeds 8
+    else:
+        assert rc == code
+
+
+def test_argument_errors_return_before_any_launch(smol):
+    cfg = _cfg(smol)
+    f = ctypes.c_void_p(0x10000)
+    big = 1 << 40
+    blk = smol.raw.smol_block_forward
+    assert blk(ctypes.byref(cfg), None, 0, f, f, 0, 1, 8, None, None, None, f, big, None) == -1
+    assert blk(ctypes.byref(cfg), f, 30, f, f, 0, 1, 8, None, None, None, f, big, None) == -1   # layer
+    assert blk(ctypes.byref(cfg), f, 0, f, f, 0, 0, 8, None, None, None, f, big, None) == -1    # B
+    assert blk(ctypes.byref(cfg), f, 0, f, f, 0, 1, 8193, None, None, None, f, big, None) == -4  # too long
+    assert blk(ctypes.byref(cfg), f, 0, ctypes.c_void_p(0x10008), f, 0, 1, 8, None, None, None, f, big,
+               None) == -3                                                                   # misaligned
+    assert blk(ctypes.byref(cfg), f, 0, f, f, 0, 1, 8, None, None, None, f, 16, None) == -5      # workspace
+    mdl = smol.raw.smol_model_forward
+    assert mdl(ctypes.byref(cfg), f, f, 1, 8193, None, f, f, big, None) == -4
+    assert mdl(ctypes.byref(cfg), f, ctypes.c_void_p(0x10002), 1, 8, None, f, f, big, None) == -3
+    assert mdl(ctypes.byref(_cfg(smol, vocab=0)), f, f, 1, 8, None, f, f, big, None) == -1
+    dec = smol.raw.smol_decode_step
+    assert dec(ctypes.byref(cfg), f, f, f, 64, f, f, 0, f, f, f, f, big, None) == -1          # S_max
+    assert dec(ctypes.byref(cfg), f, f, f, 64, f, f, 4096, f, f, f, f, 16, None) == -5
+    assert smol.last_launch_count() == 0
+
+
+def test_status_strings(smol):
+    for code in range(-8, 1):
+        assert smol.status_string(code)
+    assert "unknown" in smol.status_string(-99)

@@ -1,0 +1,188 @@
+"""GPU-vs-oracle parity through the C ABI, at sizes the fp64 oracle finishes in
+seconds that still span several tiles and a ragged tail."""
+import numpy as np
+import pytest
+import torch
+
+from llama_decoder_forward_gb300 import synth
+from oracle import oracle as O
+from parity_util import (BLOCK_REL_TOL, LOGITS_COS_MIN, LOGITS_MAX_ABS, cosine, max_abs, np32,
+                         oracle_config, oracle_layers, rel_max_err, rel_max_err_bf16_out, to_device)
+
+pytestmark = pytest.mark.gpu
+
+W = synth.WORKLOADS
+
+
+@pytest.fixture(scope="module")
+def S():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from llama_decoder_forward_gb300 import smol
+    return smol
+
+
+def run_block_case(S, wl, seed=0, check_kv=True, act=torch.float32, x_scale=1.0):
+    """One block through the C ABI vs the oracle.  act is the residual-stream
+    type of x/out (fp32: the stated bar; bf16: the bar plus the output's own
+    rounding).  k/v are bf16 cache entries, checked like bf16 outputs."""
+    inp = synth.generate(wl, seed=seed)
+    if x_scale != 1.0:
+        inp.x = (inp.x.float() * x_scale).to(torch.bfloat16)
+    dev = to_device(inp)
+    cfg = S.config_of(wl)
+    packed = S.prepare_weights(cfg, dev.layers)
+    ws = S.alloc_workspace(cfg, S.OP_BLOCK, wl.B, wl.T)
+    x = dev.x.to(act).contiguous()
+    out = torch.empty_like(x)
+    k_out = torch.empty(wl.B, wl.n_kv_heads, wl.T, wl.head_dim, dtype=torch.bfloat16, device="cuda")
+    v_out = torch.empty_like(k_out)
+    S.block_forward(cfg, packed, 0, x, out, ws, valid_start=dev.valid_start, k_out=k_out, v_out=v_out)
+    assert S.workspace_status(ws) == S.OK
+    torch.cuda.synchronize()
+    taps = {}
+    vs = None if inp.valid_start is None else inp.valid_start.numpy()
+    ref = O.block_forward(oracle_config(wl, 1), oracle_layers(inp, 1)[0], np32(inp.x), vs, taps=taps)
+    got = out.float().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    rows = np.ones((wl.B, wl.T), dtype=bool)
+    if vs is not None:
+        for b in range(wl.B):
+            rows[b, :vs[b]] = False
+    metric = rel_max_err if act == torch.float32 else rel_max_err_bf16_out
+    err = metric(got[rows], ref[rows])
+    ek = ev = 0.0
+    if check_kv:
+        kmask = np.broadcast_to(rows[:, None, :, None], taps["attention_keys"].shape)
+        ek = rel_max_err_bf16_out(np32(k_out)[kmask], taps["attention_keys"][kmask])
+        ev = rel_max_err_bf16_out(np32(v_out)[kmask], taps["attention_values"][kmask])
+    msg = f"rel max err ({act}): out {err:.3e}, k {ek:.3e}, v {ev:.3e}"
+    print(msg)
+    assert err <= BLOCK_REL_TOL and ek <= BLOCK_REL_TOL and ev <= BLOCK_REL_TOL, msg
+    return err
+
+
+@pytest.mark.parametrize("act", [torch.float32, torch.bfloat16])
+def test_block_smollm2_b1_t128(S, act):
+    run_block_case(S, W["smollm2_block_b1_t128"], act=act)
+
+
+def test_block_small_residual_input(S):
+    # input at the embedding's scale (std 0.0417): the block output is then
+    # almost entirely attention + MLP, the hardest case for the relative bar
+    run_block_case(S, W["smollm2_block_b1_t128"].scaled(B=2, T=96), x_scale=0.0417)
+
+
+@pytest.mark.parametrize("B,T", [(2, 200), (1, 1), (3, 67), (1, 385)])
+def test_block_smollm2_ragged(S, B, T):
+    run_block_case(S, W["smollm2_block_b1_t128"].scaled(B=B, T=T), seed=B * 1000 + T)
+
+
+def test_block_smollm3_shape(S):
+    run_block_case(S, W["smollm3_4blocks_b4_t4096"].scaled(B=1, T=160, n_layers=1))
+
+
+@pytest.mark.parametrize("act", [torch.float32, torch.bfloat16])
+def test_block_left_padded(S, act):
+    wl = W["slm125m_block_leftpad_b16_t1024"].scaled(B=4, T=192, len_range=(1, 192))
+    run_block_case(S, wl, seed=3, act=act)
+
+
+def test_block_left_padded_all_padding_row(S):
+    # one sequence is entirely padding (valid_start == T): its rows must stay finite
+    wl = W["slm125m_block_leftpad_b16_t1024"].scaled(B=2, T=64, len_range=(1, 64))
+    inp = synth.generate(wl, seed=5)
+    inp.valid_start = torch.tensor([64, 10], dtype=torch.int32)
+    dev = to_device(inp)
+    cfg = S.config_of(wl)
+    packed = S.prepare_weights(cfg, dev.layers)
+    ws = S.alloc_workspace(cfg, S.OP_BLOCK, 2, 64)
+    out = torch.empty_like(dev.x)
+    S.block_forward(cfg, packed, 0, dev.x, out, ws, valid_start=dev.valid_start)
+    torch.cuda.synchronize()
+    got = np32(out)
+    assert np.all(np.isfinite(got))
+    ref = O.block_forward(oracle_config(wl, 1), oracle_layers(inp, 1)[0], np32(inp.x), [64, 10])
+    assert rel_max_err_bf16_out(got[1, 10:], ref[1, 10:]) <= BLOCK_REL_TOL
+
+
+def test_block_in_place(S):
+    wl = W["smollm2_block_b1_t128"].scaled(B=2, T=130)
+    inp = synth.generate(wl, seed=9)
+    dev = to_device(inp)
+    cfg = S.config_of(wl)
+    packed = S.prepare_weights(cfg, dev.layers)
+    ws = S.alloc_workspace(cfg, S.OP_BLOCK, wl.B, wl.T)
+    x = dev.x.clone()
+    S.block_forward(cfg, packed, 0, x, x, ws)
+    torch.cuda.synchronize()
+    ref = O.block_forward(oracle_config(wl, 1), oracle_layers(inp, 1)[0], np32(inp.x))
+    assert rel_max_err_bf16_out(np32(x), ref) <= BLOCK_REL_TOL
+    # fp32 residual stream in place
+    x32 = dev.x.float().contiguous()
+    S.block_forward(cfg, packed, 0, x32, x32, ws)
+    torch.cuda.synchronize()
+    assert rel_max_err(x32.cpu().numpy(), ref) <= BLOCK_REL_TOL
+
+
+def run_model_case(S, wl, seed=0, valid_start=None):
+    inp = synth.generate(wl, seed=seed)
+    dev = to_device(inp)
+    cfg = S.config_of(wl)
+    packed = S.prepare_weights(cfg, dev.layers, dev.embed, dev.final_norm)
+    ws = S.alloc_workspace(cfg, S.OP_MODEL, wl.B, wl.T)
+    logits = torch.empty(wl.B, wl.T, wl.vocab, dtype=torch.bfloat16, device="cuda")
+    S.model_forward(cfg, packed, dev.ids, logits, ws)
+    assert S.workspace_status(ws) == S.OK
+    ref = O.model_forward(oracle_config(wl), oracle_layers(inp), np32(inp.embed), np32(inp.final_norm),
+                          inp.ids.numpy().astype(np.int64))
+    got = np32(logits)
+    assert np.all(np.isfinite(got))
+    cos, mabs = cosine(got, ref), max_abs(got, ref)
+    print(f"model: cos {cos:.7f} max abs {mabs:.3e}")
+    assert cos >= LOGITS_COS_MIN and mabs <= LOGITS_MAX_ABS, (cos, mabs)
+    return cos, mabs
+
+
+def test_model_two_layers(S):
+    run_model_case(S, W["smollm2_model_b8_t2048"].scaled(B=2, T=96, n_layers=2))
+
+
+def test_model_ragged_small_vocab(S):
+    run_model_case(S, W["smollm2_model_b8_t2048"].scaled(B=3, T=37, n_layers=3, vocab=1024), seed=4)
+
+
+def run_decode_case(S, wl, lengths, seed=0):
+    wl = wl.scaled(B=len(lengths))
+    inp = synth.generate(wl, seed=seed)
+    inp.lengths = torch.tensor(lengths, dtype=torch.int32)
+    dev = to_device(inp)
+    cfg = S.config_of(wl)
+    packed = S.prepare_weights(cfg, dev.layers, dev.embed, dev.final_norm)
+    ws = S.alloc_workspace(cfg, S.OP_DECODE, wl.B, 1)
+    L, Bn, KV, hd = wl.n_layers, wl.B, wl.n_kv_heads, wl.head_dim
+    k_new = torch.empty(L, Bn, KV, hd, dtype=torch.bfloat16, device="cuda")
+    v_new = torch.empty_like(k_new)
+    logits = torch.empty(Bn, wl.vocab, dtype=torch.bfloat16, device="cuda")
+    S.decode_step(cfg, packed, dev.ids, dev.lengths, dev.k_cache, dev.v_cache, k_new, v_new, logits, ws)
+    assert S.workspace_status(ws) == S.OK
+    ref, kr, vr = O.decode_step(oracle_config(wl), oracle_layers(inp), np32(inp.embed),
+                                np32(inp.final_norm), inp.ids.numpy().astype(np.int64),
+                                np.asarray(lengths), np32(inp.k_cache), np32(inp.v_cache))
+    got = np32(logits)
+    cos, mabs = cosine(got, ref), max_abs(got, ref)
+    ek, ev = rel_max_err_bf16_out(np32(k_new), kr), rel_max_err_bf16_out(np32(v_new), vr)
+    print(f"decode: cos {cos:.6f} max abs {mabs:.3e} k {ek:.3e} v {ev:.3e}")
+    assert cos >= LOGITS_COS_MIN and mabs <= LOGITS_MAX_ABS, (cos, mabs)
+    assert ek <= BLOCK_REL_TOL and ev <= BLOCK_REL_TOL, (ek, ev)
+    return cos, mabs
+
+
+def test_decode_small(S):
+    wl = W["smollm2_decode_b64_cache4096"].scaled(n_layers=2, s_max=700)
+    run_decode_case(S, wl, [0, 1, 511, 512, 513, 700, 37])
+
+
+def test_decode_one_chunk_many_layers(S):
+    wl = W["smollm2_decode_b64_cache4096"].scaled(n_layers=4, s_max=64, vocab=512)
+    run_decode_case(S, wl, [64, 3, 17], seed=2)
