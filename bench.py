@@ -1,0 +1,487 @@
+#!/usr/bin/env python3
+"""Throughput of the decoder forward on synthetic inputs; prints one JSON line.
+
+Headline workload: the SmolLM2-135M full-model prefill forward (30 blocks,
+tied head, vocab 49152) at batch 8 x 2048 tokens, one step = one forward
+through ``smol_model_forward``.  A second measurement, the KV-cache decode
+step (batch 64, cache lengths uniform in [1024, 4096]) through
+``smol_decode_step``, is reported in the same line under ``"decode"``.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (launched by torch.distributed.run) every rank runs an independent
+replica on its own batch (no collective on the data path; weak scaling); the
+timed region is bracketed by barriers and the slowest rank's time is used.
+``--impl reference`` times the fp64 CPU oracle on a bounded sample of the same
+workload instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from llama_decoder_forward_gb300 import synth  # noqa: E402
+
+METRIC = "prefill tokens/s SmolLM2-135M fwd (% bf16 TC peak); decode tok/s (% HBM BW)"
+PREFILL = synth.WORKLOADS["smollm2_model_b8_t2048"]
+DECODE = synth.WORKLOADS["smollm2_decode_b64_cache4096"]
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------- plumbing
+def rank_info():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def dist_init(world):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index=0):
+        self.proc = None
+        self.path = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            self.gpu = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            self.gpu = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if self.gpu:
+            cmd.insert(1, f"--id={self.gpu}")
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        for r in rows:
+            for name, v in zip(names[1:], r[5:9]):
+                if v.lower() in ("active", "1", "0x1"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def src_digest():
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "llama_decoder_forward_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch from a committed ncu capture, or None if absent or
+    taken on kernel sources that have changed since."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        data = json.load(f)
+    ent = data.get(workload, {}).get(kernel)
+    if not ent or ent.get("src_digest") != src_digest():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------- algorithmic work
+def prefill_flops_per_launch(wl):
+    M = wl.B * wl.T
+    d, H, KV, hd, I, V = wl.hidden, wl.n_heads, wl.n_kv_heads, wl.head_dim, wl.intermediate, wl.vocab
+    return {
+        "qkv_gemm_rope": 2 * M * (H + 2 * KV) * hd * d,
+        "flash_attention": 4 * hd * H * wl.B * wl.T * (wl.T + 1) // 2,   # causal-exact pairs
+        "o_gemm_residual": 2 * M * d * H * hd,
+        "gateup_gemm_swiglu": 2 * M * 2 * I * d,
+        "down_gemm_residual": 2 * M * d * I,
+        "lm_head_gemm": 2 * M * V * d,
+    }
+
+
+def prefill_flops_total(wl):
+    per = prefill_flops_per_launch(wl)
+    return wl.n_layers * (per["qkv_gemm_rope"] + per["flash_attention"] + per["o_gemm_residual"]
+                          + per["gateup_gemm_swiglu"] + per["down_gemm_residual"]) + per["lm_head_gemm"]
+
+
+def decode_bytes(wl, lengths):
+    """Algorithmic HBM bytes of one decode step: the cached K/V prefix of every
+    sequence and layer, the new K/V, all weights once, the logits."""
+    L, KV, hd, d, H, I, V = wl.n_layers, wl.n_kv_heads, wl.head_dim, wl.hidden, wl.n_heads, wl.intermediate, wl.vocab
+    kv = int(np.sum(lengths)) * L * KV * hd * 2 * 2
+    new_kv = 2 * L * wl.B * KV * hd * 2
+    weights = L * ((H + 2 * KV) * hd * d + d * H * hd + 3 * I * d + 2 * d) * 2 + V * d * 2 + d * 2
+    logits = wl.B * V * 2
+    per_attn_launch = int(np.sum(lengths + 1)) * KV * hd * 2 * 2
+    return kv + new_kv + weights + logits, per_attn_launch
+
+
+# ----------------------------------------------------------------- our arm
+def time_steps(fn, steps, world):
+    barrier(world)
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(st)
+    for _ in range(steps):
+        fn()
+    end.record(st)
+    torch.cuda.synchronize()
+    barrier(world)
+    return start.elapsed_time(end) / steps
+
+
+def kernel_breakdown(S, fn):
+    """One profiled step: total milliseconds and launch count per kernel kind."""
+    S.profile_begin(0xFFFF, 4096)
+    fn()
+    rec = S.profile_end()
+    tot, cnt = {}, {}
+    for k, ms in rec:
+        name = S.KERNEL_KINDS[k]
+        tot[name] = tot.get(name, 0.0) + ms
+        cnt[name] = cnt.get(name, 0) + 1
+    return tot, cnt
+
+
+def timed_with_kernel_events(S, fn, steps, world, kind_name):
+    """The timed region, with CUDA events around the launches of one kernel kind."""
+    kind = S.KERNEL_KINDS.index(kind_name)
+    S.profile_begin(1 << kind, 256 * steps)
+    ms = time_steps(fn, steps, world)
+    rec = S.profile_end()
+    durs = [t for k, t in rec if k == kind]
+    return ms, (sum(durs) / len(durs) if durs else None), len(durs)
+
+
+def run_prefill(S, args, rank, world, peaks, peaks_src):
+    wl = PREFILL
+    cfg = S.config_of(wl)
+    inp = synth.generate(wl, seed=rank, device="cuda")
+    packed = S.prepare_weights(cfg, inp.layers, inp.embed, inp.final_norm)
+    ws = S.alloc_workspace(cfg, S.OP_MODEL, wl.B, wl.T)
+    logits = torch.empty(wl.B, wl.T, wl.vocab, dtype=torch.bfloat16, device="cuda")
+    ids = inp.ids
+
+    def step():
+        S.model_forward(cfg, packed, ids, logits, ws)
+
+    for _ in range(args.warmup):
+        step()
+    if S.workspace_status(ws) != S.OK:
+        raise RuntimeError("a kernel reported a timeout during warm-up")
+    launches = S.last_launch_count()
+    tot, cnt = kernel_breakdown(S, step)
+    dominant = max(tot, key=tot.get)
+
+    sampler = ClockSampler()
+    sampler.start()
+    ms, dom_ms, dom_n = timed_with_kernel_events(S, step, args.steps, world, dominant)
+    clocks = sampler.stop()
+    ms = max_over_ranks(ms, world)
+    tokens = wl.B * wl.T
+    value = tokens * world / (ms / 1e3)
+
+    # end to end through the public API: ids from pinned host memory in, logits out
+    ids_host = ids.cpu().pin_memory()
+    logits_host = torch.empty(logits.shape, dtype=logits.dtype, pin_memory=True)
+
+    def e2e_step():
+        ids.copy_(ids_host, non_blocking=True)
+        S.model_forward(cfg, packed, ids, logits, ws)
+        logits_host.copy_(logits, non_blocking=True)
+
+    e2e_step()
+    e2e_steps = max(1, min(args.steps, 10))
+    e2e_ms = max_over_ranks(time_steps(e2e_step, e2e_steps, world), world)
+
+    flops = prefill_flops_per_launch(wl)
+    peak_tf = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    roof = None
+    if dom_ms:
+        if dominant in flops:
+            ach = flops[dominant] / (dom_ms / 1e3) / 1e12
+            roof = {"kernel": dominant, "bound": "tensor", "achieved": round(ach, 2), "peak": peak_tf,
+                    "unit": "TFLOP/s", "frac": round(ach / peak_tf, 4),
+                    "traffic": load_traffic(wl.name, dominant),
+                    "mean_launch_ms": round(dom_ms, 5), "launches_timed": dom_n,
+                    "peak_source": f"{peaks_src} bf16 dense, sustained (f16 runs at the bf16 rate)"}
+    step_tf = prefill_flops_total(wl) / (ms / 1e3) / 1e12
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded random weights and token ids of the SmolLM2-135M shape)",
+        "config": {"workload": f"{wl.name}: SmolLM2-135M full forward, {wl.n_layers} blocks, tied head "
+                               f"V={wl.vocab}, batch {wl.B} x {wl.T} tokens per rank",
+                   "batch_per_rank": wl.B, "seq_len": wl.T, "global_batch": wl.B * world,
+                   "parallelism": f"replicas x{world} (batch-sharded, no collective)",
+                   "precision": "bf16 weights/ids/logits; f16 tensor-core operands; fp32 accumulation "
+                                "and residual stream",
+                   "l2": "inputs larger than L2: each step writes 1.6 GB of logits and streams "
+                         ">300 MB of activations",
+                   "kernel_timing": "CUDA events around each launch of the dominant kernel inside the "
+                                    "timed region"},
+        "clocks": clocks,
+        "e2e": {"value": round(tokens * world / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": ids.numel() * 4, "d2h_bytes_per_step": logits.numel() * 2,
+                "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": launches * args.steps,
+        "roofline": roof,
+        "step_tensor_frac": round(step_tf / peak_tf, 4),
+        "step_tflops": round(step_tf, 2),
+        "kernel_ms_per_step": {k: round(v, 4) for k, v in sorted(tot.items(), key=lambda kv: -kv[1])},
+    }
+    return out, (inp, cfg)
+
+
+def run_decode(S, args, rank, world, peaks, peaks_src):
+    wl = DECODE
+    cfg = S.config_of(wl)
+    inp = synth.generate(wl, seed=100 + rank, device="cuda")
+    packed = S.prepare_weights(cfg, inp.layers, inp.embed, inp.final_norm)
+    ws = S.alloc_workspace(cfg, S.OP_DECODE, wl.B, 1)
+    L, B, KV, hd = wl.n_layers, wl.B, wl.n_kv_heads, wl.head_dim
+    k_new = torch.empty(L, B, KV, hd, dtype=torch.bfloat16, device="cuda")
+    v_new = torch.empty_like(k_new)
+    logits = torch.empty(B, wl.vocab, dtype=torch.bfloat16, device="cuda")
+
+    def step():
+        S.decode_step(cfg, packed, inp.ids, inp.lengths, inp.k_cache, inp.v_cache, k_new, v_new, logits, ws)
+
+    for _ in range(args.warmup):
+        step()
+    if S.workspace_status(ws) != S.OK:
+        raise RuntimeError("a kernel reported a timeout during warm-up")
+    launches = S.last_launch_count()
+    tot, cnt = kernel_breakdown(S, step)
+    ms, att_ms, att_n = timed_with_kernel_events(S, step, args.steps, world, "decode_attention")
+    ms = max_over_ranks(ms, world)
+    lengths = inp.lengths.cpu().numpy().astype(np.int64)
+    step_bytes, attn_bytes = decode_bytes(wl, lengths)
+    hbm = peaks["hbm_gbs"]
+    ach = attn_bytes / (att_ms / 1e3) / 1e9 if att_ms else None
+    return {
+        "workload": f"{wl.name}: SmolLM2-135M decode step, {L} blocks, batch {B}, cache lengths uniform "
+                    f"in [{wl.len_range[0]}, {wl.len_range[1]}], cache [{L},{B},{KV},{wl.s_max},{hd}] bf16",
+        "value": round(B * world / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
+        "step_hbm_gbs": round(step_bytes / (ms / 1e3) / 1e9, 1),
+        "step_hbm_frac": round(step_bytes / (ms / 1e3) / 1e9 / hbm, 4),
+        "algorithmic_bytes_per_step": step_bytes,
+        "gpu_launches": launches * args.steps,
+        "roofline": {"kernel": "decode_attention", "bound": "hbm", "achieved": round(ach, 1) if ach else None,
+                     "peak": hbm, "unit": "GB/s", "frac": round(ach / hbm, 4) if ach else None,
+                     "traffic": load_traffic(wl.name, "decode_attention"),
+                     "mean_launch_ms": round(att_ms, 5) if att_ms else None, "launches_timed": att_n,
+                     "peak_source": f"{peaks_src} copy bandwidth"},
+        "kernel_ms_per_step": {k: round(v, 4) for k, v in sorted(tot.items(), key=lambda kv: -kv[1])},
+    }
+
+
+# ----------------------------------------------------------------- the oracle (CPU) arm
+def oracle_sample_seconds(inp_cpu, cfg_o, n_tokens, layers_o, E, fn):
+    from oracle import oracle as O
+    ids = inp_cpu.ids[:1, :n_tokens].numpy().astype(np.int64)
+    t0 = time.perf_counter()
+    O.model_forward(cfg_o, layers_o, E, fn, ids)
+    return time.perf_counter() - t0
+
+
+def oracle_setup(inp):
+    from oracle import oracle as O
+    wl = inp.wl
+    f32 = lambda t: t.detach().float().cpu().numpy()
+    layers_o = [O.BlockWeights(**{k: f32(v) for k, v in lw.items()}) for lw in inp.layers]
+    cfg_o = O.Config(wl.hidden, wl.n_heads, wl.n_kv_heads, wl.head_dim, wl.intermediate, wl.n_layers,
+                     wl.vocab, wl.max_pos, wl.rms_eps, wl.rope_theta)
+    inp_cpu = synth.Inputs(wl)
+    inp_cpu.ids = inp.ids.cpu()
+    return cfg_o, layers_o, f32(inp.embed), f32(inp.final_norm), inp_cpu
+
+
+def cores_used():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def cpu_baseline(inp, target_s=15.0):
+    """The oracle as it stands, on a bounded sample: the first n tokens of one
+    sequence through all blocks and the head; n sized for ~target_s seconds."""
+    cfg_o, layers_o, E, fn, inp_cpu = oracle_setup(inp)
+    probe_n = 32
+    t_probe = oracle_sample_seconds(inp_cpu, cfg_o, probe_n, layers_o, E, fn)
+    n = int(min(PREFILL.T, max(probe_n, probe_n * target_s / max(t_probe, 1e-3))))
+    t = oracle_sample_seconds(inp_cpu, cfg_o, n, layers_o, E, fn)
+    return {"value": round(n / t, 2), "unit": "tokens/s", "cores": cores_used(), "kind": "oracle",
+            "sample": f"sequence 0, first {n} of {PREFILL.T} tokens, all {PREFILL.n_layers} blocks + "
+                      f"tied head, numpy fp64 ({t:.1f} s)"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    wl = PREFILL
+    inp = synth.generate(wl, seed=0, device="cpu")
+    cfg_o, layers_o, E, fn, inp_cpu = oracle_setup(inp)
+    probe_n = 16
+    t_probe = oracle_sample_seconds(inp_cpu, cfg_o, probe_n, layers_o, E, fn)
+    per_step = min(10.0, 150.0 / max(1, args.steps + args.warmup))
+    n = int(min(wl.T, max(8, probe_n * per_step / max(t_probe, 1e-3))))
+    for _ in range(args.warmup):
+        oracle_sample_seconds(inp_cpu, cfg_o, n, layers_o, E, fn)
+    t = sum(oracle_sample_seconds(inp_cpu, cfg_o, n, layers_o, E, fn) for _ in range(args.steps))
+    ms = t / args.steps * 1e3
+    value = round(n / (ms / 1e3), 3)
+    sample = (f"each step: sequence 0, first {n} of {wl.T} tokens, all {wl.n_layers} blocks + tied head, "
+              f"numpy fp64")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded random weights and token ids of the SmolLM2-135M shape)",
+        "config": {"workload": f"{wl.name}: SmolLM2-135M full forward (bounded sample on host cores)",
+                   "seq_len": wl.T, "parallelism": "none (host oracle)"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores_used(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+    return 0
+
+
+def profile_case(args):
+    """One step with few layers (same launch shapes as the full workload)."""
+    torch.cuda.set_device(0)
+    from llama_decoder_forward_gb300 import smol as S
+    if args.profile_case == "prefill":
+        wl = PREFILL.scaled(n_layers=args.profile_layers)
+        cfg = S.config_of(wl)
+        inp = synth.generate(wl, seed=0, device="cuda")
+        packed = S.prepare_weights(cfg, inp.layers, inp.embed, inp.final_norm)
+        ws = S.alloc_workspace(cfg, S.OP_MODEL, wl.B, wl.T)
+        logits = torch.empty(wl.B, wl.T, wl.vocab, dtype=torch.bfloat16, device="cuda")
+        S.model_forward(cfg, packed, inp.ids, logits, ws)
+    else:
+        wl = DECODE.scaled(n_layers=args.profile_layers)
+        cfg = S.config_of(wl)
+        inp = synth.generate(wl, seed=100, device="cuda")
+        packed = S.prepare_weights(cfg, inp.layers, inp.embed, inp.final_norm)
+        ws = S.alloc_workspace(cfg, S.OP_DECODE, wl.B, 1)
+        k_new = torch.empty(wl.n_layers, wl.B, wl.n_kv_heads, wl.head_dim, dtype=torch.bfloat16, device="cuda")
+        v_new = torch.empty_like(k_new)
+        logits = torch.empty(wl.B, wl.vocab, dtype=torch.bfloat16, device="cuda")
+        S.decode_step(cfg, packed, inp.ids, inp.lengths, inp.k_cache, inp.v_cache, k_new, v_new, logits, ws)
+    status = S.workspace_status(ws)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": args.profile_case, "layers": args.profile_layers, "status": status}))
+    return 0 if status == S.OK else 1
+
+
+# ----------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode-step measurement")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the oracle")
+    ap.add_argument("--profile-case", choices=["prefill", "decode"],
+                    help="run one untimed step of the workload with --profile-layers blocks and exit "
+                         "(the per-launch shapes equal the full workload's; a small case for ncu)")
+    ap.add_argument("--profile-layers", type=int, default=2)
+    args = ap.parse_args()
+    if args.profile_case:
+        return profile_case(args)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank, world, local = rank_info()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    torch.cuda.set_device(local)
+    dist_init(world)
+    from llama_decoder_forward_gb300 import smol as S   # fails loudly if libsmol.so is missing
+    peaks, peaks_src = load_peaks()
+    out, (inp, _) = run_prefill(S, args, rank, world, peaks, peaks_src)
+    if not args.no_decode:
+        out["decode"] = run_decode(S, args, rank, world, peaks, peaks_src)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(inp)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

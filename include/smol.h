@@ -200,6 +200,33 @@ int smol_workspace_status(void *ws, void *stream);
  * launched (0 after an argument error). */
 int smol_last_launch_count(void);
 
+/* ---------------------------------------------------------------------------
+ * Per-launch timing, for measurement only (off unless started; not for use
+ * inside CUDA graph capture).  Kernel kinds: */
+enum {
+  SMOL_K_EMBED = 0,      /* embedding gather + row statistics            */
+  SMOL_K_ROWSTATS = 1,   /* block input row statistics + f16 copy         */
+  SMOL_K_QKV = 2,        /* RMSNorm + QKV GEMM + RoPE                     */
+  SMOL_K_ATTN = 3,       /* causal GQA flash attention                    */
+  SMOL_K_OPROJ = 4,      /* O GEMM + residual                             */
+  SMOL_K_GATEUP = 5,     /* RMSNorm + gate/up GEMM + SwiGLU               */
+  SMOL_K_DOWN = 6,       /* down GEMM + residual                          */
+  SMOL_K_HEAD = 7,       /* final RMSNorm + tied lm_head GEMM             */
+  SMOL_K_DEC_ATTN = 8,   /* split-K decode attention                      */
+  SMOL_K_OTHER = 9,      /* packing and bookkeeping kernels               */
+  SMOL_K_COUNT = 10
+};
+/* From now on (this host thread), every launch whose kind bit is set in
+ * `kind_mask` is bracketed by CUDA events on its stream, up to `capacity`
+ * launches (events are created here, before the timed work).  Returns
+ * SMOL_OK or SMOL_ERR_CUDA. */
+int smol_profile_begin(unsigned kind_mask, int capacity);
+/* Stops recording, waits for the recorded events and writes, per recorded
+ * launch in order, its kind (kinds[i]) and duration in milliseconds (ms[i]),
+ * up to cap entries (host arrays).  Returns the number written, or a
+ * negative status. */
+int smol_profile_end(int *kinds, float *ms, int cap);
+
 /* Static text for a status code; for SMOL_ERR_CUDA, the last CUDA error text. */
 const char *smol_status_string(int status);
 

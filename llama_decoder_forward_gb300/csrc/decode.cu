@@ -21,6 +21,7 @@
 #include <math.h>
 
 #include "decode.cuh"
+#include "profile.cuh"
 #include "prims.cuh"
 
 namespace smol {
@@ -316,6 +317,11 @@ __global__ void zero_ints_kernel(int *p, int n) {
   if (i < n) p[i] = 0;
 }
 
+static cudaError_t launch_zero_ints(int *p, int n, cudaStream_t st) {
+  zero_ints_kernel<<<(unsigned)cdiv(n, 256), 256, 0, st>>>(p, n);
+  return cudaGetLastError();
+}
+
 cudaError_t run_decode(const DecodeArgs &a, void *ws, int sms, cudaStream_t st, int *launches) {
   const smol_config &c = a.cfg;
   const DecWs W = dec_ws(&c, a.B);
@@ -335,16 +341,18 @@ cudaError_t run_decode(const DecodeArgs &a, void *ws, int sms, cudaStream_t st, 
   int *counters = reinterpret_cast<int *>(wb + W.counters);
   int n = 0;
   cudaError_t e;
-#define DEC_LAUNCH(expr)             \
+#define DEC_LAUNCH_K(kind, expr)     \
   do {                               \
+    prof_before((kind), st);         \
     e = (expr);                      \
+    prof_after((kind), st);          \
     if (e != cudaSuccess) return e;  \
     ++n;                             \
   } while (0)
+#define DEC_LAUNCH(expr) DEC_LAUNCH_K(SMOL_K_OTHER, expr)
 
-  zero_ints_kernel<<<(unsigned)cdiv(B * KV, 256), 256, 0, st>>>(counters, B * KV);
-  DEC_LAUNCH(cudaGetLastError());
-  DEC_LAUNCH(launch_embed_rows(a.ids, a.embed, V, d, B, x, x32, ssq_a, st));
+  DEC_LAUNCH(launch_zero_ints(counters, B * KV, st));
+  DEC_LAUNCH_K(SMOL_K_EMBED, launch_embed_rows(a.ids, a.embed, V, d, B, x, x32, ssq_a, st));
 
   const float sl2 = 1.4426950408889634f / sqrtf((float)hd);
   for (int l = 0; l < L; ++l) {
@@ -359,7 +367,7 @@ cudaError_t run_decode(const DecodeArgs &a, void *ws, int sms, cudaStream_t st, 
     p.q = q; p.k_bf = kn; p.v_bf = vn; p.T = 1; p.H = H; p.KV = KV; p.hd = hd;
     p.rope = a.rope; p.valid_start = nullptr; p.pos_add = a.cache_len; p.pos_limit = min(a.S_max, c.max_pos - 1);
     p.max_pos = c.max_pos; p.status = status;
-    DEC_LAUNCH(launch_gemm(kEpiQkvRope, hd, x, lb + a.off_qkv, p, sms, st));
+    DEC_LAUNCH_K(SMOL_K_QKV, launch_gemm(kEpiQkvRope, hd, x, lb + a.off_qkv, p, sms, st));
 
     DecAttnParams ap{};
     ap.q = q;
@@ -374,29 +382,29 @@ cudaError_t run_decode(const DecodeArgs &a, void *ws, int sms, cudaStream_t st, 
     ap.max_splits = W.max_splits; ap.scale_log2 = sl2;
     const int lmax = min(a.S_max, c.max_pos - 1);
     dim3 grid((unsigned)cdiv(lmax + 1, kChunk), (unsigned)KV, (unsigned)B);
-    DEC_LAUNCH(launch_decode_attn(ap, hd, grid, st));
+    DEC_LAUNCH_K(SMOL_K_DEC_ATTN, launch_decode_attn(ap, hd, grid, st));
 
     GemmParams po{};
     po.M = B; po.N = d; po.K = H * hd; po.out = h; po.out_is_f16 = 1; po.out_f32 = h32; po.ldo = d; po.resid_f32 = x32;
     po.ssq_out = ssq_b;
     po.status = status;
-    DEC_LAUNCH(launch_gemm(kEpiResidual, 64, o, lb + a.off_o, po, sms, st));
+    DEC_LAUNCH_K(SMOL_K_OPROJ, launch_gemm(kEpiResidual, 64, o, lb + a.off_o, po, sms, st));
 
     GemmParams pg{};
     pg.M = B; pg.N = 2 * I; pg.K = d; pg.out = act; pg.out_is_f16 = 1; pg.ldo = I; pg.ssq_in = ssq_b;
     pg.inv_dim = 1.0f / d; pg.eps = c.rms_eps; pg.ssq_zero = ssq_a; pg.status = status;
-    DEC_LAUNCH(launch_gemm(kEpiSwiglu, 128, h, lb + a.off_gu, pg, sms, st));
+    DEC_LAUNCH_K(SMOL_K_GATEUP, launch_gemm(kEpiSwiglu, 128, h, lb + a.off_gu, pg, sms, st));
 
     GemmParams pd{};
     pd.M = B; pd.N = d; pd.K = I; pd.out = x; pd.out_is_f16 = 1; pd.out_f32 = x32; pd.ldo = d; pd.resid_f32 = h32;
     pd.ssq_out = ssq_a;
     pd.status = status;
-    DEC_LAUNCH(launch_gemm(kEpiResidual, 64, act, lb + a.off_down, pd, sms, st));
+    DEC_LAUNCH_K(SMOL_K_DOWN, launch_gemm(kEpiResidual, 64, act, lb + a.off_down, pd, sms, st));
   }
   GemmParams ph{};
   ph.M = B; ph.N = V; ph.K = d; ph.out = a.logits; ph.out_is_f16 = 0; ph.ldo = V; ph.ssq_in = ssq_a;
   ph.inv_dim = 1.0f / d; ph.eps = c.rms_eps; ph.status = status;
-  DEC_LAUNCH(launch_gemm(kEpiScale, gemm_pick_bn(kEpiScale, V, hd), x, a.head, ph, sms, st));
+  DEC_LAUNCH_K(SMOL_K_HEAD, launch_gemm(kEpiScale, gemm_pick_bn(kEpiScale, V, hd), x, a.head, ph, sms, st));
 #undef DEC_LAUNCH
   *launches = n;
   return cudaSuccess;

@@ -7,6 +7,7 @@
 
 #include "common.cuh"
 #include "decode.cuh"
+#include "profile.cuh"
 
 using namespace smol;
 
@@ -122,12 +123,15 @@ int device_sms(int *sms) {
   return SMOL_OK;
 }
 
-#define LAUNCH(expr)                                   \
+#define LAUNCH_K(kind, st, expr)                       \
   do {                                                 \
+    prof_before((kind), (st));                         \
     cudaError_t _e = (expr);                           \
+    prof_after((kind), (st));                          \
     if (_e != cudaSuccess) return cuda_fail(_e);       \
     ++g_launches;                                      \
   } while (0)
+#define LAUNCH(expr) LAUNCH_K(SMOL_K_OTHER, st, expr)
 
 struct LayerPtrs {
   const f16 *qkv, *o, *gu, *down;
@@ -181,35 +185,35 @@ int run_block(const smol_config *c, const void *packed, int layer, const BlockIO
   p.T = T; p.H = H; p.KV = KV; p.hd = hd;
   p.rope = reinterpret_cast<const float2 *>(static_cast<const uint8_t *>(packed) + PL.rope_off);
   p.valid_start = valid_start; p.max_pos = c->max_pos; p.status = status;
-  LAUNCH(launch_gemm(kEpiQkvRope, gemm_pick_bn(kEpiQkvRope, p.N, hd), io.x16, lp.qkv, p, sms, st));
+  LAUNCH_K(SMOL_K_QKV, st, launch_gemm(kEpiQkvRope, gemm_pick_bn(kEpiQkvRope, p.N, hd), io.x16, lp.qkv, p, sms, st));
 
   // 2. causal GQA attention
   AttnParams ap{};
   ap.q = q; ap.k = k; ap.v = v; ap.o = o; ap.valid_start = valid_start;
   ap.B = B; ap.T = T; ap.H = H; ap.KV = KV; ap.hd = hd;
   ap.scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
-  LAUNCH(launch_flash_attention(ap, st));
+  LAUNCH_K(SMOL_K_ATTN, st, launch_flash_attention(ap, st));
 
   // 3. O projection + residual: h = x + o Wo^T (fp32 and f16), ssq_b += rowsum(h^2)
   GemmParams po{};
   po.M = (int)M; po.N = d; po.K = H * hd;
   po.out = h; po.out_is_f16 = 1; po.out_f32 = h32; po.ldo = d; po.ssq_out = ssq_b; po.status = status;
   po.resid = io.resid_bf; po.resid_f32 = io.resid_f32;
-  LAUNCH(launch_gemm(kEpiResidual, gemm_pick_bn(kEpiResidual, d, hd), o, lp.o, po, sms, st));
+  LAUNCH_K(SMOL_K_OPROJ, st, launch_gemm(kEpiResidual, gemm_pick_bn(kEpiResidual, d, hd), o, lp.o, po, sms, st));
 
   // 4. RMSNorm2 + gate/up + SwiGLU: a = silu(g) * u ; clears ssq_a for step 5
   GemmParams pg{};
   pg.M = (int)M; pg.N = 2 * I; pg.K = d;
   pg.out = a; pg.out_is_f16 = 1; pg.ldo = I; pg.ssq_in = ssq_b; pg.inv_dim = 1.0f / d;
   pg.eps = c->rms_eps; pg.ssq_zero = ssq_a; pg.status = status;
-  LAUNCH(launch_gemm(kEpiSwiglu, gemm_pick_bn(kEpiSwiglu, 2 * I, hd), h, lp.gu, pg, sms, st));
+  LAUNCH_K(SMOL_K_GATEUP, st, launch_gemm(kEpiSwiglu, gemm_pick_bn(kEpiSwiglu, 2 * I, hd), h, lp.gu, pg, sms, st));
 
   // 5. down projection + residual: out = h + a Wd^T, ssq_a += rowsum(out^2)
   GemmParams pd{};
   pd.M = (int)M; pd.N = d; pd.K = I;
   pd.out = io.out16; pd.out_is_f16 = io.out16_is_f16; pd.out_f32 = io.out_f32; pd.ldo = d;
   pd.resid_f32 = h32; pd.ssq_out = ssq_a; pd.status = status;
-  LAUNCH(launch_gemm(kEpiResidual, gemm_pick_bn(kEpiResidual, d, hd), a, lp.down, pd, sms, st));
+  LAUNCH_K(SMOL_K_DOWN, st, launch_gemm(kEpiResidual, gemm_pick_bn(kEpiResidual, d, hd), a, lp.down, pd, sms, st));
   return SMOL_OK;
 }
 
@@ -315,11 +319,11 @@ SMOL_API int smol_block_forward(const smol_config *cfg, const void *packed, int 
   io.k_bf = static_cast<bf16 *>(k_out);
   io.v_bf = static_cast<bf16 *>(v_out);
   if (act_dtype == SMOL_ACT_F32) {
-    LAUNCH(launch_row_ssq_f32(static_cast<const float *>(x), M, cfg->hidden, x16, ssq_a, st));
+    LAUNCH_K(SMOL_K_ROWSTATS, st, launch_row_ssq_f32(static_cast<const float *>(x), M, cfg->hidden, x16, ssq_a, st));
     io.resid_f32 = static_cast<const float *>(x);
     io.out_f32 = static_cast<float *>(out);
   } else {
-    LAUNCH(launch_row_ssq(static_cast<const bf16 *>(x), M, cfg->hidden, x16, ssq_a, st));
+    LAUNCH_K(SMOL_K_ROWSTATS, st, launch_row_ssq(static_cast<const bf16 *>(x), M, cfg->hidden, x16, ssq_a, st));
     io.resid_bf = static_cast<const bf16 *>(x);
     io.out16 = out;
     io.out16_is_f16 = 0;
@@ -353,7 +357,7 @@ SMOL_API int smol_model_forward(const smol_config *cfg, const void *packed, cons
   f16 *x = reinterpret_cast<f16 *>(wsb + W.x);
   float *x32 = reinterpret_cast<float *>(wsb + W.x32);
   float *ssq_a = reinterpret_cast<float *>(wsb + W.ssq_a);
-  LAUNCH(launch_embed_rows(ids, reinterpret_cast<const bf16 *>(pk + L.embed_off), cfg->vocab,
+  LAUNCH_K(SMOL_K_EMBED, st, launch_embed_rows(ids, reinterpret_cast<const bf16 *>(pk + L.embed_off), cfg->vocab,
                            cfg->hidden, M, x, x32, ssq_a, st));
   BlockIO io{};
   io.x16 = x;
@@ -370,7 +374,7 @@ SMOL_API int smol_model_forward(const smol_config *cfg, const void *packed, cons
   p.out = logits; p.out_is_f16 = 0; p.ldo = cfg->vocab;
   p.ssq_in = ssq_a; p.inv_dim = 1.0f / cfg->hidden; p.eps = cfg->rms_eps;
   p.status = reinterpret_cast<int *>(wsb + W.status);
-  LAUNCH(launch_gemm(kEpiScale, gemm_pick_bn(kEpiScale, cfg->vocab, cfg->head_dim), x,
+  LAUNCH_K(SMOL_K_HEAD, st, launch_gemm(kEpiScale, gemm_pick_bn(kEpiScale, cfg->vocab, cfg->head_dim), x,
                      pk + L.head_off, p, sms, st));
   return SMOL_OK;
 }

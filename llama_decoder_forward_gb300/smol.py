@@ -59,7 +59,14 @@ _SIGS = {
     "smol_workspace_status": (c_int, [c_void_p, c_void_p]),
     "smol_last_launch_count": (c_int, []),
     "smol_status_string": (ctypes.c_char_p, [c_int]),
+    "smol_profile_begin": (c_int, [ctypes.c_uint, c_int]),
+    "smol_profile_end": (c_int, [POINTER(c_int), POINTER(c_float), c_int]),
 }
+
+# kernel kinds of smol_profile_begin (SMOL_K_*)
+KERNEL_KINDS = ("embed", "rowstats", "qkv_gemm_rope", "flash_attention", "o_gemm_residual",
+                "gateup_gemm_swiglu", "down_gemm_residual", "lm_head_gemm", "decode_attention", "other")
+K_EMBED, K_ROWSTATS, K_QKV, K_ATTN, K_OPROJ, K_GATEUP, K_DOWN, K_HEAD, K_DEC_ATTN, K_OTHER = range(10)
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
     _fn.restype = _res
@@ -200,6 +207,21 @@ def workspace_status(ws: torch.Tensor, stream=None) -> int:
 
 def last_launch_count() -> int:
     return _lib.smol_last_launch_count()
+
+
+def profile_begin(kind_mask: int, capacity: int) -> None:
+    """Start per-launch event timing of the kernel kinds in kind_mask."""
+    _check(_lib.smol_profile_begin(kind_mask, capacity), "smol_profile_begin")
+
+
+def profile_end(cap: int = 65536):
+    """Stop timing; returns [(kind, milliseconds), ...] in launch order."""
+    kinds = (c_int * cap)()
+    ms = (c_float * cap)()
+    n = _lib.smol_profile_end(kinds, ms, cap)
+    if n < 0:
+        raise SmolError(n, "smol_profile_end")
+    return [(kinds[i], ms[i]) for i in range(n)]
 
 
 raw = _lib   # the C entry points themselves, for callers that marshal by hand
