@@ -191,6 +191,32 @@ int smol_decode_step(const smol_config *cfg, const void *packed, const int32_t *
                      int S_max, void *k_new, void *v_new, void *logits,
                      void *ws, size_t ws_bytes, void *stream);
 
+/* ---------------------------------------------------------------------------
+ * smol_decode_step_noalloc: smol_decode_step without a caller workspace.
+ * The pages have no counterpart; this exists for callers that cannot give the
+ * library scratch memory at the moment they decode: a serving loop that
+ * forbids device allocation after start-up, a host whose allocator is not
+ * reachable from where the step is issued, or code that must not call
+ * cudaMalloc because it may synchronise the whole device.
+ *   Arguments and results are those of smol_decode_step, minus ws/ws_bytes.
+ *   Scratch: a fixed 8 MiB device array inside the library (every GPU that
+ *   loads the library holds one until the process exits).  Calls for which
+ *   smol_workspace_bytes(cfg, SMOL_OP_DECODE, B, 1) exceeds 8 MiB return
+ *   SMOL_ERR_WORKSPACE and launch nothing (SmolLM2-135M needs about 3.2 MiB
+ *   at B = 64).
+ *   The first call on a device looks up the array's device address (a host
+ *   call, cudaGetSymbolAddress); make that first call before any stream
+ *   capture on the device.  Nothing is allocated or freed, ever.
+ *   All calls share the one array: calls whose work overlaps on the GPU
+ *   (different streams, or different host threads) race on it and give
+ *   wrong results; serialise them.  Each call clears what must start at
+ *   zero, so back-to-back calls on one stream are safe.
+ * ------------------------------------------------------------------------- */
+int smol_decode_step_noalloc(const smol_config *cfg, const void *packed, const int32_t *ids,
+                             const int32_t *cache_len, int B, const void *k_cache,
+                             const void *v_cache, int S_max, void *k_new, void *v_new,
+                             void *logits, void *stream);
+
 /* Reads (synchronising `stream`) and clears the workspace status word written
  * by kernels whose bounded waits gave up.  Returns SMOL_OK, SMOL_ERR_TIMEOUT
  * or SMOL_ERR_CUDA.  Not meant for the hot path. */

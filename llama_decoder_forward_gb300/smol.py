@@ -59,6 +59,8 @@ _SIGS = {
     "smol_workspace_status": (c_int, [c_void_p, c_void_p]),
     "smol_last_launch_count": (c_int, []),
     "smol_status_string": (ctypes.c_char_p, [c_int]),
+    "smol_decode_step_noalloc": (c_int, [_CFG, c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p,
+                                         c_int, c_void_p, c_void_p, c_void_p, c_void_p]),
     "smol_profile_begin": (c_int, [ctypes.c_uint, c_int]),
     "smol_profile_end": (c_int, [POINTER(c_int), POINTER(c_float), c_int]),
 }
@@ -198,6 +200,23 @@ def decode_step(cfg: Config, packed: torch.Tensor, ids: torch.Tensor, cache_len:
     _check(_lib.smol_decode_step(ctypes.byref(cfg), _p(packed), _p(ids), _p(cache_len), B,
                                  _p(k_cache), _p(v_cache), S_max, _p(k_new), _p(v_new), _p(logits),
                                  _p(ws), ws.numel(), _stream(stream)), "smol_decode_step")
+
+
+def decode_step_noalloc(cfg: Config, packed: torch.Tensor, ids: torch.Tensor, cache_len: torch.Tensor,
+                        k_cache: torch.Tensor, v_cache: torch.Tensor, k_new: torch.Tensor,
+                        v_new: torch.Tensor, logits: torch.Tensor, stream=None) -> None:
+    """decode_step with the library's fixed device scratch instead of a workspace
+    (for callers that cannot provide device memory; calls must not overlap)."""
+    B = ids.shape[0]
+    S_max = k_cache.shape[3]
+    _dev(ids, torch.int32, "ids")
+    _dev(cache_len, torch.int32, "cache_len")
+    for name, t in (("k_cache", k_cache), ("v_cache", v_cache), ("k_new", k_new), ("v_new", v_new),
+                    ("logits", logits)):
+        _dev(t, torch.bfloat16, name)
+    _check(_lib.smol_decode_step_noalloc(ctypes.byref(cfg), _p(packed), _p(ids), _p(cache_len), B,
+                                         _p(k_cache), _p(v_cache), S_max, _p(k_new), _p(v_new),
+                                         _p(logits), _stream(stream)), "smol_decode_step_noalloc")
 
 
 def workspace_status(ws: torch.Tensor, stream=None) -> int:
