@@ -4,12 +4,19 @@
 // One CTA per SM walks tiles of 128 x BN.  Warp roles:
 //   warp 0      TMA producer: 128x64 A box and BNx64 B box per stage (128 B swizzle)
 //   warp 1      TMEM owner; lane 0 issues tcgen05.mma (M=128, N=BN, K=16) and commits
-//   warps 2..5  epilogue: tcgen05.ld 32 lanes x 16 columns per load, fused math,
-//               16-byte global stores
+//   warps 2..9  epilogue: two warps per TMEM lane quarter split the tile's columns
 // Two TMEM accumulators (2 x BN columns) let the epilogue of tile i overlap the
 // main loop of tile i+1.  Every wait is bounded; a wait that gives up records a
 // status code, raises a CTA-wide abort flag, drains in-flight copies and MMAs,
 // frees TMEM and returns.
+//
+// Epilogue data movement: tcgen05.ld gives each thread one row of the tile, so
+// a direct global access by a warp would touch 32 rows (32 cache lines) per
+// instruction.  Instead every epilogue warp owns 32-row staging tiles in shared
+// memory (128-byte rows, 16-byte chunks XOR-swizzled by row so both the
+// row-per-thread and the row-per-lane-group accesses are conflict-free);
+// global reads and writes go through them with consecutive lanes on
+// consecutive 16-byte chunks of a row (4-8 full rows per instruction).
 //
 // The epilogues implement, per output row r (one token):
 //   kEpiQkvRope  [q|k|v] = rstd_r * (x_r . W'^T); rotate-half RoPE on q and k heads
@@ -25,21 +32,39 @@
 
 namespace smol {
 
-template <int BN>
+constexpr int kEpiWarps = 8;                       // two per TMEM lane quarter
+constexpr int kSplit = kEpiWarps / 4;              // warps sharing one quarter's columns
+constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
+constexpr int kStgBytes = 32 * 128;                // one staging tile: 32 rows x 128 B
+
+// Staging tiles per epilogue warp (each a full 32 x 128-byte tile: the
+// swizzle spreads even a 64-byte-per-row payload over all 128 bytes of a
+// row): the residual epilogue double-buffers its input tile (prefetched with
+// cp.async) and adds a 16-bit output tile; the others stage one tile.
+template <int EPI>
+struct EpiStage {
+  static constexpr int kTiles = EPI == 1 /*kEpiResidual*/ ? 3 : 1;
+  static constexpr int kPerWarp = kTiles * kStgBytes;
+};
+
+template <int BN, int EPI>
 struct GemmCfg {
   static constexpr int BM = 128;
   static constexpr int BK = 64;                       // 64 x 16-bit = 128 B = one swizzle row
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES_RAW = (200 * 1024) / STAGE_BYTES;
+  static constexpr int EPI_BYTES = kEpiWarps * EpiStage<EPI>::kPerWarp;
+  static constexpr int STAGES_RAW = (232448 - 1024 - 256 - EPI_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
   static constexpr int TMEM_COLS = (2 * BN <= 128) ? 128 : (2 * BN <= 256 ? 256 : 512);
   static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + BAR_BYTES;
-  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M=128");
+  static constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
+  static_assert(BN % 64 == 0 && BN <= 256, "UMMA N for M=128 and whole 64-column epilogue units");
   static_assert(B_BYTES % 1024 == 0, "B stage must keep 1024-byte alignment");
+  static_assert(STAGES >= 3, "pipeline depth");
   static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
+  static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
 
 __device__ __forceinline__ void record_status(int *status, int code) {
@@ -51,231 +76,344 @@ __device__ __forceinline__ float row_rstd(const GemmParams &p, int row) {
   return rsqrtf(p.ssq_in[row] * p.inv_dim + p.eps);
 }
 
-__device__ __forceinline__ void store16(void *dst, const float (&v)[16], bool as_f16) {
-  uint4 w0, w1;
-  if (as_f16) {
-    w0 = make_uint4(pack_f16x2(v[0], v[1]), pack_f16x2(v[2], v[3]), pack_f16x2(v[4], v[5]),
-                    pack_f16x2(v[6], v[7]));
-    w1 = make_uint4(pack_f16x2(v[8], v[9]), pack_f16x2(v[10], v[11]), pack_f16x2(v[12], v[13]),
-                    pack_f16x2(v[14], v[15]));
-  } else {
-    w0 = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
-                    pack_bf16x2(v[6], v[7]));
-    w1 = make_uint4(pack_bf16x2(v[8], v[9]), pack_bf16x2(v[10], v[11]), pack_bf16x2(v[12], v[13]),
-                    pack_bf16x2(v[14], v[15]));
-  }
-  uint4 *d = reinterpret_cast<uint4 *>(dst);
-  d[0] = w0;
-  d[1] = w1;
+// ---------------------------------------------------------------- staging tile
+// Byte offset of 16-byte chunk c (0..7) of row r (0..31); always inside the
+// tile's 4 KB, whatever subset of chunks a caller uses.
+__device__ __forceinline__ int stg_off(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
+
+// Row-per-thread writes: 32 values as fp32 (chunks 0..7), or as 16-bit values
+// into chunks c0..c0+3.
+__device__ __forceinline__ void stg_put_f32(uint8_t *st, int r, const float (&v)[32]) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    *reinterpret_cast<float4 *>(st + stg_off(r, c)) =
+        make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
 }
 
-// element pointer into a 16-bit row-major buffer
-__device__ __forceinline__ void *elem16(void *base, long long idx) {
-  return static_cast<uint16_t *>(base) + idx;
+__device__ __forceinline__ void stg_put_16(uint8_t *st, int r, int c0, const float (&v)[32],
+                                           bool as_f16) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint4 w;
+    if (as_f16)
+      w = make_uint4(pack_f16x2(v[8 * c], v[8 * c + 1]), pack_f16x2(v[8 * c + 2], v[8 * c + 3]),
+                     pack_f16x2(v[8 * c + 4], v[8 * c + 5]), pack_f16x2(v[8 * c + 6], v[8 * c + 7]));
+    else
+      w = make_uint4(pack_bf16x2(v[8 * c], v[8 * c + 1]), pack_bf16x2(v[8 * c + 2], v[8 * c + 3]),
+                     pack_bf16x2(v[8 * c + 4], v[8 * c + 5]), pack_bf16x2(v[8 * c + 6], v[8 * c + 7]));
+    *reinterpret_cast<uint4 *>(st + stg_off(r, c0 + c)) = w;
+  }
+}
+
+// Row-per-thread reads of 32 values (fp32 chunks 0..7, or bf16 chunks 0..3).
+__device__ __forceinline__ void stg_get_f32(const uint8_t *st, int r, float (&v)[32]) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const float4 f = *reinterpret_cast<const float4 *>(st + stg_off(r, c));
+    v[4 * c] = f.x; v[4 * c + 1] = f.y; v[4 * c + 2] = f.z; v[4 * c + 3] = f.w;
+  }
+}
+
+__device__ __forceinline__ void stg_get_bf16(const uint8_t *st, int r, float (&v)[32]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint4 u = *reinterpret_cast<const uint4 *>(st + stg_off(r, c));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = unpack_bf16x2(w[e]);
+      v[8 * c + 2 * e] = f.x;
+      v[8 * c + 2 * e + 1] = f.y;
+    }
+  }
+}
+
+// Cooperative copies between the staging tile (chunks c0..c0+NC-1 of each row)
+// and NC*16 contiguous bytes per row in global memory; row rr's address is
+// g + row_off(rr) bytes.  Rows >= rows_valid are skipped.  NC is 4 or 8.
+template <int NC, typename RowOff>
+__device__ __forceinline__ void stg_to_global(const uint8_t *st, int c0, uint8_t *g, RowOff row_off,
+                                              int rows_valid, int lane) {
+  constexpr int RPI = 32 / NC;                    // rows per iteration
+#pragma unroll
+  for (int k = 0; k < 32 / RPI; ++k) {
+    const int rr = k * RPI + lane / NC, c = lane % NC;
+    const long long off = row_off(rr);            // evaluated by every lane (may shuffle)
+    if (rr < rows_valid)
+      *reinterpret_cast<uint4 *>(g + off + c * 16) =
+          *reinterpret_cast<const uint4 *>(st + stg_off(rr, c0 + c));
+  }
+}
+
+// Asynchronous (cp.async) copy of NC*16 bytes per row from global memory into
+// chunks 0..NC-1 of the staging tile; missing rows are zero-filled.  The
+// caller commits and waits.
+template <int NC>
+__device__ __forceinline__ void global_to_stg_async(uint8_t *st, const uint8_t *g, long long ld_bytes,
+                                                    int rows_valid, int lane) {
+  constexpr int RPI = 32 / NC;
+#pragma unroll
+  for (int k = 0; k < 32 / RPI; ++k) {
+    const int rr = k * RPI + lane / NC, c = lane % NC;
+    const bool ok = rr < rows_valid;
+    cp_async16(st + stg_off(rr, c), ok ? g + rr * ld_bytes + c * 16 : g, ok);
+  }
 }
 
 // ---------------------------------------------------------------- epilogues
-// All tcgen05.ld calls are executed by every lane of the warp (they are
-// warp-collective); only the global stores depend on the row bound.
+// Every tcgen05.ld is executed by all lanes (it is warp-collective); only
+// global accesses depend on the row bound.
+struct EpiCtx {
+  uint32_t taddr;     // TMEM address of (row0, column 0 of the tile)
+  int row0;           // the warp's first tile row
+  int rows_valid;     // how many of its 32 rows exist
+  int lane, n0, n_blk, split;
+  uint8_t *st;        // the warp's two staging tiles
+};
 
+// logits = rstd * D; units of 64 columns (one full 128-byte row segment).
 template <int BN>
-__device__ __forceinline__ void epi_scale(const GemmParams &p, uint32_t taddr, int row, int n0) {
-  const float rs = row_rstd(p, row);
-  const bool row_ok = row < p.M;
+__device__ __forceinline__ void epi_scale(const GemmParams &p, const EpiCtx &e) {
+  const float rs = row_rstd(p, e.row0 + e.lane);
+  const long long ld = p.ldo * 2;
+  uint8_t *gbase = static_cast<uint8_t *>(p.out) + ((long long)e.row0 * p.ldo) * 2;
 #pragma unroll 1
-  for (int c = 0; c < BN; c += 16) {
-    uint32_t r[16];
-    tmem_ld16(taddr + c, r);
+  for (int c = e.split * 64; c < BN; c += 64 * kSplit) {
+    if (e.n0 + c >= p.N) break;                   // uniform across the warp
+    uint32_t r0[32], r1[32];
+    tmem_ld32(e.taddr + c, r0);
+    tmem_ld32(e.taddr + c + 32, r1);
     tmem_ld_wait();
-    const int col = n0 + c;
-    if (row_ok && col < p.N) {
-      float v[16];
+    float v[32];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[e]) * rs;
-      store16(elem16(p.out, (long long)row * p.ldo + col), v, p.out_is_f16);
-    }
+    for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r0[k]) * rs;
+    __syncwarp();                                 // previous copy-out has read the tile
+    stg_put_16(e.st, e.lane, 0, v, p.out_is_f16);
+#pragma unroll
+    for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r1[k]) * rs;
+    stg_put_16(e.st, e.lane, 4, v, p.out_is_f16);
+    __syncwarp();
+    stg_to_global<8>(e.st, 0, gbase + (long long)(e.n0 + c) * 2,
+                     [&](int rr) { return rr * ld; }, e.rows_valid, e.lane);
   }
 }
 
-// out = resid + D.  The residual comes in fp32 or bf16; the result is written
-// in fp32 (out_f32) and/or 16 bits (out).  The row sum of squares feeding the
-// next RMSNorm is taken over the values the next step reads: fp32 when out_f32
-// is written, else the rounded 16-bit values.
+// out = resid + D (units of 32 columns).  The residual (fp32 or bf16) of unit
+// k+1 is fetched with cp.async into the other staging buffer while unit k is
+// processed (unit 0 before the accumulator is even ready); the result is
+// written in fp32 (out_f32) and/or 16 bits (out).  The row sum of squares
+// feeding the next RMSNorm is taken over the values the next step reads: fp32
+// when out_f32 is written, else the rounded 16-bit values.
 template <int BN>
-__device__ __forceinline__ void epi_residual(const GemmParams &p, uint32_t taddr, int row, int n0) {
-  const bool row_ok = row < p.M;
+__device__ __forceinline__ void residual_prefetch(const GemmParams &p, const EpiCtx &e, int c,
+                                                  uint8_t *buf) {
+  const long long off = (long long)e.row0 * p.ldo + e.n0 + c;
+  if (p.resid_f32)
+    global_to_stg_async<8>(buf, reinterpret_cast<const uint8_t *>(p.resid_f32 + off), p.ldo * 4,
+                           e.rows_valid, e.lane);
+  else
+    global_to_stg_async<4>(buf, reinterpret_cast<const uint8_t *>(p.resid + off), p.ldo * 2,
+                           e.rows_valid, e.lane);
+  cp_async_commit();
+}
+
+template <int BN>
+__device__ __forceinline__ void epi_residual(const GemmParams &p, const EpiCtx &e) {
+  const bool row_ok = e.lane < e.rows_valid;
   float part = 0.f;
+  uint8_t *buf[2] = {e.st, e.st + kStgBytes};
+  uint8_t *st16 = e.st + 2 * kStgBytes;
+  const long long row0_off = (long long)e.row0 * p.ldo;
+  // unit 0's residual was prefetched by the caller into buf[0]
+  int k = 0;
 #pragma unroll 1
-  for (int c = 0; c < BN; c += 16) {
-    uint32_t r[16];
-    tmem_ld16(taddr + c, r);
+  for (int c = e.split * 32; c < BN; c += 32 * kSplit, ++k) {
+    const int col = e.n0 + c;
+    if (col >= p.N) break;                        // uniform across the warp
+    uint8_t *cur = buf[k & 1];
+    const int cn = c + 32 * kSplit;
+    const bool has_next = cn < BN && e.n0 + cn < p.N;
+    __syncwarp();                                 // unit k-1's copy-out has read buf[(k+1)&1]
+    if (has_next) {
+      residual_prefetch<BN>(p, e, cn, buf[(k + 1) & 1]);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    uint32_t r[32];
+    tmem_ld32(e.taddr + c, r);
     tmem_ld_wait();
-    const int col = n0 + c;
-    if (row_ok && col < p.N) {
-      const long long off = (long long)row * p.ldo + col;
-      float v[16];
-      if (p.resid_f32) {
-        const float4 *src = reinterpret_cast<const float4 *>(p.resid_f32 + off);
+    __syncwarp();                                 // every lane's copies into `cur` landed
+    float v[32];
+    if (p.resid_f32) stg_get_f32(cur, e.lane, v);
+    else stg_get_bf16(cur, e.lane, v);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float4 h = src[q];
-          v[4 * q] = h.x; v[4 * q + 1] = h.y; v[4 * q + 2] = h.z; v[4 * q + 3] = h.w;
-        }
-      } else {
-        const uint4 *src = reinterpret_cast<const uint4 *>(p.resid + off);
-        const uint4 h0 = src[0], h1 = src[1];
-        const uint32_t hw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+    for (int q = 0; q < 32; ++q) v[q] += __uint_as_float(r[q]);
+    if (p.out_f32) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float2 h = unpack_bf16x2(hw[e]);
-          v[2 * e] = h.x;
-          v[2 * e + 1] = h.y;
-        }
+      for (int q = 0; q < 32; ++q) part = fmaf(v[q], v[q], part);
+      stg_put_f32(cur, e.lane, v);                // own row only: no hazard with other lanes
+    } else {
+#pragma unroll
+      for (int q = 0; q < 32; ++q) {
+        const float rv = p.out_is_f16 ? __half2float(__float2half_rn(v[q]))
+                                      : __bfloat162float(__float2bfloat16_rn(v[q]));
+        part = fmaf(rv, rv, part);
       }
-#pragma unroll
-      for (int e = 0; e < 16; ++e) v[e] += __uint_as_float(r[e]);
-      if (p.out_f32) {
-        float4 *dst = reinterpret_cast<float4 *>(p.out_f32 + off);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) part = fmaf(v[e], v[e], part);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float rv = p.out_is_f16 ? __half2float(__float2half_rn(v[e]))
-                                        : __bfloat162float(__float2bfloat16_rn(v[e]));
-          part = fmaf(rv, rv, part);
-        }
-      }
-      if (p.out) store16(elem16(p.out, off), v, p.out_is_f16);
     }
+    if (p.out) stg_put_16(st16, e.lane, 0, v, p.out_is_f16);
+    __syncwarp();
+    if (p.out_f32)
+      stg_to_global<8>(cur, 0, reinterpret_cast<uint8_t *>(p.out_f32 + row0_off + col),
+                       [&](int rr) { return rr * p.ldo * 4; }, e.rows_valid, e.lane);
+    if (p.out)
+      stg_to_global<4>(st16, 0, static_cast<uint8_t *>(p.out) + (row0_off + col) * 2,
+                       [&](int rr) { return rr * p.ldo * 2; }, e.rows_valid, e.lane);
   }
-  if (row_ok && p.ssq_out) atomicAdd(p.ssq_out + row, part);
+  cp_async_wait<0>();
+  if (row_ok && p.ssq_out) atomicAdd(p.ssq_out + e.row0 + e.lane, part);
 }
 
+// Gate and up columns come in groups of 64 + 64 per 128 accumulator columns;
+// a unit is one group: 64 outputs written as one 128-byte row segment.
 template <int BN>
-__device__ __forceinline__ void epi_swiglu(const GemmParams &p, uint32_t taddr, int row, int n0,
-                                           int n_blk) {
-  const float rs = row_rstd(p, row);
-  const bool row_ok = row < p.M;
+__device__ __forceinline__ void epi_swiglu(const GemmParams &p, const EpiCtx &e) {
+  const float rs = row_rstd(p, e.row0 + e.lane);
   const int I = p.N / 2;
+  uint8_t *gbase = static_cast<uint8_t *>(p.out) + (long long)e.row0 * p.ldo * 2;
 #pragma unroll 1
-  for (int grp = 0; grp < BN / 128; ++grp) {
-    const int out_col0 = (n0 / 128 + grp) * 64;
+  for (int grp = e.split; grp < BN / 128; grp += kSplit) {
+    const int out_col = (e.n0 / 128 + grp) * 64;
+    if (out_col >= I) break;                      // uniform across the warp
+    __syncwarp();
 #pragma unroll 1
-    for (int e0 = 0; e0 < 64; e0 += 16) {
-      uint32_t g[16], u[16];
-      tmem_ld16(taddr + grp * 128 + e0, g);
-      tmem_ld16(taddr + grp * 128 + 64 + e0, u);
+    for (int h = 0; h < 2; ++h) {
+      uint32_t g[32], up[32];
+      tmem_ld32(e.taddr + grp * 128 + h * 32, g);
+      tmem_ld32(e.taddr + grp * 128 + 64 + h * 32, up);
       tmem_ld_wait();
-      if (row_ok && out_col0 + e0 < I) {
-        float v[16];
+      float v[32];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float gv = __uint_as_float(g[e]) * rs;
-          const float uv = __uint_as_float(u[e]) * rs;
-          v[e] = gv / (1.0f + __expf(-gv)) * uv;
-        }
-        store16(elem16(p.out, (long long)row * p.ldo + out_col0 + e0), v, p.out_is_f16);
+      for (int k = 0; k < 32; ++k) {
+        const float gv = __uint_as_float(g[k]) * rs;
+        const float uv = __uint_as_float(up[k]) * rs;
+        v[k] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;   // SiLU(g) * u
       }
+      stg_put_16(e.st, e.lane, 4 * h, v, p.out_is_f16);
     }
+    __syncwarp();
+    stg_to_global<8>(e.st, 0, gbase + (long long)out_col * 2,
+                     [&](int rr) { return rr * p.ldo * 2; }, e.rows_valid, e.lane);
   }
-  if (n_blk == 0 && row_ok && p.ssq_zero) p.ssq_zero[row] = 0.f;
+  const bool row_ok = e.lane < e.rows_valid;
+  if (e.n_blk == 0 && e.split == 0 && row_ok && p.ssq_zero) p.ssq_zero[e.row0 + e.lane] = 0.f;
 }
 
+// Units of 64 accumulator columns of one head: for a q or k head the 32
+// rotation pairs (i, i + hd/2), i in [i0, i0 + 32); for a v head 64
+// consecutive columns.  Output rows of [B, heads, T, hd] are addressed per
+// row (a warp's 32 rows may cross a sequence boundary): each lane computes its
+// own row's destination and the copying lanes fetch it with a shuffle.
 template <int BN, int HD>
-__device__ __forceinline__ void epi_qkv_rope(const GemmParams &p, uint32_t taddr, int row, int n0,
-                                             int n_blk) {
+__device__ __forceinline__ void epi_qkv_rope(const GemmParams &p, const EpiCtx &e) {
+  const int row = e.row0 + e.lane;
+  const bool row_ok = e.lane < e.rows_valid;
   const float rs = row_rstd(p, row);
-  const bool row_ok = row < p.M;
-  const int rr = row_ok ? row : 0;
-  const int b = rr / p.T, t = rr - b * p.T;
+  const int rr_ = row_ok ? row : e.row0;
+  const int b = rr_ / p.T, t = rr_ - b * p.T;
   int pos = t - (p.valid_start ? p.valid_start[b] : 0);
   if (p.pos_add) {
     const int pa = p.pos_add[b];
     pos += pa < 0 ? 0 : (pa > p.pos_limit ? p.pos_limit : pa);
   }
   pos = pos < 0 ? 0 : (pos >= p.max_pos ? p.max_pos - 1 : pos);
-  const float2 *cs = p.rope + (long long)pos * (HD / 2);
+  const float4 *cs4 = reinterpret_cast<const float4 *>(p.rope + (long long)pos * (HD / 2));
+  // element offsets of (b, head 0, t, 0) in [B, H, T, hd] and [B, KV, T, hd]
+  const long long q_row = ((long long)b * p.H * p.T + t) * HD;
+  const long long kv_row = ((long long)b * p.KV * p.T + t) * HD;
+  const long long head_stride = (long long)p.T * HD;
   const int n_heads_total = p.H + 2 * p.KV;
+  constexpr int kUnitsPerHead = HD / 64;
 #pragma unroll 1
-  for (int hh = 0; hh < BN / HD; ++hh) {
-    const int gh = n0 / HD + hh;                 // global head index in [q | k | v]
-    if (gh >= n_heads_total) break;              // uniform across the warp
-    const uint32_t tcol = taddr + hh * HD;
+  for (int u = e.split; u < BN / 64; u += kSplit) {
+    const int hh = u / kUnitsPerHead, j = u - hh * kUnitsPerHead;
+    const int gh = e.n0 / HD + hh;                // global head index in [q | k | v]
+    if (gh >= n_heads_total) break;               // uniform across the warp
+    const uint32_t tcol = e.taddr + hh * HD;
     const bool is_q = gh < p.H, is_k = !is_q && gh < p.H + p.KV;
-    long long off;                               // element offset of (b, head, t, 0)
-    f16 *dst;
-    bf16 *dst_bf;
-    if (is_q) {
-      off = (((long long)b * p.H + gh) * p.T + t) * HD;
-      dst = p.q;
-      dst_bf = nullptr;
-    } else {
-      const int kvh = is_k ? gh - p.H : gh - p.H - p.KV;
-      off = (((long long)b * p.KV + kvh) * p.T + t) * HD;
-      dst = is_k ? p.k : p.v;
-      dst_bf = is_k ? p.k_bf : p.v_bf;
-    }
-    if (!is_q && !is_k) {
-#pragma unroll 1
-      for (int i0 = 0; i0 < HD; i0 += 16) {
-        uint32_t x[16];
-        tmem_ld16(tcol + i0, x);
-        tmem_ld_wait();
-        if (row_ok) {
-          float y[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) y[e] = __uint_as_float(x[e]) * rs;
-          if (dst) store16(dst + off + i0, y, true);
-          if (dst_bf) store16(dst_bf + off + i0, y, false);
-        }
-      }
-      continue;
-    }
-#pragma unroll 1
-    for (int i0 = 0; i0 < HD / 2; i0 += 16) {
-      uint32_t x1[16], x2[16];
-      tmem_ld16(tcol + i0, x1);
-      tmem_ld16(tcol + HD / 2 + i0, x2);
+    const int hsub = is_q ? gh : (is_k ? gh - p.H : gh - p.H - p.KV);
+    const long long my_row = (is_q ? q_row : kv_row) + hsub * head_stride;
+    f16 *dst = is_q ? p.q : (is_k ? p.k : p.v);
+    bf16 *dst_bf = is_q ? nullptr : (is_k ? p.k_bf : p.v_bf);
+    auto row_off = [&](int rr) { return __shfl_sync(0xffffffffu, my_row, rr) * 2; };
+    float y1[32], y2[32];
+    int seg1, seg2;                               // element offsets of the two 32-wide segments
+    if (is_q || is_k) {
+      const int i0 = j * 32;
+      uint32_t x1[32], x2[32];
+      tmem_ld32(tcol + i0, x1);
+      tmem_ld32(tcol + HD / 2 + i0, x2);
       tmem_ld_wait();
-      if (row_ok) {
-        float y1[16], y2[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float2 c = cs[i0 + e];
-          const float a = __uint_as_float(x1[e]) * rs;
-          const float bb = __uint_as_float(x2[e]) * rs;
-          y1[e] = a * c.x - bb * c.y;
-          y2[e] = a * c.y + bb * c.x;
-        }
-        if (dst) {
-          store16(dst + off + i0, y1, true);
-          store16(dst + off + HD / 2 + i0, y2, true);
-        }
-        if (dst_bf) {
-          store16(dst_bf + off + i0, y1, false);
-          store16(dst_bf + off + HD / 2 + i0, y2, false);
-        }
+      for (int k = 0; k < 32; k += 2) {
+        const float4 c = cs4[(i0 + k) >> 1];      // (cos, sin) of pairs i0+k and i0+k+1
+        const float a0 = __uint_as_float(x1[k]) * rs, b0 = __uint_as_float(x2[k]) * rs;
+        const float a1 = __uint_as_float(x1[k + 1]) * rs, b1 = __uint_as_float(x2[k + 1]) * rs;
+        y1[k] = a0 * c.x - b0 * c.y;
+        y2[k] = a0 * c.y + b0 * c.x;
+        y1[k + 1] = a1 * c.z - b1 * c.w;
+        y2[k + 1] = a1 * c.w + b1 * c.z;
+      }
+      seg1 = i0;
+      seg2 = HD / 2 + i0;
+    } else {
+      const int i0 = j * 64;
+      uint32_t x1[32], x2[32];
+      tmem_ld32(tcol + i0, x1);
+      tmem_ld32(tcol + i0 + 32, x2);
+      tmem_ld_wait();
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        y1[k] = __uint_as_float(x1[k]) * rs;
+        y2[k] = __uint_as_float(x2[k]) * rs;
+      }
+      seg1 = i0;
+      seg2 = i0 + 32;
+    }
+    const bool contiguous = seg2 == seg1 + 32;    // both segments form one 128-byte row piece
+#pragma unroll 1
+    for (int pass = 0; pass < 2; ++pass) {
+      void *base = pass == 0 ? static_cast<void *>(dst) : static_cast<void *>(dst_bf);
+      if (base == nullptr) continue;              // uniform across the warp
+      __syncwarp();
+      stg_put_16(e.st, e.lane, 0, y1, pass == 0);
+      stg_put_16(e.st, e.lane, 4, y2, pass == 0);
+      __syncwarp();
+      uint8_t *g = static_cast<uint8_t *>(base);
+      if (contiguous) {
+        stg_to_global<8>(e.st, 0, g + seg1 * 2, row_off, e.rows_valid, e.lane);
+      } else {
+        stg_to_global<4>(e.st, 0, g + seg1 * 2, row_off, e.rows_valid, e.lane);
+        stg_to_global<4>(e.st, 4, g + seg2 * 2, row_off, e.rows_valid, e.lane);
       }
     }
   }
-  if (n_blk == 0 && row_ok && p.ssq_zero) p.ssq_zero[row] = 0.f;
+  if (e.n_blk == 0 && e.split == 0 && row_ok && p.ssq_zero) p.ssq_zero[row] = 0.f;
 }
 
 // ---------------------------------------------------------------- kernel
 template <int BN, int EPI, int HD>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmParams p) {
-  using C = GemmCfg<BN>;
+  using C = GemmCfg<BN, EPI>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
   uint8_t *sA = smem;
   uint8_t *sB = smem + C::STAGES * C::A_BYTES;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sB + C::STAGES * C::B_BYTES);
+  uint8_t *sEpi = sB + C::STAGES * C::B_BYTES;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sEpi + C::EPI_BYTES);
   uint64_t *full = bars;
   uint64_t *empty = bars + C::STAGES;
   uint64_t *tfull = bars + 2 * C::STAGES;
@@ -297,7 +435,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 128);
+      mbar_init(&tempty[a], 32 * kEpiWarps);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -401,27 +539,39 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
   } else {
-    // -------------------------------------------------- epilogue (warps 2..5)
+    // -------------------------------------------------- epilogue (warps 2 .. 1+kEpiWarps)
     const int quarter = warp & 3;                 // TMEM lanes 32*quarter .. +31
+    EpiCtx e;
+    e.lane = lane;
+    e.split = (warp - 2) >> 2;                    // which share of the tile's columns
+    e.st = sEpi + (warp - 2) * EpiStage<EPI>::kPerWarp;
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const int m_blk = tile / num_n, n_blk = tile - m_blk * num_n;
+      e.row0 = m_blk * C::BM + quarter * 32;
+      e.rows_valid = min(32, max(0, p.M - e.row0));
+      e.n0 = n_blk * BN;
+      e.n_blk = n_blk;
+      if constexpr (EPI == kEpiResidual) {
+        // start fetching this warp's first residual unit while the MMAs run
+        __syncwarp();
+        if (e.n0 + e.split * 32 < p.N) residual_prefetch<BN>(p, e, e.split * 32, e.st);
+      }
       // every lane waits; the outcome is made warp-uniform because the TMEM
       // loads below are warp-collective
       const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag));
       if (!ok) {
         if (lane == 0) record_status(p.status, kDevTimeoutEpilogue);
         *abort_flag = 1;
+        cp_async_wait<0>();                       // no copy in flight when the CTA exits
         break;
       }
       tc_fence_after_sync();
-      const int row = m_blk * C::BM + quarter * 32 + lane;
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
-      const int n0 = n_blk * BN;
-      if constexpr (EPI == kEpiScale) epi_scale<BN>(p, taddr, row, n0);
-      else if constexpr (EPI == kEpiResidual) epi_residual<BN>(p, taddr, row, n0);
-      else if constexpr (EPI == kEpiSwiglu) epi_swiglu<BN>(p, taddr, row, n0, n_blk);
-      else epi_qkv_rope<BN, HD>(p, taddr, row, n0, n_blk);
+      e.taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
+      if constexpr (EPI == kEpiScale) epi_scale<BN>(p, e);
+      else if constexpr (EPI == kEpiResidual) epi_residual<BN>(p, e);
+      else if constexpr (EPI == kEpiSwiglu) epi_swiglu<BN>(p, e);
+      else epi_qkv_rope<BN, HD>(p, e);
       tc_fence_before_sync();
       mbar_arrive(&tempty[acc]);
       acc ^= 1;
@@ -457,7 +607,7 @@ static EncodeTiledFn get_encode_fn() {
 }
 
 bool make_tmap_f16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
-                    uint64_t row_pitch_elems, uint32_t box_rows) {
+                   uint64_t row_pitch_elems, uint32_t box_rows) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {cols, rows};
@@ -471,7 +621,7 @@ bool make_tmap_f16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t c
 }
 
 int gemm_pick_bn(int epi, int N, int hd) {
-  if (N <= 0 || N % 16) return 0;
+  if (N <= 0 || N % 64) return 0;
   if (epi == kEpiQkvRope) {
     if (N % hd) return 0;
     const int cands[3] = {256, 192, 128};
@@ -483,22 +633,28 @@ int gemm_pick_bn(int epi, int N, int hd) {
     if (N % 128) return 0;
     return N % 256 == 0 ? 256 : 128;
   }
+  if (epi == kEpiResidual) {                       // its staging leaves room for BN <= 192
+    const int cands[3] = {192, 128, 64};
+    for (int c : cands)
+      if (N % c == 0) return c;
+    return 64;
+  }
   const int cands[4] = {256, 192, 128, 64};
   for (int c : cands)
     if (N % c == 0) return c;
-  return 128;
+  return 64;
 }
 
 template <int BN, int EPI, int HD>
 static cudaError_t launch_impl(const CUtensorMap &ta, const CUtensorMap &tb, const GemmParams &p,
                                int num_sms, cudaStream_t stream) {
-  using C = GemmCfg<BN>;
+  using C = GemmCfg<BN, EPI>;
   auto kern = gemm_tc_kernel<BN, EPI, HD>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const long long tiles = cdiv(p.M, C::BM) * cdiv(p.N, BN);
   const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
-  kern<<<grid, 192, C::SMEM_BYTES, stream>>>(ta, tb, p);
+  kern<<<grid, kGemmThreads, C::SMEM_BYTES, stream>>>(ta, tb, p);
   return cudaGetLastError();
 }
 
@@ -515,7 +671,6 @@ cudaError_t launch_gemm(int epi, int bn, const void *A, const void *B, const Gem
       if (bn == 64) return launch_impl<64, kEpiScale, 64>(ta, tb, p, num_sms, stream);
       break;
     case kEpiResidual:
-      if (bn == 256) return launch_impl<256, kEpiResidual, 64>(ta, tb, p, num_sms, stream);
       if (bn == 192) return launch_impl<192, kEpiResidual, 64>(ta, tb, p, num_sms, stream);
       if (bn == 128) return launch_impl<128, kEpiResidual, 64>(ta, tb, p, num_sms, stream);
       if (bn == 64) return launch_impl<64, kEpiResidual, 64>(ta, tb, p, num_sms, stream);
