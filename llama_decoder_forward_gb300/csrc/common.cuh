@@ -43,6 +43,8 @@ struct GemmParams {
   float *ssq_zero;        // rows of this buffer are cleared by the n-block-0 tiles
   // kEpiQkvRope
   f16 *q, *k, *v;         // f16 [B, H, T, hd], [B, KV, T, hd], [B, KV, T, hd]; k, v optional
+  f16 *v_t;               // optional f16 V transposed: [B, KV, hd, T_pad] (keys contiguous)
+  int T_pad;              // row pitch of v_t in elements (T rounded up to a multiple of 8)
   bf16 *k_bf, *v_bf;      // optional bf16 copies of k and v (cache entries), same layout
   int T, H, KV, hd;
   const float2 *rope;     // [max_pos][hd/2] (cos, sin)
@@ -69,12 +71,19 @@ cudaError_t launch_gemm(int epi, int bn, const void *A, const void *B, const Gem
 struct AttnParams {
   const f16 *q;           // [B, H, T, hd]
   const f16 *k, *v;       // [B, KV, T, hd]
+  const f16 *v_t;         // [B, KV, hd, T_pad] (tcgen05 kernel) or nullptr
+  int T_pad;
+  int *status;            // device status word (bounded waits)
+  int num_sms;
   f16 *o;                 // [B, T, H * hd]
   const int *valid_start; // [B] or nullptr
   int B, T, H, KV, hd;
   float scale_log2;       // log2(e) / sqrt(hd)
 };
 cudaError_t launch_flash_attention(const AttnParams &p, cudaStream_t stream);
+// tcgen05 attention (head_dim 64, group of at most 4 query heads); needs v_t.
+bool attention_tc_supported(int hd, int H, int KV);
+cudaError_t launch_attention_tc(const AttnParams &p, cudaStream_t stream);
 
 // ------------------------------------------------------------------ small kernels
 cudaError_t launch_embed_rows(const int *ids, const bf16 *embed, int vocab, int d, long long rows,

@@ -380,6 +380,46 @@ __device__ __forceinline__ void epi_qkv_rope(const GemmParams &p, const EpiCtx &
       seg1 = i0;
       seg2 = i0 + 32;
     }
+    if (!is_q && !is_k && p.v_t) {
+      // V transposed ([B, KV, hd, T_pad]): stage the 32 x 64 block, then each
+      // lane writes 8 consecutive tokens of one dimension (16 bytes when the
+      // 8 rows are consecutive tokens of one sequence starting at a multiple
+      // of 8, element by element otherwise).
+      __syncwarp();
+      stg_put_16(e.st, e.lane, 0, y1, true);
+      stg_put_16(e.st, e.lane, 4, y2, true);
+      __syncwarp();
+      const long long my_vt = ((long long)b * p.KV + hsub) * HD * p.T_pad + t;
+      const int tg = e.lane & 3;
+      long long vrow[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) vrow[i] = __shfl_sync(0xffffffffu, my_vt, 8 * tg + i);
+      const bool fast = (8 * tg + 7 < e.rows_valid) && (vrow[7] == vrow[0] + 7) && ((vrow[0] & 7) == 0);
+#pragma unroll 1
+      for (int it = 0; it < 8; ++it) {
+        const int dd = it * 8 + (e.lane >> 2);    // dimension within this 64-wide unit
+        uint16_t val[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          val[i] = *reinterpret_cast<const uint16_t *>(e.st + stg_off(8 * tg + i, dd >> 3) + (dd & 7) * 2);
+        const long long dim_off = (long long)(seg1 + dd) * p.T_pad;
+        uint16_t *vt = reinterpret_cast<uint16_t *>(p.v_t);
+        if (fast) {
+          uint4 w;
+          w.x = val[0] | (uint32_t(val[1]) << 16);
+          w.y = val[2] | (uint32_t(val[3]) << 16);
+          w.z = val[4] | (uint32_t(val[5]) << 16);
+          w.w = val[6] | (uint32_t(val[7]) << 16);
+          *reinterpret_cast<uint4 *>(vt + vrow[0] + dim_off) = w;
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if (8 * tg + i < e.rows_valid) vt[vrow[i] + dim_off] = val[i];
+        }
+      }
+      dst = nullptr;                              // the row-layout f16 copy is not needed
+      if (dst_bf == nullptr) continue;
+    }
     const bool contiguous = seg2 == seg1 + 32;    // both segments form one 128-byte row piece
 #pragma unroll 1
     for (int pass = 0; pass < 2; ++pass) {

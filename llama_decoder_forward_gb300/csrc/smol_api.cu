@@ -56,9 +56,15 @@ struct WsLayout {
   size_t total;
 };
 
-WsLayout ws_layout(const smol_config *c, long long M) {
+// V is stored transposed, [B, KV, hd, T_pad], when the tcgen05 attention
+// kernel is used; T_pad = T rounded up to a multiple of 8.
+long long t_pad(int T) { return (T + 7) / 8 * 8; }
+
+WsLayout ws_layout(const smol_config *c, int B, int T) {
   WsLayout W{};
+  const long long M = (long long)B * T;
   const size_t d = c->hidden, hd = c->head_dim, H = c->n_heads, KV = c->n_kv_heads, I = c->intermediate;
+  const size_t v_elems = (size_t)B * KV * hd * t_pad(T);
   size_t o = 0;
   W.status = o; o += 1024;
   W.x = o; o = align_up(o + M * d * 2, 1024);
@@ -67,7 +73,7 @@ WsLayout ws_layout(const smol_config *c, long long M) {
   W.h32 = o; o = align_up(o + M * d * 4, 1024);
   W.q = o; o = align_up(o + M * H * hd * 2, 1024);
   W.k = o; o = align_up(o + M * KV * hd * 2, 1024);
-  W.v = o; o = align_up(o + M * KV * hd * 2, 1024);
+  W.v = o; o = align_up(o + v_elems * 2, 1024);
   W.o = o; o = align_up(o + M * H * hd * 2, 1024);
   W.a = o; o = align_up(o + M * I * 2, 1024);
   W.ssq_a = o; o = align_up(o + M * 4, 1024);
@@ -181,7 +187,14 @@ int run_block(const smol_config *c, const void *packed, int layer, const BlockIO
   GemmParams p{};
   p.M = (int)M; p.N = (H + 2 * KV) * hd; p.K = d;
   p.ssq_in = ssq_a; p.inv_dim = 1.0f / d; p.eps = c->rms_eps; p.ssq_zero = ssq_b;
-  p.q = q; p.k = k; p.v = v; p.k_bf = io.k_bf; p.v_bf = io.v_bf;
+  const bool tc_attn = attention_tc_supported(hd, H, KV);
+  p.q = q; p.k = k; p.k_bf = io.k_bf; p.v_bf = io.v_bf;
+  if (tc_attn) {
+    p.v_t = v;
+    p.T_pad = (int)t_pad(T);
+  } else {
+    p.v = v;
+  }
   p.T = T; p.H = H; p.KV = KV; p.hd = hd;
   p.rope = reinterpret_cast<const float2 *>(static_cast<const uint8_t *>(packed) + PL.rope_off);
   p.valid_start = valid_start; p.max_pos = c->max_pos; p.status = status;
@@ -192,7 +205,15 @@ int run_block(const smol_config *c, const void *packed, int layer, const BlockIO
   ap.q = q; ap.k = k; ap.v = v; ap.o = o; ap.valid_start = valid_start;
   ap.B = B; ap.T = T; ap.H = H; ap.KV = KV; ap.hd = hd;
   ap.scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
-  LAUNCH_K(SMOL_K_ATTN, st, launch_flash_attention(ap, st));
+  ap.status = status;
+  if (tc_attn) {
+    ap.v = nullptr;
+    ap.v_t = v;
+    ap.T_pad = (int)t_pad(T);
+    LAUNCH_K(SMOL_K_ATTN, st, launch_attention_tc(ap, st));
+  } else {
+    LAUNCH_K(SMOL_K_ATTN, st, launch_flash_attention(ap, st));
+  }
 
   // 3. O projection + residual: h = x + o Wo^T (fp32 and f16), ssq_b += rowsum(h^2)
   GemmParams po{};
@@ -287,7 +308,7 @@ SMOL_API size_t smol_workspace_bytes(const smol_config *cfg, int op, int B, int 
   if (op == SMOL_OP_DECODE) return decode_ws_bytes(cfg, B);
   if (T <= 0) return 0;
   if (op != SMOL_OP_BLOCK && op != SMOL_OP_MODEL) return 0;
-  return ws_layout(cfg, (long long)B * T).total;
+  return ws_layout(cfg, B, T).total;
 }
 
 SMOL_API int smol_block_forward(const smol_config *cfg, const void *packed, int layer, const void *x,
@@ -305,7 +326,7 @@ SMOL_API int smol_block_forward(const smol_config *cfg, const void *packed, int 
       (k_out && !aligned16(k_out)) || (v_out && !aligned16(v_out)) ||
       (valid_start && (reinterpret_cast<uintptr_t>(valid_start) & 3u)))
     return SMOL_ERR_MISALIGNED;
-  const WsLayout W = ws_layout(cfg, (long long)B * T);
+  const WsLayout W = ws_layout(cfg, B, T);
   if (ws_bytes < W.total) return SMOL_ERR_WORKSPACE;
   int sms;
   if ((rc = device_sms(&sms))) return rc;
@@ -345,7 +366,7 @@ SMOL_API int smol_model_forward(const smol_config *cfg, const void *packed, cons
       (reinterpret_cast<uintptr_t>(ids) & 3u) ||
       (valid_start && (reinterpret_cast<uintptr_t>(valid_start) & 3u)))
     return SMOL_ERR_MISALIGNED;
-  const WsLayout W = ws_layout(cfg, (long long)B * T);
+  const WsLayout W = ws_layout(cfg, B, T);
   if (ws_bytes < W.total) return SMOL_ERR_WORKSPACE;
   int sms;
   if ((rc = device_sms(&sms))) return rc;
