@@ -238,7 +238,7 @@ static cudaError_t launch_fa(const AttnParams &p, cudaStream_t stream) {
   if (threads > 512) return cudaErrorInvalidConfiguration;
   const size_t smem = (size_t)(G * BQ + 4 * BK) * HD * sizeof(f16);
   auto kern = flash_attn_kernel<HD, BQ, BK>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = ensure_smem_attr<flash_attn_kernel<HD, BQ, BK>>((int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)cdiv(p.T, BQ), (unsigned)p.KV, (unsigned)p.B);
   kern<<<grid, threads, smem, stream>>>(p);

@@ -411,7 +411,7 @@ cudaError_t launch_gh(const AttnParams &a, const CUtensorMap &tq, const CUtensor
                       const CUtensorMap &tv, cudaStream_t st) {
   using C = AtCfg<GH>;
   auto kern = attn_tc_kernel<GH>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t e = ensure_smem_attr<attn_tc_kernel<GH>>(C::SMEM);
   if (e != cudaSuccess) return e;
   AtParams p{};
   p.o = a.o;
@@ -437,10 +437,10 @@ bool attention_tc_supported(int hd, int H, int KV) {
 cudaError_t launch_attention_tc(const AttnParams &a, cudaStream_t st) {
   if (!attention_tc_supported(a.hd, a.H, a.KV) || a.v_t == nullptr) return cudaErrorInvalidConfiguration;
   CUtensorMap tq, tk, tv;
-  if (!make_tmap_f16(&tq, a.q, (uint64_t)a.B * a.H * a.T, kHD, kHD, kBQ)) return cudaErrorInvalidValue;
-  if (!make_tmap_f16(&tk, a.k, (uint64_t)a.B * a.KV * a.T, kHD, kHD, kBK)) return cudaErrorInvalidValue;
+  if (!get_tmap_f16(&tq, a.q, (uint64_t)a.B * a.H * a.T, kHD, kHD, kBQ)) return cudaErrorInvalidValue;
+  if (!get_tmap_f16(&tk, a.k, (uint64_t)a.B * a.KV * a.T, kHD, kHD, kBK)) return cudaErrorInvalidValue;
   // V^T: rows are (b, kv head, dim), columns are keys; columns >= T read as zero
-  if (!make_tmap_f16(&tv, a.v_t, (uint64_t)a.B * a.KV * kHD, a.T, a.T_pad, kHD)) return cudaErrorInvalidValue;
+  if (!get_tmap_f16(&tv, a.v_t, (uint64_t)a.B * a.KV * kHD, a.T, a.T_pad, kHD)) return cudaErrorInvalidValue;
   const int G = a.H / a.KV;
   switch (G) {
     case 1: return launch_gh<1>(a, tq, tk, tv, st);

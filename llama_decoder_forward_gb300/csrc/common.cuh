@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "smol.h"
 
 namespace smol {
@@ -55,10 +57,29 @@ struct GemmParams {
   int *status;            // device status word
 };
 
+// Raises the dynamic shared-memory limit of kernel `Kern` to `bytes`, once per
+// device (the host call is not repeated on every launch).
+template <auto Kern>
+cudaError_t ensure_smem_attr(int bytes) {
+  static std::atomic<int> done[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+    return cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (done[dev].load(std::memory_order_relaxed) >= bytes) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done[dev].store(bytes, std::memory_order_relaxed);
+  return e;
+}
+
 // Encodes a 2-D f16 tensor map (rows x cols, row pitch in elements) with a
 // box of box_rows x 64 columns and 128-byte swizzle.  Returns false on error.
 bool make_tmap_f16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
                     uint64_t row_pitch_elems, uint32_t box_rows);
+// The same through a small per-process cache keyed by (device, arguments):
+// encoding is a host call of a few microseconds, and the same buffers recur on
+// every forward.
+bool get_tmap_f16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                  uint64_t row_pitch_elems, uint32_t box_rows);
 
 // Chooses the N tile for an epilogue and problem; 0 if unsupported.
 int gemm_pick_bn(int epi, int N, int hd);

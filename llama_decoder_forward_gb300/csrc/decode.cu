@@ -12,10 +12,12 @@
 // Decode attention is bound by HBM bandwidth (it streams the cache).  One CTA
 // owns (sequence b, kv head, a chunk of kChunk keys) and all g query heads of
 // that kv head, so each cached key/value is read once for the whole group.
-// Keys are spread over lane groups of hd/8 lanes (16-byte loads, 8 dims per
-// lane); each lane group takes 4 keys per step (8 loads in flight per lane),
-// reduces the q.k partial dots with shuffles and updates an online softmax in
-// the exp2 domain.  Partial (max, sum, output) triples are merged inside the
+// One thread fetches the chunk's K and V rows with two bulk copies (the TMA
+// engine) into shared memory, so the whole chunk is in flight at once while
+// other CTAs on the SM compute.  Keys are then spread over lane groups of hd/8
+// lanes (16-byte reads, 8 dims per lane); each lane group takes 4 keys per
+// step, reduces the q.k partial dots with shuffles and updates an online
+// softmax in the exp2 domain.  Partial (max, sum, output) triples are merged inside the
 // warp, then across warps in shared memory, then across chunks by the last
 // CTA of the (b, kv head) pair (an atomic arrival counter, no waiting).
 #include <math.h>
@@ -26,8 +28,8 @@
 
 namespace smol {
 
-constexpr int kChunk = 512;        // keys per CTA
-constexpr int kDecWarps = 8;       // warps per CTA
+constexpr int kChunk = 256;        // keys per CTA
+constexpr int kDecWarps = 4;       // warps per CTA
 
 struct DecWs {
   size_t status, x, x32, h, h32, q, o, a, ssq_a, ssq_b, part_m, part_l, part_o, counters, total;
@@ -72,19 +74,277 @@ struct DecAttnParams {
   int *counters;            // [B, KV], zero between layers
   int B, H, KV, S_max, max_pos, max_splits;
   float scale_log2;
+  int *status;              // workspace status word (bounded wait)
+  int layer;                // layer index (row offset into the whole-cache tensor maps)
 };
 
-__device__ __forceinline__ uint4 ld_stream(const bf16 *p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
+// Writes this CTA's (max, sum, output) triple for each head of the group and,
+// if it is the last CTA of its (sequence, kv head) to finish, merges all the
+// chunks' triples into the attention output.  red_m/red_l/red_o hold the
+// per-warp triples ([NW][GM], [NW][GM], [NW][GM][HD]) in shared memory.
+template <int HD, int GM, int NW>
+__device__ __forceinline__ void chunk_partial_and_combine(const DecAttnParams &p, int b, int kvh,
+                                                          int split, int nsplit, const float *red_m,
+                                                          const float *red_l, const float *red_o,
+                                                          int *s_last) {
+  const int G = p.H / p.KV;
+  const long long row = (long long)b * p.KV + kvh;
+  const long long pbase = (long long)b * p.H + kvh * G;   // first head of the group
+  for (int t = threadIdx.x; t < G * HD; t += blockDim.x) {
+    const int g = t / HD, dim = t - g * HD;
+    float M = -INFINITY;
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, red_m[w * GM + g]);
+    const float Mu = (M == -INFINITY) ? 0.f : M;
+    float Ls = 0.f, Os = 0.f;
+    for (int w = 0; w < NW; ++w) {
+      const float f = exp2f(red_m[w * GM + g] - Mu);
+      Ls += red_l[w * GM + g] * f;
+      Os += red_o[(w * GM + g) * HD + dim] * f;
+    }
+    const long long ps = (pbase + g) * p.max_splits + split;
+    if (dim == 0) {
+      p.part_m[ps] = M;
+      p.part_l[ps] = Ls;
+    }
+    p.part_o[ps * HD + dim] = Os;
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int prev = atomicAdd(p.counters + row, 1);
+    *s_last = (prev == nsplit - 1);
+  }
+  __syncthreads();
+  if (!*s_last) return;
+  __threadfence();
+  for (int t = threadIdx.x; t < G * HD; t += blockDim.x) {
+    const int g = t / HD, dim = t - g * HD;
+    const long long ps0 = (pbase + g) * p.max_splits;
+    float M = -INFINITY;
+    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, __ldcg(p.part_m + ps0 + s));
+    const float Mu = (M == -INFINITY) ? 0.f : M;
+    float Ls = 0.f, Os = 0.f;
+    for (int s = 0; s < nsplit; ++s) {
+      const float f = exp2f(__ldcg(p.part_m + ps0 + s) - Mu);
+      Ls += __ldcg(p.part_l + ps0 + s) * f;
+      Os += __ldcg(p.part_o + (ps0 + s) * HD + dim) * f;
+    }
+    p.o[(pbase + g) * HD + dim] = __float2half_rn(Ls > 0.f ? Os / Ls : 0.f);
+  }
+  if (threadIdx.x == 0) p.counters[row] = 0;        // ready for the next layer
 }
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void *ptr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(ptr)));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void *ptr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(ptr)));
+}
+// Splits x into bf16 hi + lo with hi + lo == x to about 16 significant bits.
+__device__ __forceinline__ void split_bf16(float x, float &hi, float &lo) {
+  hi = __bfloat162float(__float2bfloat16_rn(x));
+  lo = x - hi;
+}
+
+// Decode attention on tensor cores (hd = 64).  One CTA = (sequence, kv head,
+// 256-key chunk); 2-D TMA (128-byte swizzle) brings the chunk's K and V rows
+// into shared memory; each of the 4 warps takes 64 keys with mma.sync
+// m16n8k16 (bf16, the cache's type).  The g query heads of the group occupy
+// A rows 0..g-1 as the bf16 "hi" part of q and rows 8..8+g-1 as the "lo"
+// remainder, so one MMA yields both halves and their sum (in the same
+// thread) carries q to ~16 bits; the probabilities P are split the same way
+// for P V.  Keys past the chunk's valid range are masked (V rows zeroed so
+// unused cache slots cannot inject NaN).
+template <int GM>
+__global__ void __launch_bounds__(128) decode_attn_mma_kernel(const __grid_constant__ CUtensorMap tmK,
+                                                              const __grid_constant__ CUtensorMap tmV,
+                                                              const DecAttnParams p) {
+  constexpr int HD = 64, NW = 4;
+  extern __shared__ uint8_t dsm_raw[];
+  uint8_t *dsm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t *sK = dsm;                     // [256 keys][128 B], 16-byte chunks swizzled by key & 7
+  uint8_t *sV = dsm + kChunk * 128;
+  uint64_t *kv_bar = reinterpret_cast<uint64_t *>(dsm + 2 * kChunk * 128);
+  int *s_last = reinterpret_cast<int *>(kv_bar + 1);
+  float *red_m = reinterpret_cast<float *>(kv_bar + 2);     // [NW][GM]
+  float *red_l = red_m + NW * GM;                            // [NW][GM]
+  float *red_o = red_l + NW * GM;                            // [NW][GM][HD]
+
+  const int G = p.H / p.KV;
+  const int b = blockIdx.z, kvh = blockIdx.y, split = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int Lb = p.cache_len[b];
+  const int lmax = min(p.S_max, p.max_pos - 1);
+  Lb = Lb < 0 ? 0 : (Lb > lmax ? lmax : Lb);
+  const int n_keys = Lb + 1;
+  const int nsplit = (n_keys + kChunk - 1) / kChunk;
+  if (split >= nsplit) return;
+  const int k_begin = split * kChunk;
+  const int n_valid = min(kChunk, n_keys - k_begin);
+  const long long row = (long long)b * p.KV + kvh;
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int y = static_cast<int>(((long long)p.layer * p.B + b) * p.KV + kvh) * p.S_max + k_begin;
+    mbar_arrive_expect_tx(kv_bar, 2 * kChunk * 128);
+    tma_load_2d(sK, &tmK, kv_bar, 0, y);
+    tma_load_2d(sV, &tmV, kv_bar, 0, y);
+  }
+  // q as A fragments (rows r < G: hi; rows r + 8: lo), built while the copy flies
+  const int r = lane >> 2, c2 = (lane & 3) * 2;
+  uint32_t qa[4][4];
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    if (r < G) {
+      const f16 *qr = p.q + ((long long)b * p.H + kvh * G + r) * HD + kk * 16 + c2;
+      const float2 lo2 = unpack_f16x2(*reinterpret_cast<const uint32_t *>(qr));
+      const float2 hi2 = unpack_f16x2(*reinterpret_cast<const uint32_t *>(qr + 8));
+      float h0, l0, h1, l1, h2, l2, h3, l3;
+      split_bf16(lo2.x, h0, l0);
+      split_bf16(lo2.y, h1, l1);
+      split_bf16(hi2.x, h2, l2);
+      split_bf16(hi2.y, h3, l3);
+      qa[kk][0] = pack_bf16x2(h0, h1);
+      qa[kk][1] = pack_bf16x2(l0, l1);
+      qa[kk][2] = pack_bf16x2(h2, h3);
+      qa[kk][3] = pack_bf16x2(l2, l3);
+    } else {
+      qa[kk][0] = qa[kk][1] = qa[kk][2] = qa[kk][3] = 0u;
+    }
+  }
+  {
+    int no_abort = 0;
+    const bool landed = mbar_wait_bounded(kv_bar, 0, &no_abort);
+    if (!__syncthreads_and(landed)) {
+      if (threadIdx.x == 0) atomicCAS(p.status, 0, kDevTimeoutProducer);
+      mbar_wait_bounded(kv_bar, 0, &no_abort);   // (bounded) drain before exiting
+      return;
+    }
+  }
+  // the new token's key/value into its slot; zero V rows past the valid keys
+  if (Lb >= k_begin && Lb < k_begin + kChunk) {
+    const int slot = Lb - k_begin;
+    if (threadIdx.x < 8) {
+      const int c = threadIdx.x;
+      *reinterpret_cast<uint4 *>(sK + slot * 128 + ((c ^ (slot & 7)) << 4)) =
+          reinterpret_cast<const uint4 *>(p.k_new + row * HD)[c];
+      *reinterpret_cast<uint4 *>(sV + slot * 128 + ((c ^ (slot & 7)) << 4)) =
+          reinterpret_cast<const uint4 *>(p.v_new + row * HD)[c];
+    }
+  }
+  for (int i = n_valid * 8 + threadIdx.x; i < kChunk * 8; i += blockDim.x)
+    reinterpret_cast<uint4 *>(sV)[i] = make_uint4(0u, 0u, 0u, 0u);
+  __syncthreads();
+
+  const int kw0 = warp * 64;                       // this warp's first key (chunk-relative)
+  float mw = -INFINITY, lw = 0.f;
+  float o[8][4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  if (kw0 < n_valid) {                             // warp-uniform
+    float s[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int key = kw0 + j * 16 + (lane & 7) + ((lane >> 4) << 3);
+        const int chunk = kk * 2 + ((lane >> 3) & 1);
+        uint32_t bk[4];
+        ldsm_x4(bk, sK + key * 128 + ((chunk ^ (key & 7)) << 4));
+        mma_bf16_16816(s[2 * j], qa[kk], bk[0], bk[1]);
+        mma_bf16_16816(s[2 * j + 1], qa[kk], bk[2], bk[3]);
+      }
+    }
+    // head r's score = hi row + lo row; mask keys past the valid range
+    float sc[8][2];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int key = kw0 + 8 * j + c2 + e;
+        const float v = key < n_valid ? (s[j][e] + s[j][2 + e]) * p.scale_log2 : -INFINITY;
+        sc[j][e] = v;
+        mx = fmaxf(mx, v);
+      }
+    }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float mu = (mx == -INFINITY) ? 0.f : mx;
+    float sum = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      sc[j][0] = exp2f(sc[j][0] - mu);
+      sc[j][1] = exp2f(sc[j][1] - mu);
+      sum += sc[j][0] + sc[j][1];
+    }
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    mw = mx;
+    lw = sum;
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      float h0, l0, h1, l1, h2, l2, h3, l3;
+      split_bf16(sc[2 * kk][0], h0, l0);
+      split_bf16(sc[2 * kk][1], h1, l1);
+      split_bf16(sc[2 * kk + 1][0], h2, l2);
+      split_bf16(sc[2 * kk + 1][1], h3, l3);
+      const uint32_t a[4] = {pack_bf16x2(h0, h1), pack_bf16x2(l0, l1), pack_bf16x2(h2, h3),
+                             pack_bf16x2(l2, l3)};
+#pragma unroll
+      for (int nd = 0; nd < 4; ++nd) {
+        const int key = kw0 + kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+        const int chunk = nd * 2 + (lane >> 4);
+        uint32_t bv[4];
+        ldsm_x4_t(bv, sV + key * 128 + ((chunk ^ (key & 7)) << 4));
+        mma_bf16_16816(o[2 * nd], a, bv[0], bv[1]);
+        mma_bf16_16816(o[2 * nd + 1], a, bv[2], bv[3]);
+      }
+    }
+  }
+  // this warp's triple for head r (lanes 4r..4r+3), output dims 8i + c2 + e
+  if (r < G) {
+    if ((lane & 3) == 0) {
+      red_m[warp * GM + r] = mw;
+      red_l[warp * GM + r] = lw;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      red_o[(warp * GM + r) * HD + 8 * i + c2] = o[i][0] + o[i][2];
+      red_o[(warp * GM + r) * HD + 8 * i + c2 + 1] = o[i][1] + o[i][3];
+    }
+  }
+  __syncthreads();
+  chunk_partial_and_combine<HD, GM, NW>(p, b, kvh, split, nsplit, red_m, red_l, red_o, s_last);
+}
+
 
 // GM: compile-time bound on the group size g = H / KV (arrays are sized GM).
 template <int HD, int GM>
-__global__ void __launch_bounds__(kDecWarps * 32, 2) decode_attn_kernel(const DecAttnParams p) {
+__global__ void __launch_bounds__(kDecWarps * 32) decode_attn_kernel(const DecAttnParams p) {
+  extern __shared__ __align__(128) uint8_t dsm[];
+  bf16 *sK = reinterpret_cast<bf16 *>(dsm);          // [kChunk][HD]
+  bf16 *sV = sK + kChunk * HD;                       // [kChunk][HD]
+  uint64_t *kv_bar = reinterpret_cast<uint64_t *>(sV + kChunk * HD);
   constexpr int LPK = HD / 8;            // lanes per key
   constexpr int KPW = 32 / LPK;          // keys per warp step (per lane group: 1)
   constexpr int NB = 4;                  // keys per lane group per step
@@ -135,6 +395,42 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_attn_kernel(const De
   const bf16 *kn = p.k_new + row * HD;
   const bf16 *vn = p.v_new + row * HD;
 
+  // the chunk's cached rows [k_begin, min(k_end, Lb)) arrive by bulk copy; the
+  // new key (index Lb), if it falls in this chunk, is copied by the threads
+  const int n_cached = max(0, min(k_end, Lb) - k_begin);
+  if (threadIdx.x == 0) {
+    mbar_init(kv_bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (n_cached > 0) {
+      const uint32_t bytes = static_cast<uint32_t>(n_cached) * HD * 2;
+      mbar_arrive_expect_tx(kv_bar, 2 * bytes);
+      bulk_load(sK, kc + (long long)k_begin * HD, bytes, kv_bar);
+      bulk_load(sV, vc + (long long)k_begin * HD, bytes, kv_bar);
+    } else {
+      mbar_arrive(kv_bar);
+    }
+  }
+  if (Lb >= k_begin && Lb < k_end) {
+    const int slot = Lb - k_begin;
+    for (int i = threadIdx.x; i < HD / 8; i += blockDim.x) {
+      reinterpret_cast<uint4 *>(sK + slot * HD)[i] = reinterpret_cast<const uint4 *>(kn)[i];
+      reinterpret_cast<uint4 *>(sV + slot * HD)[i] = reinterpret_cast<const uint4 *>(vn)[i];
+    }
+  }
+  {
+    int no_abort = 0;
+    const bool landed = mbar_wait_bounded(kv_bar, 0, &no_abort);
+    if (!__syncthreads_and(landed)) {
+      if (threadIdx.x == 0) atomicCAS(p.status, 0, kDevTimeoutProducer);
+      // wait (bounded) once more for the copies before the CTA exits
+      mbar_wait_bounded(kv_bar, 0, &no_abort);
+      return;
+    }
+  }
+
   const int step = kDecWarps * KPW * NB;           // keys per CTA step
   // The trip count depends on the warp only: every lane runs every iteration,
   // so the full-warp shuffles below never see a lane that has left the loop.
@@ -146,11 +442,9 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_attn_kernel(const De
     for (int i = 0; i < NB; ++i) {
       const int j = base + i;
       valid[i] = j < k_end;
-      const bf16 *kp = (j < Lb) ? kc + (long long)j * HD : kn;
-      const bf16 *vp = (j < Lb) ? vc + (long long)j * HD : vn;
       if (valid[i]) {
-        kr[i] = ld_stream(kp + sub * 8);
-        vr[i] = ld_stream(vp + sub * 8);
+        kr[i] = *reinterpret_cast<const uint4 *>(sK + (j - k_begin) * HD + sub * 8);
+        vr[i] = *reinterpret_cast<const uint4 *>(sV + (j - k_begin) * HD + sub * 8);
       } else {
         kr[i] = make_uint4(0, 0, 0, 0);
         vr[i] = make_uint4(0, 0, 0, 0);
@@ -235,81 +529,74 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_attn_kernel(const De
     }
   }
 
-  __shared__ float red_m[kDecWarps][GM], red_l[kDecWarps][GM];
-  __shared__ float red_o[kDecWarps][GM][HD];
+  __shared__ float red_m[kDecWarps * GM], red_l[kDecWarps * GM];
+  __shared__ float red_o[kDecWarps * GM * HD];
   __shared__ int s_last;
   if (grp == 0) {
 #pragma unroll
     for (int g = 0; g < GM; ++g) {
       if (g < G) {
         if (sub == 0) {
-          red_m[warp][g] = m[g];
-          red_l[warp][g] = l[g];
+          red_m[warp * GM + g] = m[g];
+          red_l[warp * GM + g] = l[g];
         }
 #pragma unroll
-        for (int e = 0; e < 8; ++e) red_o[warp][g][sub * 8 + e] = acc[g][e];
+        for (int e = 0; e < 8; ++e) red_o[(warp * GM + g) * HD + sub * 8 + e] = acc[g][e];
       }
     }
   }
   __syncthreads();
-  const long long pbase = (long long)b * p.H + kvh * G;   // first head of the group
-  for (int t = threadIdx.x; t < G * HD; t += blockDim.x) {
-    const int g = t / HD, dim = t - g * HD;
-    float M = -INFINITY;
-    for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, red_m[w][g]);
-    const float Mu = (M == -INFINITY) ? 0.f : M;
-    float Ls = 0.f, Os = 0.f;
-    for (int w = 0; w < kDecWarps; ++w) {
-      const float f = exp2f(red_m[w][g] - Mu);
-      Ls += red_l[w][g] * f;
-      Os += red_o[w][g][dim] * f;
-    }
-    const long long ps = (pbase + g) * p.max_splits + split;
-    if (dim == 0) {
-      p.part_m[ps] = M;
-      p.part_l[ps] = Ls;
-    }
-    p.part_o[ps * HD + dim] = Os;
-  }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const int prev = atomicAdd(p.counters + row, 1);
-    s_last = (prev == nsplit - 1);
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  for (int t = threadIdx.x; t < G * HD; t += blockDim.x) {
-    const int g = t / HD, dim = t - g * HD;
-    const long long ps0 = (pbase + g) * p.max_splits;
-    float M = -INFINITY;
-    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, __ldcg(p.part_m + ps0 + s));
-    const float Mu = (M == -INFINITY) ? 0.f : M;
-    float Ls = 0.f, Os = 0.f;
-    for (int s = 0; s < nsplit; ++s) {
-      const float f = exp2f(__ldcg(p.part_m + ps0 + s) - Mu);
-      Ls += __ldcg(p.part_l + ps0 + s) * f;
-      Os += __ldcg(p.part_o + (ps0 + s) * HD + dim) * f;
-    }
-    p.o[(pbase + g) * HD + dim] = __float2half_rn(Ls > 0.f ? Os / Ls : 0.f);
-  }
-  if (threadIdx.x == 0) p.counters[row] = 0;        // ready for the next layer
+  chunk_partial_and_combine<HD, GM, kDecWarps>(p, b, kvh, split, nsplit, red_m, red_l, red_o, &s_last);
+}
+
+template <int HD, int GM>
+static cudaError_t launch_decode_attn_g(const DecAttnParams &ap, dim3 grid, cudaStream_t st) {
+  const int smem = 2 * kChunk * HD * 2 + 16;
+  auto kern = decode_attn_kernel<HD, GM>;
+  cudaError_t e = ensure_smem_attr<decode_attn_kernel<HD, GM>>(smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kDecWarps * 32, smem, st>>>(ap);
+  return cudaGetLastError();
 }
 
 template <int HD>
 static cudaError_t launch_decode_attn_hd(const DecAttnParams &ap, dim3 grid, cudaStream_t st) {
   const int G = ap.H / ap.KV;
-  if (G == 1) decode_attn_kernel<HD, 1><<<grid, kDecWarps * 32, 0, st>>>(ap);
-  else if (G == 2) decode_attn_kernel<HD, 2><<<grid, kDecWarps * 32, 0, st>>>(ap);
-  else if (G == 3) decode_attn_kernel<HD, 3><<<grid, kDecWarps * 32, 0, st>>>(ap);
-  else if (G == 4) decode_attn_kernel<HD, 4><<<grid, kDecWarps * 32, 0, st>>>(ap);
-  else decode_attn_kernel<HD, 8><<<grid, kDecWarps * 32, 0, st>>>(ap);
+  if (G == 1) return launch_decode_attn_g<HD, 1>(ap, grid, st);
+  if (G == 2) return launch_decode_attn_g<HD, 2>(ap, grid, st);
+  if (G == 3) return launch_decode_attn_g<HD, 3>(ap, grid, st);
+  if (G == 4) return launch_decode_attn_g<HD, 4>(ap, grid, st);
+  return launch_decode_attn_g<HD, 8>(ap, grid, st);
+}
+
+template <int GM>
+static cudaError_t launch_decode_attn_mma_g(const CUtensorMap &tk, const CUtensorMap &tv,
+                                            const DecAttnParams &ap, dim3 grid, cudaStream_t st) {
+  constexpr int NW = 4, HD = 64;
+  const int smem = 1024 + 2 * kChunk * 128 + 16 + (2 * NW * GM + NW * GM * HD) * 4;
+  cudaError_t e = ensure_smem_attr<decode_attn_mma_kernel<GM>>(smem);
+  if (e != cudaSuccess) return e;
+  decode_attn_mma_kernel<GM><<<grid, NW * 32, smem, st>>>(tk, tv, ap);
   return cudaGetLastError();
 }
 
-static cudaError_t launch_decode_attn(const DecAttnParams &ap, int hd, dim3 grid, cudaStream_t st) {
-  return hd == 64 ? launch_decode_attn_hd<64>(ap, grid, st) : launch_decode_attn_hd<128>(ap, grid, st);
+// head_dim 64 runs on tensor cores (the cache seen as one 2-D tensor of
+// L*B*KV*S_max rows of 64 values); other head sizes on the CUDA-core kernel.
+static cudaError_t launch_decode_attn(const DecAttnParams &ap, int hd, dim3 grid, cudaStream_t st,
+                                      const bf16 *k_all, const bf16 *v_all, int L) {
+  if (hd == 64) {
+    CUtensorMap tk, tv;
+    const uint64_t rows = (uint64_t)L * ap.B * ap.KV * ap.S_max;
+    if (!get_tmap_f16(&tk, k_all, rows, 64, 64, kChunk)) return cudaErrorInvalidValue;
+    if (!get_tmap_f16(&tv, v_all, rows, 64, 64, kChunk)) return cudaErrorInvalidValue;
+    const int G = ap.H / ap.KV;
+    if (G == 1) return launch_decode_attn_mma_g<1>(tk, tv, ap, grid, st);
+    if (G == 2) return launch_decode_attn_mma_g<2>(tk, tv, ap, grid, st);
+    if (G == 3) return launch_decode_attn_mma_g<3>(tk, tv, ap, grid, st);
+    if (G == 4) return launch_decode_attn_mma_g<4>(tk, tv, ap, grid, st);
+    return launch_decode_attn_mma_g<8>(tk, tv, ap, grid, st);
+  }
+  return launch_decode_attn_hd<128>(ap, grid, st);
 }
 
 __global__ void zero_ints_kernel(int *p, int n) {
@@ -379,10 +666,11 @@ cudaError_t run_decode(const DecodeArgs &a, void *ws, int sms, cudaStream_t st, 
     ap.part_o = reinterpret_cast<float *>(wb + W.part_o);
     ap.counters = counters;
     ap.B = B; ap.H = H; ap.KV = KV; ap.S_max = a.S_max; ap.max_pos = c.max_pos;
-    ap.max_splits = W.max_splits; ap.scale_log2 = sl2;
+    ap.max_splits = W.max_splits; ap.scale_log2 = sl2; ap.status = status;
     const int lmax = min(a.S_max, c.max_pos - 1);
     dim3 grid((unsigned)cdiv(lmax + 1, kChunk), (unsigned)KV, (unsigned)B);
-    DEC_LAUNCH_K(SMOL_K_DEC_ATTN, launch_decode_attn(ap, hd, grid, st));
+    ap.layer = l;
+    DEC_LAUNCH_K(SMOL_K_DEC_ATTN, launch_decode_attn(ap, hd, grid, st, a.k_cache, a.v_cache, L));
 
     GemmParams po{};
     po.M = B; po.N = d; po.K = H * hd; po.out = h; po.out_is_f16 = 1; po.out_f32 = h32; po.ldo = d; po.resid_f32 = x32;

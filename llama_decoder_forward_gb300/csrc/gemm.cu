@@ -27,6 +27,9 @@
 //   kEpiScale    logits = rstd * D  (section 7 final norm + tied lm_head).
 #include <stdio.h>
 
+#include <mutex>
+#include <unordered_map>
+
 #include "common.cuh"
 #include "prims.cuh"
 
@@ -660,6 +663,50 @@ bool make_tmap_f16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t c
   return r == CUDA_SUCCESS;
 }
 
+namespace {
+struct TmapKey {
+  const void *base;
+  uint64_t rows, cols, pitch;
+  uint32_t box;
+  int dev;
+  bool operator==(const TmapKey &o) const {
+    return base == o.base && rows == o.rows && cols == o.cols && pitch == o.pitch && box == o.box &&
+           dev == o.dev;
+  }
+};
+struct TmapKeyHash {
+  size_t operator()(const TmapKey &k) const {
+    size_t h = reinterpret_cast<uintptr_t>(k.base);
+    for (uint64_t v : {k.rows, k.cols, k.pitch, (uint64_t)k.box, (uint64_t)k.dev})
+      h = h * 1000003u ^ static_cast<size_t>(v);
+    return h;
+  }
+};
+std::mutex g_tmap_mu;
+std::unordered_map<TmapKey, CUtensorMap, TmapKeyHash> g_tmap_cache;
+constexpr size_t kTmapCacheMax = 4096;
+}  // namespace
+
+bool get_tmap_f16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                  uint64_t row_pitch_elems, uint32_t box_rows) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const TmapKey key{base, rows, cols, row_pitch_elems, box_rows, dev};
+  {
+    std::lock_guard<std::mutex> lock(g_tmap_mu);
+    auto it = g_tmap_cache.find(key);
+    if (it != g_tmap_cache.end()) {
+      *map = it->second;
+      return true;
+    }
+  }
+  if (!make_tmap_f16(map, base, rows, cols, row_pitch_elems, box_rows)) return false;
+  std::lock_guard<std::mutex> lock(g_tmap_mu);
+  if (g_tmap_cache.size() >= kTmapCacheMax) g_tmap_cache.clear();
+  g_tmap_cache.emplace(key, *map);
+  return true;
+}
+
 int gemm_pick_bn(int epi, int N, int hd) {
   if (N <= 0 || N % 64) return 0;
   if (epi == kEpiQkvRope) {
@@ -690,7 +737,7 @@ static cudaError_t launch_impl(const CUtensorMap &ta, const CUtensorMap &tb, con
                                int num_sms, cudaStream_t stream) {
   using C = GemmCfg<BN, EPI>;
   auto kern = gemm_tc_kernel<BN, EPI, HD>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  cudaError_t e = ensure_smem_attr<gemm_tc_kernel<BN, EPI, HD>>(C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const long long tiles = cdiv(p.M, C::BM) * cdiv(p.N, BN);
   const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
@@ -701,8 +748,8 @@ static cudaError_t launch_impl(const CUtensorMap &ta, const CUtensorMap &tb, con
 cudaError_t launch_gemm(int epi, int bn, const void *A, const void *B, const GemmParams &p,
                         int num_sms, cudaStream_t stream) {
   CUtensorMap ta, tb;
-  if (!make_tmap_f16(&ta, A, p.M, p.K, p.K, 128)) return cudaErrorInvalidValue;
-  if (!make_tmap_f16(&tb, B, p.N, p.K, p.K, bn)) return cudaErrorInvalidValue;
+  if (!get_tmap_f16(&ta, A, p.M, p.K, p.K, 128)) return cudaErrorInvalidValue;
+  if (!get_tmap_f16(&tb, B, p.N, p.K, p.K, bn)) return cudaErrorInvalidValue;
   switch (epi) {
     case kEpiScale:
       if (bn == 256) return launch_impl<256, kEpiScale, 64>(ta, tb, p, num_sms, stream);
