@@ -55,6 +55,7 @@ struct GemmParams {
   int pos_limit;
   int max_pos;
   int *status;            // device status word
+  int raster_m;           // set by launch_gemm: 1 = consecutive tiles walk down M (B tile reused)
 };
 
 // Raises the dynamic shared-memory limit of kernel `Kern` to `bytes`, once per

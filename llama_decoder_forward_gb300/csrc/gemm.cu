@@ -1,7 +1,14 @@
 // gemm.cu - persistent tcgen05 GEMM with fused decoder epilogues (sm_103a).
 //
 // D[M, N] = A[M, K] * B[N, K]^T, f16 operands, fp32 accumulation in TMEM.
-// One CTA per SM walks tiles of 128 x BN.  Warp roles:
+// One CTA per SM walks tiles of 128 x BN.  With PAIR == 2 two CTAs (a
+// cluster of 2 on one TPC) share each 256 x BN tile: the even CTA issues
+// cta_group::2 MMAs (M = 256) that read each CTA's own 128-row A box and
+// half of the B box from each CTA's shared memory and write each CTA's 128
+// rows into its own TMEM.  Per SM that halves the B bytes written by TMA and
+// read by the tensor pipe; with one CTA, shared-memory bandwidth (TMA fill
+// plus MMA operand reads) rather than the tensor pipe bounds these
+// narrow-K GEMMs.  Warp roles:
 //   warp 0      TMA producer: 128x64 A box and BNx64 B box per stage (128 B swizzle)
 //   warp 1      TMEM owner; lane 0 issues tcgen05.mma (M=128, N=BN, K=16) and commits
 //   warps 2..9  epilogue: two warps per TMEM lane quarter split the tile's columns
@@ -50,12 +57,12 @@ struct EpiStage {
   static constexpr int kPerWarp = kTiles * kStgBytes;
 };
 
-template <int BN, int EPI>
+template <int BN, int EPI, int PAIR>
 struct GemmCfg {
-  static constexpr int BM = 128;
+  static constexpr int BM = 128;                      // rows per CTA
   static constexpr int BK = 64;                       // 64 x 16-bit = 128 B = one swizzle row
   static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int B_BYTES = (BN / PAIR) * BK * 2;  // this CTA's share of the B box
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int EPI_BYTES = kEpiWarps * EpiStage<EPI>::kPerWarp;
   static constexpr int STAGES_RAW = (232448 - 1024 - 256 - EPI_BYTES) / STAGE_BYTES;
@@ -322,7 +329,7 @@ __device__ __forceinline__ void epi_qkv_rope(const GemmParams &p, const EpiCtx &
   const int row = e.row0 + e.lane;
   const bool row_ok = e.lane < e.rows_valid;
   const float rs = row_rstd(p, row);
-  const int rr_ = row_ok ? row : e.row0;
+  const int rr_ = row_ok ? row : min(e.row0, p.M - 1);   // rows past M: any valid index
   const int b = rr_ / p.T, t = rr_ - b * p.T;
   int pos = t - (p.valid_start ? p.valid_start[b] : 0);
   if (p.pos_add) {
@@ -445,11 +452,13 @@ __device__ __forceinline__ void epi_qkv_rope(const GemmParams &p, const EpiCtx &
 }
 
 // ---------------------------------------------------------------- kernel
-template <int BN, int EPI, int HD>
+template <int BN, int EPI, int HD, int PAIR>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmParams p) {
-  using C = GemmCfg<BN, EPI>;
+  using C = GemmCfg<BN, EPI, PAIR>;
+  static_assert(PAIR == 1 || PAIR == 2, "one CTA or a CTA pair");
+  static_assert((BN / PAIR) % 8 == 0, "B share must be whole 8-row swizzle atoms");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -468,8 +477,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int num_n = static_cast<int>(cdiv(p.N, BN));
-  const int num_tiles = static_cast<int>(cdiv(p.M, C::BM)) * num_n;
+  // a "tile" below is PAIR vertically adjacent 128 x BN tiles, one per CTA
+  const int num_mg = static_cast<int>(cdiv(cdiv(p.M, C::BM), PAIR));
+  const int num_tiles = num_mg * num_n;
+  // tile order: with raster_m, concurrently running CTAs share one B tile (and
+  // walk all of A, which then stays in L2) - for B larger than A, e.g. the
+  // vocabulary projection; otherwise they share A and walk B
   const int num_kb = static_cast<int>(cdiv(p.K, C::BK));
+  const int rank = PAIR > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int first_tile = blockIdx.x / PAIR, tile_step = gridDim.x / PAIR;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -478,7 +494,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 32 * kEpiWarps);
+      mbar_init(&tempty[a], PAIR * kEpiWarps);   // one arrival per epilogue warp (of both CTAs)
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -487,13 +503,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tma_prefetch_desc(&tmB);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, C::TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (PAIR == 1) {
+      tmem_alloc(tmem_slot, C::TMEM_COLS);
+      tmem_relinquish();
+    } else {
+      tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
+      tmem_relinquish_pair();
+    }
   }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
+  if constexpr (PAIR > 1) cluster_sync_all();     // the peer's barriers exist before any use
   const uint32_t tmem_base = *tmem_slot;
+  // cluster addresses of the even CTA's full[0] and tempty[0] (pairs only)
+  const uint32_t full0_leader = PAIR > 1 ? mapa_shared(smem_u32(full), 0) : 0u;
+  const uint32_t tempty0_leader = PAIR > 1 ? mapa_shared(smem_u32(tempty), 0) : 0u;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -501,16 +526,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t stage = 0, phase = 0;
       long long issued = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const int m_blk = tile / num_n, n_blk = tile - m_blk * num_n;
+      for (int tile = first_tile; tile < num_tiles && ok; tile += tile_step) {
+        const int m_grp = p.raster_m ? tile % num_mg : tile / num_n;
+        const int n_blk = p.raster_m ? tile / num_mg : tile - m_grp * num_n;
+        const int m_blk = m_grp * PAIR + rank;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-          tma_load_2d(sA + stage * C::A_BYTES, &tmA, &full[stage], kb * C::BK, m_blk * C::BM);
-          tma_load_2d(sB + stage * C::B_BYTES, &tmB, &full[stage], kb * C::BK, n_blk * BN);
+          if constexpr (PAIR == 1) {
+            mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+            tma_load_2d(sA + stage * C::A_BYTES, &tmA, &full[stage], kb * C::BK, m_blk * C::BM);
+            tma_load_2d(sB + stage * C::B_BYTES, &tmB, &full[stage], kb * C::BK, n_blk * BN);
+          } else {
+            // both CTAs' boxes are counted on the even CTA's barrier, which its MMA waits on
+            if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
+            const uint32_t fb = full0_leader + 8u * stage;
+            tma_load_2d_pair(sA + stage * C::A_BYTES, &tmA, fb, kb * C::BK, m_blk * C::BM);
+            tma_load_2d_pair(sB + stage * C::B_BYTES, &tmB, fb, kb * C::BK,
+                             n_blk * BN + rank * (BN / PAIR));
+          }
           ++issued;
           if (++stage == C::STAGES) {
             stage = 0;
@@ -532,12 +568,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ------------------------------------------------ MMA issuer
-      constexpr uint32_t kIdesc = idesc_f16_f32(C::BM, BN);
+    if (lane == 0 && rank == 0) {
+      // ------------------------------------------------ MMA issuer (the even CTA of a pair)
+      constexpr uint32_t kIdesc = idesc_f16_f32(C::BM * PAIR, BN);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true, any = false;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      for (int tile = first_tile; tile < num_tiles && ok; tile += tile_step) {
         if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, abort_flag)) {
           ok = false;
           break;
@@ -555,17 +591,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
           for (int k = 0; k < C::BK / 16; ++k) {
             // +32 bytes per K step of 16 elements (encoded >> 4)
-            umma_f16(d_tmem, a_desc + 2 * k, b_desc + 2 * k, kIdesc, (kb | k) != 0);
+            if constexpr (PAIR == 1)
+              umma_f16(d_tmem, a_desc + 2 * k, b_desc + 2 * k, kIdesc, (kb | k) != 0);
+            else
+              umma_f16_pair(d_tmem, a_desc + 2 * k, b_desc + 2 * k, kIdesc, (kb | k) != 0);
           }
           any = true;
-          umma_commit(&empty[stage]);
+          if constexpr (PAIR == 1) umma_commit(&empty[stage]);
+          else umma_commit_pair(&empty[stage], 0x3);     // frees the stage in both CTAs
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
-        umma_commit(&tfull[acc]);
+        if constexpr (PAIR == 1) umma_commit(&tfull[acc]);
+        else umma_commit_pair(&tfull[acc], 0x3);         // both CTAs' accumulators are ready
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1;
       }
@@ -574,7 +615,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         *abort_flag = 1;
         if (any) {
           // wait (bounded) for the MMAs already issued before TMEM is freed
-          umma_commit(drain);
+          if constexpr (PAIR == 1) umma_commit(drain);
+          else umma_commit_pair(drain, 0x1);
           int dummy = 0;
           if (!mbar_wait_bounded(drain, 0, reinterpret_cast<volatile int *>(&dummy)))
             record_status(p.status, kDevTimeoutDrain);
@@ -589,8 +631,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     e.split = (warp - 2) >> 2;                    // which share of the tile's columns
     e.st = sEpi + (warp - 2) * EpiStage<EPI>::kPerWarp;
     uint32_t acc = 0, acc_phase = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-      const int m_blk = tile / num_n, n_blk = tile - m_blk * num_n;
+    for (int tile = first_tile; tile < num_tiles; tile += tile_step) {
+      const int m_grp = p.raster_m ? tile % num_mg : tile / num_n;
+      const int n_blk = p.raster_m ? tile / num_mg : tile - m_grp * num_n;
+      const int m_blk = m_grp * PAIR + rank;
       e.row0 = m_blk * C::BM + quarter * 32;
       e.rows_valid = min(32, max(0, p.M - e.row0));
       e.n0 = n_blk * BN;
@@ -616,7 +660,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       else if constexpr (EPI == kEpiSwiglu) epi_swiglu<BN>(p, e);
       else epi_qkv_rope<BN, HD>(p, e);
       tc_fence_before_sync();
-      mbar_arrive(&tempty[acc]);
+      __syncwarp();
+      // the accumulator may be overwritten once every warp's tcgen05.ld has
+      // completed (its stores need not be visible): a relaxed arrival, on the
+      // even CTA's barrier for a pair
+      if (lane == 0)
+        mbar_arrive_relaxed_cluster((PAIR == 1 ? smem_u32(tempty) : tempty0_leader) + 8u * acc);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
@@ -624,9 +673,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   tc_fence_before_sync();
   __syncthreads();
+  // neither CTA of a pair frees TMEM or leaves while the other may still use it
+  if constexpr (PAIR > 1) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, C::TMEM_COLS);
+    if constexpr (PAIR == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+    else tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
   }
 }
 
@@ -732,24 +784,75 @@ int gemm_pick_bn(int epi, int N, int hd) {
   return 64;
 }
 
+// CTA pairs for problems with at least kPairMinMBlocks row blocks of 128;
+// single CTAs otherwise (decode-sized M).
+constexpr int kPairMinMBlocks = 8;
+
+// How many clusters of the kernel can be resident at once (cached per device).
+template <auto Kern>
+static int max_active_clusters(cudaLaunchConfig_t cfg, int fallback) {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fallback;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  if (cudaOccupancyMaxActiveClusters(&n, Kern, &cfg) != cudaSuccess || n <= 0) {
+    (void)cudaGetLastError();
+    return fallback;
+  }
+  cache[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+template <int BN, int EPI, int HD, int PAIR>
+static cudaError_t launch_pair(const CUtensorMap &ta, const CUtensorMap &tb, const GemmParams &p,
+                               int num_sms, cudaStream_t stream) {
+  using C = GemmCfg<BN, EPI, PAIR>;
+  constexpr auto kern = gemm_tc_kernel<BN, EPI, HD, PAIR>;
+  cudaError_t e = ensure_smem_attr<kern>(C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const long long groups = cdiv(cdiv(p.M, C::BM), PAIR) * cdiv(p.N, BN);
+  if constexpr (PAIR == 1) {
+    const int grid = static_cast<int>(groups < num_sms ? groups : num_sms);
+    kern<<<grid, kGemmThreads, C::SMEM_BYTES, stream>>>(ta, tb, p);
+    return cudaGetLastError();
+  } else {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = PAIR;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(num_sms / PAIR * PAIR));
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const long long pairs_max = max_active_clusters<kern>(cfg, num_sms / PAIR);
+    const long long pairs = groups < pairs_max ? groups : pairs_max;
+    cfg.gridDim = dim3(static_cast<unsigned>(pairs * PAIR));
+    return cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
+  }
+}
+
+static int gemm_pair(const GemmParams &p) { return cdiv(p.M, 128) >= kPairMinMBlocks ? 2 : 1; }
+
 template <int BN, int EPI, int HD>
 static cudaError_t launch_impl(const CUtensorMap &ta, const CUtensorMap &tb, const GemmParams &p,
                                int num_sms, cudaStream_t stream) {
-  using C = GemmCfg<BN, EPI>;
-  auto kern = gemm_tc_kernel<BN, EPI, HD>;
-  cudaError_t e = ensure_smem_attr<gemm_tc_kernel<BN, EPI, HD>>(C::SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  const long long tiles = cdiv(p.M, C::BM) * cdiv(p.N, BN);
-  const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
-  kern<<<grid, kGemmThreads, C::SMEM_BYTES, stream>>>(ta, tb, p);
-  return cudaGetLastError();
+  if (gemm_pair(p) == 1) return launch_pair<BN, EPI, HD, 1>(ta, tb, p, num_sms, stream);
+  return launch_pair<BN, EPI, HD, 2>(ta, tb, p, num_sms, stream);
 }
 
-cudaError_t launch_gemm(int epi, int bn, const void *A, const void *B, const GemmParams &p,
+cudaError_t launch_gemm(int epi, int bn, const void *A, const void *B, const GemmParams &p_in,
                         int num_sms, cudaStream_t stream) {
+  GemmParams p = p_in;
+  p.raster_m = (long long)p.N > (long long)p.M ? 1 : 0;   // keep the larger operand's tiles hot
   CUtensorMap ta, tb;
   if (!get_tmap_f16(&ta, A, p.M, p.K, p.K, 128)) return cudaErrorInvalidValue;
-  if (!get_tmap_f16(&tb, B, p.N, p.K, p.K, bn)) return cudaErrorInvalidValue;
+  // each CTA of a pair loads half of the B box
+  if (!get_tmap_f16(&tb, B, p.N, p.K, p.K, bn / gemm_pair(p))) return cudaErrorInvalidValue;
   switch (epi) {
     case kEpiScale:
       if (bn == 256) return launch_impl<256, kEpiScale, 64>(ta, tb, p, num_sms, stream);
