@@ -18,6 +18,11 @@ typedef __half f16;
 
 __host__ __device__ constexpr long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 
+// RoPE table: rows 0..63 hold (cos, sin)(b * f_i), rows 64 + a hold
+// (cos, sin)(64 * a * f_i), i < hd/2; a position 64a + b combines the two by
+// the angle-sum identities.
+__host__ __device__ constexpr long long rope_table_rows(int max_pos) { return 64 + cdiv(max_pos, 64); }
+
 // ------------------------------------------------------------------ GEMM
 // D[M, N] = A[M, K] * B[N, K]^T on tcgen05 with one of these epilogues.
 enum Epilogue : int {
@@ -36,7 +41,8 @@ struct GemmParams {
   int out_is_f16;         // element type of `out`: 1 = f16, 0 = bf16
   long long ldo;
   const bf16 *resid;      // kEpiResidual: bf16 residual rows (leading dimension ldo), or
-  const float *resid_f32; //   fp32 residual rows (exactly one of the two is set)
+  const f16 *resid_f16;   //   f16 residual rows, or
+  const float *resid_f32; //   fp32 residual rows (exactly one of the three is set)
   float *out_f32;         // kEpiResidual: optional fp32 copy of the output rows
   const float *ssq_in;    // per-row sum of squares feeding rstd (nullptr: scale 1)
   float inv_dim;          // 1 / d for the mean of squares
@@ -49,13 +55,14 @@ struct GemmParams {
   int T_pad;              // row pitch of v_t in elements (T rounded up to a multiple of 8)
   bf16 *k_bf, *v_bf;      // optional bf16 copies of k and v (cache entries), same layout
   int T, H, KV, hd;
-  const float2 *rope;     // [max_pos][hd/2] (cos, sin)
+  const float2 *rope;     // [rope_table_rows(max_pos)][hd/2] (cos, sin), two-level
   const int *valid_start; // [B] or nullptr: position t - valid_start[b]
   const int *pos_add;     // [B] or nullptr: adds clamp(pos_add[b], 0, pos_limit) (decode)
   int pos_limit;
   int max_pos;
   int *status;            // device status word
   int raster_m;           // set by launch_gemm: 1 = consecutive tiles walk down M (B tile reused)
+  int epi_tma;            // set by launch_gemm: which epilogue tensor maps are valid
 };
 
 // Raises the dynamic shared-memory limit of kernel `Kern` to `bytes`, once per
@@ -76,11 +83,17 @@ cudaError_t ensure_smem_attr(int bytes) {
 // box of box_rows x 64 columns and 128-byte swizzle.  Returns false on error.
 bool make_tmap_f16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
                     uint64_t row_pitch_elems, uint32_t box_rows);
+// General 2-D map of 16-bit elements: box of box_rows x box_cols, 128-byte
+// swizzle or none.
+bool make_tmap_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                  uint64_t row_pitch_elems, uint32_t box_cols, uint32_t box_rows, bool swizzle128);
 // The same through a small per-process cache keyed by (device, arguments):
 // encoding is a host call of a few microseconds, and the same buffers recur on
 // every forward.
 bool get_tmap_f16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
                   uint64_t row_pitch_elems, uint32_t box_rows);
+bool get_tmap_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                 uint64_t row_pitch_elems, uint32_t box_cols, uint32_t box_rows, bool swizzle128);
 
 // Chooses the N tile for an epilogue and problem; 0 if unsupported.
 int gemm_pick_bn(int epi, int N, int hd);

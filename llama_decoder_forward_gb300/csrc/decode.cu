@@ -32,7 +32,7 @@ constexpr int kChunk = 256;        // keys per CTA
 constexpr int kDecWarps = 4;       // warps per CTA
 
 struct DecWs {
-  size_t status, x, x32, h, h32, q, o, a, ssq_a, ssq_b, part_m, part_l, part_o, counters, total;
+  size_t status, x, h, q, o, a, ssq_a, ssq_b, part_m, part_l, part_o, counters, total;
   int max_splits;
 };
 
@@ -46,9 +46,7 @@ static DecWs dec_ws(const smol_config *c, int B) {
   size_t o = 0;
   W.status = o; o += 1024;
   W.x = o; o = align_up(o + B * d * 2, 1024);
-  W.x32 = o; o = align_up(o + B * d * 4, 1024);
   W.h = o; o = align_up(o + B * d * 2, 1024);
-  W.h32 = o; o = align_up(o + B * d * 4, 1024);
   W.q = o; o = align_up(o + B * H * hd * 2, 1024);
   W.o = o; o = align_up(o + B * H * hd * 2, 1024);
   W.a = o; o = align_up(o + B * I * 2, 1024);
@@ -618,8 +616,6 @@ cudaError_t run_decode(const DecodeArgs &a, void *ws, int sms, cudaStream_t st, 
   int *status = reinterpret_cast<int *>(wb + W.status);
   f16 *x = reinterpret_cast<f16 *>(wb + W.x);
   f16 *h = reinterpret_cast<f16 *>(wb + W.h);
-  float *x32 = reinterpret_cast<float *>(wb + W.x32);
-  float *h32 = reinterpret_cast<float *>(wb + W.h32);
   f16 *q = reinterpret_cast<f16 *>(wb + W.q);
   f16 *o = reinterpret_cast<f16 *>(wb + W.o);
   f16 *act = reinterpret_cast<f16 *>(wb + W.a);
@@ -639,7 +635,7 @@ cudaError_t run_decode(const DecodeArgs &a, void *ws, int sms, cudaStream_t st, 
 #define DEC_LAUNCH(expr) DEC_LAUNCH_K(SMOL_K_OTHER, expr)
 
   DEC_LAUNCH(launch_zero_ints(counters, B * KV, st));
-  DEC_LAUNCH_K(SMOL_K_EMBED, launch_embed_rows(a.ids, a.embed, V, d, B, x, x32, ssq_a, st));
+  DEC_LAUNCH_K(SMOL_K_EMBED, launch_embed_rows(a.ids, a.embed, V, d, B, x, nullptr, ssq_a, st));
 
   const float sl2 = 1.4426950408889634f / sqrtf((float)hd);
   for (int l = 0; l < L; ++l) {
@@ -673,7 +669,7 @@ cudaError_t run_decode(const DecodeArgs &a, void *ws, int sms, cudaStream_t st, 
     DEC_LAUNCH_K(SMOL_K_DEC_ATTN, launch_decode_attn(ap, hd, grid, st, a.k_cache, a.v_cache, L));
 
     GemmParams po{};
-    po.M = B; po.N = d; po.K = H * hd; po.out = h; po.out_is_f16 = 1; po.out_f32 = h32; po.ldo = d; po.resid_f32 = x32;
+    po.M = B; po.N = d; po.K = H * hd; po.out = h; po.out_is_f16 = 1; po.ldo = d; po.resid_f16 = x;
     po.ssq_out = ssq_b;
     po.status = status;
     DEC_LAUNCH_K(SMOL_K_OPROJ, launch_gemm(kEpiResidual, 64, o, lb + a.off_o, po, sms, st));
@@ -684,7 +680,7 @@ cudaError_t run_decode(const DecodeArgs &a, void *ws, int sms, cudaStream_t st, 
     DEC_LAUNCH_K(SMOL_K_GATEUP, launch_gemm(kEpiSwiglu, 128, h, lb + a.off_gu, pg, sms, st));
 
     GemmParams pd{};
-    pd.M = B; pd.N = d; pd.K = I; pd.out = x; pd.out_is_f16 = 1; pd.out_f32 = x32; pd.ldo = d; pd.resid_f32 = h32;
+    pd.M = B; pd.N = d; pd.K = I; pd.out = x; pd.out_is_f16 = 1; pd.ldo = d; pd.resid_f16 = h;
     pd.ssq_out = ssq_a;
     pd.status = status;
     DEC_LAUNCH_K(SMOL_K_DOWN, launch_gemm(kEpiResidual, 64, act, lb + a.off_down, pd, sms, st));

@@ -13,7 +13,7 @@ struct DecodeArgs {
   const bf16 *k_cache, *v_cache;   // [L, B, KV, S_max, hd]
   bf16 *k_new, *v_new;     // [L, B, KV, hd]
   bf16 *logits;            // [B, V]
-  const float2 *rope;      // [max_pos][hd/2]
+  const float2 *rope;      // two-level (cos, sin) table, see rope_table_rows
   const bf16 *embed;       // bf16 table for the gather
   const f16 *head;         // f16 norm-folded tied head
   const uint8_t *layer0;   // first packed layer

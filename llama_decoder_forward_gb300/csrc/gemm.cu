@@ -33,6 +33,7 @@
 //   kEpiSwiglu   a = SiLU(rstd*g) * (rstd*u)  (section 5 SmolMLP; components.py SwiGLU_FFN);
 //   kEpiScale    logits = rstd * D  (section 7 final norm + tied lm_head).
 #include <stdio.h>
+#include <string.h>
 
 #include <mutex>
 #include <unordered_map>
@@ -47,13 +48,24 @@ constexpr int kSplit = kEpiWarps / 4;              // warps sharing one quarter'
 constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
 constexpr int kStgBytes = 32 * 128;                // one staging tile: 32 rows x 128 B
 
-// Staging tiles per epilogue warp (each a full 32 x 128-byte tile: the
-// swizzle spreads even a 64-byte-per-row payload over all 128 bytes of a
-// row): the residual epilogue double-buffers its input tile (prefetched with
-// cp.async) and adds a 16-bit output tile; the others stage one tile.
+// Tensor maps of the epilogues' TMA traffic; GemmParams::epi_tma says which
+// are valid.  Boxes are one warp's staging tile: 32 rows x 64 16-bit columns
+// (128-byte swizzle, the staging layout below), or for V^T 64 dims x 32 tokens.
+struct EpiMaps {
+  CUtensorMap out;     // 16-bit output rows [M, out columns] (pitch ldo)
+  CUtensorMap resid;   // 16-bit residual rows [M, N] (pitch ldo)
+  CUtensorMap q, k;    // [B*H*T, 64] and [B*KV*T, 64]
+  CUtensorMap vt;      // [B*KV*64, T] with pitch T_pad, no swizzle
+};
+enum EpiTma : int { kTmaOut = 1, kTmaResid = 2, kTmaQkv = 4 };
+
+// Staging tiles (4 KB each) per epilogue warp: two for the residual and QKV
+// epilogues (residual units loaded ahead of the accumulator; alternating
+// tiles let one TMA store drain while the next unit is staged), one for the
+// others.
 template <int EPI>
 struct EpiStage {
-  static constexpr int kTiles = EPI == 1 /*kEpiResidual*/ ? 3 : 1;
+  static constexpr int kTiles = (EPI == 1 /*kEpiResidual*/ || EPI == 0 /*kEpiQkvRope*/) ? 2 : 1;
   static constexpr int kPerWarp = kTiles * kStgBytes;
 };
 
@@ -73,7 +85,7 @@ struct GemmCfg {
   static_assert(BN % 64 == 0 && BN <= 256, "UMMA N for M=128 and whole 64-column epilogue units");
   static_assert(B_BYTES % 1024 == 0, "B stage must keep 1024-byte alignment");
   static_assert(STAGES >= 3, "pipeline depth");
-  static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
+  static_assert((2 * STAGES + 5 + kEpiWarps) * 8 + 8 <= BAR_BYTES, "barrier area");
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
 
@@ -87,8 +99,9 @@ __device__ __forceinline__ float row_rstd(const GemmParams &p, int row) {
 }
 
 // ---------------------------------------------------------------- staging tile
-// Byte offset of 16-byte chunk c (0..7) of row r (0..31); always inside the
-// tile's 4 KB, whatever subset of chunks a caller uses.
+// Byte offset of 16-byte chunk c (0..7) of row r (0..31): the 128-byte
+// swizzle of TMA (tile base 1024-byte aligned), conflict-free both for one
+// row per thread and for consecutive lanes on consecutive chunks of a row.
 __device__ __forceinline__ int stg_off(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
 
 // Row-per-thread writes: 32 values as fp32 (chunks 0..7), or as 16-bit values
@@ -115,7 +128,7 @@ __device__ __forceinline__ void stg_put_16(uint8_t *st, int r, int c0, const flo
   }
 }
 
-// Row-per-thread reads of 32 values (fp32 chunks 0..7, or bf16 chunks 0..3).
+// Row-per-thread reads of 32 values (fp32 chunks 0..7, or 16-bit chunks c0..c0+3).
 __device__ __forceinline__ void stg_get_f32(const uint8_t *st, int r, float (&v)[32]) {
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
@@ -124,14 +137,15 @@ __device__ __forceinline__ void stg_get_f32(const uint8_t *st, int r, float (&v)
   }
 }
 
-__device__ __forceinline__ void stg_get_bf16(const uint8_t *st, int r, float (&v)[32]) {
+__device__ __forceinline__ void stg_get_16(const uint8_t *st, int r, int c0, float (&v)[32],
+                                           bool is_f16) {
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    const uint4 u = *reinterpret_cast<const uint4 *>(st + stg_off(r, c));
+    const uint4 u = *reinterpret_cast<const uint4 *>(st + stg_off(r, c0 + c));
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float2 f = unpack_bf16x2(w[e]);
+      const float2 f = is_f16 ? unpack_f16x2(w[e]) : unpack_bf16x2(w[e]);
       v[8 * c + 2 * e] = f.x;
       v[8 * c + 2 * e + 1] = f.y;
     }
@@ -141,6 +155,8 @@ __device__ __forceinline__ void stg_get_bf16(const uint8_t *st, int r, float (&v
 // Cooperative copies between the staging tile (chunks c0..c0+NC-1 of each row)
 // and NC*16 contiguous bytes per row in global memory; row rr's address is
 // g + row_off(rr) bytes.  Rows >= rows_valid are skipped.  NC is 4 or 8.
+// (Used where a TMA box does not fit: rows of a warp crossing a sequence,
+// decode-sized problems, fp32 data.)
 template <int NC, typename RowOff>
 __device__ __forceinline__ void stg_to_global(const uint8_t *st, int c0, uint8_t *g, RowOff row_off,
                                               int rows_valid, int lane) {
@@ -170,6 +186,34 @@ __device__ __forceinline__ void global_to_stg_async(uint8_t *st, const uint8_t *
   }
 }
 
+// Before a staging tile is rewritten: lane 0 waits until at most N of its
+// earlier bulk groups may still be reading shared memory, then the warp
+// proceeds together (this also orders the lanes' earlier reads of the tile).
+template <int N>
+__device__ __forceinline__ void stg_reuse_wait(int lane) {
+  if (lane == 0) bulk_wait_group_read<N>();
+  __syncwarp();
+}
+
+// Every lane's writes of the staged box are made visible to the async proxy;
+// lane 0 issues its TMA store (none for a warp without rows) and commits one
+// bulk group.
+__device__ __forceinline__ void stg_tma_store(const CUtensorMap *map, const uint8_t *tile, int x,
+                                              int y, int lane, int rows_valid) {
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    if (rows_valid > 0) tma_store_2d(map, tile, x, y);
+    bulk_commit_group();
+  }
+}
+
+// An empty bulk group, so that every use of an alternating staging tile is
+// one group whatever path wrote it out.
+__device__ __forceinline__ void stg_empty_group(int lane) {
+  if (lane == 0) bulk_commit_group();
+}
+
 // ---------------------------------------------------------------- epilogues
 // Every tcgen05.ld is executed by all lanes (it is warp-collective); only
 // global accesses depend on the row bound.
@@ -178,13 +222,18 @@ struct EpiCtx {
   int row0;           // the warp's first tile row
   int rows_valid;     // how many of its 32 rows exist
   int lane, n0, n_blk, split;
-  uint8_t *st;        // the warp's two staging tiles
+  uint8_t *st;        // the warp's staging tiles
+  const EpiMaps *maps;
+  uint64_t *rbar;     // the warp's residual-load barrier and its next parity
+  uint32_t rphase;
+  uint32_t seq;       // staging uses so far (selects the alternating tile)
 };
 
 // logits = rstd * D; units of 64 columns (one full 128-byte row segment).
 template <int BN>
-__device__ __forceinline__ void epi_scale(const GemmParams &p, const EpiCtx &e) {
+__device__ __forceinline__ void epi_scale(const GemmParams &p, EpiCtx &e) {
   const float rs = row_rstd(p, e.row0 + e.lane);
+  const bool tma = p.epi_tma & kTmaOut;
   const long long ld = p.ldo * 2;
   uint8_t *gbase = static_cast<uint8_t *>(p.out) + ((long long)e.row0 * p.ldo) * 2;
 #pragma unroll 1
@@ -197,72 +246,131 @@ __device__ __forceinline__ void epi_scale(const GemmParams &p, const EpiCtx &e) 
     float v[32];
 #pragma unroll
     for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r0[k]) * rs;
-    __syncwarp();                                 // previous copy-out has read the tile
+    stg_reuse_wait<0>(e.lane);
     stg_put_16(e.st, e.lane, 0, v, p.out_is_f16);
 #pragma unroll
     for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r1[k]) * rs;
     stg_put_16(e.st, e.lane, 4, v, p.out_is_f16);
-    __syncwarp();
-    stg_to_global<8>(e.st, 0, gbase + (long long)(e.n0 + c) * 2,
-                     [&](int rr) { return rr * ld; }, e.rows_valid, e.lane);
+    if (tma) {
+      stg_tma_store(&e.maps->out, e.st, e.n0 + c, e.row0, e.lane, e.rows_valid);
+    } else {
+      __syncwarp();
+      stg_to_global<8>(e.st, 0, gbase + (long long)(e.n0 + c) * 2,
+                       [&](int rr) { return rr * ld; }, e.rows_valid, e.lane);
+    }
   }
 }
 
-// out = resid + D (units of 32 columns).  The residual (fp32 or bf16) of unit
-// k+1 is fetched with cp.async into the other staging buffer while unit k is
-// processed (unit 0 before the accumulator is even ready); the result is
-// written in fp32 (out_f32) and/or 16 bits (out).  The row sum of squares
-// feeding the next RMSNorm is taken over the values the next step reads: fp32
-// when out_f32 is written, else the rounded 16-bit values.
+// ---- residual: out = resid + D.
+// Fast path (16-bit residual in, 16-bit result out): the warp's residual
+// units of 64 columns are fetched by TMA into its staging tiles before the
+// accumulator is ready, the sum is written back in place and stored by TMA.
+// Row sums of squares (feeding the next RMSNorm) are taken over the rounded
+// 16-bit values the next step reads.
 template <int BN>
-__device__ __forceinline__ void residual_prefetch(const GemmParams &p, const EpiCtx &e, int c,
-                                                  uint8_t *buf) {
+__device__ __forceinline__ int residual_units(const GemmParams &p, const EpiCtx &e) {
+  int nu = 0;
+  if (e.rows_valid <= 0) return 0;                // a CTA of a pair past the last row block
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int c = (e.split + kSplit * k) * 64;
+    if (c < BN && e.n0 + c < p.N) ++nu;
+  }
+  return nu;
+}
+
+template <int BN>
+__device__ __forceinline__ void residual_load_tma(const GemmParams &p, EpiCtx &e) {
+  const int nu = residual_units<BN>(p, e);
+  if (nu == 0) return;
+  stg_reuse_wait<0>(e.lane);                      // earlier stores have read the tiles
+  if (e.lane == 0) {
+    mbar_arrive_expect_tx(e.rbar, nu * kStgBytes);
+    for (int k = 0; k < nu; ++k)
+      tma_load_2d(e.st + k * kStgBytes, &e.maps->resid, e.rbar, e.n0 + (e.split + kSplit * k) * 64,
+                  e.row0);
+  }
+}
+
+template <int BN>
+__device__ __forceinline__ bool epi_residual_tma(const GemmParams &p, EpiCtx &e,
+                                                 volatile int *abort_flag) {
+  const int nu = residual_units<BN>(p, e);
+  if (nu == 0) return true;
+  const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(e.rbar, e.rphase, abort_flag));
+  e.rphase ^= 1u;
+  if (!ok) return false;
+  const bool resid_f16 = p.resid_f16 != nullptr;
+  float part = 0.f;
+#pragma unroll 1
+  for (int k = 0; k < nu; ++k) {
+    const int c = (e.split + kSplit * k) * 64;
+    uint8_t *tile = e.st + k * kStgBytes;
+    uint32_t r[32];
+    float v[32];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      tmem_ld32(e.taddr + c + 32 * h, r);
+      tmem_ld_wait();
+      stg_get_16(tile, e.lane, 4 * h, v, resid_f16);
+#pragma unroll
+      for (int q = 0; q < 32; ++q) {
+        const float x = v[q] + __uint_as_float(r[q]);
+        const float rx = p.out_is_f16 ? __half2float(__float2half_rn(x))
+                                      : __bfloat162float(__float2bfloat16_rn(x));
+        v[q] = rx;
+        part = fmaf(rx, rx, part);
+      }
+      stg_put_16(tile, e.lane, 4 * h, v, p.out_is_f16);   // own row only: in place
+    }
+    stg_tma_store(&e.maps->out, tile, e.n0 + c, e.row0, e.lane, e.rows_valid);
+  }
+  if (e.lane < e.rows_valid && p.ssq_out) atomicAdd(p.ssq_out + e.row0 + e.lane, part);
+  return true;
+}
+
+// General path (fp32 residual and/or fp32 output; 32-column units; cp.async
+// and per-lane stores): tile 0 holds the residual unit, tile 1 the 16-bit result.
+template <int BN>
+__device__ __forceinline__ void residual_prefetch_lane(const GemmParams &p, const EpiCtx &e, int c,
+                                                       uint8_t *buf) {
   const long long off = (long long)e.row0 * p.ldo + e.n0 + c;
   if (p.resid_f32)
     global_to_stg_async<8>(buf, reinterpret_cast<const uint8_t *>(p.resid_f32 + off), p.ldo * 4,
                            e.rows_valid, e.lane);
   else
-    global_to_stg_async<4>(buf, reinterpret_cast<const uint8_t *>(p.resid + off), p.ldo * 2,
-                           e.rows_valid, e.lane);
+    global_to_stg_async<4>(buf,
+                           p.resid_f16 ? reinterpret_cast<const uint8_t *>(p.resid_f16 + off)
+                                       : reinterpret_cast<const uint8_t *>(p.resid + off),
+                           p.ldo * 2, e.rows_valid, e.lane);
   cp_async_commit();
 }
 
 template <int BN>
-__device__ __forceinline__ void epi_residual(const GemmParams &p, const EpiCtx &e) {
+__device__ __forceinline__ void epi_residual_lane(const GemmParams &p, EpiCtx &e) {
   const bool row_ok = e.lane < e.rows_valid;
   float part = 0.f;
-  uint8_t *buf[2] = {e.st, e.st + kStgBytes};
-  uint8_t *st16 = e.st + 2 * kStgBytes;
+  uint8_t *buf = e.st, *st16 = e.st + kStgBytes;
   const long long row0_off = (long long)e.row0 * p.ldo;
-  // unit 0's residual was prefetched by the caller into buf[0]
-  int k = 0;
+  // unit 0's residual was prefetched by the caller into buf
 #pragma unroll 1
-  for (int c = e.split * 32; c < BN; c += 32 * kSplit, ++k) {
+  for (int c = e.split * 32; c < BN; c += 32 * kSplit) {
     const int col = e.n0 + c;
     if (col >= p.N) break;                        // uniform across the warp
-    uint8_t *cur = buf[k & 1];
-    const int cn = c + 32 * kSplit;
-    const bool has_next = cn < BN && e.n0 + cn < p.N;
-    __syncwarp();                                 // unit k-1's copy-out has read buf[(k+1)&1]
-    if (has_next) {
-      residual_prefetch<BN>(p, e, cn, buf[(k + 1) & 1]);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
+    cp_async_wait<0>();
     uint32_t r[32];
     tmem_ld32(e.taddr + c, r);
     tmem_ld_wait();
-    __syncwarp();                                 // every lane's copies into `cur` landed
+    __syncwarp();                                 // every lane's copies into buf landed
     float v[32];
-    if (p.resid_f32) stg_get_f32(cur, e.lane, v);
-    else stg_get_bf16(cur, e.lane, v);
+    if (p.resid_f32) stg_get_f32(buf, e.lane, v);
+    else stg_get_16(buf, e.lane, 0, v, p.resid_f16 != nullptr);
 #pragma unroll
     for (int q = 0; q < 32; ++q) v[q] += __uint_as_float(r[q]);
     if (p.out_f32) {
 #pragma unroll
       for (int q = 0; q < 32; ++q) part = fmaf(v[q], v[q], part);
-      stg_put_f32(cur, e.lane, v);                // own row only: no hazard with other lanes
+      stg_put_f32(buf, e.lane, v);                // own row only: no hazard with other lanes
     } else {
 #pragma unroll
       for (int q = 0; q < 32; ++q) {
@@ -274,11 +382,14 @@ __device__ __forceinline__ void epi_residual(const GemmParams &p, const EpiCtx &
     if (p.out) stg_put_16(st16, e.lane, 0, v, p.out_is_f16);
     __syncwarp();
     if (p.out_f32)
-      stg_to_global<8>(cur, 0, reinterpret_cast<uint8_t *>(p.out_f32 + row0_off + col),
+      stg_to_global<8>(buf, 0, reinterpret_cast<uint8_t *>(p.out_f32 + row0_off + col),
                        [&](int rr) { return rr * p.ldo * 4; }, e.rows_valid, e.lane);
     if (p.out)
       stg_to_global<4>(st16, 0, static_cast<uint8_t *>(p.out) + (row0_off + col) * 2,
                        [&](int rr) { return rr * p.ldo * 2; }, e.rows_valid, e.lane);
+    __syncwarp();                                 // copy-out has read buf and st16
+    const int cn = c + 32 * kSplit;
+    if (cn < BN && e.n0 + cn < p.N) residual_prefetch_lane<BN>(p, e, cn, buf);
   }
   cp_async_wait<0>();
   if (row_ok && p.ssq_out) atomicAdd(p.ssq_out + e.row0 + e.lane, part);
@@ -287,15 +398,16 @@ __device__ __forceinline__ void epi_residual(const GemmParams &p, const EpiCtx &
 // Gate and up columns come in groups of 64 + 64 per 128 accumulator columns;
 // a unit is one group: 64 outputs written as one 128-byte row segment.
 template <int BN>
-__device__ __forceinline__ void epi_swiglu(const GemmParams &p, const EpiCtx &e) {
+__device__ __forceinline__ void epi_swiglu(const GemmParams &p, EpiCtx &e) {
   const float rs = row_rstd(p, e.row0 + e.lane);
   const int I = p.N / 2;
+  const bool tma = p.epi_tma & kTmaOut;
   uint8_t *gbase = static_cast<uint8_t *>(p.out) + (long long)e.row0 * p.ldo * 2;
 #pragma unroll 1
   for (int grp = e.split; grp < BN / 128; grp += kSplit) {
     const int out_col = (e.n0 / 128 + grp) * 64;
     if (out_col >= I) break;                      // uniform across the warp
-    __syncwarp();
+    stg_reuse_wait<0>(e.lane);
 #pragma unroll 1
     for (int h = 0; h < 2; ++h) {
       uint32_t g[32], up[32];
@@ -311,9 +423,13 @@ __device__ __forceinline__ void epi_swiglu(const GemmParams &p, const EpiCtx &e)
       }
       stg_put_16(e.st, e.lane, 4 * h, v, p.out_is_f16);
     }
-    __syncwarp();
-    stg_to_global<8>(e.st, 0, gbase + (long long)out_col * 2,
-                     [&](int rr) { return rr * p.ldo * 2; }, e.rows_valid, e.lane);
+    if (tma) {
+      stg_tma_store(&e.maps->out, e.st, out_col, e.row0, e.lane, e.rows_valid);
+    } else {
+      __syncwarp();
+      stg_to_global<8>(e.st, 0, gbase + (long long)out_col * 2,
+                       [&](int rr) { return rr * p.ldo * 2; }, e.rows_valid, e.lane);
+    }
   }
   const bool row_ok = e.lane < e.rows_valid;
   if (e.n_blk == 0 && e.split == 0 && row_ok && p.ssq_zero) p.ssq_zero[e.row0 + e.lane] = 0.f;
@@ -322,10 +438,16 @@ __device__ __forceinline__ void epi_swiglu(const GemmParams &p, const EpiCtx &e)
 // Units of 64 accumulator columns of one head: for a q or k head the 32
 // rotation pairs (i, i + hd/2), i in [i0, i0 + 32); for a v head 64
 // consecutive columns.  Output rows of [B, heads, T, hd] are addressed per
-// row (a warp's 32 rows may cross a sequence boundary): each lane computes its
-// own row's destination and the copying lanes fetch it with a shuffle.
+// row.  When the warp's 32 rows are 32 tokens of one sequence (and hd = 64) a
+// head's 32 x 64 block is one TMA box: q and k rows go out through the
+// swizzled staging tile, V^T through a [64 dims][32 tokens] tile.  Otherwise
+// (a warp crossing a sequence, decode) each lane computes its own row's
+// destination and the copying lanes fetch it with a shuffle.
+// cos/sin come from a two-level table (fine rows 0..63: angle b*f_i; coarse
+// rows 64 + a: angle 64*a*f_i; pos = 64a + b) combined by the angle-sum
+// identities, which keeps the table small enough to stay in L1.
 template <int BN, int HD>
-__device__ __forceinline__ void epi_qkv_rope(const GemmParams &p, const EpiCtx &e) {
+__device__ __forceinline__ void epi_qkv_rope(const GemmParams &p, EpiCtx &e) {
   const int row = e.row0 + e.lane;
   const bool row_ok = e.lane < e.rows_valid;
   const float rs = row_rstd(p, row);
@@ -337,13 +459,17 @@ __device__ __forceinline__ void epi_qkv_rope(const GemmParams &p, const EpiCtx &
     pos += pa < 0 ? 0 : (pa > p.pos_limit ? p.pos_limit : pa);
   }
   pos = pos < 0 ? 0 : (pos >= p.max_pos ? p.max_pos - 1 : pos);
-  const float4 *cs4 = reinterpret_cast<const float4 *>(p.rope + (long long)pos * (HD / 2));
+  const float4 *fine4 = reinterpret_cast<const float4 *>(p.rope) + (pos & 63) * (HD / 4);
+  const float4 *coarse4 = reinterpret_cast<const float4 *>(p.rope) + (64 + (pos >> 6)) * (HD / 4);
   // element offsets of (b, head 0, t, 0) in [B, H, T, hd] and [B, KV, T, hd]
   const long long q_row = ((long long)b * p.H * p.T + t) * HD;
   const long long kv_row = ((long long)b * p.KV * p.T + t) * HD;
   const long long head_stride = (long long)p.T * HD;
   const int n_heads_total = p.H + 2 * p.KV;
   constexpr int kUnitsPerHead = HD / 64;
+  // whole-warp TMA boxes: 32 existing rows that are tokens t0..t0+31 of one sequence
+  const int wb = min(e.row0, p.M - 1) / p.T, wt0 = min(e.row0, p.M - 1) - wb * p.T;
+  const bool warp_box = HD == 64 && (p.epi_tma & kTmaQkv) && e.rows_valid == 32 && wt0 + 31 < p.T;
 #pragma unroll 1
   for (int u = e.split; u < BN / 64; u += kSplit) {
     const int hh = u / kUnitsPerHead, j = u - hh * kUnitsPerHead;
@@ -366,13 +492,16 @@ __device__ __forceinline__ void epi_qkv_rope(const GemmParams &p, const EpiCtx &
       tmem_ld_wait();
 #pragma unroll
       for (int k = 0; k < 32; k += 2) {
-        const float4 c = cs4[(i0 + k) >> 1];      // (cos, sin) of pairs i0+k and i0+k+1
+        const float4 f = fine4[(i0 + k) >> 1];    // (cos, sin) of b*f for pairs i0+k, i0+k+1
+        const float4 g = coarse4[(i0 + k) >> 1];  // the same for 64*a*f
+        const float c0 = g.x * f.x - g.y * f.y, s0 = g.y * f.x + g.x * f.y;
+        const float c1 = g.z * f.z - g.w * f.w, s1 = g.w * f.z + g.z * f.w;
         const float a0 = __uint_as_float(x1[k]) * rs, b0 = __uint_as_float(x2[k]) * rs;
         const float a1 = __uint_as_float(x1[k + 1]) * rs, b1 = __uint_as_float(x2[k + 1]) * rs;
-        y1[k] = a0 * c.x - b0 * c.y;
-        y2[k] = a0 * c.y + b0 * c.x;
-        y1[k + 1] = a1 * c.z - b1 * c.w;
-        y2[k + 1] = a1 * c.w + b1 * c.z;
+        y1[k] = a0 * c0 - b0 * s0;
+        y2[k] = a0 * s0 + b0 * c0;
+        y1[k + 1] = a1 * c1 - b1 * s1;
+        y2[k + 1] = a1 * s1 + b1 * c1;
       }
       seg1 = i0;
       seg2 = HD / 2 + i0;
@@ -391,61 +520,80 @@ __device__ __forceinline__ void epi_qkv_rope(const GemmParams &p, const EpiCtx &
       seg2 = i0 + 32;
     }
     if (!is_q && !is_k && p.v_t) {
-      // V transposed ([B, KV, hd, T_pad]): stage the 32 x 64 block, then each
-      // lane writes 8 consecutive tokens of one dimension (16 bytes when the
-      // 8 rows are consecutive tokens of one sequence starting at a multiple
-      // of 8, element by element otherwise).
-      __syncwarp();
-      stg_put_16(e.st, e.lane, 0, y1, true);
-      stg_put_16(e.st, e.lane, 4, y2, true);
-      __syncwarp();
-      const long long my_vt = ((long long)b * p.KV + hsub) * HD * p.T_pad + t;
-      const int tg = e.lane & 3;
-      long long vrow[8];
+      // V transposed ([B, KV, hd, T_pad]), keys contiguous
+      uint8_t *tile = e.st + (e.seq++ & 1u) * kStgBytes;
+      stg_reuse_wait<1>(e.lane);
+      if (warp_box && (wt0 & 7) == 0) {
+        // [64 dims][32 tokens] tile, one TMA box at (token t0, row (b, kv head, dim 0))
+        __half *tt = reinterpret_cast<__half *>(tile);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) vrow[i] = __shfl_sync(0xffffffffu, my_vt, 8 * tg + i);
-      const bool fast = (8 * tg + 7 < e.rows_valid) && (vrow[7] == vrow[0] + 7) && ((vrow[0] & 7) == 0);
+        for (int k = 0; k < 32; ++k) {
+          tt[k * 32 + e.lane] = __float2half_rn(y1[k]);
+          tt[(32 + k) * 32 + e.lane] = __float2half_rn(y2[k]);
+        }
+        stg_tma_store(&e.maps->vt, tile, wt0, (wb * p.KV + hsub) * HD, e.lane, e.rows_valid);
+      } else {
+        // stage the 32 x 64 block, then each lane writes 8 consecutive tokens
+        // of one dimension (16 bytes when the 8 rows are consecutive tokens of
+        // one sequence starting at a multiple of 8, element by element otherwise)
+        stg_put_16(tile, e.lane, 0, y1, true);
+        stg_put_16(tile, e.lane, 4, y2, true);
+        __syncwarp();
+        const long long my_vt = ((long long)b * p.KV + hsub) * HD * p.T_pad + t;
+        const int tg = e.lane & 3;
+        long long vrow[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) vrow[i] = __shfl_sync(0xffffffffu, my_vt, 8 * tg + i);
+        const bool fast = (8 * tg + 7 < e.rows_valid) && (vrow[7] == vrow[0] + 7) && ((vrow[0] & 7) == 0);
 #pragma unroll 1
-      for (int it = 0; it < 8; ++it) {
-        const int dd = it * 8 + (e.lane >> 2);    // dimension within this 64-wide unit
-        uint16_t val[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          val[i] = *reinterpret_cast<const uint16_t *>(e.st + stg_off(8 * tg + i, dd >> 3) + (dd & 7) * 2);
-        const long long dim_off = (long long)(seg1 + dd) * p.T_pad;
-        uint16_t *vt = reinterpret_cast<uint16_t *>(p.v_t);
-        if (fast) {
-          uint4 w;
-          w.x = val[0] | (uint32_t(val[1]) << 16);
-          w.y = val[2] | (uint32_t(val[3]) << 16);
-          w.z = val[4] | (uint32_t(val[5]) << 16);
-          w.w = val[6] | (uint32_t(val[7]) << 16);
-          *reinterpret_cast<uint4 *>(vt + vrow[0] + dim_off) = w;
-        } else {
+        for (int it = 0; it < 8; ++it) {
+          const int dd = it * 8 + (e.lane >> 2);  // dimension within this 64-wide unit
+          uint16_t val[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            if (8 * tg + i < e.rows_valid) vt[vrow[i] + dim_off] = val[i];
+            val[i] = *reinterpret_cast<const uint16_t *>(tile + stg_off(8 * tg + i, dd >> 3) + (dd & 7) * 2);
+          const long long dim_off = (long long)(seg1 + dd) * p.T_pad;
+          uint16_t *vt = reinterpret_cast<uint16_t *>(p.v_t);
+          if (fast) {
+            uint4 w;
+            w.x = val[0] | (uint32_t(val[1]) << 16);
+            w.y = val[2] | (uint32_t(val[3]) << 16);
+            w.z = val[4] | (uint32_t(val[5]) << 16);
+            w.w = val[6] | (uint32_t(val[7]) << 16);
+            *reinterpret_cast<uint4 *>(vt + vrow[0] + dim_off) = w;
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              if (8 * tg + i < e.rows_valid) vt[vrow[i] + dim_off] = val[i];
+          }
         }
+        stg_empty_group(e.lane);
       }
       dst = nullptr;                              // the row-layout f16 copy is not needed
-      if (dst_bf == nullptr) continue;
     }
     const bool contiguous = seg2 == seg1 + 32;    // both segments form one 128-byte row piece
 #pragma unroll 1
     for (int pass = 0; pass < 2; ++pass) {
       void *base = pass == 0 ? static_cast<void *>(dst) : static_cast<void *>(dst_bf);
       if (base == nullptr) continue;              // uniform across the warp
-      __syncwarp();
-      stg_put_16(e.st, e.lane, 0, y1, pass == 0);
-      stg_put_16(e.st, e.lane, 4, y2, pass == 0);
+      uint8_t *tile = e.st + (e.seq++ & 1u) * kStgBytes;
+      stg_reuse_wait<1>(e.lane);
+      stg_put_16(tile, e.lane, 0, y1, pass == 0);
+      stg_put_16(tile, e.lane, 4, y2, pass == 0);
+      if (pass == 0 && warp_box && (is_q || is_k)) {
+        const int y = ((wb * (is_q ? p.H : p.KV)) + hsub) * p.T + wt0;
+        stg_tma_store(is_q ? &e.maps->q : &e.maps->k, tile, 0, y, e.lane, e.rows_valid);
+        continue;
+      }
       __syncwarp();
       uint8_t *g = static_cast<uint8_t *>(base);
       if (contiguous) {
-        stg_to_global<8>(e.st, 0, g + seg1 * 2, row_off, e.rows_valid, e.lane);
+        stg_to_global<8>(tile, 0, g + seg1 * 2, row_off, e.rows_valid, e.lane);
       } else {
-        stg_to_global<4>(e.st, 0, g + seg1 * 2, row_off, e.rows_valid, e.lane);
-        stg_to_global<4>(e.st, 4, g + seg2 * 2, row_off, e.rows_valid, e.lane);
+        stg_to_global<4>(tile, 0, g + seg1 * 2, row_off, e.rows_valid, e.lane);
+        stg_to_global<4>(tile, 4, g + seg2 * 2, row_off, e.rows_valid, e.lane);
       }
+      stg_empty_group(e.lane);
     }
   }
   if (e.n_blk == 0 && e.split == 0 && row_ok && p.ssq_zero) p.ssq_zero[row] = 0.f;
@@ -455,7 +603,7 @@ __device__ __forceinline__ void epi_qkv_rope(const GemmParams &p, const EpiCtx &
 template <int BN, int EPI, int HD, int PAIR>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const GemmParams p) {
+                   const __grid_constant__ EpiMaps maps, const GemmParams p) {
   using C = GemmCfg<BN, EPI, PAIR>;
   static_assert(PAIR == 1 || PAIR == 2, "one CTA or a CTA pair");
   static_assert((BN / PAIR) % 8 == 0, "B share must be whole 8-row swizzle atoms");
@@ -471,7 +619,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t *tfull = bars + 2 * C::STAGES;
   uint64_t *tempty = tfull + 2;
   uint64_t *drain = tempty + 2;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  uint64_t *rbar = drain + 1;                       // one per epilogue warp (residual loads)
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(rbar + kEpiWarps);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -497,6 +646,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&tempty[a], PAIR * kEpiWarps);   // one arrival per epilogue warp (of both CTAs)
     }
     mbar_init(drain, 1);
+    for (int w = 0; w < kEpiWarps; ++w) mbar_init(&rbar[w], 1);
     *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
@@ -630,6 +780,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     e.lane = lane;
     e.split = (warp - 2) >> 2;                    // which share of the tile's columns
     e.st = sEpi + (warp - 2) * EpiStage<EPI>::kPerWarp;
+    e.maps = &maps;
+    e.rbar = &rbar[warp - 2];
+    e.rphase = 0;
+    e.seq = 0;
+    const bool resid_tma = EPI == kEpiResidual && (p.epi_tma & kTmaResid);
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = first_tile; tile < num_tiles; tile += tile_step) {
       const int m_grp = p.raster_m ? tile % num_mg : tile / num_n;
@@ -640,9 +795,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       e.n0 = n_blk * BN;
       e.n_blk = n_blk;
       if constexpr (EPI == kEpiResidual) {
-        // start fetching this warp's first residual unit while the MMAs run
-        __syncwarp();
-        if (e.n0 + e.split * 32 < p.N) residual_prefetch<BN>(p, e, e.split * 32, e.st);
+        // start fetching this warp's residual while the MMAs run
+        if (resid_tma) {
+          residual_load_tma<BN>(p, e);
+        } else {
+          __syncwarp();
+          if (e.n0 + e.split * 32 < p.N) residual_prefetch_lane<BN>(p, e, e.split * 32, e.st);
+        }
       }
       // every lane waits; the outcome is made warp-uniform because the TMEM
       // loads below are warp-collective
@@ -651,14 +810,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (lane == 0) record_status(p.status, kDevTimeoutEpilogue);
         *abort_flag = 1;
         cp_async_wait<0>();                       // no copy in flight when the CTA exits
+        if (resid_tma && residual_units<BN>(p, e) > 0) {
+          int dummy = 0;
+          mbar_wait_bounded(e.rbar, e.rphase, reinterpret_cast<volatile int *>(&dummy));
+        }
         break;
       }
       tc_fence_after_sync();
       e.taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
-      if constexpr (EPI == kEpiScale) epi_scale<BN>(p, e);
-      else if constexpr (EPI == kEpiResidual) epi_residual<BN>(p, e);
-      else if constexpr (EPI == kEpiSwiglu) epi_swiglu<BN>(p, e);
-      else epi_qkv_rope<BN, HD>(p, e);
+      if constexpr (EPI == kEpiScale) {
+        epi_scale<BN>(p, e);
+      } else if constexpr (EPI == kEpiResidual) {
+        if (resid_tma) {
+          if (!epi_residual_tma<BN>(p, e, abort_flag)) {
+            if (lane == 0) record_status(p.status, kDevTimeoutEpilogue);
+            *abort_flag = 1;
+            break;
+          }
+        } else {
+          epi_residual_lane<BN>(p, e);
+        }
+      } else if constexpr (EPI == kEpiSwiglu) {
+        epi_swiglu<BN>(p, e);
+      } else {
+        epi_qkv_rope<BN, HD>(p, e);
+      }
       tc_fence_before_sync();
       __syncwarp();
       // the accumulator may be overwritten once every warp's tcgen05.ld has
@@ -669,6 +845,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
+    if (lane == 0) bulk_wait_group<0>();          // this warp's TMA stores are complete
   }
 
   tc_fence_before_sync();
@@ -701,35 +878,42 @@ static EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-bool make_tmap_f16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
-                   uint64_t row_pitch_elems, uint32_t box_rows) {
+bool make_tmap_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                  uint64_t row_pitch_elems, uint32_t box_cols, uint32_t box_rows, bool swizzle128) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {row_pitch_elems * 2};
-  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims,
-                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+bool make_tmap_f16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                   uint64_t row_pitch_elems, uint32_t box_rows) {
+  return make_tmap_2d(map, base, rows, cols, row_pitch_elems, 64, box_rows, true);
 }
 
 namespace {
 struct TmapKey {
   const void *base;
   uint64_t rows, cols, pitch;
-  uint32_t box;
-  int dev;
+  uint32_t box_cols, box_rows;
+  int swz, dev;
   bool operator==(const TmapKey &o) const {
-    return base == o.base && rows == o.rows && cols == o.cols && pitch == o.pitch && box == o.box &&
-           dev == o.dev;
+    return base == o.base && rows == o.rows && cols == o.cols && pitch == o.pitch &&
+           box_cols == o.box_cols && box_rows == o.box_rows && swz == o.swz && dev == o.dev;
   }
 };
 struct TmapKeyHash {
   size_t operator()(const TmapKey &k) const {
     size_t h = reinterpret_cast<uintptr_t>(k.base);
-    for (uint64_t v : {k.rows, k.cols, k.pitch, (uint64_t)k.box, (uint64_t)k.dev})
+    for (uint64_t v : {k.rows, k.cols, k.pitch, (uint64_t)k.box_cols, (uint64_t)k.box_rows,
+                       (uint64_t)k.swz, (uint64_t)k.dev})
       h = h * 1000003u ^ static_cast<size_t>(v);
     return h;
   }
@@ -739,11 +923,11 @@ std::unordered_map<TmapKey, CUtensorMap, TmapKeyHash> g_tmap_cache;
 constexpr size_t kTmapCacheMax = 4096;
 }  // namespace
 
-bool get_tmap_f16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
-                  uint64_t row_pitch_elems, uint32_t box_rows) {
+bool get_tmap_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                 uint64_t row_pitch_elems, uint32_t box_cols, uint32_t box_rows, bool swizzle128) {
   int dev = 0;
   cudaGetDevice(&dev);
-  const TmapKey key{base, rows, cols, row_pitch_elems, box_rows, dev};
+  const TmapKey key{base, rows, cols, row_pitch_elems, box_cols, box_rows, swizzle128 ? 1 : 0, dev};
   {
     std::lock_guard<std::mutex> lock(g_tmap_mu);
     auto it = g_tmap_cache.find(key);
@@ -752,11 +936,16 @@ bool get_tmap_f16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t co
       return true;
     }
   }
-  if (!make_tmap_f16(map, base, rows, cols, row_pitch_elems, box_rows)) return false;
+  if (!make_tmap_2d(map, base, rows, cols, row_pitch_elems, box_cols, box_rows, swizzle128)) return false;
   std::lock_guard<std::mutex> lock(g_tmap_mu);
   if (g_tmap_cache.size() >= kTmapCacheMax) g_tmap_cache.clear();
   g_tmap_cache.emplace(key, *map);
   return true;
+}
+
+bool get_tmap_f16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                  uint64_t row_pitch_elems, uint32_t box_rows) {
+  return get_tmap_2d(map, base, rows, cols, row_pitch_elems, 64, box_rows, true);
 }
 
 int gemm_pick_bn(int epi, int N, int hd) {
@@ -805,8 +994,8 @@ static int max_active_clusters(cudaLaunchConfig_t cfg, int fallback) {
 }
 
 template <int BN, int EPI, int HD, int PAIR>
-static cudaError_t launch_pair(const CUtensorMap &ta, const CUtensorMap &tb, const GemmParams &p,
-                               int num_sms, cudaStream_t stream) {
+static cudaError_t launch_pair(const CUtensorMap &ta, const CUtensorMap &tb, const EpiMaps &maps,
+                               const GemmParams &p, int num_sms, cudaStream_t stream) {
   using C = GemmCfg<BN, EPI, PAIR>;
   constexpr auto kern = gemm_tc_kernel<BN, EPI, HD, PAIR>;
   cudaError_t e = ensure_smem_attr<kern>(C::SMEM_BYTES);
@@ -814,7 +1003,7 @@ static cudaError_t launch_pair(const CUtensorMap &ta, const CUtensorMap &tb, con
   const long long groups = cdiv(cdiv(p.M, C::BM), PAIR) * cdiv(p.N, BN);
   if constexpr (PAIR == 1) {
     const int grid = static_cast<int>(groups < num_sms ? groups : num_sms);
-    kern<<<grid, kGemmThreads, C::SMEM_BYTES, stream>>>(ta, tb, p);
+    kern<<<grid, kGemmThreads, C::SMEM_BYTES, stream>>>(ta, tb, maps, p);
     return cudaGetLastError();
   } else {
     cudaLaunchAttribute attr[1];
@@ -832,17 +1021,17 @@ static cudaError_t launch_pair(const CUtensorMap &ta, const CUtensorMap &tb, con
     const long long pairs_max = max_active_clusters<kern>(cfg, num_sms / PAIR);
     const long long pairs = groups < pairs_max ? groups : pairs_max;
     cfg.gridDim = dim3(static_cast<unsigned>(pairs * PAIR));
-    return cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
+    return cudaLaunchKernelEx(&cfg, kern, ta, tb, maps, p);
   }
 }
 
 static int gemm_pair(const GemmParams &p) { return cdiv(p.M, 128) >= kPairMinMBlocks ? 2 : 1; }
 
 template <int BN, int EPI, int HD>
-static cudaError_t launch_impl(const CUtensorMap &ta, const CUtensorMap &tb, const GemmParams &p,
-                               int num_sms, cudaStream_t stream) {
-  if (gemm_pair(p) == 1) return launch_pair<BN, EPI, HD, 1>(ta, tb, p, num_sms, stream);
-  return launch_pair<BN, EPI, HD, 2>(ta, tb, p, num_sms, stream);
+static cudaError_t launch_impl(const CUtensorMap &ta, const CUtensorMap &tb, const EpiMaps &maps,
+                               const GemmParams &p, int num_sms, cudaStream_t stream) {
+  if (gemm_pair(p) == 1) return launch_pair<BN, EPI, HD, 1>(ta, tb, maps, p, num_sms, stream);
+  return launch_pair<BN, EPI, HD, 2>(ta, tb, maps, p, num_sms, stream);
 }
 
 cudaError_t launch_gemm(int epi, int bn, const void *A, const void *B, const GemmParams &p_in,
@@ -853,31 +1042,52 @@ cudaError_t launch_gemm(int epi, int bn, const void *A, const void *B, const Gem
   if (!get_tmap_f16(&ta, A, p.M, p.K, p.K, 128)) return cudaErrorInvalidValue;
   // each CTA of a pair loads half of the B box
   if (!get_tmap_f16(&tb, B, p.N, p.K, p.K, bn / gemm_pair(p))) return cudaErrorInvalidValue;
+  // epilogue tensor maps (a map that cannot be encoded leaves its per-lane path in use)
+  EpiMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  p.epi_tma = 0;
+  if ((epi == kEpiScale || epi == kEpiSwiglu) && p.out) {
+    const uint64_t cols = epi == kEpiSwiglu ? p.N / 2 : p.N;
+    if (get_tmap_2d(&maps.out, p.out, p.M, cols, p.ldo, 64, 32, true)) p.epi_tma |= kTmaOut;
+  }
+  if (epi == kEpiResidual && p.out && !p.out_f32 && !p.resid_f32) {
+    const void *r16 = p.resid_f16 ? static_cast<const void *>(p.resid_f16) : static_cast<const void *>(p.resid);
+    if (r16 && get_tmap_2d(&maps.out, p.out, p.M, p.N, p.ldo, 64, 32, true) &&
+        get_tmap_2d(&maps.resid, r16, p.M, p.N, p.ldo, 64, 32, true))
+      p.epi_tma |= kTmaOut | kTmaResid;
+  }
+  if (epi == kEpiQkvRope && p.hd == 64 && p.T >= 32 && p.q && p.k && p.v_t && p.M % p.T == 0) {
+    const uint64_t Bq = (uint64_t)(p.M / p.T);
+    if (get_tmap_2d(&maps.q, p.q, Bq * p.H * p.T, 64, 64, 64, 32, true) &&
+        get_tmap_2d(&maps.k, p.k, Bq * p.KV * p.T, 64, 64, 64, 32, true) &&
+        get_tmap_2d(&maps.vt, p.v_t, Bq * p.KV * 64, p.T, p.T_pad, 32, 64, false))
+      p.epi_tma |= kTmaQkv;
+  }
   switch (epi) {
     case kEpiScale:
-      if (bn == 256) return launch_impl<256, kEpiScale, 64>(ta, tb, p, num_sms, stream);
-      if (bn == 192) return launch_impl<192, kEpiScale, 64>(ta, tb, p, num_sms, stream);
-      if (bn == 128) return launch_impl<128, kEpiScale, 64>(ta, tb, p, num_sms, stream);
-      if (bn == 64) return launch_impl<64, kEpiScale, 64>(ta, tb, p, num_sms, stream);
+      if (bn == 256) return launch_impl<256, kEpiScale, 64>(ta, tb, maps, p, num_sms, stream);
+      if (bn == 192) return launch_impl<192, kEpiScale, 64>(ta, tb, maps, p, num_sms, stream);
+      if (bn == 128) return launch_impl<128, kEpiScale, 64>(ta, tb, maps, p, num_sms, stream);
+      if (bn == 64) return launch_impl<64, kEpiScale, 64>(ta, tb, maps, p, num_sms, stream);
       break;
     case kEpiResidual:
-      if (bn == 192) return launch_impl<192, kEpiResidual, 64>(ta, tb, p, num_sms, stream);
-      if (bn == 128) return launch_impl<128, kEpiResidual, 64>(ta, tb, p, num_sms, stream);
-      if (bn == 64) return launch_impl<64, kEpiResidual, 64>(ta, tb, p, num_sms, stream);
+      if (bn == 192) return launch_impl<192, kEpiResidual, 64>(ta, tb, maps, p, num_sms, stream);
+      if (bn == 128) return launch_impl<128, kEpiResidual, 64>(ta, tb, maps, p, num_sms, stream);
+      if (bn == 64) return launch_impl<64, kEpiResidual, 64>(ta, tb, maps, p, num_sms, stream);
       break;
     case kEpiSwiglu:
-      if (bn == 256) return launch_impl<256, kEpiSwiglu, 64>(ta, tb, p, num_sms, stream);
-      if (bn == 128) return launch_impl<128, kEpiSwiglu, 64>(ta, tb, p, num_sms, stream);
+      if (bn == 256) return launch_impl<256, kEpiSwiglu, 64>(ta, tb, maps, p, num_sms, stream);
+      if (bn == 128) return launch_impl<128, kEpiSwiglu, 64>(ta, tb, maps, p, num_sms, stream);
       break;
     case kEpiQkvRope:
       if (p.hd == 64) {
-        if (bn == 256) return launch_impl<256, kEpiQkvRope, 64>(ta, tb, p, num_sms, stream);
-        if (bn == 192) return launch_impl<192, kEpiQkvRope, 64>(ta, tb, p, num_sms, stream);
-        if (bn == 128) return launch_impl<128, kEpiQkvRope, 64>(ta, tb, p, num_sms, stream);
-        if (bn == 64) return launch_impl<64, kEpiQkvRope, 64>(ta, tb, p, num_sms, stream);
+        if (bn == 256) return launch_impl<256, kEpiQkvRope, 64>(ta, tb, maps, p, num_sms, stream);
+        if (bn == 192) return launch_impl<192, kEpiQkvRope, 64>(ta, tb, maps, p, num_sms, stream);
+        if (bn == 128) return launch_impl<128, kEpiQkvRope, 64>(ta, tb, maps, p, num_sms, stream);
+        if (bn == 64) return launch_impl<64, kEpiQkvRope, 64>(ta, tb, maps, p, num_sms, stream);
       } else if (p.hd == 128) {
-        if (bn == 256) return launch_impl<256, kEpiQkvRope, 128>(ta, tb, p, num_sms, stream);
-        if (bn == 128) return launch_impl<128, kEpiQkvRope, 128>(ta, tb, p, num_sms, stream);
+        if (bn == 256) return launch_impl<256, kEpiQkvRope, 128>(ta, tb, maps, p, num_sms, stream);
+        if (bn == 128) return launch_impl<128, kEpiQkvRope, 128>(ta, tb, maps, p, num_sms, stream);
       }
       break;
   }

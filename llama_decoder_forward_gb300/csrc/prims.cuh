@@ -156,6 +156,30 @@ __device__ __forceinline__ void tma_load_2d_pair(void *smem_dst, const CUtensorM
       : "memory");
 }
 
+// 2-D tiled store shared -> global (TMA), tracked as a bulk group of the
+// issuing thread.  Rows or columns outside the tensor are not written.  The
+// shared-memory source must have been written before a fence.proxy.async.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *smem_src, int x,
+                                             int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(smem_src)), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// At most N of this thread's bulk groups may still be reading shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// At most N of this thread's bulk groups may still be incomplete.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // ---------------------------------------------------------------- cp.async
 // 16-byte asynchronous global -> shared copy; with valid == false the 16
 // bytes are zero-filled and nothing is read.

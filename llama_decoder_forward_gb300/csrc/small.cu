@@ -127,18 +127,21 @@ __global__ void interleave_gate_up_kernel(const bf16 *__restrict__ wg, const bf1
   }
 }
 
-// table[pos][i] = (cos, sin)(pos * theta^(-2i/hd)) computed in double and
-// stored as fp32 ("model.py" (SmolLM2-135M) section 3 rope_freqs /
-// build_rope_cache; "components.py" RotaryEmbedding).  Exact integer positions.
+// Two-level RoPE table ("model.py" (SmolLM2-135M) section 3 rope_freqs /
+// build_rope_cache; "components.py" RotaryEmbedding): row r < 64 holds
+// (cos, sin)(r * f_i), row 64 + a holds (cos, sin)(64 * a * f_i), with
+// f_i = theta^(-2i/hd); angles in double, stored as fp32.  Position 64a + b
+// is recovered as cos = C_a C_b - S_a S_b, sin = S_a C_b + C_a S_b.
 __global__ void rope_table_kernel(int max_pos, int hd, double theta, float2 *__restrict__ table) {
   const int half = hd / 2;
-  const long long n = (long long)max_pos * half;
+  const long long n = rope_table_rows(max_pos) * half;
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < n;
        idx += (long long)gridDim.x * blockDim.x) {
-    const long long pos = idx / half;
-    const int i = static_cast<int>(idx - pos * half);
+    const long long row = idx / half;
+    const int i = static_cast<int>(idx - row * half);
     const double inv_freq = pow(theta, -2.0 * i / hd);
-    const double ang = static_cast<double>(pos) * inv_freq;
+    const double pos = row < 64 ? static_cast<double>(row) : 64.0 * static_cast<double>(row - 64);
+    const double ang = pos * inv_freq;
     table[idx] = make_float2(static_cast<float>(cos(ang)), static_cast<float>(sin(ang)));
   }
 }
@@ -183,7 +186,7 @@ cudaError_t launch_interleave_gate_up(const bf16 *wg, const bf16 *wu, const bf16
 }
 
 cudaError_t launch_rope_table(int max_pos, int hd, float theta, float2 *table, cudaStream_t stream) {
-  rope_table_kernel<<<grid_for((long long)max_pos * (hd / 2), 256), 256, 0, stream>>>(
+  rope_table_kernel<<<grid_for(rope_table_rows(max_pos) * (hd / 2), 256), 256, 0, stream>>>(
       max_pos, hd, static_cast<double>(theta), table);
   return cudaGetLastError();
 }

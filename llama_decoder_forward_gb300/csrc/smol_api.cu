@@ -32,7 +32,7 @@ PackLayout pack_layout(const smol_config *c, int n_layers, int with_embed) {
   PackLayout L{};
   const size_t d = c->hidden, hd = c->head_dim, H = c->n_heads, KV = c->n_kv_heads, I = c->intermediate;
   L.rope_off = 0;
-  L.rope_bytes = align_up((size_t)c->max_pos * (hd / 2) * sizeof(float2), 1024);
+  L.rope_bytes = align_up((size_t)rope_table_rows(c->max_pos) * (hd / 2) * sizeof(float2), 1024);
   L.layer0_off = L.rope_bytes;
   size_t o = 0;
   L.off_qkv = o; o = align_up(o + (H + 2 * KV) * hd * d * 2, 1024);
@@ -52,7 +52,7 @@ PackLayout pack_layout(const smol_config *c, int n_layers, int with_embed) {
 }
 
 struct WsLayout {
-  size_t status, x, x32, h, h32, q, k, v, o, a, ssq_a, ssq_b;
+  size_t status, x, h, q, k, v, o, a, ssq_a, ssq_b;
   size_t total;
 };
 
@@ -68,9 +68,7 @@ WsLayout ws_layout(const smol_config *c, int B, int T) {
   size_t o = 0;
   W.status = o; o += 1024;
   W.x = o; o = align_up(o + M * d * 2, 1024);
-  W.x32 = o; o = align_up(o + M * d * 4, 1024);
   W.h = o; o = align_up(o + M * d * 2, 1024);
-  W.h32 = o; o = align_up(o + M * d * 4, 1024);
   W.q = o; o = align_up(o + M * H * hd * 2, 1024);
   W.k = o; o = align_up(o + M * KV * hd * 2, 1024);
   W.v = o; o = align_up(o + v_elems * 2, 1024);
@@ -155,7 +153,8 @@ LayerPtrs layer_ptrs(const smol_config *c, const void *packed, int layer) {
 // Where one block reads its input and writes its output.
 struct BlockIO {
   const f16 *x16;         // f16 copy of the input: the QKV GEMM operand
-  const bf16 *resid_bf;   // residual input in bf16, or
+  const f16 *resid_f16;   // residual input in f16 (the model's residual stream), or
+  const bf16 *resid_bf;   //   in bf16, or
   const float *resid_f32; //   in fp32
   void *out16;            // 16-bit output (may alias the input) or nullptr
   int out16_is_f16;
@@ -165,7 +164,7 @@ struct BlockIO {
 
 // One decoder block on M = B*T rows.  ssq_a holds the per-row sum of squares
 // of the input; the output's sum of squares is accumulated into ssq_a (which
-// is cleared in between).  The block-internal residual h is kept in fp32.
+// is cleared in between).  The block-internal residual h is kept in f16.
 int run_block(const smol_config *c, const void *packed, int layer, const BlockIO &io, int B, int T,
               const int32_t *valid_start, const WsLayout &W, uint8_t *ws, int sms, cudaStream_t st) {
   const long long M = (long long)B * T;
@@ -180,7 +179,6 @@ int run_block(const smol_config *c, const void *packed, int layer, const BlockIO
   f16 *v = reinterpret_cast<f16 *>(ws + W.v);
   f16 *o = reinterpret_cast<f16 *>(ws + W.o);
   f16 *h = reinterpret_cast<f16 *>(ws + W.h);
-  float *h32 = reinterpret_cast<float *>(ws + W.h32);
   f16 *a = reinterpret_cast<f16 *>(ws + W.a);
 
   // 1. RMSNorm1 + QKV projection + RoPE (norm weight folded into W)
@@ -215,11 +213,11 @@ int run_block(const smol_config *c, const void *packed, int layer, const BlockIO
     LAUNCH_K(SMOL_K_ATTN, st, launch_flash_attention(ap, st));
   }
 
-  // 3. O projection + residual: h = x + o Wo^T (fp32 and f16), ssq_b += rowsum(h^2)
+  // 3. O projection + residual: h = x + o Wo^T (f16), ssq_b += rowsum(h^2)
   GemmParams po{};
   po.M = (int)M; po.N = d; po.K = H * hd;
-  po.out = h; po.out_is_f16 = 1; po.out_f32 = h32; po.ldo = d; po.ssq_out = ssq_b; po.status = status;
-  po.resid = io.resid_bf; po.resid_f32 = io.resid_f32;
+  po.out = h; po.out_is_f16 = 1; po.ldo = d; po.ssq_out = ssq_b; po.status = status;
+  po.resid = io.resid_bf; po.resid_f16 = io.resid_f16; po.resid_f32 = io.resid_f32;
   LAUNCH_K(SMOL_K_OPROJ, st, launch_gemm(kEpiResidual, gemm_pick_bn(kEpiResidual, d, hd), o, lp.o, po, sms, st));
 
   // 4. RMSNorm2 + gate/up + SwiGLU: a = silu(g) * u ; clears ssq_a for step 5
@@ -233,7 +231,7 @@ int run_block(const smol_config *c, const void *packed, int layer, const BlockIO
   GemmParams pd{};
   pd.M = (int)M; pd.N = d; pd.K = I;
   pd.out = io.out16; pd.out_is_f16 = io.out16_is_f16; pd.out_f32 = io.out_f32; pd.ldo = d;
-  pd.resid_f32 = h32; pd.ssq_out = ssq_a; pd.status = status;
+  pd.resid_f16 = h; pd.ssq_out = ssq_a; pd.status = status;
   LAUNCH_K(SMOL_K_DOWN, st, launch_gemm(kEpiResidual, gemm_pick_bn(kEpiResidual, d, hd), a, lp.down, pd, sms, st));
   return SMOL_OK;
 }
@@ -376,16 +374,15 @@ SMOL_API int smol_model_forward(const smol_config *cfg, const void *packed, cons
   const PackLayout L = pack_layout(cfg, cfg->n_layers, 1);
   const uint8_t *pk = static_cast<const uint8_t *>(packed);
   f16 *x = reinterpret_cast<f16 *>(wsb + W.x);
-  float *x32 = reinterpret_cast<float *>(wsb + W.x32);
   float *ssq_a = reinterpret_cast<float *>(wsb + W.ssq_a);
   LAUNCH_K(SMOL_K_EMBED, st, launch_embed_rows(ids, reinterpret_cast<const bf16 *>(pk + L.embed_off), cfg->vocab,
-                           cfg->hidden, M, x, x32, ssq_a, st));
+                           cfg->hidden, M, x, nullptr, ssq_a, st));
+  // the residual stream is f16: each block reads x and writes its output over it
   BlockIO io{};
   io.x16 = x;
-  io.resid_f32 = x32;
+  io.resid_f16 = x;
   io.out16 = x;
   io.out16_is_f16 = 1;
-  io.out_f32 = x32;
   for (int l = 0; l < cfg->n_layers; ++l) {
     rc = run_block(cfg, packed, l, io, B, T, valid_start, W, wsb, sms, st);
     if (rc) return rc;

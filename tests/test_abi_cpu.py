@@ -46,7 +46,7 @@ def test_size_queries(smol):
     cfg = _cfg(smol)
     d, hd, H, KV, I, V = 576, 64, 9, 3, 1536, 49152
     layer = (H + 2 * KV) * hd * d * 2 + d * H * hd * 2 + 2 * I * d * 2 + d * I * 2
-    rope = 8192 * (hd // 2) * 8
+    rope = (64 + 8192 // 64) * (hd // 2) * 8     # two-level (cos, sin) table
     total = smol.packed_bytes(cfg, 30, True)
     assert total >= rope + 30 * layer + 2 * V * d * 2
     assert total < rope + 30 * layer + 2 * V * d * 2 + 64 * 1024
