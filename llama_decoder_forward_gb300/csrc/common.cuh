@@ -18,9 +18,13 @@ typedef __half f16;
 
 __host__ __device__ constexpr long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 
-// RoPE table: rows 0..63 hold (cos, sin)(b * f_i), rows 64 + a hold
-// (cos, sin)(64 * a * f_i), i < hd/2; a position 64a + b combines the two by
-// the angle-sum identities.
+// RoPE table, two levels: a position pos = 64a + b is recovered from
+// (cos, sin)(b f_i) and (cos, sin)(64 a f_i) by the angle-sum identities.
+// Stored as float4 entries holding pairs i = 2j and 2j + 1:
+//   fine   entry (j, b), b < 64:          index j * 64 + b
+//   coarse entry (j, a), a < cdiv(max_pos, 64): index (hd/4) * 64 + j * cdiv(max_pos, 64) + a
+// so that consecutive positions are consecutive entries (coalesced loads).
+// rope_table_rows counts float2 rows of hd/2 entries each.
 __host__ __device__ constexpr long long rope_table_rows(int max_pos) { return 64 + cdiv(max_pos, 64); }
 
 // ------------------------------------------------------------------ GEMM

@@ -443,9 +443,9 @@ __device__ __forceinline__ void epi_swiglu(const GemmParams &p, EpiCtx &e) {
 // swizzled staging tile, V^T through a [64 dims][32 tokens] tile.  Otherwise
 // (a warp crossing a sequence, decode) each lane computes its own row's
 // destination and the copying lanes fetch it with a shuffle.
-// cos/sin come from a two-level table (fine rows 0..63: angle b*f_i; coarse
-// rows 64 + a: angle 64*a*f_i; pos = 64a + b) combined by the angle-sum
-// identities, which keeps the table small enough to stay in L1.
+// cos/sin come from a two-level table (fine: angle b*f_i; coarse: angle
+// 64*a*f_i; pos = 64a + b) combined by the angle-sum identities: the fine
+// part stays in L1, and consecutive rows (positions) read consecutive entries.
 template <int BN, int HD>
 __device__ __forceinline__ void epi_qkv_rope(const GemmParams &p, EpiCtx &e) {
   const int row = e.row0 + e.lane;
@@ -459,8 +459,10 @@ __device__ __forceinline__ void epi_qkv_rope(const GemmParams &p, EpiCtx &e) {
     pos += pa < 0 ? 0 : (pa > p.pos_limit ? p.pos_limit : pa);
   }
   pos = pos < 0 ? 0 : (pos >= p.max_pos ? p.max_pos - 1 : pos);
-  const float4 *fine4 = reinterpret_cast<const float4 *>(p.rope) + (pos & 63) * (HD / 4);
-  const float4 *coarse4 = reinterpret_cast<const float4 *>(p.rope) + (64 + (pos >> 6)) * (HD / 4);
+  // entry (j, pos & 63) of the fine part and (j, pos >> 6) of the coarse part
+  const int n_coarse = static_cast<int>(cdiv(p.max_pos, 64));
+  const float4 *fine4 = reinterpret_cast<const float4 *>(p.rope) + (pos & 63);
+  const float4 *coarse4 = reinterpret_cast<const float4 *>(p.rope) + (HD / 4) * 64 + (pos >> 6);
   // element offsets of (b, head 0, t, 0) in [B, H, T, hd] and [B, KV, T, hd]
   const long long q_row = ((long long)b * p.H * p.T + t) * HD;
   const long long kv_row = ((long long)b * p.KV * p.T + t) * HD;
@@ -492,8 +494,9 @@ __device__ __forceinline__ void epi_qkv_rope(const GemmParams &p, EpiCtx &e) {
       tmem_ld_wait();
 #pragma unroll
       for (int k = 0; k < 32; k += 2) {
-        const float4 f = fine4[(i0 + k) >> 1];    // (cos, sin) of b*f for pairs i0+k, i0+k+1
-        const float4 g = coarse4[(i0 + k) >> 1];  // the same for 64*a*f
+        const int jj = (i0 + k) >> 1;             // pairs i0+k and i0+k+1
+        const float4 f = fine4[jj * 64];          // (cos, sin) of b*f
+        const float4 g = coarse4[jj * n_coarse];  // (cos, sin) of 64*a*f
         const float c0 = g.x * f.x - g.y * f.y, s0 = g.y * f.x + g.x * f.y;
         const float c1 = g.z * f.z - g.w * f.w, s1 = g.w * f.z + g.z * f.w;
         const float a0 = __uint_as_float(x1[k]) * rs, b0 = __uint_as_float(x2[k]) * rs;

@@ -128,21 +128,29 @@ __global__ void interleave_gate_up_kernel(const bf16 *__restrict__ wg, const bf1
 }
 
 // Two-level RoPE table ("model.py" (SmolLM2-135M) section 3 rope_freqs /
-// build_rope_cache; "components.py" RotaryEmbedding): row r < 64 holds
-// (cos, sin)(r * f_i), row 64 + a holds (cos, sin)(64 * a * f_i), with
-// f_i = theta^(-2i/hd); angles in double, stored as fp32.  Position 64a + b
-// is recovered as cos = C_a C_b - S_a S_b, sin = S_a C_b + C_a S_b.
-__global__ void rope_table_kernel(int max_pos, int hd, double theta, float2 *__restrict__ table) {
-  const int half = hd / 2;
-  const long long n = rope_table_rows(max_pos) * half;
+// build_rope_cache; "components.py" RotaryEmbedding), f_i = theta^(-2i/hd):
+// fine entries hold (cos, sin)(b f_i) for b < 64, coarse entries
+// (cos, sin)(64 a f_i); angles in double, stored as fp32, float4 entries of
+// the pairs i = 2j, 2j + 1, laid out position-fastest (see rope_table_rows).
+__global__ void rope_table_kernel(int max_pos, int hd, double theta, float4 *__restrict__ table) {
+  const int quarter = hd / 4;
+  const long long nc = cdiv(max_pos, 64);
+  const long long n = (64 + nc) * quarter;
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < n;
        idx += (long long)gridDim.x * blockDim.x) {
-    const long long row = idx / half;
-    const int i = static_cast<int>(idx - row * half);
-    const double inv_freq = pow(theta, -2.0 * i / hd);
-    const double pos = row < 64 ? static_cast<double>(row) : 64.0 * static_cast<double>(row - 64);
-    const double ang = pos * inv_freq;
-    table[idx] = make_float2(static_cast<float>(cos(ang)), static_cast<float>(sin(ang)));
+    long long j, pos;
+    if (idx < 64LL * quarter) {
+      j = idx / 64;
+      pos = idx - j * 64;
+    } else {
+      const long long r = idx - 64LL * quarter;
+      j = r / nc;
+      pos = 64 * (r - j * nc);
+    }
+    const double a0 = static_cast<double>(pos) * pow(theta, -2.0 * (2 * j) / hd);
+    const double a1 = static_cast<double>(pos) * pow(theta, -2.0 * (2 * j + 1) / hd);
+    table[idx] = make_float4(static_cast<float>(cos(a0)), static_cast<float>(sin(a0)),
+                             static_cast<float>(cos(a1)), static_cast<float>(sin(a1)));
   }
 }
 
@@ -186,8 +194,8 @@ cudaError_t launch_interleave_gate_up(const bf16 *wg, const bf16 *wu, const bf16
 }
 
 cudaError_t launch_rope_table(int max_pos, int hd, float theta, float2 *table, cudaStream_t stream) {
-  rope_table_kernel<<<grid_for(rope_table_rows(max_pos) * (hd / 2), 256), 256, 0, stream>>>(
-      max_pos, hd, static_cast<double>(theta), table);
+  rope_table_kernel<<<grid_for(rope_table_rows(max_pos) * (hd / 4), 256), 256, 0, stream>>>(
+      max_pos, hd, static_cast<double>(theta), reinterpret_cast<float4 *>(table));
   return cudaGetLastError();
 }
 
