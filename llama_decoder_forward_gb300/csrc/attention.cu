@@ -55,9 +55,10 @@ __global__ void __launch_bounds__(512, 1) flash_attn_kernel(const AttnParams p) 
   f16 *sK = sQ + G * BQ * HD;                                     // [2][BK][HD]
   f16 *sV = sK + 2 * BK * HD;                                     // [2][BK][HD]
 
-  const int nqb = gridDim.x;
-  const int qb = nqb - 1 - blockIdx.x;                            // longest blocks first
-  const int kvh = blockIdx.y, b = blockIdx.z;
+  // query block = slow launch index, descending: longest causal blocks first
+  const int nqb = gridDim.y;
+  const int qb = nqb - 1 - blockIdx.y;
+  const int kvh = blockIdx.x % p.KV, b = blockIdx.x / p.KV;
   const int q0 = qb * BQ;
   const int T = p.T;
   const int vs = p.valid_start ? min(max(p.valid_start[b], 0), T) : 0;
@@ -240,7 +241,7 @@ static cudaError_t launch_fa(const AttnParams &p, cudaStream_t stream) {
   auto kern = flash_attn_kernel<HD, BQ, BK>;
   cudaError_t e = ensure_smem_attr<flash_attn_kernel<HD, BQ, BK>>((int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)cdiv(p.T, BQ), (unsigned)p.KV, (unsigned)p.B);
+  dim3 grid((unsigned)(p.B * p.KV), (unsigned)cdiv(p.T, BQ), 1u);
   kern<<<grid, threads, smem, stream>>>(p);
   return cudaGetLastError();
 }
