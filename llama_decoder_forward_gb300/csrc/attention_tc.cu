@@ -6,24 +6,22 @@
 // probs @ v; query head h reads key/value head h // g as in the "SmolLM3"
 // page's "Grouped-query attention").  Rows with no visible key produce 0.
 //
-// One CTA owns (sequence b, kv head, a tile of 128 query tokens) and GH <= 3
-// query heads of that kv head.  Each K tile [64 keys x 64] and V^T tile
-// [64 x 64 keys] is loaded once by TMA into shared memory and serves all GH
-// heads: K/V are never expanded per query head.  Per (kv tile, head) "slot":
-//   S = Q_h K^T        tcgen05.mma, M=128 N=64 K=64, fp32 in TMEM
-//   P = exp2(S*c - m)  four softmax warps, one query row per thread (no
-//                      cross-thread reductions); P is written as packed f16
-//                      over S's own TMEM columns
-//   O_h += P V         tcgen05.mma with A (= P) read from TMEM, M=128 N=64 K=64
-// The CTA is serial (S, softmax, P V, next S) and small - 256 TMEM columns
-// (O for GH heads + one S tile) and ~100 KB of shared memory - so two CTAs
-// share an SM and the tensor core works for one while the other's softmax
-// runs (and one's prologue/epilogue overlaps the other's main loop).
+// One CTA owns (sequence b, kv head, a tile of 128 query tokens) and the GH
+// query heads of that kv head.  Each K tile [128 keys x 64] and V^T tile
+// [64 x 128 keys] is loaded once by TMA into shared memory and serves all GH
+// heads: K/V are never expanded per query head.  Per (kv tile, head):
+//   S = Q_h K^T        tcgen05.mma, M=128 N=128 K=64, fp32 in TMEM (two S buffers,
+//                      so the MMA for the next head runs while this one's softmax does)
+//   P = exp2(S*c - m)  eight softmax warps, one query row per thread per half tile; P is
+//                      written as packed f16 into the S buffer's own TMEM columns
+//   O_h += P V         tcgen05.mma with A (= P) read from TMEM, M=128 N=64 K=128, fp32
+//                      accumulator in TMEM; shared memory only feeds Q, K and V^T
 // The running max is updated lazily: O_h is rescaled in TMEM only when a row's
 // max grows by more than 2^8 (otherwise P may exceed 1 by up to 256, exact in
 // the fp32 sums and within f16 range), the FlashAttention-4 idea.
 // Warp 0 issues TMA, warp 1 allocates TMEM and one lane issues every MMA,
-// warps 2..5 do the softmax and the final normalisation.  All waits are
+// warps 2..9 (two groups of four, each taking half of every tile's keys) do
+// the softmax and the final normalisation.  All waits are
 // bounded (status word + abort flag, copies and MMAs drained before exit).
 #include <math.h>
 
@@ -35,27 +33,26 @@ namespace smol {
 namespace {
 
 constexpr int kBQ = 128;      // query rows per tile (UMMA M)
-constexpr int kBK = 64;       // keys per KV tile
+constexpr int kBK = 128;      // keys per KV tile
 constexpr int kHD = 64;
-constexpr int kNS = 3;        // K / V^T pipeline stages
-constexpr int kThreads = 192;   // producer, MMA, one softmax warpgroup
+constexpr int kThreads = 320;   // producer, MMA, two softmax warpgroups
 
 template <int GH>
 struct AtCfg {
   static constexpr int Q_BYTES = kBQ * kHD * 2;         // one head: [128][64] f16
-  static constexpr int K_BYTES = kBK * kHD * 2;         // [64 keys][64]
-  static constexpr int VT_BYTES = kHD * kBK * 2;        // [64 dims][64 keys]
+  static constexpr int K_BYTES = kBK * kHD * 2;         // [128 keys][64]
+  static constexpr int VT_SUB = kHD * 64 * 2;           // [64 dims][64 keys]
+  static constexpr int VT_BYTES = 2 * VT_SUB;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + GH * Q_BYTES;
-  static constexpr int OFF_VT = OFF_K + kNS * K_BYTES;
-  static constexpr int OFF_BAR = OFF_VT + kNS * VT_BYTES;
-  static constexpr int SMEM_RAW = 1024 + OFF_BAR + 256;
-  // at least 80 KB so that no third CTA (whose TMEM allocation would wait) joins two on an SM
-  static constexpr int SMEM = SMEM_RAW < 81920 ? 81920 : SMEM_RAW;
-  static constexpr int TMEM_S = GH * kHD;               // S (and P over its first 32 columns)
-  static constexpr int TMEM_COLS = 256;
-  static_assert(GH >= 1 && GH <= 3, "O accumulators and one S tile in 256 columns");
-  static_assert(SMEM <= 116736, "two CTAs per SM");
+  static constexpr int OFF_VT = OFF_K + 2 * K_BYTES;
+  static constexpr int OFF_RED = OFF_VT + 2 * VT_BYTES;  // [2][2][128] row maxes, [2][4][128] row sums
+  static constexpr int OFF_BAR = OFF_RED + (2 * 2 * 128 + 2 * 4 * 128) * 4;
+  static constexpr int SMEM = 1024 + OFF_BAR + 256;
+  static constexpr int TMEM_S = 256;                    // S buffers at columns 256 + sb*128;
+                                                        // P (f16) overwrites columns 0..63 of its S
+  static_assert(GH >= 1 && GH * kHD <= 256, "O accumulators must fit below the S buffers");
+  static_assert(SMEM <= 232448, "shared memory per CTA");
 };
 
 struct AtParams {
@@ -81,12 +78,34 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// AND of `pred` over the 256 softmax threads (named barrier 1); also a
+// barrier between the two softmax warpgroups.
+__device__ __forceinline__ bool softmax_and(bool pred) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, 256, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(out)
+      : "r"((uint32_t)pred)
+      : "memory");
+  return out != 0;
+}
+
+// max(a, b, c) in one instruction (three-input max of sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ void at_status(int *status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
 
 template <int GH>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmVt, const AtParams p) {
   using C = AtCfg<GH>;
@@ -98,13 +117,13 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint8_t *sVt = smem + C::OFF_VT;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
   uint64_t *q_full = bars;
-  uint64_t *kv_full = bars + 1;              // [kNS]
-  uint64_t *kv_empty = bars + 1 + kNS;       // [kNS]
-  uint64_t *s_full = bars + 1 + 2 * kNS;     // S(s) computed
-  uint64_t *p_full = s_full + 1;             // P(s) written (128 arrivals)
-  uint64_t *s_free = s_full + 2;             // P(s) V done: S/P columns free, O_h current
-  uint64_t *o_done = s_full + 3;             // every MMA of the CTA complete
-  uint64_t *drain = s_full + 4;
+  uint64_t *kv_full = bars + 1;     // [2]
+  uint64_t *kv_empty = bars + 3;    // [2]
+  uint64_t *s_full = bars + 5;      // [2] S(s) computed
+  uint64_t *s_free = bars + 7;      // [2] PV(s) done: the S/P columns may be overwritten
+  uint64_t *p_full = bars + 9;      // [2] P(s) written into TMEM
+  uint64_t *o_ready = bars + 13;    // [GH]
+  uint64_t *drain = bars + 13 + GH;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -128,14 +147,14 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int i = 0; i < kNS; ++i) {
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 1);
+      mbar_init(&p_full[i], 256);
     }
-    mbar_init(s_full, 1);
-    mbar_init(p_full, 128);
-    mbar_init(s_free, 1);
-    mbar_init(o_done, 1);
+    for (int h = 0; h < GH; ++h) mbar_init(&o_ready[h], 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -144,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     tma_prefetch_desc(&tmVt);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
   tc_fence_before_sync();
@@ -162,14 +181,16 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int h = 0; h < GH; ++h)
         tma_load_2d(sQ + h * C::Q_BYTES, &tmQ, q_full, 0, ((b * p.H) + h_first + h) * T + q0);
       for (int it = 0; it < ntiles && ok; ++it) {
-        const int j = j_lo + it, st = it % kNS;
-        if (!mbar_wait_bounded(&kv_empty[st], ((it / kNS) & 1) ^ 1, abort_flag)) {
+        const int j = j_lo + it, st = it & 1;
+        if (!mbar_wait_bounded(&kv_empty[st], ((it >> 1) & 1) ^ 1, abort_flag)) {
           ok = false;
           break;
         }
         mbar_arrive_expect_tx(&kv_full[st], C::K_BYTES + C::VT_BYTES);
         tma_load_2d(sK + st * C::K_BYTES, &tmK, &kv_full[st], 0, (b * p.KV + kvh) * T + j * kBK);
         tma_load_2d(sVt + st * C::VT_BYTES, &tmVt, &kv_full[st], j * kBK, (b * p.KV + kvh) * kHD);
+        tma_load_2d(sVt + st * C::VT_BYTES + C::VT_SUB, &tmVt, &kv_full[st], j * kBK + 64,
+                    (b * p.KV + kvh) * kHD);
         ++issued;
       }
       // wait (bounded) until every copy this thread issued has landed
@@ -178,9 +199,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (!ok) {
         at_status(p.status, kAtTimeoutLoad);
         *abort_flag = 1;
-        const long long first = issued > kNS ? issued - kNS : 0;
+        const long long first = issued > 2 ? issued - 2 : 0;
         for (long long i = first; i < issued; ++i)
-          if (!mbar_wait_bounded(&kv_full[i % kNS], (uint32_t)((i / kNS) & 1),
+          if (!mbar_wait_bounded(&kv_full[i & 1], (uint32_t)((i >> 1) & 1),
                                  reinterpret_cast<volatile int *>(&dummy)))
             at_status(p.status, kAtTimeoutDrain);
       }
@@ -188,34 +209,43 @@ __global__ void __launch_bounds__(kThreads, 2)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------------------------------------------- MMA issuer
-      constexpr uint32_t kIdesc = idesc_f16_f32(kBQ, 64);   // both MMAs: M=128, N=64
+      constexpr uint32_t kIdescS = idesc_f16_f32(kBQ, kBK);
+      constexpr uint32_t kIdescO = idesc_f16_f32(kBQ, kHD);
       bool ok = mbar_wait_bounded(q_full, 0, abort_flag), any = false;
-      for (int s = 0; s < nslots && ok; ++s) {
-        const int it = s / GH, h = s - it * GH, st = it % kNS;
-        // S(s) = Q_h K_j^T over S's columns, once P(s-1) V has read them
-        if (s > 0 && !mbar_wait_bounded(s_free, (s - 1) & 1, abort_flag)) { ok = false; break; }
-        if (h == 0 && !mbar_wait_bounded(&kv_full[st], (it / kNS) & 1, abort_flag)) { ok = false; break; }
-        tc_fence_after_sync();
-        const uint64_t a = sdesc_kmajor_sw128(smem_u32(sQ + h * C::Q_BYTES));
-        const uint64_t bk = sdesc_kmajor_sw128(smem_u32(sK + st * C::K_BYTES));
+      for (int s = 0; s <= nslots && ok; ++s) {
+        if (s < nslots) {
+          // S(s) = Q_h K_j^T into S buffer s & 1
+          const int it = s / GH, h = s - it * GH, sb = s & 1;
+          if (!mbar_wait_bounded(&s_free[sb], ((s >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+          if (h == 0 && !mbar_wait_bounded(&kv_full[it & 1], (it >> 1) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after_sync();
+          const uint64_t a = sdesc_kmajor_sw128(smem_u32(sQ + h * C::Q_BYTES));
+          const uint64_t bk = sdesc_kmajor_sw128(smem_u32(sK + (it & 1) * C::K_BYTES));
 #pragma unroll
-        for (int k = 0; k < kHD / 16; ++k)
-          umma_f16(tmem + C::TMEM_S, a + 2 * k, bk + 2 * k, kIdesc, k > 0);
-        any = true;
-        umma_commit(s_full);
-        // O_h += P(s) V_j once the softmax has written P(s)
-        if (!mbar_wait_bounded(p_full, s & 1, abort_flag)) { ok = false; break; }
-        tc_fence_after_sync();
-        const uint64_t bv = sdesc_kmajor_sw128(smem_u32(sVt + st * C::VT_BYTES));
+          for (int k = 0; k < kHD / 16; ++k)
+            umma_f16(tmem + C::TMEM_S + sb * kBK, a + 2 * k, bk + 2 * k, kIdescS, k > 0);
+          any = true;
+          umma_commit(&s_full[sb]);
+        }
+        if (s >= 1) {
+          // O_h += P(s-1) V_j
+          const int ps = s - 1, it = ps / GH, h = ps - it * GH, pb = ps & 1;
+          if (!mbar_wait_bounded(&p_full[pb], (ps >> 1) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after_sync();
 #pragma unroll
-        for (int k = 0; k < kBK / 16; ++k)   // 16 keys of P = 8 TMEM columns per MMA
-          umma_f16_tmem_a(tmem + h * kHD, tmem + C::TMEM_S + k * 8, bv + 2 * k, kIdesc, (it | k) != 0);
-        umma_commit(s_free);
-        if (h == GH - 1) umma_commit(&kv_empty[st]);
+          for (int kb = 0; kb < 2; ++kb) {
+            const uint64_t bv = sdesc_kmajor_sw128(smem_u32(sVt + (it & 1) * C::VT_BYTES + kb * C::VT_SUB));
+#pragma unroll
+            for (int k = 0; k < 4; ++k)   // 16 keys of P = 8 TMEM columns per MMA
+              umma_f16_tmem_a(tmem + h * kHD, tmem + C::TMEM_S + pb * kBK + (kb * 4 + k) * 8, bv + 2 * k,
+                              kIdescO, (it | kb | k) != 0);
+          }
+          umma_commit(&s_free[pb]);
+          umma_commit(&o_ready[h]);
+          if (h == GH - 1) umma_commit(&kv_empty[it & 1]);
+        }
       }
-      if (ok) {
-        umma_commit(o_done);
-      } else {
+      if (!ok) {
         at_status(p.status, kAtTimeoutMma);
         *abort_flag = 1;
         if (any) {
@@ -227,14 +257,20 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
   } else {
-    // ---------------------------------------------- softmax: warps 2..5, one
-    // query row per thread, all 64 keys of every tile
+    // ---------------------------------------------- softmax: warps 2..5 take keys
+    // 0..63 of every tile (group 0), warps 6..9 keys 64..127 (group 1); one
+    // query row per thread.  The groups exchange partial row maxes in shared
+    // memory at a named-barrier reduction that also ANDs their health, so a
+    // bounded wait that gives up in one group stops both together.
     const int quarter = warp & 3;
+    const int grp = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;              // query row within the tile
     const int t = q0 + r;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float sl2 = p.scale_log2;
-    float m[GH], l[GH];                             // running max (exp2 domain) and sum
+    float *red_max = reinterpret_cast<float *>(smem + C::OFF_RED);          // [2][2][128]
+    float *red_sum = red_max + 2 * 2 * 128;                                   // [2][4][128]
+    float m[GH], l[GH];                             // running max (shared value), partial sums
 #pragma unroll
     for (int h = 0; h < GH; ++h) {
       m[h] = -INFINITY;
@@ -242,32 +278,40 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     bool alive = true;
     for (int s = 0; s < nslots; ++s) {
-      const int it = s / GH, h = s - it * GH;
-      const int k0 = (j_lo + it) * kBK;             // first key of this tile
-      if (!__all_sync(0xffffffffu, mbar_wait_bounded(s_full, s & 1, abort_flag))) {
-        alive = false;
-        break;
-      }
-      tc_fence_after_sync();
-      const bool need_mask = (k0 + kBK - 1 > q0) || (k0 < vs);
+      const int it = s / GH, h = s - it * GH, sb = s & 1;
+      const int k0 = (j_lo + it) * kBK + grp * 64;  // first key of this group's half tile
+      const bool ok = alive && __all_sync(0xffffffffu, mbar_wait_bounded(&s_full[sb], (s >> 1) & 1, abort_flag));
+      const bool need_mask = (k0 + 63 > q0) || (k0 < vs);
       uint32_t sv[64];
-      tmem_ld32(lane_base + C::TMEM_S, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-      tmem_ld32(lane_base + C::TMEM_S + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-      tmem_ld_wait();
-      // eight independent max chains (a single chain is latency-bound)
-      float mc[8];
+      float mx = -INFINITY;
+      if (ok) {
+        tc_fence_after_sync();
+        const uint32_t s_col = lane_base + C::TMEM_S + sb * kBK + grp * 64;
+        tmem_ld32(s_col, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+        tmem_ld32(s_col + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+        tmem_ld_wait();
+        // eight independent max chains (a single chain is latency-bound)
+        float mc[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) mc[q] = -INFINITY;
-      const int hi = t - k0, lo = vs - k0;          // keys k0+e visible iff lo <= e <= hi
-      if (need_mask) {
+        for (int q = 0; q < 8; ++q) mc[q] = -INFINITY;
+        if (need_mask) {
+          const int hi = t - k0, lo = vs - k0;
 #pragma unroll
-        for (int e = 0; e < 64; ++e)
-          if (e <= hi && e >= lo) mc[e & 7] = fmaxf(mc[e & 7], __uint_as_float(sv[e]));
-      } else {
+          for (int e = 0; e < 64; ++e)
+            if (e <= hi && e >= lo) mc[e & 7] = fmaxf(mc[e & 7], __uint_as_float(sv[e]));
+        } else {
 #pragma unroll
-        for (int e = 0; e < 64; ++e) mc[e & 7] = fmaxf(mc[e & 7], __uint_as_float(sv[e]));
+          for (int e = 0; e < 64; e += 2)
+            mc[(e >> 1) & 7] = fmax3(mc[(e >> 1) & 7], __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
+        }
+        mx = fmaxf(fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3])), fmaxf(fmaxf(mc[4], mc[5]), fmaxf(mc[6], mc[7])));
       }
-      float mxa = fmaxf(fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3])), fmaxf(fmaxf(mc[4], mc[5]), fmaxf(mc[6], mc[7])));
+      red_max[((s & 1) * 2 + grp) * 128 + r] = mx;
+      tc_fence_before_sync();                       // both groups' S reads precede any P write
+      alive = softmax_and(ok);
+      tc_fence_after_sync();
+      if (!alive) break;
+      float mxa = fmaxf(mx, red_max[((s & 1) * 2 + (grp ^ 1)) * 128 + r]);
       mxa = (mxa == -INFINITY) ? -INFINITY : mxa * sl2;   // into the exp2 domain
       float mh = m[h];
       float alpha = 1.f;
@@ -281,25 +325,30 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       m[h] = mh;
       if (__any_sync(0xffffffffu, resc)) {
-        // O_h holds every earlier P V (the MMA issued S(s) only after the
-        // previous P V completed); rescale in TMEM.  tcgen05.ld/st are
-        // warp-collective: every lane takes part, alpha = 1 where the row's
-        // max did not move
-        uint32_t ov[32];
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          tmem_ld32(lane_base + h * kHD + half * 32, ov);
+        // O_h must hold every earlier P V before it is rescaled; each group
+        // rescales its 32 of the head's 64 columns
+        if (__all_sync(0xffffffffu, mbar_wait_bounded(&o_ready[h], (it - 1) & 1, abort_flag))) {
+          tc_fence_after_sync();
+          uint32_t ov[32];
+          tmem_ld32(lane_base + h * kHD + grp * 32, ov);
           tmem_ld_wait();
 #pragma unroll
           for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-          tmem_st32(lane_base + h * kHD + half * 32, ov);
+          tmem_st32(lane_base + h * kHD + grp * 32, ov);
+          tmem_st_wait();
+        } else {
+          alive = false;
         }
       }
+      if (!alive) continue;                         // the next reduction stops both groups
       const float mu = (mh == -INFINITY) ? 0.f : mh;
-      // p = 2^(s*c - m) as f16, packed two keys per TMEM column over S's first 32 columns
+      // p = 2^(s*c - m) as f16, packed two keys per TMEM column into the first
+      // 64 columns of this S buffer (this group's 64 keys -> 32 columns)
       uint32_t pk[32];
       float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // eight partial sums
       if (need_mask) {
+        // keys k0+e visible iff lo <= e <= hi (causal and padding limits)
+        const int hi = t - k0, lo = vs - k0;
 #pragma unroll
         for (int e = 0; e < 64; e += 2) {
           const float x0 = (e <= hi && e >= lo) ? fmaf(__uint_as_float(sv[e]), sl2, -mu) : -INFINITY;
@@ -319,38 +368,43 @@ __global__ void __launch_bounds__(kThreads, 2)
           pk[e >> 1] = pack_f16x2(p0, p1);
         }
       }
-      tmem_st32(lane_base + C::TMEM_S, pk);
-      tmem_st_wait();                               // P (and any O rescale) visible to the MMA
+      tmem_st32(lane_base + C::TMEM_S + sb * kBK + grp * 32, pk);
+      tmem_st_wait();
       l[h] += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       tc_fence_before_sync();
-      mbar_arrive(p_full);
+      mbar_arrive(&p_full[sb]);
     }
     // ------------------------------------------------ normalise and store
-    if (alive && !__all_sync(0xffffffffu, mbar_wait_bounded(o_done, 0, abort_flag))) alive = false;
+#pragma unroll
+    for (int h = 0; h < GH; ++h) red_sum[(grp * 4 + h) * 128 + r] = l[h];
+    alive = softmax_and(alive);
     if (!alive) {
       if (lane == 0) at_status(p.status, kAtTimeoutSoftmax);
       *abort_flag = 1;
     } else {
-      tc_fence_after_sync();
       const bool row_ok = t < T;
       const long long ldo = (long long)p.H * kHD;
 #pragma unroll 1
       for (int h = 0; h < GH; ++h) {
-        const float inv = l[h] > 0.f ? 1.f / l[h] : 0.f;
-#pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
-          uint32_t ov[32];
-          tmem_ld32(lane_base + h * kHD + half * 32, ov);
-          tmem_ld_wait();
-          if (row_ok) {
-            f16 *dst = p.o + ((long long)b * T + t) * ldo + (long long)(h_first + h) * kHD + half * 32;
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&o_ready[h], (ntiles - 1) & 1, abort_flag))) {
+          if (lane == 0) at_status(p.status, kAtTimeoutSoftmax);
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after_sync();
+        const float lt = red_sum[h * 128 + r] + red_sum[(4 + h) * 128 + r];
+        const float inv = lt > 0.f ? 1.f / lt : 0.f;
+        uint32_t ov[32];
+        tmem_ld32(lane_base + h * kHD + grp * 32, ov);
+        tmem_ld_wait();
+        if (row_ok) {
+          f16 *dst = p.o + ((long long)b * T + t) * ldo + (long long)(h_first + h) * kHD + grp * 32;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const float *f = reinterpret_cast<const float *>(&ov[8 * q]);
-              const uint4 w = make_uint4(pack_f16x2(f[0] * inv, f[1] * inv), pack_f16x2(f[2] * inv, f[3] * inv),
-                                         pack_f16x2(f[4] * inv, f[5] * inv), pack_f16x2(f[6] * inv, f[7] * inv));
-              *reinterpret_cast<uint4 *>(dst + 8 * q) = w;
-            }
+          for (int q = 0; q < 4; ++q) {
+            const float *f = reinterpret_cast<const float *>(&ov[8 * q]);
+            const uint4 w = make_uint4(pack_f16x2(f[0] * inv, f[1] * inv), pack_f16x2(f[2] * inv, f[3] * inv),
+                                       pack_f16x2(f[4] * inv, f[5] * inv), pack_f16x2(f[6] * inv, f[7] * inv));
+            *reinterpret_cast<uint4 *>(dst + 8 * q) = w;
           }
         }
       }
@@ -361,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem, C::TMEM_COLS);
+    tmem_dealloc(tmem, 512);
   }
 }
 
@@ -370,7 +424,7 @@ cudaError_t launch_gh(const AttnParams &a, const CUtensorMap &tq, const CUtensor
                       const CUtensorMap &tv, cudaStream_t st) {
   using C = AtCfg<GH>;
   auto kern = attn_tc_kernel<GH>;
-  cudaError_t e = ensure_smem_attr<attn_tc_kernel<GH>>(C::SMEM);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   AtParams p{};
   p.o = a.o;
@@ -396,18 +450,18 @@ bool attention_tc_supported(int hd, int H, int KV) {
 cudaError_t launch_attention_tc(const AttnParams &a, cudaStream_t st) {
   if (!attention_tc_supported(a.hd, a.H, a.KV) || a.v_t == nullptr) return cudaErrorInvalidConfiguration;
   CUtensorMap tq, tk, tv;
-  if (!get_tmap_f16(&tq, a.q, (uint64_t)a.B * a.H * a.T, kHD, kHD, kBQ)) return cudaErrorInvalidValue;
-  if (!get_tmap_f16(&tk, a.k, (uint64_t)a.B * a.KV * a.T, kHD, kHD, kBK)) return cudaErrorInvalidValue;   // [64 keys] boxes
+  if (!make_tmap_f16(&tq, a.q, (uint64_t)a.B * a.H * a.T, kHD, kHD, kBQ)) return cudaErrorInvalidValue;
+  if (!make_tmap_f16(&tk, a.k, (uint64_t)a.B * a.KV * a.T, kHD, kHD, kBK)) return cudaErrorInvalidValue;
   // V^T: rows are (b, kv head, dim), columns are keys; columns >= T read as zero
-  if (!get_tmap_f16(&tv, a.v_t, (uint64_t)a.B * a.KV * kHD, a.T, a.T_pad, kHD)) return cudaErrorInvalidValue;
+  if (!make_tmap_f16(&tv, a.v_t, (uint64_t)a.B * a.KV * kHD, a.T, a.T_pad, kHD)) return cudaErrorInvalidValue;
   const int G = a.H / a.KV;
   switch (G) {
     case 1: return launch_gh<1>(a, tq, tk, tv, st);
     case 2: return launch_gh<2>(a, tq, tk, tv, st);
     case 3: return launch_gh<3>(a, tq, tk, tv, st);
-    case 4: return launch_gh<2>(a, tq, tk, tv, st);   // two CTAs per group of four
+    case 4: return launch_gh<4>(a, tq, tk, tv, st);
     case 6: return launch_gh<3>(a, tq, tk, tv, st);   // two CTAs per group of six
-    case 8: return launch_gh<2>(a, tq, tk, tv, st);   // four CTAs per group of eight
+    case 8: return launch_gh<4>(a, tq, tk, tv, st);
   }
   return cudaErrorInvalidConfiguration;
 }
