@@ -67,6 +67,7 @@ struct GemmParams {
   int *status;            // device status word
   int raster_m;           // set by launch_gemm: 1 = consecutive tiles walk down M (B tile reused)
   int epi_tma;            // set by launch_gemm: which epilogue tensor maps are valid
+  int pdl;                // launch as a programmatic dependent of the preceding kernel
 };
 
 // Raises the dynamic shared-memory limit of kernel `Kern` to `bytes`, once per

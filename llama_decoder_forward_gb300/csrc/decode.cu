@@ -76,6 +76,24 @@ struct DecAttnParams {
   int layer;                // layer index (row offset into the whole-cache tensor maps)
 };
 
+// Launches `kern` as a programmatic dependent of the preceding kernel in the
+// stream (it calls griddep_wait() before touching that kernel's outputs).
+template <typename Kern, typename... Args>
+static cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, int smem, cudaStream_t st,
+                              const Args &...args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Writes this CTA's (max, sum, output) triple for each head of the group and,
 // if it is the last CTA of its (sequence, kv head) to finish, merges all the
 // chunks' triples into the attention output.  red_m/red_l/red_o hold the
@@ -200,11 +218,15 @@ __global__ void __launch_bounds__(128) decode_attn_mma_kernel(const __grid_const
   }
   __syncthreads();
   if (threadIdx.x == 0) {
+    // the cache is an input of the step, not written by any kernel of it: its
+    // chunk is requested before waiting for the preceding kernel
     const int y = static_cast<int>(((long long)p.layer * p.B + b) * p.KV + kvh) * p.S_max + k_begin;
     mbar_arrive_expect_tx(kv_bar, 2 * kChunk * 128);
     tma_load_2d(sK, &tmK, kv_bar, 0, y);
     tma_load_2d(sV, &tmV, kv_bar, 0, y);
+    griddep_launch_dependents();
   }
+  griddep_wait();                                  // q, k_new, v_new, partials, counters
   // q as A fragments (rows r < G: hi; rows r + 8: lo), built while the copy flies
   const int r = lane >> 2, c2 = (lane & 3) * 2;
   uint32_t qa[4][4];
@@ -339,6 +361,8 @@ __global__ void __launch_bounds__(128) decode_attn_mma_kernel(const __grid_const
 // GM: compile-time bound on the group size g = H / KV (arrays are sized GM).
 template <int HD, int GM>
 __global__ void __launch_bounds__(kDecWarps * 32) decode_attn_kernel(const DecAttnParams p) {
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  griddep_wait();
   extern __shared__ __align__(128) uint8_t dsm[];
   bf16 *sK = reinterpret_cast<bf16 *>(dsm);          // [kChunk][HD]
   bf16 *sV = sK + kChunk * HD;                       // [kChunk][HD]
@@ -550,11 +574,10 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_attn_kernel(const DecAt
 template <int HD, int GM>
 static cudaError_t launch_decode_attn_g(const DecAttnParams &ap, dim3 grid, cudaStream_t st) {
   const int smem = 2 * kChunk * HD * 2 + 16;
-  auto kern = decode_attn_kernel<HD, GM>;
-  cudaError_t e = ensure_smem_attr<decode_attn_kernel<HD, GM>>(smem);
+  constexpr auto kern = decode_attn_kernel<HD, GM>;
+  cudaError_t e = ensure_smem_attr<kern>(smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kDecWarps * 32, smem, st>>>(ap);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(kDecWarps * 32), smem, st, ap);
 }
 
 template <int HD>
@@ -572,10 +595,10 @@ static cudaError_t launch_decode_attn_mma_g(const CUtensorMap &tk, const CUtenso
                                             const DecAttnParams &ap, dim3 grid, cudaStream_t st) {
   constexpr int NW = 4, HD = 64;
   const int smem = 1024 + 2 * kChunk * 128 + 16 + (2 * NW * GM + NW * GM * HD) * 4;
-  cudaError_t e = ensure_smem_attr<decode_attn_mma_kernel<GM>>(smem);
+  constexpr auto kern = decode_attn_mma_kernel<GM>;
+  cudaError_t e = ensure_smem_attr<kern>(smem);
   if (e != cudaSuccess) return e;
-  decode_attn_mma_kernel<GM><<<grid, NW * 32, smem, st>>>(tk, tv, ap);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(NW * 32), smem, st, tk, tv, ap);
 }
 
 // head_dim 64 runs on tensor cores (the cache seen as one 2-D tensor of
@@ -649,7 +672,7 @@ cudaError_t run_decode(const DecodeArgs &a, void *ws, int sms, cudaStream_t st, 
     p.ssq_in = ssq_a; p.inv_dim = 1.0f / d; p.eps = c.rms_eps; p.ssq_zero = ssq_b;
     p.q = q; p.k_bf = kn; p.v_bf = vn; p.T = 1; p.H = H; p.KV = KV; p.hd = hd;
     p.rope = a.rope; p.valid_start = nullptr; p.pos_add = a.cache_len; p.pos_limit = min(a.S_max, c.max_pos - 1);
-    p.max_pos = c.max_pos; p.status = status;
+    p.max_pos = c.max_pos; p.status = status; p.pdl = 1;
     DEC_LAUNCH_K(SMOL_K_QKV, launch_gemm(kEpiQkvRope, hd, x, lb + a.off_qkv, p, sms, st));
 
     DecAttnParams ap{};
@@ -671,23 +694,23 @@ cudaError_t run_decode(const DecodeArgs &a, void *ws, int sms, cudaStream_t st, 
     GemmParams po{};
     po.M = B; po.N = d; po.K = H * hd; po.out = h; po.out_is_f16 = 1; po.ldo = d; po.resid_f16 = x;
     po.ssq_out = ssq_b;
-    po.status = status;
+    po.status = status; po.pdl = 1;
     DEC_LAUNCH_K(SMOL_K_OPROJ, launch_gemm(kEpiResidual, 64, o, lb + a.off_o, po, sms, st));
 
     GemmParams pg{};
     pg.M = B; pg.N = 2 * I; pg.K = d; pg.out = act; pg.out_is_f16 = 1; pg.ldo = I; pg.ssq_in = ssq_b;
-    pg.inv_dim = 1.0f / d; pg.eps = c.rms_eps; pg.ssq_zero = ssq_a; pg.status = status;
+    pg.inv_dim = 1.0f / d; pg.eps = c.rms_eps; pg.ssq_zero = ssq_a; pg.status = status; pg.pdl = 1;
     DEC_LAUNCH_K(SMOL_K_GATEUP, launch_gemm(kEpiSwiglu, 128, h, lb + a.off_gu, pg, sms, st));
 
     GemmParams pd{};
     pd.M = B; pd.N = d; pd.K = I; pd.out = x; pd.out_is_f16 = 1; pd.ldo = d; pd.resid_f16 = h;
     pd.ssq_out = ssq_a;
-    pd.status = status;
+    pd.status = status; pd.pdl = 1;
     DEC_LAUNCH_K(SMOL_K_DOWN, launch_gemm(kEpiResidual, 64, act, lb + a.off_down, pd, sms, st));
   }
   GemmParams ph{};
   ph.M = B; ph.N = V; ph.K = d; ph.out = a.logits; ph.out_is_f16 = 0; ph.ldo = V; ph.ssq_in = ssq_a;
-  ph.inv_dim = 1.0f / d; ph.eps = c.rms_eps; ph.status = status;
+  ph.inv_dim = 1.0f / d; ph.eps = c.rms_eps; ph.status = status; ph.pdl = 1;
   DEC_LAUNCH_K(SMOL_K_HEAD, launch_gemm(kEpiScale, gemm_pick_bn(kEpiScale, V, hd), x, a.head, ph, sms, st));
 #undef DEC_LAUNCH
   *launches = n;

@@ -637,6 +637,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // vocabulary projection; otherwise they share A and walk B
   const int num_kb = static_cast<int>(cdiv(p.K, C::BK));
   const int rank = PAIR > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  // tile -> (row group, column block)
+  auto decode_tile = [&](int tile, int &m_grp, int &n_blk) {
+    m_grp = p.raster_m ? tile % num_mg : tile / num_n;
+    n_blk = p.raster_m ? tile / num_mg : tile - m_grp * num_n;
+  };
   const int first_tile = blockIdx.x / PAIR, tile_step = gridDim.x / PAIR;
 
   if (threadIdx.x == 0) {
@@ -673,33 +678,56 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t full0_leader = PAIR > 1 ? mapa_shared(smem_u32(full), 0) : 0u;
   const uint32_t tempty0_leader = PAIR > 1 ? mapa_shared(smem_u32(tempty), 0) : 0u;
 
+  if (threadIdx.x == 0) griddep_launch_dependents();
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------ TMA producer
       uint32_t stage = 0, phase = 0;
       long long issued = 0;
       bool ok = true;
+      auto load_b = [&](uint32_t st, int kb, int n_blk) {
+        if constexpr (PAIR == 1)
+          tma_load_2d(sB + st * C::B_BYTES, &tmB, &full[st], kb * C::BK, n_blk * BN);
+        else
+          tma_load_2d_pair(sB + st * C::B_BYTES, &tmB, full0_leader + 8u * st, kb * C::BK,
+                           n_blk * BN + rank * (BN / PAIR));
+      };
+      auto arm = [&](uint32_t st) {
+        // with a pair both CTAs' boxes are counted on the even CTA's barrier
+        if constexpr (PAIR == 1) mbar_arrive_expect_tx(&full[st], C::STAGE_BYTES);
+        else if (rank == 0) mbar_arrive_expect_tx(&full[st], 2 * C::STAGE_BYTES);
+      };
+      // The weights (B) do not depend on the preceding kernel: the first
+      // stages' B boxes are requested before waiting for it, A (activations)
+      // after.
+      int pre = 0;
+      if (first_tile < num_tiles) {
+        int m_grp, n_blk;
+        decode_tile(first_tile, m_grp, n_blk);
+        pre = num_kb < C::STAGES ? num_kb : C::STAGES;
+        for (int kb = 0; kb < pre; ++kb) {
+          arm(kb);
+          load_b(kb, kb, n_blk);
+        }
+      }
+      griddep_wait();
       for (int tile = first_tile; tile < num_tiles && ok; tile += tile_step) {
-        const int m_grp = p.raster_m ? tile % num_mg : tile / num_n;
-        const int n_blk = p.raster_m ? tile / num_mg : tile - m_grp * num_n;
+        int m_grp, n_blk;
+        decode_tile(tile, m_grp, n_blk);
         const int m_blk = m_grp * PAIR + rank;
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag)) {
+          const bool preloaded = issued < pre;     // stage armed and its B requested above
+          if (!preloaded && !mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag)) {
             ok = false;
             break;
           }
-          if constexpr (PAIR == 1) {
-            mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+          if (!preloaded) arm(stage);
+          if constexpr (PAIR == 1)
             tma_load_2d(sA + stage * C::A_BYTES, &tmA, &full[stage], kb * C::BK, m_blk * C::BM);
-            tma_load_2d(sB + stage * C::B_BYTES, &tmB, &full[stage], kb * C::BK, n_blk * BN);
-          } else {
-            // both CTAs' boxes are counted on the even CTA's barrier, which its MMA waits on
-            if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
-            const uint32_t fb = full0_leader + 8u * stage;
-            tma_load_2d_pair(sA + stage * C::A_BYTES, &tmA, fb, kb * C::BK, m_blk * C::BM);
-            tma_load_2d_pair(sB + stage * C::B_BYTES, &tmB, fb, kb * C::BK,
-                             n_blk * BN + rank * (BN / PAIR));
-          }
+          else
+            tma_load_2d_pair(sA + stage * C::A_BYTES, &tmA, full0_leader + 8u * stage, kb * C::BK,
+                             m_blk * C::BM);
+          if (!preloaded) load_b(stage, kb, n_blk);
           ++issued;
           if (++stage == C::STAGES) {
             stage = 0;
@@ -778,6 +806,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else {
     // -------------------------------------------------- epilogue (warps 2 .. 1+kEpiWarps)
+    griddep_wait();                               // reads and writes activations
     const int quarter = warp & 3;                 // TMEM lanes 32*quarter .. +31
     EpiCtx e;
     e.lane = lane;
@@ -790,8 +819,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const bool resid_tma = EPI == kEpiResidual && (p.epi_tma & kTmaResid);
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = first_tile; tile < num_tiles; tile += tile_step) {
-      const int m_grp = p.raster_m ? tile % num_mg : tile / num_n;
-      const int n_blk = p.raster_m ? tile / num_mg : tile - m_grp * num_n;
+      int m_grp, n_blk;
+      decode_tile(tile, m_grp, n_blk);
       const int m_blk = m_grp * PAIR + rank;
       e.row0 = m_blk * C::BM + quarter * 32;
       e.rows_valid = min(32, max(0, p.M - e.row0));
@@ -1004,23 +1033,36 @@ static cudaError_t launch_pair(const CUtensorMap &ta, const CUtensorMap &tb, con
   cudaError_t e = ensure_smem_attr<kern>(C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const long long groups = cdiv(cdiv(p.M, C::BM), PAIR) * cdiv(p.N, BN);
+  cudaLaunchAttribute attr[2];
+  int nattr = 0;
+  if (p.pdl) {
+    attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[nattr].val.programmaticStreamSerializationAllowed = 1;
+    ++nattr;
+  }
   if constexpr (PAIR == 1) {
     const int grid = static_cast<int>(groups < num_sms ? groups : num_sms);
-    kern<<<grid, kGemmThreads, C::SMEM_BYTES, stream>>>(ta, tb, maps, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = nattr;
+    return cudaLaunchKernelEx(&cfg, kern, ta, tb, maps, p);
   } else {
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = PAIR;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    attr[nattr].id = cudaLaunchAttributeClusterDimension;
+    attr[nattr].val.clusterDim.x = PAIR;
+    attr[nattr].val.clusterDim.y = 1;
+    attr[nattr].val.clusterDim.z = 1;
+    ++nattr;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(num_sms / PAIR * PAIR));
     cfg.blockDim = dim3(kGemmThreads);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = nattr;
     const long long pairs_max = max_active_clusters<kern>(cfg, num_sms / PAIR);
     const long long pairs = groups < pairs_max ? groups : pairs_max;
     cfg.gridDim = dim3(static_cast<unsigned>(pairs * PAIR));

@@ -96,6 +96,20 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
   }
 }
 
+// ---------------------------------------------------------------- dependent launch
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialization attribute may start before its predecessor in the
+// stream has finished.  griddep_wait() blocks until every predecessor grid
+// has completed and its memory is visible; everything a kernel does before it
+// must not touch data a predecessor writes or reads.  (Without the attribute
+// both are no-ops.)
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the dependent grid be scheduled once every CTA of this grid has
+// executed this (or exited).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
