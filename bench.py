@@ -263,9 +263,15 @@ def run_prefill(S, args, rank, world, peaks, peaks_src):
 
     sampler = ClockSampler()
     sampler.start()
-    ms, dom_ms, dom_n = timed_with_kernel_events(S, step, args.steps, world, dominant)
+    # eager calls with CUDA events around every launch of the dominant kernel
+    # (its achieved rate), then the headline: the same step replayed as one
+    # CUDA graph (what a serving loop runs; no per-launch host cost)
+    eager_ms, dom_ms, dom_n = timed_with_kernel_events(S, step, args.steps, world, dominant)
+    eager_ms = max_over_ranks(eager_ms, world)
+    graph = capture_graph(step)
+    graph_ms = max_over_ranks(time_steps(graph.replay, args.steps, world), world) if graph else None
     clocks = sampler.stop()
-    ms = max_over_ranks(ms, world)
+    ms = graph_ms if graph_ms is not None else eager_ms
     tokens = wl.B * wl.T
     value = tokens * world / (ms / 1e3)
 
@@ -281,9 +287,6 @@ def run_prefill(S, args, rank, world, peaks, peaks_src):
     e2e_step()
     e2e_steps = max(1, min(args.steps, 10))
     e2e_ms = max_over_ranks(time_steps(e2e_step, e2e_steps, world), world)
-
-    graph = capture_graph(step)
-    graph_ms = max_over_ranks(time_steps(graph.replay, args.steps, world), world) if graph else None
 
     flops = prefill_flops_per_launch(wl)
     peak_tf = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
@@ -306,8 +309,8 @@ def run_prefill(S, args, rank, world, peaks, peaks_src):
                                f"V={wl.vocab}, batch {wl.B} x {wl.T} tokens per rank",
                    "batch_per_rank": wl.B, "seq_len": wl.T, "global_batch": wl.B * world,
                    "parallelism": f"replicas x{world} (batch-sharded, no collective)",
-                   "precision": "bf16 weights/ids/logits; f16 tensor-core operands; fp32 accumulation "
-                                "and residual stream",
+                   "precision": "bf16 weights/ids/logits; f16 tensor-core operands and residual "
+                                "stream; fp32 accumulation and softmax",
                    "l2": "inputs larger than L2: each step writes 1.6 GB of logits and streams "
                          ">300 MB of activations",
                    "kernel_timing": "CUDA events around each launch of the dominant kernel inside the "
@@ -317,8 +320,8 @@ def run_prefill(S, args, rank, world, peaks, peaks_src):
                 "h2d_bytes_per_step": ids.numel() * 4, "d2h_bytes_per_step": logits.numel() * 2,
                 "ms_per_step": round(e2e_ms, 4)},
         "gpu_launches": launches * args.steps,
-        "graph_replay": None if graph_ms is None else {
-            "ms_per_step": round(graph_ms, 4), "value": round(tokens * world / (graph_ms / 1e3), 1)},
+        "timing": "CUDA-graph replay of the step" if graph_ms is not None else "eager calls",
+        "eager_ms_per_step": round(eager_ms, 4),
         "roofline": roof,
         "step_tensor_frac": round(step_tf / peak_tf, 4),
         "step_tflops": round(step_tf, 2),
