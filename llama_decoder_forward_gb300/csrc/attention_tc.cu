@@ -205,46 +205,62 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdescS = idesc_f16_f32(kBQ, kBK);
       constexpr uint32_t kIdescO = idesc_f16_f32(kBQ, kHD);
       bool ok = mbar_wait_bounded(q_full, 0, abort_flag), any = false;
-      int n_s[2] = {0, 0};                        // S tiles issued per query tile
+      int n_pv[2] = {0, 0};                       // P V products issued per query tile
+      auto active = [&](int x, int j) { return j >= lo[x] && j <= hi[x]; };
+      // S_X(j) = Q_X K_j^T into S_X (j's K tile is in stage (j - j_lo) % kNS)
+      auto issue_s = [&](int x, int j) {
+        const int st = (j - j_lo) % kNS;
+        const uint64_t a = sdesc_kmajor_sw128(smem_u32(sQ + x * C::Q_BYTES));
+        const uint64_t bk = sdesc_kmajor_sw128(smem_u32(sK + st * C::K_BYTES));
+#pragma unroll
+        for (int k = 0; k < kHD / 16; ++k)
+          umma_f16(tmem + x * kBK, a + 2 * k, bk + 2 * k, kIdescS, k > 0);
+        umma_commit(&s_full[x]);
+        any = true;
+      };
+      // the tiles' first S
+      if (ok && !mbar_wait_bounded(&kv_full[0], 0, abort_flag)) ok = false;
+      if (ok) {
+        tc_fence_after_sync();
+        for (int x = 0; x < 2; ++x)
+          if (active(x, j_lo)) issue_s(x, j_lo);
+      }
+      // Per KV tile j, per query tile X: P_X(j) V_j as soon as softmax X has
+      // written P_X(j), then right away S_X(j+1) - so the tensor core turns to
+      // X's next scores while the other tile's softmax is still running (ping-pong).
       for (int it = 0; it < ntiles && ok; ++it) {
         const int j = j_lo + it, st = it % kNS;
-        if (!mbar_wait_bounded(&kv_full[st], (it / kNS) & 1, abort_flag)) { ok = false; break; }
-        tc_fence_after_sync();
-        const uint64_t bk = sdesc_kmajor_sw128(smem_u32(sK + st * C::K_BYTES));
-        // S_X = Q_X K_j^T for each tile that sees block j (S_X free once P_X(j-1) V is done)
+        bool next_ready = false;
+#pragma unroll 1
+        for (int x = 0; x < 2 && ok; ++x) {
+          if (active(x, j)) {
+            if (!mbar_wait_bounded(&p_full[x], n_pv[x] & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after_sync();
 #pragma unroll
-        for (int x = 0; x < 2; ++x) {
-          if (j < lo[x] || j > hi[x]) continue;
-          if (n_s[x] > 0 && !mbar_wait_bounded(&s_free[x], (n_s[x] - 1) & 1, abort_flag)) { ok = false; break; }
-          tc_fence_after_sync();
-          const uint64_t a = sdesc_kmajor_sw128(smem_u32(sQ + x * C::Q_BYTES));
+            for (int kb = 0; kb < 2; ++kb) {
+              const uint64_t bv = sdesc_kmajor_sw128(smem_u32(sVt + st * C::VT_BYTES + kb * C::VT_SUB));
 #pragma unroll
-          for (int k = 0; k < kHD / 16; ++k)
-            umma_f16(tmem + x * kBK, a + 2 * k, bk + 2 * k, kIdescS, k > 0);
-          any = true;
-          umma_commit(&s_full[x]);
-        }
-        if (!ok) break;
-        // O_X += P_X V_j once softmax X has written P_X
-#pragma unroll
-        for (int x = 0; x < 2; ++x) {
-          if (j < lo[x] || j > hi[x]) continue;
-          if (!mbar_wait_bounded(&p_full[x], n_s[x] & 1, abort_flag)) { ok = false; break; }
-          tc_fence_after_sync();
-#pragma unroll
-          for (int kb = 0; kb < 2; ++kb) {
-            const uint64_t bv = sdesc_kmajor_sw128(smem_u32(sVt + st * C::VT_BYTES + kb * C::VT_SUB));
-#pragma unroll
-            for (int k = 0; k < 4; ++k)   // 16 keys of P = 8 TMEM columns per MMA
-              umma_f16_tmem_a(tmem + C::TMEM_O + x * kHD, tmem + x * kBK + (kb * 4 + k) * 8, bv + 2 * k,
-                              kIdescO, (j > lo[x]) || kb || k);
+              for (int k = 0; k < 4; ++k)   // 16 keys of P = 8 TMEM columns per MMA
+                umma_f16_tmem_a(tmem + C::TMEM_O + x * kHD, tmem + x * kBK + (kb * 4 + k) * 8, bv + 2 * k,
+                                kIdescO, (j > lo[x]) || kb || k);
+            }
+            umma_commit(&s_free[x]);
+            if (j == hi[x]) umma_commit(&o_done[x]);
+            ++n_pv[x];
           }
-          umma_commit(&s_free[x]);
-          if (j == hi[x]) umma_commit(&o_done[x]);
-          ++n_s[x];
+          if (active(x, j + 1)) {
+            if (!next_ready) {
+              if (!mbar_wait_bounded(&kv_full[(it + 1) % kNS], ((it + 1) / kNS) & 1, abort_flag)) { ok = false; break; }
+              next_ready = true;
+            }
+            // S_X shares its columns with P_X: the P V just issued must be done
+            if (n_pv[x] > 0 && !mbar_wait_bounded(&s_free[x], (n_pv[x] - 1) & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after_sync();
+            issue_s(x, j + 1);
+          }
         }
         if (!ok) break;
-        umma_commit(&kv_empty[st]);
+        umma_commit(&kv_empty[st]);               // both tiles' P V of block j issued
       }
       if (!ok) {
         at_status(p.status, kAtTimeoutMma);
@@ -281,26 +297,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after_sync();
       const bool need_mask = (k0 + kBK - 1 > tq0) || (k0 < vs);
       const int hi_e = t - k0, lo_e = vs - k0;      // keys k0+e visible iff lo_e <= e <= hi_e
-      // pass 1: row max over the 128 scores (four chunks of 32 columns)
-      float mx = -INFINITY;
+      // pass 1, the row max: the 128 scores in four loads in flight, one wait
+      float mx;
+      {
+        uint32_t sv[128];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t sv[32];
-        tmem_ld32(s_col + 32 * c, sv);
+        for (int c = 0; c < 4; ++c)
+          tmem_ld32(s_col + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sv[32 * c]));
         tmem_ld_wait();
         float mc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         if (need_mask) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int ee = 32 * c + e;
-            if (ee <= hi_e && ee >= lo_e) mc[e & 3] = fmaxf(mc[e & 3], __uint_as_float(sv[e]));
-          }
+          for (int e = 0; e < 128; ++e)
+            if (e <= hi_e && e >= lo_e) mc[e & 3] = fmaxf(mc[e & 3], __uint_as_float(sv[e]));
         } else {
 #pragma unroll
-          for (int e = 0; e < 32; e += 2)
+          for (int e = 0; e < 128; e += 2)
             mc[(e >> 1) & 3] = fmax3(mc[(e >> 1) & 3], __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
         }
-        mx = fmax3(mx, fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3]));
+        mx = fmax3(fmaxf(mc[0], mc[1]), mc[2], mc[3]);
       }
       const float mxa = (mx == -INFINITY) ? -INFINITY : mx * sl2;   // into the exp2 domain
       float alpha = 1.f;
@@ -327,19 +342,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const float mu = (m == -INFINITY) ? 0.f : m;
-      // pass 2: p = 2^(s*c - m) as f16, chunk c (32 keys) -> TMEM columns
-      // 16c..16c+15 of S_X (over scores already read)
+      // pass 2: p = 2^(s*c - m) as f16 pairs over S_X's first 64 columns, in
+      // two halves of 64 keys (half h -> columns 32h..32h+31, over scores
+      // already read)
       float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t sv[32];
-        tmem_ld32(s_col + 32 * c, sv);
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t sv[64];
+        tmem_ld32(s_col + 64 * hf, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+        tmem_ld32(s_col + 64 * hf + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
         tmem_ld_wait();
-        uint32_t pk[16];
+        uint32_t pk[32];
         if (need_mask) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const int ee = 32 * c + e;
+          for (int e = 0; e < 64; e += 2) {
+            const int ee = 64 * hf + e;
             const float x0 = (ee <= hi_e && ee >= lo_e) ? fmaf(__uint_as_float(sv[e]), sl2, -mu) : -INFINITY;
             const float x1 = (ee + 1 <= hi_e && ee + 1 >= lo_e) ? fmaf(__uint_as_float(sv[e + 1]), sl2, -mu) : -INFINITY;
             const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
@@ -348,14 +365,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         } else {
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
+          for (int e = 0; e < 64; e += 2) {
             const float p0 = ex2_approx(fmaf(__uint_as_float(sv[e]), sl2, -mu));
             const float p1 = ex2_approx(fmaf(__uint_as_float(sv[e + 1]), sl2, -mu));
             ps[(e >> 1) & 3] += p0 + p1;
             pk[e >> 1] = pack_f16x2(p0, p1);
           }
         }
-        tmem_st16(s_col + 16 * c, pk);
+        tmem_st32(s_col + 32 * hf, pk);
       }
       tmem_st_wait();                               // P (and any O rescale) visible to the MMA
       l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
