@@ -6,23 +6,23 @@
 // probs @ v; query head h reads key/value head h // g as in the "SmolLM3"
 // page's "Grouped-query attention").  Rows with no visible key produce 0.
 //
-// One CTA owns (sequence b, query head h, 256 query tokens as two 128-row
-// tiles A and B) and reads K/V of kv head h // g: never expanded per query
-// head (the g heads of a group read the same K/V tiles, from L2).  Per
-// 128-key tile j and query tile X:
-//   S_X = Q_X K_j^T    tcgen05.mma M=128 N=128 K=64 into S_X (TMEM, fp32)
-//   P_X = exp2(S*c-m)  softmax warpgroup X: one query row per thread, all 128
-//                      keys (no reduction across threads); P as packed f16 over
-//                      S_X's own TMEM columns
-//   O_X += P_X V_j     tcgen05.mma with A (= P_X) read from TMEM, M=128 N=64 K=128
-// The two tiles ping-pong: while warpgroup A turns S_A into P_A, the tensor
-// core computes S_B or P_B V, and the other way round.  The running max is
-// updated lazily: O_X is rescaled in TMEM only when a row's max grows by more
-// than 2^8 (otherwise P may exceed 1 by up to 256, exact in the fp32 sums and
-// within f16 range), the FlashAttention-4 idea.  Warp 0 issues TMA, warp 1
-// allocates TMEM and one lane issues every MMA, warps 2..5 / 6..9 are the two
-// softmax warpgroups.  All waits are bounded (status word + abort flag, copies
-// and MMAs drained before exit).
+// One CTA owns (sequence b, kv head, a tile of 128 query tokens) and the GH
+// query heads of that kv head.  Each K tile [128 keys x 64] and V^T tile
+// [64 x 128 keys] is loaded once by TMA into shared memory and serves all GH
+// heads: K/V are never expanded per query head.  Per (kv tile, head):
+//   S = Q_h K^T        tcgen05.mma, M=128 N=128 K=64, fp32 in TMEM (two S buffers,
+//                      so the MMA for the next head runs while this one's softmax does)
+//   P = exp2(S*c - m)  eight softmax warps, one query row per thread per half tile; P is
+//                      written as packed f16 into the S buffer's own TMEM columns
+//   O_h += P V         tcgen05.mma with A (= P) read from TMEM, M=128 N=64 K=128, fp32
+//                      accumulator in TMEM; shared memory only feeds Q, K and V^T
+// The running max is updated lazily: O_h is rescaled in TMEM only when a row's
+// max grows by more than 2^8 (otherwise P may exceed 1 by up to 256, exact in
+// the fp32 sums and within f16 range), the FlashAttention-4 idea.
+// Warp 0 issues TMA, warp 1 allocates TMEM and one lane issues every MMA,
+// warps 2..9 (two groups of four, each taking half of every tile's keys) do
+// the softmax and the final normalisation.  All waits are
+// bounded (status word + abort flag, copies and MMAs drained before exit).
 #include <math.h>
 
 #include "common.cuh"
@@ -35,28 +35,30 @@ namespace {
 constexpr int kBQ = 128;      // query rows per tile (UMMA M)
 constexpr int kBK = 128;      // keys per KV tile
 constexpr int kHD = 64;
-constexpr int kNS = 3;        // K / V^T pipeline stages
-constexpr int kThreads = 320; // producer, MMA, two softmax warpgroups
+constexpr int kThreads = 320;   // producer, MMA, two softmax warpgroups
 
+template <int GH>
 struct AtCfg {
-  static constexpr int Q_BYTES = kBQ * kHD * 2;         // one tile: [128][64] f16
+  static constexpr int Q_BYTES = kBQ * kHD * 2;         // one head: [128][64] f16
   static constexpr int K_BYTES = kBK * kHD * 2;         // [128 keys][64]
   static constexpr int VT_SUB = kHD * 64 * 2;           // [64 dims][64 keys]
   static constexpr int VT_BYTES = 2 * VT_SUB;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
-  static constexpr int OFF_VT = OFF_K + kNS * K_BYTES;
-  static constexpr int OFF_BAR = OFF_VT + kNS * VT_BYTES;
+  static constexpr int OFF_K = OFF_Q + GH * Q_BYTES;
+  static constexpr int OFF_VT = OFF_K + 2 * K_BYTES;
+  static constexpr int OFF_RED = OFF_VT + 2 * VT_BYTES;  // [2][2][128] row maxes, [2][4][128] row sums
+  static constexpr int OFF_BAR = OFF_RED + (2 * 2 * 128 + 2 * 4 * 128) * 4;
   static constexpr int SMEM = 1024 + OFF_BAR + 256;
-  // TMEM columns: S_A 0..127, S_B 128..255 (P over their first 64), O_A 256.., O_B 320..
-  static constexpr int TMEM_O = 256;
+  static constexpr int TMEM_S = 256;                    // S buffers at columns 256 + sb*128;
+                                                        // P (f16) overwrites columns 0..63 of its S
+  static_assert(GH >= 1 && GH * kHD <= 256, "O accumulators must fit below the S buffers");
   static_assert(SMEM <= 232448, "shared memory per CTA");
 };
 
 struct AtParams {
   f16 *o;                   // [B, T, H*hd]
   const int *valid_start;
-  int B, T, H, KV, G;
+  int B, T, H, KV, G, GH, n_hsub;
   float scale_log2;
   int *status;
 };
@@ -76,6 +78,21 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// AND of `pred` over the 256 softmax threads (named barrier 1); also a
+// barrier between the two softmax warpgroups.
+__device__ __forceinline__ bool softmax_and(bool pred) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, 256, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(out)
+      : "r"((uint32_t)pred)
+      : "memory");
+  return out != 0;
+}
+
 // max(a, b, c) in one instruction (three-input max of sm_100 and later).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
@@ -87,22 +104,11 @@ __device__ __forceinline__ void at_status(int *status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
 
-// KV-tile range [lo, hi] of a 128-row query tile starting at q0 (hi < lo: the
-// tile has no rows).
-__device__ __forceinline__ void tile_range(int q0, int T, int vs, int &lo, int &hi) {
-  if (q0 >= T) {
-    lo = 0;
-    hi = -1;
-    return;
-  }
-  hi = min(q0 + kBQ - 1, T - 1) / kBK;
-  lo = min(vs / kBK, hi);          // an all-padding tile still runs one (masked) tile
-}
-
+template <int GH>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmVt, const AtParams p) {
-  using C = AtCfg;
+  using C = AtCfg<GH>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -111,43 +117,44 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *sVt = smem + C::OFF_VT;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
   uint64_t *q_full = bars;
-  uint64_t *kv_full = bars + 1;              // [kNS]
-  uint64_t *kv_empty = bars + 1 + kNS;       // [kNS]
-  uint64_t *s_full = bars + 1 + 2 * kNS;     // [2] S_X(j) computed
-  uint64_t *p_full = s_full + 2;             // [2] P_X(j) written (128 arrivals)
-  uint64_t *s_free = s_full + 4;             // [2] P_X(j) V done: S_X free, O_X current
-  uint64_t *o_done = s_full + 6;             // [2] every MMA of tile X complete
-  uint64_t *drain = s_full + 8;
+  uint64_t *kv_full = bars + 1;     // [2]
+  uint64_t *kv_empty = bars + 3;    // [2]
+  uint64_t *s_full = bars + 5;      // [2] S(s) computed
+  uint64_t *s_free = bars + 7;      // [2] PV(s) done: the S/P columns may be overwritten
+  uint64_t *p_full = bars + 9;      // [2] P(s) written into TMEM
+  uint64_t *o_ready = bars + 13;    // [GH]
+  uint64_t *drain = bars + 13 + GH;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = p.T;
-  // blocks are launched in linear order (x fastest): the query pair is the
-  // slow index, descending, so the longest causal rows start first
-  const int q0 = (gridDim.y - 1 - blockIdx.y) * (2 * kBQ);
-  const int b = blockIdx.x / p.H, h = blockIdx.x - b * p.H;
-  const int kvh = h / p.G;
+  // blocks are launched in linear order (x fastest): the query tile is the
+  // slow index, descending, so every sequence's longest causal tiles start
+  // first and the short ones fill the tail (longest-processing-time order)
+  const int q0 = (gridDim.y - 1 - blockIdx.y) * kBQ;
+  const int groups = p.KV * p.n_hsub;
+  const int b = blockIdx.x / groups;
+  const int kvh = (blockIdx.x - b * groups) / p.n_hsub;
+  const int hsub = blockIdx.x - b * groups - kvh * p.n_hsub;
+  const int h_first = kvh * p.G + hsub * GH;
   const int vs = p.valid_start ? min(max(p.valid_start[b], 0), T) : 0;
-  int lo[2], hi[2];
-  tile_range(q0, T, vs, lo[0], hi[0]);
-  tile_range(q0 + kBQ, T, vs, lo[1], hi[1]);
-  const int j_lo = hi[1] >= lo[1] ? min(lo[0], lo[1]) : lo[0];
-  const int j_hi = max(hi[0], hi[1]);
-  const int ntiles = j_hi - j_lo + 1;            // KV tiles loaded (>= 1: tile A has rows)
+  const int last_q = min(q0 + kBQ - 1, T - 1);
+  const int j_hi = last_q / kBK;
+  const int j_lo = min(vs / kBK, j_hi);          // an all-padding tile still runs one (masked) tile
+  const int ntiles = j_hi - j_lo + 1;
+  const int nslots = ntiles * GH;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int i = 0; i < kNS; ++i) {
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 1);
+      mbar_init(&p_full[i], 256);
     }
-    for (int x = 0; x < 2; ++x) {
-      mbar_init(&s_full[x], 1);
-      mbar_init(&p_full[x], 128);
-      mbar_init(&s_free[x], 1);
-      mbar_init(&o_done[x], 1);
-    }
+    for (int h = 0; h < GH; ++h) mbar_init(&o_ready[h], 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -170,12 +177,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       int dummy = 0;
       long long issued = 0;                       // kv stages issued (for the drain)
       bool ok = true;
-      mbar_arrive_expect_tx(q_full, 2 * C::Q_BYTES);
-      for (int x = 0; x < 2; ++x)                 // rows past T (tile B of the tail) read other rows
-        tma_load_2d(sQ + x * C::Q_BYTES, &tmQ, q_full, 0, (b * p.H + h) * T + q0 + x * kBQ);
+      mbar_arrive_expect_tx(q_full, GH * C::Q_BYTES);
+      for (int h = 0; h < GH; ++h)
+        tma_load_2d(sQ + h * C::Q_BYTES, &tmQ, q_full, 0, ((b * p.H) + h_first + h) * T + q0);
       for (int it = 0; it < ntiles && ok; ++it) {
-        const int j = j_lo + it, st = it % kNS;
-        if (!mbar_wait_bounded(&kv_empty[st], ((it / kNS) & 1) ^ 1, abort_flag)) {
+        const int j = j_lo + it, st = it & 1;
+        if (!mbar_wait_bounded(&kv_empty[st], ((it >> 1) & 1) ^ 1, abort_flag)) {
           ok = false;
           break;
         }
@@ -192,9 +199,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) {
         at_status(p.status, kAtTimeoutLoad);
         *abort_flag = 1;
-        const long long first = issued > kNS ? issued - kNS : 0;
+        const long long first = issued > 2 ? issued - 2 : 0;
         for (long long i = first; i < issued; ++i)
-          if (!mbar_wait_bounded(&kv_full[i % kNS], (uint32_t)((i / kNS) & 1),
+          if (!mbar_wait_bounded(&kv_full[i & 1], (uint32_t)((i >> 1) & 1),
                                  reinterpret_cast<volatile int *>(&dummy)))
             at_status(p.status, kAtTimeoutDrain);
       }
@@ -205,62 +212,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdescS = idesc_f16_f32(kBQ, kBK);
       constexpr uint32_t kIdescO = idesc_f16_f32(kBQ, kHD);
       bool ok = mbar_wait_bounded(q_full, 0, abort_flag), any = false;
-      int n_pv[2] = {0, 0};                       // P V products issued per query tile
-      auto active = [&](int x, int j) { return j >= lo[x] && j <= hi[x]; };
-      // S_X(j) = Q_X K_j^T into S_X (j's K tile is in stage (j - j_lo) % kNS)
-      auto issue_s = [&](int x, int j) {
-        const int st = (j - j_lo) % kNS;
-        const uint64_t a = sdesc_kmajor_sw128(smem_u32(sQ + x * C::Q_BYTES));
-        const uint64_t bk = sdesc_kmajor_sw128(smem_u32(sK + st * C::K_BYTES));
+      for (int s = 0; s <= nslots && ok; ++s) {
+        if (s < nslots) {
+          // S(s) = Q_h K_j^T into S buffer s & 1
+          const int it = s / GH, h = s - it * GH, sb = s & 1;
+          if (!mbar_wait_bounded(&s_free[sb], ((s >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+          if (h == 0 && !mbar_wait_bounded(&kv_full[it & 1], (it >> 1) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after_sync();
+          const uint64_t a = sdesc_kmajor_sw128(smem_u32(sQ + h * C::Q_BYTES));
+          const uint64_t bk = sdesc_kmajor_sw128(smem_u32(sK + (it & 1) * C::K_BYTES));
 #pragma unroll
-        for (int k = 0; k < kHD / 16; ++k)
-          umma_f16(tmem + x * kBK, a + 2 * k, bk + 2 * k, kIdescS, k > 0);
-        umma_commit(&s_full[x]);
-        any = true;
-      };
-      // the tiles' first S
-      if (ok && !mbar_wait_bounded(&kv_full[0], 0, abort_flag)) ok = false;
-      if (ok) {
-        tc_fence_after_sync();
-        for (int x = 0; x < 2; ++x)
-          if (active(x, j_lo)) issue_s(x, j_lo);
-      }
-      // Per KV tile j, per query tile X: P_X(j) V_j as soon as softmax X has
-      // written P_X(j), then right away S_X(j+1) - so the tensor core turns to
-      // X's next scores while the other tile's softmax is still running (ping-pong).
-      for (int it = 0; it < ntiles && ok; ++it) {
-        const int j = j_lo + it, st = it % kNS;
-        bool next_ready = false;
-#pragma unroll 1
-        for (int x = 0; x < 2 && ok; ++x) {
-          if (active(x, j)) {
-            if (!mbar_wait_bounded(&p_full[x], n_pv[x] & 1, abort_flag)) { ok = false; break; }
-            tc_fence_after_sync();
-#pragma unroll
-            for (int kb = 0; kb < 2; ++kb) {
-              const uint64_t bv = sdesc_kmajor_sw128(smem_u32(sVt + st * C::VT_BYTES + kb * C::VT_SUB));
-#pragma unroll
-              for (int k = 0; k < 4; ++k)   // 16 keys of P = 8 TMEM columns per MMA
-                umma_f16_tmem_a(tmem + C::TMEM_O + x * kHD, tmem + x * kBK + (kb * 4 + k) * 8, bv + 2 * k,
-                                kIdescO, (j > lo[x]) || kb || k);
-            }
-            umma_commit(&s_free[x]);
-            if (j == hi[x]) umma_commit(&o_done[x]);
-            ++n_pv[x];
-          }
-          if (active(x, j + 1)) {
-            if (!next_ready) {
-              if (!mbar_wait_bounded(&kv_full[(it + 1) % kNS], ((it + 1) / kNS) & 1, abort_flag)) { ok = false; break; }
-              next_ready = true;
-            }
-            // S_X shares its columns with P_X: the P V just issued must be done
-            if (n_pv[x] > 0 && !mbar_wait_bounded(&s_free[x], (n_pv[x] - 1) & 1, abort_flag)) { ok = false; break; }
-            tc_fence_after_sync();
-            issue_s(x, j + 1);
-          }
+          for (int k = 0; k < kHD / 16; ++k)
+            umma_f16(tmem + C::TMEM_S + sb * kBK, a + 2 * k, bk + 2 * k, kIdescS, k > 0);
+          any = true;
+          umma_commit(&s_full[sb]);
         }
-        if (!ok) break;
-        umma_commit(&kv_empty[st]);               // both tiles' P V of block j issued
+        if (s >= 1) {
+          // O_h += P(s-1) V_j
+          const int ps = s - 1, it = ps / GH, h = ps - it * GH, pb = ps & 1;
+          if (!mbar_wait_bounded(&p_full[pb], (ps >> 1) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after_sync();
+#pragma unroll
+          for (int kb = 0; kb < 2; ++kb) {
+            const uint64_t bv = sdesc_kmajor_sw128(smem_u32(sVt + (it & 1) * C::VT_BYTES + kb * C::VT_SUB));
+#pragma unroll
+            for (int k = 0; k < 4; ++k)   // 16 keys of P = 8 TMEM columns per MMA
+              umma_f16_tmem_a(tmem + h * kHD, tmem + C::TMEM_S + pb * kBK + (kb * 4 + k) * 8, bv + 2 * k,
+                              kIdescO, (it | kb | k) != 0);
+          }
+          umma_commit(&s_free[pb]);
+          umma_commit(&o_ready[h]);
+          if (h == GH - 1) umma_commit(&kv_empty[it & 1]);
+        }
       }
       if (!ok) {
         at_status(p.status, kAtTimeoutMma);
@@ -274,136 +257,154 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ---------------------------------------------- softmax warpgroup x (warps
-    // 2..5: tile A, 6..9: tile B), one query row per thread, all 128 keys
-    const int x = (warp - 2) >> 2;
+    // ---------------------------------------------- softmax: warps 2..5 take keys
+    // 0..63 of every tile (group 0), warps 6..9 keys 64..127 (group 1); one
+    // query row per thread.  The groups exchange partial row maxes in shared
+    // memory at a named-barrier reduction that also ANDs their health, so a
+    // bounded wait that gives up in one group stops both together.
     const int quarter = warp & 3;
+    const int grp = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;              // query row within the tile
-    const int t = q0 + x * kBQ + r;
-    const int tq0 = q0 + x * kBQ;
+    const int t = q0 + r;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const uint32_t s_col = lane_base + x * kBK;
-    const uint32_t o_col = lane_base + C::TMEM_O + x * kHD;
     const float sl2 = p.scale_log2;
-    float m = -INFINITY, l = 0.f;                   // running max (exp2 domain) and sum
+    float *red_max = reinterpret_cast<float *>(smem + C::OFF_RED);          // [2][2][128]
+    float *red_sum = red_max + 2 * 2 * 128;                                   // [2][4][128]
+    float m[GH], l[GH];                             // running max (shared value), partial sums
+#pragma unroll
+    for (int h = 0; h < GH; ++h) {
+      m[h] = -INFINITY;
+      l[h] = 0.f;
+    }
     bool alive = true;
-    int n = 0;
-    for (int j = lo[x]; j <= hi[x]; ++j, ++n) {
-      const int k0 = j * kBK;                       // first key of this tile
-      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&s_full[x], n & 1, abort_flag))) {
-        alive = false;
-        break;
-      }
-      tc_fence_after_sync();
-      const bool need_mask = (k0 + kBK - 1 > tq0) || (k0 < vs);
-      const int hi_e = t - k0, lo_e = vs - k0;      // keys k0+e visible iff lo_e <= e <= hi_e
-      // pass 1, the row max: the 128 scores in four loads in flight, one wait
-      float mx;
-      {
-        uint32_t sv[128];
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          tmem_ld32(s_col + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sv[32 * c]));
+    for (int s = 0; s < nslots; ++s) {
+      const int it = s / GH, h = s - it * GH, sb = s & 1;
+      const int k0 = (j_lo + it) * kBK + grp * 64;  // first key of this group's half tile
+      const bool ok = alive && __all_sync(0xffffffffu, mbar_wait_bounded(&s_full[sb], (s >> 1) & 1, abort_flag));
+      const bool need_mask = (k0 + 63 > q0) || (k0 < vs);
+      uint32_t sv[64];
+      float mx = -INFINITY;
+      if (ok) {
+        tc_fence_after_sync();
+        const uint32_t s_col = lane_base + C::TMEM_S + sb * kBK + grp * 64;
+        tmem_ld32(s_col, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+        tmem_ld32(s_col + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
         tmem_ld_wait();
-        float mc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        if (need_mask) {
+        // eight independent max chains (a single chain is latency-bound)
+        float mc[8];
 #pragma unroll
-          for (int e = 0; e < 128; ++e)
-            if (e <= hi_e && e >= lo_e) mc[e & 3] = fmaxf(mc[e & 3], __uint_as_float(sv[e]));
+        for (int q = 0; q < 8; ++q) mc[q] = -INFINITY;
+        if (need_mask) {
+          const int hi = t - k0, lo = vs - k0;
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            if (e <= hi && e >= lo) mc[e & 7] = fmaxf(mc[e & 7], __uint_as_float(sv[e]));
         } else {
 #pragma unroll
-          for (int e = 0; e < 128; e += 2)
-            mc[(e >> 1) & 3] = fmax3(mc[(e >> 1) & 3], __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
+          for (int e = 0; e < 64; e += 2)
+            mc[(e >> 1) & 7] = fmax3(mc[(e >> 1) & 7], __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
         }
-        mx = fmax3(fmaxf(mc[0], mc[1]), mc[2], mc[3]);
+        mx = fmaxf(fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3])), fmaxf(fmaxf(mc[4], mc[5]), fmaxf(mc[6], mc[7])));
       }
-      const float mxa = (mx == -INFINITY) ? -INFINITY : mx * sl2;   // into the exp2 domain
+      red_max[((s & 1) * 2 + grp) * 128 + r] = mx;
+      tc_fence_before_sync();                       // both groups' S reads precede any P write
+      alive = softmax_and(ok);
+      tc_fence_after_sync();
+      if (!alive) break;
+      float mxa = fmaxf(mx, red_max[((s & 1) * 2 + (grp ^ 1)) * 128 + r]);
+      mxa = (mxa == -INFINITY) ? -INFINITY : mxa * sl2;   // into the exp2 domain
+      float mh = m[h];
       float alpha = 1.f;
-      const bool resc = (m != -INFINITY) && (mxa > m + 8.f);
+      const bool resc = (mh != -INFINITY) && (mxa > mh + 8.f);
       if (resc) {
-        alpha = ex2_approx(m - mxa);
-        l *= alpha;
-        m = mxa;
-      } else if (m == -INFINITY) {
-        m = mxa;                                    // first visible key(s) of this row
+        alpha = ex2_approx(mh - mxa);
+        l[h] *= alpha;
+        mh = mxa;
+      } else if (mh == -INFINITY) {
+        mh = mxa;                                   // first visible key(s) of this row
       }
+      m[h] = mh;
       if (__any_sync(0xffffffffu, resc)) {
-        // O_X holds every earlier P V (S_X(j) was issued after P_X(j-1) V had
-        // completed); rescale it in TMEM.  tcgen05.ld/st are warp-collective:
-        // every lane takes part, alpha = 1 where the row's max did not move
-        uint32_t ov[32];
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          tmem_ld32(o_col + 32 * half, ov);
+        // O_h must hold every earlier P V before it is rescaled; each group
+        // rescales its 32 of the head's 64 columns
+        if (__all_sync(0xffffffffu, mbar_wait_bounded(&o_ready[h], (it - 1) & 1, abort_flag))) {
+          tc_fence_after_sync();
+          uint32_t ov[32];
+          tmem_ld32(lane_base + h * kHD + grp * 32, ov);
           tmem_ld_wait();
 #pragma unroll
           for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-          tmem_st32(o_col + 32 * half, ov);
-        }
-      }
-      const float mu = (m == -INFINITY) ? 0.f : m;
-      // pass 2: p = 2^(s*c - m) as f16 pairs over S_X's first 64 columns, in
-      // two halves of 64 keys (half h -> columns 32h..32h+31, over scores
-      // already read)
-      float ps[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t sv[64];
-        tmem_ld32(s_col + 64 * hf, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-        tmem_ld32(s_col + 64 * hf + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-        tmem_ld_wait();
-        uint32_t pk[32];
-        if (need_mask) {
-#pragma unroll
-          for (int e = 0; e < 64; e += 2) {
-            const int ee = 64 * hf + e;
-            const float x0 = (ee <= hi_e && ee >= lo_e) ? fmaf(__uint_as_float(sv[e]), sl2, -mu) : -INFINITY;
-            const float x1 = (ee + 1 <= hi_e && ee + 1 >= lo_e) ? fmaf(__uint_as_float(sv[e + 1]), sl2, -mu) : -INFINITY;
-            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-            ps[(e >> 1) & 3] += p0 + p1;
-            pk[e >> 1] = pack_f16x2(p0, p1);
-          }
+          tmem_st32(lane_base + h * kHD + grp * 32, ov);
+          tmem_st_wait();
         } else {
-#pragma unroll
-          for (int e = 0; e < 64; e += 2) {
-            const float p0 = ex2_approx(fmaf(__uint_as_float(sv[e]), sl2, -mu));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(sv[e + 1]), sl2, -mu));
-            ps[(e >> 1) & 3] += p0 + p1;
-            pk[e >> 1] = pack_f16x2(p0, p1);
-          }
+          alive = false;
         }
-        tmem_st32(s_col + 32 * hf, pk);
       }
-      tmem_st_wait();                               // P (and any O rescale) visible to the MMA
-      l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+      if (!alive) continue;                         // the next reduction stops both groups
+      const float mu = (mh == -INFINITY) ? 0.f : mh;
+      // p = 2^(s*c - m) as f16, packed two keys per TMEM column into the first
+      // 64 columns of this S buffer (this group's 64 keys -> 32 columns)
+      uint32_t pk[32];
+      float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // eight partial sums
+      if (need_mask) {
+        // keys k0+e visible iff lo <= e <= hi (causal and padding limits)
+        const int hi = t - k0, lo = vs - k0;
+#pragma unroll
+        for (int e = 0; e < 64; e += 2) {
+          const float x0 = (e <= hi && e >= lo) ? fmaf(__uint_as_float(sv[e]), sl2, -mu) : -INFINITY;
+          const float x1 = (e + 1 <= hi && e + 1 >= lo) ? fmaf(__uint_as_float(sv[e + 1]), sl2, -mu) : -INFINITY;
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          ps[e & 7] += p0;
+          ps[(e + 1) & 7] += p1;
+          pk[e >> 1] = pack_f16x2(p0, p1);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 64; e += 2) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(sv[e]), sl2, -mu));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(sv[e + 1]), sl2, -mu));
+          ps[e & 7] += p0;
+          ps[(e + 1) & 7] += p1;
+          pk[e >> 1] = pack_f16x2(p0, p1);
+        }
+      }
+      tmem_st32(lane_base + C::TMEM_S + sb * kBK + grp * 32, pk);
+      tmem_st_wait();
+      l[h] += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       tc_fence_before_sync();
-      mbar_arrive(&p_full[x]);
+      mbar_arrive(&p_full[sb]);
     }
     // ------------------------------------------------ normalise and store
-    if (hi[x] >= lo[x]) {
-      if (alive && !__all_sync(0xffffffffu, mbar_wait_bounded(&o_done[x], 0, abort_flag))) alive = false;
-      if (!alive) {
-        if (lane == 0) at_status(p.status, kAtTimeoutSoftmax);
-        *abort_flag = 1;
-      } else {
-        tc_fence_after_sync();
-        const bool row_ok = t < T;
-        const long long ldo = (long long)p.H * kHD;
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-#pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
-          uint32_t ov[32];
-          tmem_ld32(o_col + 32 * half, ov);
-          tmem_ld_wait();
-          if (row_ok) {
-            f16 *dst = p.o + ((long long)b * T + t) * ldo + (long long)h * kHD + half * 32;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const float *f = reinterpret_cast<const float *>(&ov[8 * q]);
-              const uint4 w = make_uint4(pack_f16x2(f[0] * inv, f[1] * inv), pack_f16x2(f[2] * inv, f[3] * inv),
-                                         pack_f16x2(f[4] * inv, f[5] * inv), pack_f16x2(f[6] * inv, f[7] * inv));
-              *reinterpret_cast<uint4 *>(dst + 8 * q) = w;
-            }
+    for (int h = 0; h < GH; ++h) red_sum[(grp * 4 + h) * 128 + r] = l[h];
+    alive = softmax_and(alive);
+    if (!alive) {
+      if (lane == 0) at_status(p.status, kAtTimeoutSoftmax);
+      *abort_flag = 1;
+    } else {
+      const bool row_ok = t < T;
+      const long long ldo = (long long)p.H * kHD;
+#pragma unroll 1
+      for (int h = 0; h < GH; ++h) {
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&o_ready[h], (ntiles - 1) & 1, abort_flag))) {
+          if (lane == 0) at_status(p.status, kAtTimeoutSoftmax);
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after_sync();
+        const float lt = red_sum[h * 128 + r] + red_sum[(4 + h) * 128 + r];
+        const float inv = lt > 0.f ? 1.f / lt : 0.f;
+        uint32_t ov[32];
+        tmem_ld32(lane_base + h * kHD + grp * 32, ov);
+        tmem_ld_wait();
+        if (row_ok) {
+          f16 *dst = p.o + ((long long)b * T + t) * ldo + (long long)(h_first + h) * kHD + grp * 32;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float *f = reinterpret_cast<const float *>(&ov[8 * q]);
+            const uint4 w = make_uint4(pack_f16x2(f[0] * inv, f[1] * inv), pack_f16x2(f[2] * inv, f[3] * inv),
+                                       pack_f16x2(f[4] * inv, f[5] * inv), pack_f16x2(f[6] * inv, f[7] * inv));
+            *reinterpret_cast<uint4 *>(dst + 8 * q) = w;
           }
         }
       }
@@ -418,36 +419,51 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-cudaError_t launch_at(const AttnParams &a, const CUtensorMap &tq, const CUtensorMap &tk,
+template <int GH>
+cudaError_t launch_gh(const AttnParams &a, const CUtensorMap &tq, const CUtensorMap &tk,
                       const CUtensorMap &tv, cudaStream_t st) {
-  using C = AtCfg;
-  constexpr auto kern = attn_tc_kernel;
-  cudaError_t e = ensure_smem_attr<kern>(C::SMEM);
+  using C = AtCfg<GH>;
+  auto kern = attn_tc_kernel<GH>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   AtParams p{};
   p.o = a.o;
   p.valid_start = a.valid_start;
   p.B = a.B; p.T = a.T; p.H = a.H; p.KV = a.KV;
   p.G = a.H / a.KV;
+  p.GH = GH;
+  p.n_hsub = p.G / GH;
   p.scale_log2 = a.scale_log2;
   p.status = a.status;
-  dim3 grid((unsigned)(a.B * a.H), (unsigned)cdiv(a.T, 2 * kBQ), 1u);
+  dim3 grid((unsigned)(a.B * a.KV * p.n_hsub), (unsigned)cdiv(a.T, kBQ), 1u);
   kern<<<grid, kThreads, C::SMEM, st>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-bool attention_tc_supported(int hd, int H, int KV) { return hd == kHD && KV > 0 && H % KV == 0; }
+bool attention_tc_supported(int hd, int H, int KV) {
+  const int G = H / KV;
+  return hd == kHD && (G == 1 || G == 2 || G == 3 || G == 4 || G == 6 || G == 8);
+}
 
 cudaError_t launch_attention_tc(const AttnParams &a, cudaStream_t st) {
   if (!attention_tc_supported(a.hd, a.H, a.KV) || a.v_t == nullptr) return cudaErrorInvalidConfiguration;
   CUtensorMap tq, tk, tv;
-  if (!get_tmap_f16(&tq, a.q, (uint64_t)a.B * a.H * a.T, kHD, kHD, kBQ)) return cudaErrorInvalidValue;
-  if (!get_tmap_f16(&tk, a.k, (uint64_t)a.B * a.KV * a.T, kHD, kHD, kBK)) return cudaErrorInvalidValue;
+  if (!make_tmap_f16(&tq, a.q, (uint64_t)a.B * a.H * a.T, kHD, kHD, kBQ)) return cudaErrorInvalidValue;
+  if (!make_tmap_f16(&tk, a.k, (uint64_t)a.B * a.KV * a.T, kHD, kHD, kBK)) return cudaErrorInvalidValue;
   // V^T: rows are (b, kv head, dim), columns are keys; columns >= T read as zero
-  if (!get_tmap_f16(&tv, a.v_t, (uint64_t)a.B * a.KV * kHD, a.T, a.T_pad, kHD)) return cudaErrorInvalidValue;
-  return launch_at(a, tq, tk, tv, st);
+  if (!make_tmap_f16(&tv, a.v_t, (uint64_t)a.B * a.KV * kHD, a.T, a.T_pad, kHD)) return cudaErrorInvalidValue;
+  const int G = a.H / a.KV;
+  switch (G) {
+    case 1: return launch_gh<1>(a, tq, tk, tv, st);
+    case 2: return launch_gh<2>(a, tq, tk, tv, st);
+    case 3: return launch_gh<3>(a, tq, tk, tv, st);
+    case 4: return launch_gh<4>(a, tq, tk, tv, st);
+    case 6: return launch_gh<3>(a, tq, tk, tv, st);   // two CTAs per group of six
+    case 8: return launch_gh<4>(a, tq, tk, tv, st);
+  }
+  return cudaErrorInvalidConfiguration;
 }
 
 }  // namespace smol
