@@ -358,6 +358,365 @@ __global__ void __launch_bounds__(128) decode_attn_mma_kernel(const __grid_const
 }
 
 
+// Persistent decode attention on tensor cores (hd = 64).  The work items are
+// (sequence, kv head, 256-key chunk), numbered sequence-major; CTA c takes the
+// contiguous range [c*per, (c+1)*per) (per = ceil(items / CTAs)), so every CTA
+// streams about the same number of K/V bytes.  A producer warp keeps a ring of
+// kDecStages chunks in flight (two 2-D TMA boxes each, 128-byte swizzle); eight
+// compute warps take 32 keys each of every chunk with the same bf16 hi/lo
+// mma.sync scheme as decode_attn_mma_kernel and carry a running (max, sum,
+// output) per warp across the chunks of one (sequence, kv head).  When a
+// CTA's run of chunks of a pair ends, the warps merge; a pair covered by one
+// CTA is written directly, otherwise each CTA writes a partial and the last to
+// finish (atomic counter, no waiting) merges them.
+constexpr int kDecStages = 3;
+constexpr int kDecMaxB = 2048;                    // prefix table in shared memory
+
+__device__ __forceinline__ void compute_bar() {   // the compute warps of the persistent kernel
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+}
+// AND of pred over the compute warps (also a barrier among them).
+__device__ __forceinline__ bool compute_and(bool pred) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, 256, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(out)
+      : "r"((uint32_t)pred)
+      : "memory");
+  return out != 0;
+}
+
+constexpr int kPersistWarps = 8;                 // compute warps: 32 keys of every chunk each
+
+template <int GM>
+__global__ void __launch_bounds__((kPersistWarps + 1) * 32, 1) decode_attn_persist_kernel(const __grid_constant__ CUtensorMap tmK,
+                                                                     const __grid_constant__ CUtensorMap tmV,
+                                                                     const DecAttnParams p) {
+  constexpr int HD = 64, NW = kPersistWarps, NS = kDecStages;
+  constexpr int KPW = kChunk / NW;                // keys per warp
+  static_assert(NW * 32 == 256, "compute_bar / compute_and count 256 threads");
+  constexpr int N16 = KPW / 16;                   // 16-key groups per warp
+  constexpr int STAGE = 2 * kChunk * 128;         // K and V rows of one chunk
+  extern __shared__ uint8_t dsm_raw[];
+  uint8_t *dsm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t *full = reinterpret_cast<uint64_t *>(dsm + NS * STAGE);   // [NS]
+  uint64_t *empty = full + NS;                                        // [NS], one arrival per compute warp
+  int *s_last = reinterpret_cast<int *>(empty + NS);
+  volatile int *abort_flag = s_last + 1;
+  float *red_m = reinterpret_cast<float *>(s_last + 4);               // [NW][GM]
+  float *red_l = red_m + NW * GM;                                     // [NW][GM]
+  float *red_o = red_l + NW * GM;                                     // [NW][GM][HD]
+  int *prefix = reinterpret_cast<int *>(red_o + NW * GM * HD);        // [B + 1] chunks before sequence b
+
+  const int G = p.H / p.KV;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int lmax = min(p.S_max, p.max_pos - 1);
+  auto clamp_len = [&](int L) { return L < 0 ? 0 : (L > lmax ? lmax : L); };
+
+  // chunk counts and their prefix sums (cache_len is an input of the step)
+  if (warp == 0) {
+    int run = 0;
+    for (int b0 = 0; b0 < p.B; b0 += 32) {
+      const int bb = b0 + lane;
+      const int n = bb < p.B ? (clamp_len(p.cache_len[bb]) + 1 + kChunk - 1) / kChunk : 0;
+      int v = n;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += t;
+      }
+      if (bb < p.B) prefix[bb + 1] = run + v;
+      run += __shfl_sync(0xffffffffu, v, 31);
+    }
+    if (lane == 0) prefix[0] = 0;
+  }
+  if (threadIdx.x == 32) {
+    for (int s2 = 0; s2 < NS; ++s2) {
+      mbar_init(&full[s2], 1);
+      mbar_init(&empty[s2], NW);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const int total = p.KV * prefix[p.B];
+  const int per = (total + gridDim.x - 1) / gridDim.x;
+  const int i0 = blockIdx.x * per, i1 = min(total, i0 + per);
+  if (i0 >= i1) return;                            // uniform: nothing for this CTA
+  // item -> (sequence, kv head, chunk, chunks of the sequence)
+  auto decode_item = [&](int i, int &b, int &kvh, int &ch, int &nsp) {
+    int lo = 0, hi = p.B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.KV * prefix[mid] <= i) lo = mid;
+      else hi = mid - 1;
+    }
+    b = lo;
+    nsp = prefix[b + 1] - prefix[b];
+    const int r = i - p.KV * prefix[b];
+    kvh = r / nsp;
+    ch = r - kvh * nsp;
+  };
+
+  if (warp == NW) {
+    // ------------------------------------------------ producer (the cache is
+    // an input of the step: requested before waiting on the preceding kernel)
+    if (lane == 0) {
+      griddep_launch_dependents();
+      int stage = 0, phase = 0;
+      long long issued = 0;
+      bool ok = true;
+      for (int i = i0; i < i1; ++i) {
+        int b, kvh, ch, nsp;
+        decode_item(i, b, kvh, ch, nsp);
+        if (!mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const int y = static_cast<int>(((long long)p.layer * p.B + b) * p.KV + kvh) * p.S_max + ch * kChunk;
+        mbar_arrive_expect_tx(&full[stage], STAGE);
+        tma_load_2d(dsm + stage * STAGE, &tmK, &full[stage], 0, y);
+        tma_load_2d(dsm + stage * STAGE + kChunk * 128, &tmV, &full[stage], 0, y);
+        ++issued;
+        if (++stage == NS) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) {
+        atomicCAS(p.status, 0, kDevTimeoutProducer);
+        *abort_flag = 1;
+      }
+      // every copy issued has landed before the CTA may exit
+      int dummy = 0;
+      const long long first = issued > NS ? issued - NS : 0;
+      for (long long j = first; j < issued; ++j)
+        if (!mbar_wait_bounded(&full[j % NS], (uint32_t)((j / NS) & 1), reinterpret_cast<volatile int *>(&dummy)))
+          atomicCAS(p.status, 0, kDevTimeoutDrain);
+    }
+    return;
+  }
+
+  // -------------------------------------------------- compute warps 0..3
+  griddep_wait();                                  // q, k_new, v_new, partials, counters
+  const int r = lane >> 2, c2 = (lane & 3) * 2;    // fragment row (head) and column pair
+  const int kw0 = warp * KPW;                      // this warp's keys within a chunk
+  int stage = 0, phase = 0;
+  int cur_pair = -1;
+  uint32_t qa[4][4];
+  float mw = -INFINITY, lw = 0.f;                  // running max / sum of head r (this warp)
+  float o[8][4];
+  bool alive = true;
+  for (int i = i0; i < i1; ++i) {
+    int b, kvh, ch, nsp;
+    decode_item(i, b, kvh, ch, nsp);
+    const int pair = b * p.KV + kvh;
+    if (pair != cur_pair) {
+      cur_pair = pair;
+      mw = -INFINITY;
+      lw = 0.f;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) o[q][0] = o[q][1] = o[q][2] = o[q][3] = 0.f;
+      // q as A fragments (rows r < G: bf16 hi part; rows r + 8: the lo remainder)
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        if (r < G) {
+          const f16 *qr = p.q + ((long long)b * p.H + kvh * G + r) * HD + kk * 16 + c2;
+          const float2 a2 = unpack_f16x2(*reinterpret_cast<const uint32_t *>(qr));
+          const float2 b2 = unpack_f16x2(*reinterpret_cast<const uint32_t *>(qr + 8));
+          float h0, l0, h1, l1, h2, l2, h3, l3;
+          split_bf16(a2.x, h0, l0);
+          split_bf16(a2.y, h1, l1);
+          split_bf16(b2.x, h2, l2);
+          split_bf16(b2.y, h3, l3);
+          qa[kk][0] = pack_bf16x2(h0, h1);
+          qa[kk][1] = pack_bf16x2(l0, l1);
+          qa[kk][2] = pack_bf16x2(h2, h3);
+          qa[kk][3] = pack_bf16x2(l2, l3);
+        } else {
+          qa[kk][0] = qa[kk][1] = qa[kk][2] = qa[kk][3] = 0u;
+        }
+      }
+    }
+    const int Lb = clamp_len(p.cache_len[b]);
+    const int k_begin = ch * kChunk;
+    const int n_valid = min(kChunk, Lb + 1 - k_begin);
+    // the four warps decide together (they meet at named barriers below)
+    if (!compute_and(mbar_wait_bounded(&full[stage], phase, abort_flag))) {
+      alive = false;
+      break;
+    }
+    uint8_t *sK = dsm + stage * STAGE, *sV = sK + kChunk * 128;
+    // this warp's keys: the new token's key/value into its slot, V rows past
+    // the valid keys zeroed (unused cache slots must not inject NaN)
+    const int slot = Lb - k_begin;
+    if (slot >= kw0 && slot < kw0 + KPW && lane < 8) {
+      const long long row = (long long)b * p.KV + kvh;
+      *reinterpret_cast<uint4 *>(sK + slot * 128 + ((lane ^ (slot & 7)) << 4)) =
+          reinterpret_cast<const uint4 *>(p.k_new + row * HD)[lane];
+      *reinterpret_cast<uint4 *>(sV + slot * 128 + ((lane ^ (slot & 7)) << 4)) =
+          reinterpret_cast<const uint4 *>(p.v_new + row * HD)[lane];
+    }
+    for (int e = max(n_valid, kw0) * 8 + lane; e < (kw0 + KPW) * 8; e += 32)
+      reinterpret_cast<uint4 *>(sV)[e] = make_uint4(0u, 0u, 0u, 0u);
+    __syncwarp();
+    if (kw0 < n_valid) {                           // warp-uniform
+      float s[2 * N16][4];
+#pragma unroll
+      for (int q = 0; q < 2 * N16; ++q) s[q][0] = s[q][1] = s[q][2] = s[q][3] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+        for (int j = 0; j < N16; ++j) {
+          const int key = kw0 + j * 16 + (lane & 7) + ((lane >> 4) << 3);
+          const int chunk = kk * 2 + ((lane >> 3) & 1);
+          uint32_t bk[4];
+          ldsm_x4(bk, sK + key * 128 + ((chunk ^ (key & 7)) << 4));
+          mma_bf16_16816(s[2 * j], qa[kk], bk[0], bk[1]);
+          mma_bf16_16816(s[2 * j + 1], qa[kk], bk[2], bk[3]);
+        }
+      }
+      // head r's score = hi row + lo row, in the exp2 domain; keys past the valid range masked
+      float sc[2 * N16][2];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 2 * N16; ++j) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int key = kw0 + 8 * j + c2 + e;
+          const float v = key < n_valid ? (s[j][e] + s[j][2 + e]) * p.scale_log2 : -INFINITY;
+          sc[j][e] = v;
+          mx = fmaxf(mx, v);
+        }
+      }
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float m_new = fmaxf(mw, mx);
+      const float mu = (m_new == -INFINITY) ? 0.f : m_new;
+      const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - mu);    // rescale of the running state
+      float sum = 0.f;
+#pragma unroll
+      for (int j = 0; j < 2 * N16; ++j) {
+        sc[j][0] = exp2f(sc[j][0] - mu);
+        sc[j][1] = exp2f(sc[j][1] - mu);
+        sum += sc[j][0] + sc[j][1];
+      }
+      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+      lw = lw * f + sum;
+      mw = m_new;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        o[q][0] *= f; o[q][1] *= f; o[q][2] *= f; o[q][3] *= f;
+      }
+#pragma unroll
+      for (int kk = 0; kk < N16; ++kk) {
+        float h0, l0, h1, l1, h2, l2, h3, l3;
+        split_bf16(sc[2 * kk][0], h0, l0);
+        split_bf16(sc[2 * kk][1], h1, l1);
+        split_bf16(sc[2 * kk + 1][0], h2, l2);
+        split_bf16(sc[2 * kk + 1][1], h3, l3);
+        const uint32_t a[4] = {pack_bf16x2(h0, h1), pack_bf16x2(l0, l1), pack_bf16x2(h2, h3),
+                               pack_bf16x2(l2, l3)};
+#pragma unroll
+        for (int nd = 0; nd < 4; ++nd) {
+          const int key = kw0 + kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+          const int chunk = nd * 2 + (lane >> 4);
+          uint32_t bv[4];
+          ldsm_x4_t(bv, sV + key * 128 + ((chunk ^ (key & 7)) << 4));
+          mma_bf16_16816(o[2 * nd], a, bv[0], bv[1]);
+          mma_bf16_16816(o[2 * nd + 1], a, bv[2], bv[3]);
+        }
+      }
+    }
+    // the stage goes back to the producer (generic writes above precede the next TMA fill)
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[stage]);
+    if (++stage == NS) {
+      stage = 0;
+      phase ^= 1;
+    }
+    if (i + 1 < i1 && ch + 1 < nsp) continue;      // this CTA's run of the pair goes on
+    // ---- end of this CTA's run of chunks of the pair: merge the warps
+    if (r < G) {
+      if ((lane & 3) == 0) {
+        red_m[warp * GM + r] = mw;
+        red_l[warp * GM + r] = lw;
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        red_o[(warp * GM + r) * HD + 8 * q + c2] = o[q][0] + o[q][2];
+        red_o[(warp * GM + r) * HD + 8 * q + c2 + 1] = o[q][1] + o[q][3];
+      }
+    }
+    compute_bar();
+    const int pair_first = p.KV * prefix[b] + kvh * nsp;   // the pair's first item
+    const int c_first = pair_first / per;
+    const int nseg = (pair_first + nsp - 1) / per - c_first + 1;
+    const int seg = blockIdx.x - c_first;
+    const long long pbase = (long long)b * p.H + kvh * G;   // first query head of the group
+    for (int t = threadIdx.x; t < G * HD; t += NW * 32) {
+      const int g = t / HD, dim = t - g * HD;
+      float M = -INFINITY;
+      for (int w = 0; w < NW; ++w) M = fmaxf(M, red_m[w * GM + g]);
+      const float Mu = (M == -INFINITY) ? 0.f : M;
+      float Ls = 0.f, Os = 0.f;
+      for (int w = 0; w < NW; ++w) {
+        const float fw = exp2f(red_m[w * GM + g] - Mu);
+        Ls += red_l[w * GM + g] * fw;
+        Os += red_o[(w * GM + g) * HD + dim] * fw;
+      }
+      if (nseg == 1) {
+        p.o[(pbase + g) * HD + dim] = __float2half_rn(Ls > 0.f ? Os / Ls : 0.f);
+      } else {
+        const long long ps = (pbase + g) * p.max_splits + seg;
+        if (dim == 0) {
+          p.part_m[ps] = M;
+          p.part_l[ps] = Ls;
+        }
+        p.part_o[ps * HD + dim] = Os;
+      }
+    }
+    if (nseg > 1) {
+      __threadfence();
+      compute_bar();
+      if (threadIdx.x == 0) {
+        const int prev = atomicAdd(p.counters + pair, 1);
+        *s_last = (prev == nseg - 1);
+        if (prev == nseg - 1) p.counters[pair] = 0;   // ready for the next layer
+      }
+      compute_bar();
+      if (*s_last) {
+        __threadfence();
+        for (int t = threadIdx.x; t < G * HD; t += NW * 32) {
+          const int g = t / HD, dim = t - g * HD;
+          const long long ps0 = (pbase + g) * p.max_splits;
+          float M = -INFINITY;
+          for (int s2 = 0; s2 < nseg; ++s2) M = fmaxf(M, __ldcg(p.part_m + ps0 + s2));
+          const float Mu = (M == -INFINITY) ? 0.f : M;
+          float Ls = 0.f, Os = 0.f;
+          for (int s2 = 0; s2 < nseg; ++s2) {
+            const float fw = exp2f(__ldcg(p.part_m + ps0 + s2) - Mu);
+            Ls += __ldcg(p.part_l + ps0 + s2) * fw;
+            Os += __ldcg(p.part_o + (ps0 + s2) * HD + dim) * fw;
+          }
+          p.o[(pbase + g) * HD + dim] = __float2half_rn(Ls > 0.f ? Os / Ls : 0.f);
+        }
+      }
+    }
+    compute_bar();                                  // red_* reused by the next run
+  }
+  if (!alive) {
+    if (lane == 0) atomicCAS(p.status, 0, kDevTimeoutEpilogue);
+    *abort_flag = 1;
+  }
+}
+
 // GM: compile-time bound on the group size g = H / KV (arrays are sized GM).
 template <int HD, int GM>
 __global__ void __launch_bounds__(kDecWarps * 32) decode_attn_kernel(const DecAttnParams p) {
@@ -601,16 +960,35 @@ static cudaError_t launch_decode_attn_mma_g(const CUtensorMap &tk, const CUtenso
   return launch_pdl(kern, grid, dim3(NW * 32), smem, st, tk, tv, ap);
 }
 
+template <int GM>
+static cudaError_t launch_decode_attn_persist_g(const CUtensorMap &tk, const CUtensorMap &tv,
+                                                const DecAttnParams &ap, int sms, cudaStream_t st) {
+  constexpr int NW = kPersistWarps, HD = 64;
+  const int smem = 1024 + kDecStages * 2 * kChunk * 128 + 2 * kDecStages * 8 + 16 +
+                   (2 * NW * GM + NW * GM * HD) * 4 + (ap.B + 1) * 4;
+  constexpr auto kern = decode_attn_persist_kernel<GM>;
+  cudaError_t e = ensure_smem_attr<kern>(smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(kern, dim3(sms), dim3((NW + 1) * 32), smem, st, tk, tv, ap);
+}
+
 // head_dim 64 runs on tensor cores (the cache seen as one 2-D tensor of
 // L*B*KV*S_max rows of 64 values); other head sizes on the CUDA-core kernel.
 static cudaError_t launch_decode_attn(const DecAttnParams &ap, int hd, dim3 grid, cudaStream_t st,
-                                      const bf16 *k_all, const bf16 *v_all, int L) {
+                                      const bf16 *k_all, const bf16 *v_all, int L, int sms) {
   if (hd == 64) {
     CUtensorMap tk, tv;
     const uint64_t rows = (uint64_t)L * ap.B * ap.KV * ap.S_max;
     if (!get_tmap_f16(&tk, k_all, rows, 64, 64, kChunk)) return cudaErrorInvalidValue;
     if (!get_tmap_f16(&tv, v_all, rows, 64, 64, kChunk)) return cudaErrorInvalidValue;
     const int G = ap.H / ap.KV;
+    if (ap.B <= kDecMaxB) {
+      if (G == 1) return launch_decode_attn_persist_g<1>(tk, tv, ap, sms, st);
+      if (G == 2) return launch_decode_attn_persist_g<2>(tk, tv, ap, sms, st);
+      if (G == 3) return launch_decode_attn_persist_g<3>(tk, tv, ap, sms, st);
+      if (G == 4) return launch_decode_attn_persist_g<4>(tk, tv, ap, sms, st);
+      return launch_decode_attn_persist_g<8>(tk, tv, ap, sms, st);
+    }
     if (G == 1) return launch_decode_attn_mma_g<1>(tk, tv, ap, grid, st);
     if (G == 2) return launch_decode_attn_mma_g<2>(tk, tv, ap, grid, st);
     if (G == 3) return launch_decode_attn_mma_g<3>(tk, tv, ap, grid, st);
@@ -689,7 +1067,7 @@ cudaError_t run_decode(const DecodeArgs &a, void *ws, int sms, cudaStream_t st, 
     const int lmax = min(a.S_max, c.max_pos - 1);
     dim3 grid((unsigned)cdiv(lmax + 1, kChunk), (unsigned)KV, (unsigned)B);
     ap.layer = l;
-    DEC_LAUNCH_K(SMOL_K_DEC_ATTN, launch_decode_attn(ap, hd, grid, st, a.k_cache, a.v_cache, L));
+    DEC_LAUNCH_K(SMOL_K_DEC_ATTN, launch_decode_attn(ap, hd, grid, st, a.k_cache, a.v_cache, L, sms));
 
     GemmParams po{};
     po.M = B; po.N = d; po.K = H * hd; po.out = h; po.out_is_f16 = 1; po.ldo = d; po.resid_f16 = x;
