@@ -361,75 +361,76 @@ __global__ void __launch_bounds__(128) decode_attn_mma_kernel(const __grid_const
 // Persistent decode attention on tensor cores (hd = 64).  The work items are
 // (sequence, kv head, 256-key chunk), numbered sequence-major; CTA c takes the
 // contiguous range [c*per, (c+1)*per) (per = ceil(items / CTAs)), so every CTA
-// streams about the same number of K/V bytes.  A producer warp keeps a ring of
-// kDecStages chunks in flight (two 2-D TMA boxes each, 128-byte swizzle); eight
-// compute warps take 32 keys each of every chunk with the same bf16 hi/lo
-// mma.sync scheme as decode_attn_mma_kernel and carry a running (max, sum,
-// output) per warp across the chunks of one (sequence, kv head).  When a
-// CTA's run of chunks of a pair ends, the warps merge; a pair covered by one
-// CTA is written directly, otherwise each CTA writes a partial and the last to
-// finish (atomic counter, no waiting) merges them.
-constexpr int kDecStages = 3;
-constexpr int kDecMaxB = 2048;                    // prefix table in shared memory
-
-__device__ __forceinline__ void compute_bar() {   // the compute warps of the persistent kernel
-  asm volatile("bar.sync 1, 256;" ::: "memory");
-}
-// AND of pred over the compute warps (also a barrier among them).
-__device__ __forceinline__ bool compute_and(bool pred) {
-  uint32_t out;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, 1, 256, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(out)
-      : "r"((uint32_t)pred)
-      : "memory");
-  return out != 0;
-}
-
-constexpr int kPersistWarps = 8;                 // compute warps: 32 keys of every chunk each
+// streams about the same number of K/V bytes.  Three kinds of warps:
+//  - a producer warp keeps a ring of NS chunks in flight (two 2-D TMA boxes
+//    each, 128-byte swizzle);
+//  - eight compute warps take 32 keys each of every chunk with the same bf16
+//    hi/lo mma.sync scheme as decode_attn_mma_kernel and carry a running
+//    (max, sum, output) per warp across the chunks of one (sequence, kv head).
+//    They never wait for one another: each releases a ring slot on its own;
+//  - two merge warps: when a CTA's run of chunks of a pair ends, the compute
+//    warps hand their states over through one of two shared-memory buffers
+//    (runs alternate between them) and go on with the next pair, while the
+//    buffer's merge warp combines the eight states.  A pair covered by one CTA is written directly; otherwise each
+//    CTA writes a partial and the last to finish (atomic counter, no waiting)
+//    merges them.
+constexpr int kDecMaxB = 2048;                    // per-sequence tables in shared memory
+constexpr int kPersistWarps = 8;                  // compute warps: 32 keys of every chunk each
 
 template <int GM>
-__global__ void __launch_bounds__((kPersistWarps + 1) * 32, 1) decode_attn_persist_kernel(const __grid_constant__ CUtensorMap tmK,
+__host__ __device__ constexpr int persist_stages() { return GM <= 4 ? 3 : 2; }
+
+// Shared memory of the persistent kernel: ring, barriers, two merge buffers,
+// the clamped cache lengths and the chunk prefix sums.
+template <int GM>
+constexpr int persist_smem_fixed() {
+  return 1024 + persist_stages<GM>() * 2 * kChunk * 128 + (2 * persist_stages<GM>() + 4) * 8 + 16 +
+         2 * kPersistWarps * GM * (2 + 64) * 4;
+}
+
+template <int GM>
+__global__ void __launch_bounds__((kPersistWarps + 3) * 32, 1) decode_attn_persist_kernel(const __grid_constant__ CUtensorMap tmK,
                                                                      const __grid_constant__ CUtensorMap tmV,
                                                                      const DecAttnParams p) {
-  constexpr int HD = 64, NW = kPersistWarps, NS = kDecStages;
+  constexpr int HD = 64, NW = kPersistWarps, NS = persist_stages<GM>();
   constexpr int KPW = kChunk / NW;                // keys per warp
-  static_assert(NW * 32 == 256, "compute_bar / compute_and count 256 threads");
   constexpr int N16 = KPW / 16;                   // 16-key groups per warp
   constexpr int STAGE = 2 * kChunk * 128;         // K and V rows of one chunk
+  constexpr int RED = NW * GM * (2 + HD);         // floats of one merge buffer
   extern __shared__ uint8_t dsm_raw[];
   uint8_t *dsm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint64_t *full = reinterpret_cast<uint64_t *>(dsm + NS * STAGE);   // [NS]
-  uint64_t *empty = full + NS;                                        // [NS], one arrival per compute warp
-  int *s_last = reinterpret_cast<int *>(empty + NS);
-  volatile int *abort_flag = s_last + 1;
-  float *red_m = reinterpret_cast<float *>(s_last + 4);               // [NW][GM]
-  float *red_l = red_m + NW * GM;                                     // [NW][GM]
-  float *red_o = red_l + NW * GM;                                     // [NW][GM][HD]
-  int *prefix = reinterpret_cast<int *>(red_o + NW * GM * HD);        // [B + 1] chunks before sequence b
+  uint64_t *empty = full + NS;                                        // [NS], NW arrivals
+  uint64_t *mfull = empty + NS;                                       // [2], NW * 32 arrivals
+  uint64_t *mempty = mfull + 2;                                       // [2], 32 arrivals (merge warp m owns buffer m)
+  volatile int *abort_flag = reinterpret_cast<int *>(mempty + 2);
+  float *red = reinterpret_cast<float *>(mempty + 2) + 4;             // [2][RED]
+  int *lens = reinterpret_cast<int *>(red + 2 * RED);                 // [B] clamped cache lengths
+  int *prefix = lens + p.B;                                           // [B + 1] chunks before sequence b
 
   const int G = p.H / p.KV;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int lmax = min(p.S_max, p.max_pos - 1);
-  auto clamp_len = [&](int L) { return L < 0 ? 0 : (L > lmax ? lmax : L); };
 
-  // chunk counts and their prefix sums (cache_len is an input of the step)
+  // clamped lengths, chunk counts and their prefix sums (cache_len is an input of the step)
   if (warp == 0) {
     int run = 0;
     for (int b0 = 0; b0 < p.B; b0 += 32) {
       const int bb = b0 + lane;
-      const int n = bb < p.B ? (clamp_len(p.cache_len[bb]) + 1 + kChunk - 1) / kChunk : 0;
+      int Lb = bb < p.B ? p.cache_len[bb] : 0;
+      Lb = Lb < 0 ? 0 : (Lb > lmax ? lmax : Lb);
+      const int n = bb < p.B ? (Lb + 1 + kChunk - 1) / kChunk : 0;
       int v = n;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int t = __shfl_up_sync(0xffffffffu, v, o);
         if (lane >= o) v += t;
       }
-      if (bb < p.B) prefix[bb + 1] = run + v;
+      if (bb < p.B) {
+        lens[bb] = Lb;
+        prefix[bb + 1] = run + v;
+      }
       run += __shfl_sync(0xffffffffu, v, 31);
     }
     if (lane == 0) prefix[0] = 0;
@@ -439,6 +440,10 @@ __global__ void __launch_bounds__((kPersistWarps + 1) * 32, 1) decode_attn_persi
       mbar_init(&full[s2], 1);
       mbar_init(&empty[s2], NW);
     }
+    for (int s2 = 0; s2 < 2; ++s2) {
+      mbar_init(&mfull[s2], NW * 32);
+      mbar_init(&mempty[s2], 32);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -447,8 +452,9 @@ __global__ void __launch_bounds__((kPersistWarps + 1) * 32, 1) decode_attn_persi
   const int per = (total + gridDim.x - 1) / gridDim.x;
   const int i0 = blockIdx.x * per, i1 = min(total, i0 + per);
   if (i0 >= i1) return;                            // uniform: nothing for this CTA
-  // item -> (sequence, kv head, chunk, chunks of the sequence)
-  auto decode_item = [&](int i, int &b, int &kvh, int &ch, int &nsp) {
+  // item -> (sequence, kv head, chunk, chunks of the sequence): a search for
+  // the first item, then one step per item
+  auto seek = [&](int i, int &b, int &kvh, int &ch, int &nsp) {
     int lo = 0, hi = p.B - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -461,6 +467,14 @@ __global__ void __launch_bounds__((kPersistWarps + 1) * 32, 1) decode_attn_persi
     kvh = r / nsp;
     ch = r - kvh * nsp;
   };
+  auto step = [&](int &b, int &kvh, int &ch, int &nsp) {
+    if (++ch < nsp) return;
+    ch = 0;
+    if (++kvh < p.KV) return;
+    kvh = 0;
+    ++b;
+    nsp = b < p.B ? prefix[b + 1] - prefix[b] : 0;
+  };
 
   if (warp == NW) {
     // ------------------------------------------------ producer (the cache is
@@ -470,9 +484,9 @@ __global__ void __launch_bounds__((kPersistWarps + 1) * 32, 1) decode_attn_persi
       int stage = 0, phase = 0;
       long long issued = 0;
       bool ok = true;
-      for (int i = i0; i < i1; ++i) {
-        int b, kvh, ch, nsp;
-        decode_item(i, b, kvh, ch, nsp);
+      int b, kvh, ch, nsp;
+      seek(i0, b, kvh, ch, nsp);
+      for (int i = i0; i < i1; ++i, step(b, kvh, ch, nsp)) {
         if (!mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag)) {
           ok = false;
           break;
@@ -501,19 +515,142 @@ __global__ void __launch_bounds__((kPersistWarps + 1) * 32, 1) decode_attn_persi
     return;
   }
 
-  // -------------------------------------------------- compute warps 0..3
-  griddep_wait();                                  // q, k_new, v_new, partials, counters
+  if (warp > NW) {
+    // ------------------------------------------------ merge warps: warp NW + 1 + m
+    // takes the runs with index % 2 == m through merge buffer m
+    const int mwarp = warp - (NW + 1);
+    griddep_wait();                                // o, partials and counters
+    int b, kvh, ch, nsp;
+    seek(i0, b, kvh, ch, nsp);
+    int run = 0, mph = 0;
+    for (int i = i0; i < i1; ++i, step(b, kvh, ch, nsp)) {
+      if (i + 1 < i1 && ch + 1 < nsp) continue;    // the CTA's run of this pair goes on
+      if ((run++ & 1) != mwarp) continue;
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&mfull[mwarp], mph, abort_flag))) {
+        if (lane == 0) atomicCAS(p.status, 0, kDevTimeoutEpilogue);
+        *abort_flag = 1;
+        break;
+      }
+      mph ^= 1;
+      const float *rm = red + mwarp * RED, *rl = rm + NW * GM, *ro = rl + NW * GM;
+      float Ms[GM], Ls[GM], O0[GM], O1[GM];
+#pragma unroll
+      for (int g = 0; g < GM; ++g) {
+        Ms[g] = -INFINITY;
+        Ls[g] = O0[g] = O1[g] = 0.f;
+        if (g < G) {
+#pragma unroll
+          for (int w = 0; w < NW; ++w) Ms[g] = fmaxf(Ms[g], rm[w * GM + g]);
+          const float Mu = (Ms[g] == -INFINITY) ? 0.f : Ms[g];
+#pragma unroll
+          for (int w = 0; w < NW; ++w) {
+            const float fw = exp2f(rm[w * GM + g] - Mu);
+            Ls[g] += rl[w * GM + g] * fw;
+            O0[g] += ro[(w * GM + g) * HD + lane] * fw;
+            O1[g] += ro[(w * GM + g) * HD + lane + 32] * fw;
+          }
+        }
+      }
+      mbar_arrive(&mempty[mwarp]);                 // the buffer goes back to the compute warps
+      const int pair = b * p.KV + kvh;
+      const int pair_first = p.KV * prefix[b] + kvh * nsp;   // the pair's first item
+      const int c_first = pair_first / per;
+      const int nseg = (pair_first + nsp - 1) / per - c_first + 1;
+      const int seg = blockIdx.x - c_first;
+      const long long pbase = (long long)b * p.H + kvh * G;   // first query head of the group
+      if (nseg > 1) {
+#pragma unroll
+        for (int g = 0; g < GM; ++g)
+          if (g < G) {
+            const long long ps = (pbase + g) * p.max_splits + seg;
+            if (lane == 0) {
+              p.part_m[ps] = Ms[g];
+              p.part_l[ps] = Ls[g];
+            }
+            p.part_o[ps * HD + lane] = O0[g];
+            p.part_o[ps * HD + lane + 32] = O1[g];
+          }
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+          __threadfence();                         // the warp's partials before the arrival
+          const int prev = atomicAdd(p.counters + pair, 1);
+          last = (prev == nseg - 1);
+          if (last) {
+            p.counters[pair] = 0;                  // ready for the next layer
+            __threadfence();
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, last, 0)) continue;
+        // the last segment to finish merges the others into its own state
+        // (still in registers), U segments' loads in flight at a time
+        constexpr int U = GM <= 4 ? 4 : 2;
+        for (int s0 = 0; s0 < nseg; s0 += U) {
+          float vm[U][GM], vl[U][GM], v0[U][GM], v1[U][GM];
+#pragma unroll
+          for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int g = 0; g < GM; ++g) {
+              const int s2 = s0 + u;
+              const bool ok = g < G && s2 < nseg && s2 != seg;
+              const long long ps = (pbase + g) * p.max_splits + s2;
+              vm[u][g] = ok ? __ldcg(p.part_m + ps) : -INFINITY;
+              vl[u][g] = ok ? __ldcg(p.part_l + ps) : 0.f;
+              v0[u][g] = ok ? __ldcg(p.part_o + ps * HD + lane) : 0.f;
+              v1[u][g] = ok ? __ldcg(p.part_o + ps * HD + lane + 32) : 0.f;
+            }
+#pragma unroll
+          for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int g = 0; g < GM; ++g) {
+              const float mn = fmaxf(Ms[g], vm[u][g]);
+              const float mu = (mn == -INFINITY) ? 0.f : mn;
+              const float fa = exp2f(Ms[g] - mu), fb = exp2f(vm[u][g] - mu);
+              Ls[g] = Ls[g] * fa + vl[u][g] * fb;
+              O0[g] = O0[g] * fa + v0[u][g] * fb;
+              O1[g] = O1[g] * fa + v1[u][g] * fb;
+              Ms[g] = mn;
+            }
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < GM; ++g)
+        if (g < G) {
+          const float inv = Ls[g] > 0.f ? 1.f / Ls[g] : 0.f;
+          p.o[(pbase + g) * HD + lane] = __float2half_rn(O0[g] * inv);
+          p.o[(pbase + g) * HD + lane + 32] = __float2half_rn(O1[g] * inv);
+        }
+    }
+    return;
+  }
+
+  // -------------------------------------------------- compute warps 0..NW-1
+  griddep_wait();                                  // q, k_new, v_new
   const int r = lane >> 2, c2 = (lane & 3) * 2;    // fragment row (head) and column pair
   const int kw0 = warp * KPW;                      // this warp's keys within a chunk
-  int stage = 0, phase = 0;
+  int b, kvh, ch, nsp;
+  seek(i0, b, kvh, ch, nsp);
+  // raw q words of head r of a pair (dims kk*16 + c2 + {0,1} and + 8 + {0,1})
+  uint32_t qraw[8];
+  auto load_q = [&](int qb, int qkvh) {
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      if (r < G && qb < p.B) {
+        const f16 *qr = p.q + ((long long)qb * p.H + qkvh * G + r) * HD + kk * 16 + c2;
+        qraw[2 * kk] = *reinterpret_cast<const uint32_t *>(qr);
+        qraw[2 * kk + 1] = *reinterpret_cast<const uint32_t *>(qr + 8);
+      } else {
+        qraw[2 * kk] = qraw[2 * kk + 1] = 0u;
+      }
+    }
+  };
+  load_q(b, kvh);
+  int stage = 0, phase = 0, mb = 0, mph = 0;
   int cur_pair = -1;
   uint32_t qa[4][4];
   float mw = -INFINITY, lw = 0.f;                  // running max / sum of head r (this warp)
   float o[8][4];
-  bool alive = true;
-  for (int i = i0; i < i1; ++i) {
-    int b, kvh, ch, nsp;
-    decode_item(i, b, kvh, ch, nsp);
+  for (int i = i0; i < i1; ++i, step(b, kvh, ch, nsp)) {
     const int pair = b * p.KV + kvh;
     if (pair != cur_pair) {
       cur_pair = pair;
@@ -524,30 +661,27 @@ __global__ void __launch_bounds__((kPersistWarps + 1) * 32, 1) decode_attn_persi
       // q as A fragments (rows r < G: bf16 hi part; rows r + 8: the lo remainder)
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
-        if (r < G) {
-          const f16 *qr = p.q + ((long long)b * p.H + kvh * G + r) * HD + kk * 16 + c2;
-          const float2 a2 = unpack_f16x2(*reinterpret_cast<const uint32_t *>(qr));
-          const float2 b2 = unpack_f16x2(*reinterpret_cast<const uint32_t *>(qr + 8));
-          float h0, l0, h1, l1, h2, l2, h3, l3;
-          split_bf16(a2.x, h0, l0);
-          split_bf16(a2.y, h1, l1);
-          split_bf16(b2.x, h2, l2);
-          split_bf16(b2.y, h3, l3);
-          qa[kk][0] = pack_bf16x2(h0, h1);
-          qa[kk][1] = pack_bf16x2(l0, l1);
-          qa[kk][2] = pack_bf16x2(h2, h3);
-          qa[kk][3] = pack_bf16x2(l2, l3);
-        } else {
-          qa[kk][0] = qa[kk][1] = qa[kk][2] = qa[kk][3] = 0u;
-        }
+        const float2 a2 = unpack_f16x2(qraw[2 * kk]);
+        const float2 b2 = unpack_f16x2(qraw[2 * kk + 1]);
+        float h0, l0, h1, l1, h2, l2, h3, l3;
+        split_bf16(a2.x, h0, l0);
+        split_bf16(a2.y, h1, l1);
+        split_bf16(b2.x, h2, l2);
+        split_bf16(b2.y, h3, l3);
+        qa[kk][0] = pack_bf16x2(h0, h1);
+        qa[kk][1] = pack_bf16x2(l0, l1);
+        qa[kk][2] = pack_bf16x2(h2, h3);
+        qa[kk][3] = pack_bf16x2(l2, l3);
       }
+      // the next pair's q is read while this one's chunks stream
+      load_q(kvh + 1 < p.KV ? b : b + 1, kvh + 1 < p.KV ? kvh + 1 : 0);
     }
-    const int Lb = clamp_len(p.cache_len[b]);
+    const int Lb = lens[b];
     const int k_begin = ch * kChunk;
     const int n_valid = min(kChunk, Lb + 1 - k_begin);
-    // the four warps decide together (they meet at named barriers below)
-    if (!compute_and(mbar_wait_bounded(&full[stage], phase, abort_flag))) {
-      alive = false;
+    if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[stage], phase, abort_flag))) {
+      if (lane == 0) atomicCAS(p.status, 0, kDevTimeoutEpilogue);
+      *abort_flag = 1;
       break;
     }
     uint8_t *sK = dsm + stage * STAGE, *sV = sK + kChunk * 128;
@@ -641,79 +775,30 @@ __global__ void __launch_bounds__((kPersistWarps + 1) * 32, 1) decode_attn_persi
       stage = 0;
       phase ^= 1;
     }
-    if (i + 1 < i1 && ch + 1 < nsp) continue;      // this CTA's run of the pair goes on
-    // ---- end of this CTA's run of chunks of the pair: merge the warps
+    if (i + 1 < i1 && ch + 1 < nsp) continue;      // this CTA's run of chunks of the pair goes on
+    // ---- end of the run: this warp's state goes to the merge warp
+    if (!__all_sync(0xffffffffu, mbar_wait_bounded(&mempty[mb], mph ^ 1, abort_flag))) {
+      if (lane == 0) atomicCAS(p.status, 0, kDevTimeoutEpilogue);
+      *abort_flag = 1;
+      break;
+    }
+    float *rm = red + mb * RED, *rl = rm + NW * GM, *ro = rl + NW * GM;
     if (r < G) {
       if ((lane & 3) == 0) {
-        red_m[warp * GM + r] = mw;
-        red_l[warp * GM + r] = lw;
+        rm[warp * GM + r] = mw;
+        rl[warp * GM + r] = lw;
       }
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        red_o[(warp * GM + r) * HD + 8 * q + c2] = o[q][0] + o[q][2];
-        red_o[(warp * GM + r) * HD + 8 * q + c2 + 1] = o[q][1] + o[q][3];
+        ro[(warp * GM + r) * HD + 8 * q + c2] = o[q][0] + o[q][2];
+        ro[(warp * GM + r) * HD + 8 * q + c2 + 1] = o[q][1] + o[q][3];
       }
     }
-    compute_bar();
-    const int pair_first = p.KV * prefix[b] + kvh * nsp;   // the pair's first item
-    const int c_first = pair_first / per;
-    const int nseg = (pair_first + nsp - 1) / per - c_first + 1;
-    const int seg = blockIdx.x - c_first;
-    const long long pbase = (long long)b * p.H + kvh * G;   // first query head of the group
-    for (int t = threadIdx.x; t < G * HD; t += NW * 32) {
-      const int g = t / HD, dim = t - g * HD;
-      float M = -INFINITY;
-      for (int w = 0; w < NW; ++w) M = fmaxf(M, red_m[w * GM + g]);
-      const float Mu = (M == -INFINITY) ? 0.f : M;
-      float Ls = 0.f, Os = 0.f;
-      for (int w = 0; w < NW; ++w) {
-        const float fw = exp2f(red_m[w * GM + g] - Mu);
-        Ls += red_l[w * GM + g] * fw;
-        Os += red_o[(w * GM + g) * HD + dim] * fw;
-      }
-      if (nseg == 1) {
-        p.o[(pbase + g) * HD + dim] = __float2half_rn(Ls > 0.f ? Os / Ls : 0.f);
-      } else {
-        const long long ps = (pbase + g) * p.max_splits + seg;
-        if (dim == 0) {
-          p.part_m[ps] = M;
-          p.part_l[ps] = Ls;
-        }
-        p.part_o[ps * HD + dim] = Os;
-      }
+    mbar_arrive(&mfull[mb]);
+    if (++mb == 2) {
+      mb = 0;
+      mph ^= 1;
     }
-    if (nseg > 1) {
-      __threadfence();
-      compute_bar();
-      if (threadIdx.x == 0) {
-        const int prev = atomicAdd(p.counters + pair, 1);
-        *s_last = (prev == nseg - 1);
-        if (prev == nseg - 1) p.counters[pair] = 0;   // ready for the next layer
-      }
-      compute_bar();
-      if (*s_last) {
-        __threadfence();
-        for (int t = threadIdx.x; t < G * HD; t += NW * 32) {
-          const int g = t / HD, dim = t - g * HD;
-          const long long ps0 = (pbase + g) * p.max_splits;
-          float M = -INFINITY;
-          for (int s2 = 0; s2 < nseg; ++s2) M = fmaxf(M, __ldcg(p.part_m + ps0 + s2));
-          const float Mu = (M == -INFINITY) ? 0.f : M;
-          float Ls = 0.f, Os = 0.f;
-          for (int s2 = 0; s2 < nseg; ++s2) {
-            const float fw = exp2f(__ldcg(p.part_m + ps0 + s2) - Mu);
-            Ls += __ldcg(p.part_l + ps0 + s2) * fw;
-            Os += __ldcg(p.part_o + (ps0 + s2) * HD + dim) * fw;
-          }
-          p.o[(pbase + g) * HD + dim] = __float2half_rn(Ls > 0.f ? Os / Ls : 0.f);
-        }
-      }
-    }
-    compute_bar();                                  // red_* reused by the next run
-  }
-  if (!alive) {
-    if (lane == 0) atomicCAS(p.status, 0, kDevTimeoutEpilogue);
-    *abort_flag = 1;
   }
 }
 
@@ -963,13 +1048,11 @@ static cudaError_t launch_decode_attn_mma_g(const CUtensorMap &tk, const CUtenso
 template <int GM>
 static cudaError_t launch_decode_attn_persist_g(const CUtensorMap &tk, const CUtensorMap &tv,
                                                 const DecAttnParams &ap, int sms, cudaStream_t st) {
-  constexpr int NW = kPersistWarps, HD = 64;
-  const int smem = 1024 + kDecStages * 2 * kChunk * 128 + 2 * kDecStages * 8 + 16 +
-                   (2 * NW * GM + NW * GM * HD) * 4 + (ap.B + 1) * 4;
+  const int smem = persist_smem_fixed<GM>() + (2 * ap.B + 1) * 4;
   constexpr auto kern = decode_attn_persist_kernel<GM>;
   cudaError_t e = ensure_smem_attr<kern>(smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(sms), dim3((NW + 1) * 32), smem, st, tk, tv, ap);
+  return launch_pdl(kern, dim3(sms), dim3((kPersistWarps + 3) * 32), smem, st, tk, tv, ap);
 }
 
 // head_dim 64 runs on tensor cores (the cache seen as one 2-D tensor of
