@@ -107,6 +107,13 @@ int gemm_pick_bn(int epi, int N, int hd);
 cudaError_t launch_gemm(int epi, int bn, const void *A, const void *B, const GemmParams &p,
                         int num_sms, cudaStream_t stream);
 
+// Decode-sized projections (M <= 64 rows) on narrow column units: the
+// residual, SwiGLU and QKV/RoPE epilogues of launch_gemm with f16 operands
+// (A: M x K, W: N x K, K-contiguous); see decode_gemm.cu for what is covered.
+bool skinny_gemm_supported(int epi, const GemmParams &p);
+cudaError_t launch_skinny_gemm(int epi, const void *A, const void *W, const GemmParams &p,
+                               cudaStream_t stream);
+
 // ------------------------------------------------------------------ attention
 struct AttnParams {
   const f16 *q;           // [B, H, T, hd]

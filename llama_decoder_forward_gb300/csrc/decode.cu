@@ -1091,6 +1091,13 @@ static cudaError_t launch_zero_ints(int *p, int n, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// The narrow-unit kernel for batches of at most 64 rows, the tile GEMM otherwise.
+static cudaError_t dec_gemm(int epi, int bn, const void *A, const void *W, const GemmParams &p, int sms,
+                            cudaStream_t st) {
+  if (skinny_gemm_supported(epi, p)) return launch_skinny_gemm(epi, A, W, p, st);
+  return launch_gemm(epi, bn, A, W, p, sms, st);
+}
+
 cudaError_t run_decode(const DecodeArgs &a, void *ws, int sms, cudaStream_t st, int *launches) {
   const smol_config &c = a.cfg;
   const DecWs W = dec_ws(&c, a.B);
@@ -1134,7 +1141,7 @@ cudaError_t run_decode(const DecodeArgs &a, void *ws, int sms, cudaStream_t st, 
     p.q = q; p.k_bf = kn; p.v_bf = vn; p.T = 1; p.H = H; p.KV = KV; p.hd = hd;
     p.rope = a.rope; p.valid_start = nullptr; p.pos_add = a.cache_len; p.pos_limit = min(a.S_max, c.max_pos - 1);
     p.max_pos = c.max_pos; p.status = status; p.pdl = 1;
-    DEC_LAUNCH_K(SMOL_K_QKV, launch_gemm(kEpiQkvRope, hd, x, lb + a.off_qkv, p, sms, st));
+    DEC_LAUNCH_K(SMOL_K_QKV, dec_gemm(kEpiQkvRope, hd, x, lb + a.off_qkv, p, sms, st));
 
     DecAttnParams ap{};
     ap.q = q;
@@ -1156,18 +1163,18 @@ cudaError_t run_decode(const DecodeArgs &a, void *ws, int sms, cudaStream_t st, 
     po.M = B; po.N = d; po.K = H * hd; po.out = h; po.out_is_f16 = 1; po.ldo = d; po.resid_f16 = x;
     po.ssq_out = ssq_b;
     po.status = status; po.pdl = 1;
-    DEC_LAUNCH_K(SMOL_K_OPROJ, launch_gemm(kEpiResidual, 64, o, lb + a.off_o, po, sms, st));
+    DEC_LAUNCH_K(SMOL_K_OPROJ, dec_gemm(kEpiResidual, 64, o, lb + a.off_o, po, sms, st));
 
     GemmParams pg{};
     pg.M = B; pg.N = 2 * I; pg.K = d; pg.out = act; pg.out_is_f16 = 1; pg.ldo = I; pg.ssq_in = ssq_b;
     pg.inv_dim = 1.0f / d; pg.eps = c.rms_eps; pg.ssq_zero = ssq_a; pg.status = status; pg.pdl = 1;
-    DEC_LAUNCH_K(SMOL_K_GATEUP, launch_gemm(kEpiSwiglu, 128, h, lb + a.off_gu, pg, sms, st));
+    DEC_LAUNCH_K(SMOL_K_GATEUP, dec_gemm(kEpiSwiglu, 128, h, lb + a.off_gu, pg, sms, st));
 
     GemmParams pd{};
     pd.M = B; pd.N = d; pd.K = I; pd.out = x; pd.out_is_f16 = 1; pd.ldo = d; pd.resid_f16 = h;
     pd.ssq_out = ssq_a;
     pd.status = status; pd.pdl = 1;
-    DEC_LAUNCH_K(SMOL_K_DOWN, launch_gemm(kEpiResidual, 64, act, lb + a.off_down, pd, sms, st));
+    DEC_LAUNCH_K(SMOL_K_DOWN, dec_gemm(kEpiResidual, 64, act, lb + a.off_down, pd, sms, st));
   }
   GemmParams ph{};
   ph.M = B; ph.N = V; ph.K = d; ph.out = a.logits; ph.out_is_f16 = 0; ph.ldo = V; ph.ssq_in = ssq_a;
