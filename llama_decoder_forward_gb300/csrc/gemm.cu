@@ -984,7 +984,12 @@ int gemm_pick_bn(int epi, int N, int hd) {
   if (N <= 0 || N % 64) return 0;
   if (epi == kEpiQkvRope) {
     if (N % hd) return 0;
-    const int cands[3] = {256, 192, 128};
+    // 256 columns (four 64-wide head units, two per epilogue warp) even when
+    // the last tile is ragged: the RoPE units cost about twice the MMAs of a
+    // tile, so an even split between the warps matters more than the columns
+    // the last tile computes in vain
+    if (N >= 256) return 256;
+    const int cands[2] = {192, 128};
     for (int c : cands)
       if (c % hd == 0 && N % c == 0) return c;
     return hd == 64 ? 128 : 256;                  // ragged last tile (whole heads)
