@@ -227,12 +227,13 @@ struct EpiCtx {
   uint64_t *rbar;     // the warp's residual-load barrier and its next parity
   uint32_t rphase;
   uint32_t seq;       // staging uses so far (selects the alternating tile)
+  float rs;           // the lane's row scale rstd, read before the accumulator is waited for
 };
 
 // logits = rstd * D; units of 64 columns (one full 128-byte row segment).
 template <int BN>
 __device__ __forceinline__ void epi_scale(const GemmParams &p, EpiCtx &e) {
-  const float rs = row_rstd(p, e.row0 + e.lane);
+  const float rs = e.rs;
   const bool tma = p.epi_tma & kTmaOut;
   const long long ld = p.ldo * 2;
   uint8_t *gbase = static_cast<uint8_t *>(p.out) + ((long long)e.row0 * p.ldo) * 2;
@@ -399,7 +400,7 @@ __device__ __forceinline__ void epi_residual_lane(const GemmParams &p, EpiCtx &e
 // a unit is one group: 64 outputs written as one 128-byte row segment.
 template <int BN>
 __device__ __forceinline__ void epi_swiglu(const GemmParams &p, EpiCtx &e) {
-  const float rs = row_rstd(p, e.row0 + e.lane);
+  const float rs = e.rs;
   const int I = p.N / 2;
   const bool tma = p.epi_tma & kTmaOut;
   uint8_t *gbase = static_cast<uint8_t *>(p.out) + (long long)e.row0 * p.ldo * 2;
@@ -450,7 +451,7 @@ template <int BN, int HD>
 __device__ __forceinline__ void epi_qkv_rope(const GemmParams &p, EpiCtx &e) {
   const int row = e.row0 + e.lane;
   const bool row_ok = e.lane < e.rows_valid;
-  const float rs = row_rstd(p, row);
+  const float rs = e.rs;
   const int rr_ = row_ok ? row : min(e.row0, p.M - 1);   // rows past M: any valid index
   const int b = rr_ / p.T, t = rr_ - b * p.T;
   int pos = t - (p.valid_start ? p.valid_start[b] : 0);
@@ -637,10 +638,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // vocabulary projection; otherwise they share A and walk B
   const int num_kb = static_cast<int>(cdiv(p.K, C::BK));
   const int rank = PAIR > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-  // tile -> (row group, column block)
+  // tile -> (row group, column block).  Without raster_m the column block is
+  // rotated by the row group, so that a CTA striding through the tiles by the
+  // grid size meets every column block even when the grid is a multiple of
+  // their number (column blocks can differ in cost: the QKV epilogue rotates
+  // q and k heads but not v heads).
   auto decode_tile = [&](int tile, int &m_grp, int &n_blk) {
     m_grp = p.raster_m ? tile % num_mg : tile / num_n;
-    n_blk = p.raster_m ? tile / num_mg : tile - m_grp * num_n;
+    n_blk = p.raster_m ? tile / num_mg : (tile - m_grp * num_n + m_grp) % num_n;
   };
   const int first_tile = blockIdx.x / PAIR, tile_step = gridDim.x / PAIR;
 
@@ -826,6 +831,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       e.rows_valid = min(32, max(0, p.M - e.row0));
       e.n0 = n_blk * BN;
       e.n_blk = n_blk;
+      if constexpr (EPI != kEpiResidual) e.rs = row_rstd(p, e.row0 + lane);
       if constexpr (EPI == kEpiResidual) {
         // start fetching this warp's residual while the MMAs run
         if (resid_tma) {
