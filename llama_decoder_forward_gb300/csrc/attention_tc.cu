@@ -171,9 +171,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
+  if (threadIdx.x == 0) griddep_launch_dependents();
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------------- TMA producer
+      griddep_wait();                             // q, k and V^T come from the preceding kernel
       int dummy = 0;
       long long issued = 0;                       // kv stages issued (for the drain)
       bool ok = true;
@@ -257,6 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
+    griddep_wait();                               // o is written below
     // ---------------------------------------------- softmax: warps 2..5 take keys
     // 0..63 of every tile (group 0), warps 6..9 keys 64..127 (group 1); one
     // query row per thread.  The groups exchange partial row maxes in shared
@@ -436,8 +439,19 @@ cudaError_t launch_gh(const AttnParams &a, const CUtensorMap &tq, const CUtensor
   p.scale_log2 = a.scale_log2;
   p.status = a.status;
   dim3 grid((unsigned)(a.B * a.KV * p.n_hsub), (unsigned)cdiv(a.T, kBQ), 1u);
-  kern<<<grid, kThreads, C::SMEM, st>>>(tq, tk, tv, p);
-  return cudaGetLastError();
+  // as a programmatic dependent: CTAs set up barriers and TMEM while the
+  // preceding kernel drains, and wait for it before touching its outputs
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, p);
 }
 
 }  // namespace

@@ -126,6 +126,7 @@ struct AttnParams {
   const int *valid_start; // [B] or nullptr
   int B, T, H, KV, hd;
   float scale_log2;       // log2(e) / sqrt(hd)
+  int pdl;                // tcgen05 kernel: launch as a programmatic dependent of the preceding kernel
 };
 cudaError_t launch_flash_attention(const AttnParams &p, cudaStream_t stream);
 // tcgen05 attention (head_dim 64, group of at most 4 query heads); needs v_t.

@@ -196,6 +196,9 @@ int run_block(const smol_config *c, const void *packed, int layer, const BlockIO
   p.T = T; p.H = H; p.KV = KV; p.hd = hd;
   p.rope = reinterpret_cast<const float2 *>(static_cast<const uint8_t *>(packed) + PL.rope_off);
   p.valid_start = valid_start; p.max_pos = c->max_pos; p.status = status;
+  // every kernel of the block is a programmatic dependent of the one before
+  // (each waits for it with griddepcontrol.wait before touching its data)
+  p.pdl = 1;
   LAUNCH_K(SMOL_K_QKV, st, launch_gemm(kEpiQkvRope, gemm_pick_bn(kEpiQkvRope, p.N, hd), io.x16, lp.qkv, p, sms, st));
 
   // 2. causal GQA attention
@@ -204,6 +207,7 @@ int run_block(const smol_config *c, const void *packed, int layer, const BlockIO
   ap.B = B; ap.T = T; ap.H = H; ap.KV = KV; ap.hd = hd;
   ap.scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
   ap.status = status;
+  ap.pdl = 1;
   if (tc_attn) {
     ap.v = nullptr;
     ap.v_t = v;
@@ -217,21 +221,21 @@ int run_block(const smol_config *c, const void *packed, int layer, const BlockIO
   GemmParams po{};
   po.M = (int)M; po.N = d; po.K = H * hd;
   po.out = h; po.out_is_f16 = 1; po.ldo = d; po.ssq_out = ssq_b; po.status = status;
-  po.resid = io.resid_bf; po.resid_f16 = io.resid_f16; po.resid_f32 = io.resid_f32;
+  po.resid = io.resid_bf; po.resid_f16 = io.resid_f16; po.resid_f32 = io.resid_f32; po.pdl = 1;
   LAUNCH_K(SMOL_K_OPROJ, st, launch_gemm(kEpiResidual, gemm_pick_bn(kEpiResidual, d, hd), o, lp.o, po, sms, st));
 
   // 4. RMSNorm2 + gate/up + SwiGLU: a = silu(g) * u ; clears ssq_a for step 5
   GemmParams pg{};
   pg.M = (int)M; pg.N = 2 * I; pg.K = d;
   pg.out = a; pg.out_is_f16 = 1; pg.ldo = I; pg.ssq_in = ssq_b; pg.inv_dim = 1.0f / d;
-  pg.eps = c->rms_eps; pg.ssq_zero = ssq_a; pg.status = status;
+  pg.eps = c->rms_eps; pg.ssq_zero = ssq_a; pg.status = status; pg.pdl = 1;
   LAUNCH_K(SMOL_K_GATEUP, st, launch_gemm(kEpiSwiglu, gemm_pick_bn(kEpiSwiglu, 2 * I, hd), h, lp.gu, pg, sms, st));
 
   // 5. down projection + residual: out = h + a Wd^T, ssq_a += rowsum(out^2)
   GemmParams pd{};
   pd.M = (int)M; pd.N = d; pd.K = I;
   pd.out = io.out16; pd.out_is_f16 = io.out16_is_f16; pd.out_f32 = io.out_f32; pd.ldo = d;
-  pd.resid_f16 = h; pd.ssq_out = ssq_a; pd.status = status;
+  pd.resid_f16 = h; pd.ssq_out = ssq_a; pd.status = status; pd.pdl = 1;
   LAUNCH_K(SMOL_K_DOWN, st, launch_gemm(kEpiResidual, gemm_pick_bn(kEpiResidual, d, hd), a, lp.down, pd, sms, st));
   return SMOL_OK;
 }
@@ -392,6 +396,7 @@ SMOL_API int smol_model_forward(const smol_config *cfg, const void *packed, cons
   p.out = logits; p.out_is_f16 = 0; p.ldo = cfg->vocab;
   p.ssq_in = ssq_a; p.inv_dim = 1.0f / cfg->hidden; p.eps = cfg->rms_eps;
   p.status = reinterpret_cast<int *>(wsb + W.status);
+  p.pdl = 1;
   LAUNCH_K(SMOL_K_HEAD, st, launch_gemm(kEpiScale, gemm_pick_bn(kEpiScale, cfg->vocab, cfg->head_dim), x,
                      pk + L.head_off, p, sms, st));
   return SMOL_OK;
