@@ -87,6 +87,29 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     fence_barrier_init();
   }
   __syncthreads();
+  // QKV: this thread's rotation factors (fine and coarse (cos, sin) entries of
+  // its two pairs at its row's position) depend only on inputs of the step,
+  // so they are read before the wait on the preceding kernel
+  float c0 = 1.f, s0 = 0.f, c1 = 1.f, s1 = 0.f;
+  if constexpr (EPI == kEpiQkvRope) {
+    const int row = threadIdx.x >> 2, c = (threadIdx.x & 3) * 2;
+    if (row < p.M && (u >> 2) < p.H + p.KV) {
+      int pos = 0;
+      if (p.pos_add) {
+        const int pa = p.pos_add[row];                  // one token per sequence
+        pos = pa < 0 ? 0 : (pa > p.pos_limit ? p.pos_limit : pa);
+      }
+      pos = pos < 0 ? 0 : (pos >= p.max_pos ? p.max_pos - 1 : pos);
+      const int n_coarse = static_cast<int>(cdiv(p.max_pos, 64));
+      const int jj = ((u & 3) * 8 + c) >> 1;            // pairs i0+c and i0+c+1
+      const float4 f = reinterpret_cast<const float4 *>(p.rope)[jj * 64 + (pos & 63)];
+      const float4 gq = reinterpret_cast<const float4 *>(p.rope)[16 * 64 + jj * n_coarse + (pos >> 6)];
+      c0 = gq.x * f.x - gq.y * f.y;
+      s0 = gq.y * f.x + gq.x * f.y;
+      c1 = gq.z * f.z - gq.w * f.w;
+      s1 = gq.w * f.z + gq.z * f.w;
+    }
+  }
   if (threadIdx.x == 0) {
     griddep_launch_dependents();
     // weights first (inputs of the step), then the rows the preceding kernel wrote
@@ -244,19 +267,6 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     const bool is_q = gh < p.H, is_k = !is_q && gh < p.H + p.KV;
     float ylo[2], yhi[2];
     if (is_q || is_k) {
-      const int b = row;                              // one token per sequence
-      int pos = 0;
-      if (p.pos_add) {
-        const int pa = p.pos_add[b];
-        pos = pa < 0 ? 0 : (pa > p.pos_limit ? p.pos_limit : pa);
-      }
-      pos = pos < 0 ? 0 : (pos >= p.max_pos ? p.max_pos - 1 : pos);
-      const int n_coarse = static_cast<int>(cdiv(p.max_pos, 64));
-      const int jj = (i0 + c) >> 1;                   // pairs i0+c and i0+c+1
-      const float4 f = reinterpret_cast<const float4 *>(p.rope)[jj * 64 + (pos & 63)];
-      const float4 gq = reinterpret_cast<const float4 *>(p.rope)[16 * 64 + jj * n_coarse + (pos >> 6)];
-      const float c0 = gq.x * f.x - gq.y * f.y, s0 = gq.y * f.x + gq.x * f.y;
-      const float c1 = gq.z * f.z - gq.w * f.w, s1 = gq.w * f.z + gq.z * f.w;
       ylo[0] = a[0] * c0 - bb[0] * s0;
       yhi[0] = a[0] * s0 + bb[0] * c0;
       ylo[1] = a[1] * c1 - bb[1] * s1;
