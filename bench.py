@@ -275,18 +275,59 @@ def run_prefill(S, args, rank, world, peaks, peaks_src):
     tokens = wl.B * wl.T
     value = tokens * world / (ms / 1e3)
 
-    # end to end through the public API: ids from pinned host memory in, logits out
+    # end to end through the public API, as a serving loop runs it: every step
+    # copies its ids in from pinned host memory, runs the forward and copies
+    # all of its logits out to pinned host memory; the copy-out of step i runs
+    # on a second stream while step i+1 computes (two logits buffers)
     ids_host = ids.cpu().pin_memory()
-    logits_host = torch.empty(logits.shape, dtype=logits.dtype, pin_memory=True)
+    logits_dev = [logits, torch.empty_like(logits)]
+    logits_host = [torch.empty(logits.shape, dtype=logits.dtype, pin_memory=True) for _ in range(2)]
+    # the copy-out is split over several streams, so that several copy engines share it
+    copy_streams = [torch.cuda.Stream() for _ in range(4)]
+    done = [None, None]
 
-    def e2e_step():
+    def e2e_step(i):
+        main = torch.cuda.current_stream()
+        j = i & 1
+        if done[j] is not None:
+            for ev in done[j]:
+                main.wait_event(ev)               # the copy-out of step i-2 has read this buffer
         ids.copy_(ids_host, non_blocking=True)
-        S.model_forward(cfg, packed, ids, logits, ws)
-        logits_host.copy_(logits, non_blocking=True)
+        S.model_forward(cfg, packed, ids, logits_dev[j], ws)
+        ready = torch.cuda.Event()
+        ready.record(main)
+        src, dst = logits_dev[j].view(-1), logits_host[j].view(-1)
+        n = src.numel()
+        evs = []
+        for c, cs in enumerate(copy_streams):
+            lo, hi = n * c // len(copy_streams), n * (c + 1) // len(copy_streams)
+            cs.wait_event(ready)
+            with torch.cuda.stream(cs):
+                dst[lo:hi].copy_(src[lo:hi], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(cs)
+                evs.append(ev)
+        done[j] = evs
 
-    e2e_step()
-    e2e_steps = max(1, min(args.steps, 10))
-    e2e_ms = max_over_ranks(time_steps(e2e_step, e2e_steps, world), world)
+    def e2e_run(steps):
+        barrier(world)
+        torch.cuda.synchronize()
+        main = torch.cuda.current_stream()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(main)
+        for i in range(steps):
+            e2e_step(i)
+        for cs in copy_streams:
+            main.wait_stream(cs)                  # the last logits are on the host
+        end.record(main)
+        torch.cuda.synchronize()
+        barrier(world)
+        return start.elapsed_time(end) / steps
+
+    e2e_run(2)
+    e2e_steps = max(2, min(args.steps, 10))
+    e2e_ms = max_over_ranks(e2e_run(e2e_steps), world)
 
     flops = prefill_flops_per_launch(wl)
     peak_tf = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
@@ -318,7 +359,9 @@ def run_prefill(S, args, rank, world, peaks, peaks_src):
         "clocks": clocks,
         "e2e": {"value": round(tokens * world / (e2e_ms / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": ids.numel() * 4, "d2h_bytes_per_step": logits.numel() * 2,
-                "ms_per_step": round(e2e_ms, 4)},
+                "ms_per_step": round(e2e_ms, 4),
+                "how": "eager model_forward calls; per step: ids in from pinned host memory, all "
+                       "logits out to pinned host memory on four copy streams overlapping the next step"},
         "gpu_launches": launches * args.steps,
         "timing": "CUDA-graph replay of the step" if graph_ms is not None else "eager calls",
         "eager_ms_per_step": round(eager_ms, 4),
