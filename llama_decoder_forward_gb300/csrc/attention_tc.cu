@@ -47,7 +47,9 @@ struct AtCfg {
   static constexpr int OFF_K = OFF_Q + GH * Q_BYTES;
   static constexpr int OFF_VT = OFF_K + 2 * K_BYTES;
   static constexpr int OFF_RED = OFF_VT + 2 * VT_BYTES;  // [2][2][128] row maxes, [2][4][128] row sums
-  static constexpr int OFF_BAR = OFF_RED + (2 * 2 * 128 + 2 * 4 * 128) * 4;
+  static constexpr int OFF_STG = OFF_RED + (2 * 2 * 128 + 2 * 4 * 128) * 4;   // output staging:
+  static constexpr int STG_WARP = 32 * 32 * 2;          // [head][softmax warp][32 rows][32 f16]
+  static constexpr int OFF_BAR = OFF_STG + GH * 8 * STG_WARP;
   static constexpr int SMEM = 1024 + OFF_BAR + 256;
   static constexpr int TMEM_S = 256;                    // S buffers at columns 256 + sb*128;
                                                         // P (f16) overwrites columns 0..63 of its S
@@ -107,7 +109,8 @@ __device__ __forceinline__ void at_status(int *status, int code) {
 template <int GH>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmVt, const AtParams p) {
+                   const __grid_constant__ CUtensorMap tmVt, const __grid_constant__ CUtensorMap tmO,
+                   const AtParams p) {
   using C = AtCfg<GH>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -161,6 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmVt);
+    tma_prefetch_desc(&tmO);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
@@ -386,6 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       *abort_flag = 1;
     } else {
       const bool row_ok = t < T;
+      const bool warp_rows_ok = q0 + quarter * 32 + 31 < T;   // all 32 rows of this warp exist
       const long long ldo = (long long)p.H * kHD;
 #pragma unroll 1
       for (int h = 0; h < GH; ++h) {
@@ -400,18 +405,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t ov[32];
         tmem_ld32(lane_base + h * kHD + grp * 32, ov);
         tmem_ld_wait();
-        if (row_ok) {
+        uint4 w[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float *f = reinterpret_cast<const float *>(&ov[8 * q]);
+          w[q] = make_uint4(pack_f16x2(f[0] * inv, f[1] * inv), pack_f16x2(f[2] * inv, f[3] * inv),
+                            pack_f16x2(f[4] * inv, f[5] * inv), pack_f16x2(f[6] * inv, f[7] * inv));
+        }
+        if (warp_rows_ok) {
+          // the warp's 32 rows x 32 columns go out as one TMA box (a lane per
+          // row would make every store instruction 32 separate row segments)
+          uint8_t *stg = smem + C::OFF_STG + (h * 8 + (warp - 2)) * C::STG_WARP;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4 *>(stg + lane * 64 + q * 16) = w[q];
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmO, stg, (h_first + h) * kHD + grp * 32, b * T + q0 + quarter * 32);
+            bulk_commit_group();
+          }
+        } else if (row_ok) {
           f16 *dst = p.o + ((long long)b * T + t) * ldo + (long long)(h_first + h) * kHD + grp * 32;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float *f = reinterpret_cast<const float *>(&ov[8 * q]);
-            const uint4 w = make_uint4(pack_f16x2(f[0] * inv, f[1] * inv), pack_f16x2(f[2] * inv, f[3] * inv),
-                                       pack_f16x2(f[4] * inv, f[5] * inv), pack_f16x2(f[6] * inv, f[7] * inv));
-            *reinterpret_cast<uint4 *>(dst + 8 * q) = w;
-          }
+          for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4 *>(dst + 8 * q) = w[q];
         }
       }
     }
+    if (lane == 0) bulk_wait_group_read<0>();     // the staging blocks are read before the CTA exits
   }
 
   tc_fence_before_sync();
@@ -424,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int GH>
 cudaError_t launch_gh(const AttnParams &a, const CUtensorMap &tq, const CUtensorMap &tk,
-                      const CUtensorMap &tv, cudaStream_t st) {
+                      const CUtensorMap &tv, const CUtensorMap &to, cudaStream_t st) {
   using C = AtCfg<GH>;
   auto kern = attn_tc_kernel<GH>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -451,7 +471,7 @@ cudaError_t launch_gh(const AttnParams &a, const CUtensorMap &tq, const CUtensor
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = a.pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, p);
+  return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, to, p);
 }
 
 }  // namespace
@@ -463,19 +483,22 @@ bool attention_tc_supported(int hd, int H, int KV) {
 
 cudaError_t launch_attention_tc(const AttnParams &a, cudaStream_t st) {
   if (!attention_tc_supported(a.hd, a.H, a.KV) || a.v_t == nullptr) return cudaErrorInvalidConfiguration;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   if (!make_tmap_f16(&tq, a.q, (uint64_t)a.B * a.H * a.T, kHD, kHD, kBQ)) return cudaErrorInvalidValue;
   if (!make_tmap_f16(&tk, a.k, (uint64_t)a.B * a.KV * a.T, kHD, kHD, kBK)) return cudaErrorInvalidValue;
   // V^T: rows are (b, kv head, dim), columns are keys; columns >= T read as zero
   if (!make_tmap_f16(&tv, a.v_t, (uint64_t)a.B * a.KV * kHD, a.T, a.T_pad, kHD)) return cudaErrorInvalidValue;
+  // output rows [B*T, H*hd]: a softmax warp's 32 rows x 32 columns per box
+  if (!make_tmap_2d(&to, a.o, (uint64_t)a.B * a.T, (uint64_t)a.H * kHD, (uint64_t)a.H * kHD, 32, 32, false))
+    return cudaErrorInvalidValue;
   const int G = a.H / a.KV;
   switch (G) {
-    case 1: return launch_gh<1>(a, tq, tk, tv, st);
-    case 2: return launch_gh<2>(a, tq, tk, tv, st);
-    case 3: return launch_gh<3>(a, tq, tk, tv, st);
-    case 4: return launch_gh<4>(a, tq, tk, tv, st);
-    case 6: return launch_gh<3>(a, tq, tk, tv, st);   // two CTAs per group of six
-    case 8: return launch_gh<4>(a, tq, tk, tv, st);
+    case 1: return launch_gh<1>(a, tq, tk, tv, to, st);
+    case 2: return launch_gh<2>(a, tq, tk, tv, to, st);
+    case 3: return launch_gh<3>(a, tq, tk, tv, to, st);
+    case 4: return launch_gh<4>(a, tq, tk, tv, to, st);
+    case 6: return launch_gh<3>(a, tq, tk, tv, to, st);   // two CTAs per group of six
+    case 8: return launch_gh<4>(a, tq, tk, tv, to, st);
   }
   return cudaErrorInvalidConfiguration;
 }

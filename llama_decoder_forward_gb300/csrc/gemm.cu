@@ -78,7 +78,10 @@ struct GemmCfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int EPI_BYTES = kEpiWarps * EpiStage<EPI>::kPerWarp;
   static constexpr int STAGES_RAW = (232448 - 1024 - 256 - EPI_BYTES) / STAGE_BYTES;
-  static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+  // the QKV epilogue's RoPE table reads want L1, which the shared-memory
+  // carve-out shrinks: that epilogue keeps at most four stages
+  static constexpr int STAGES_CAP = EPI == 0 /*kEpiQkvRope*/ ? 4 : 8;
+  static constexpr int STAGES = STAGES_RAW > STAGES_CAP ? STAGES_CAP : STAGES_RAW;
   static constexpr int TMEM_COLS = (2 * BN <= 128) ? 128 : (2 * BN <= 256 ? 256 : 512);
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
