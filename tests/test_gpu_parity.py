@@ -186,3 +186,18 @@ def test_decode_small(S):
 def test_decode_one_chunk_many_layers(S):
     wl = W["smollm2_decode_b64_cache4096"].scaled(n_layers=4, s_max=64, vocab=512)
     run_decode_case(S, wl, [64, 3, 17], seed=2)
+
+
+def test_decode_batch_beyond_narrow_units(S):
+    # B > 64: the projections run on the tile GEMM instead of the narrow-unit kernel
+    wl = W["smollm2_decode_b64_cache4096"].scaled(n_layers=2, s_max=320, vocab=1024)
+    lengths = [int(v) for v in np.random.default_rng(5).integers(0, 321, size=80)]
+    run_decode_case(S, wl, lengths, seed=6)
+
+
+def test_decode_head_dim_128(S):
+    # SmolLM3-shaped layer (hd 128): CUDA-core decode attention, tile-GEMM projections
+    wl = W["smollm2_decode_b64_cache4096"].scaled(
+        hidden=2048, n_heads=16, n_kv_heads=4, head_dim=128, intermediate=11008, n_layers=1,
+        vocab=512, s_max=300, rms_eps=1e-6, rope_theta=1e6, w_std=0.02)
+    run_decode_case(S, wl, [0, 129, 300], seed=7)
