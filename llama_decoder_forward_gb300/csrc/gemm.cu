@@ -77,14 +77,17 @@ struct GemmCfg {
   static constexpr int B_BYTES = (BN / PAIR) * BK * 2;  // this CTA's share of the B box
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int EPI_BYTES = kEpiWarps * EpiStage<EPI>::kPerWarp;
-  static constexpr int STAGES_RAW = (232448 - 1024 - 256 - EPI_BYTES) / STAGE_BYTES;
+  // QKV (hd 64): the fine part of the RoPE table (64 positions x 16 float4)
+  // is copied to shared memory once per CTA
+  static constexpr int TAB_BYTES = EPI == 0 /*kEpiQkvRope*/ ? 64 * 16 * 16 : 0;
+  static constexpr int STAGES_RAW = (232448 - 1024 - 256 - EPI_BYTES - TAB_BYTES) / STAGE_BYTES;
   // the QKV epilogue's RoPE table reads want L1, which the shared-memory
   // carve-out shrinks: that epilogue keeps at most four stages
   static constexpr int STAGES_CAP = EPI == 0 /*kEpiQkvRope*/ ? 4 : 8;
   static constexpr int STAGES = STAGES_RAW > STAGES_CAP ? STAGES_CAP : STAGES_RAW;
   static constexpr int TMEM_COLS = (2 * BN <= 128) ? 128 : (2 * BN <= 256 ? 256 : 512);
   static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
+  static constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + EPI_BYTES + TAB_BYTES + BAR_BYTES;
   static_assert(BN % 64 == 0 && BN <= 256, "UMMA N for M=128 and whole 64-column epilogue units");
   static_assert(B_BYTES % 1024 == 0, "B stage must keep 1024-byte alignment");
   static_assert(STAGES >= 3, "pipeline depth");
@@ -231,6 +234,7 @@ struct EpiCtx {
   uint32_t rphase;
   uint32_t seq;       // staging uses so far (selects the alternating tile)
   float rs;           // the lane's row scale rstd, read before the accumulator is waited for
+  const float4 *tab;  // fine RoPE entries in shared memory (QKV, hd 64), else nullptr
 };
 
 // logits = rstd * D; units of 64 columns (one full 128-byte row segment).
@@ -465,7 +469,7 @@ __device__ __forceinline__ void epi_qkv_rope(const GemmParams &p, EpiCtx &e) {
   pos = pos < 0 ? 0 : (pos >= p.max_pos ? p.max_pos - 1 : pos);
   // entry (j, pos & 63) of the fine part and (j, pos >> 6) of the coarse part
   const int n_coarse = static_cast<int>(cdiv(p.max_pos, 64));
-  const float4 *fine4 = reinterpret_cast<const float4 *>(p.rope) + (pos & 63);
+  const float4 *fine4 = (HD == 64 && e.tab ? e.tab : reinterpret_cast<const float4 *>(p.rope)) + (pos & 63);
   const float4 *coarse4 = reinterpret_cast<const float4 *>(p.rope) + (HD / 4) * 64 + (pos >> 6);
   // element offsets of (b, head 0, t, 0) in [B, H, T, hd] and [B, KV, T, hd]
   const long long q_row = ((long long)b * p.H * p.T + t) * HD;
@@ -620,7 +624,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint8_t *sA = smem;
   uint8_t *sB = smem + C::STAGES * C::A_BYTES;
   uint8_t *sEpi = sB + C::STAGES * C::B_BYTES;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sEpi + C::EPI_BYTES);
+  float4 *sTab = reinterpret_cast<float4 *>(sEpi + C::EPI_BYTES);   // [16][64] fine RoPE entries (QKV)
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sEpi + C::EPI_BYTES + C::TAB_BYTES);
   uint64_t *full = bars;
   uint64_t *empty = bars + C::STAGES;
   uint64_t *tfull = bars + 2 * C::STAGES;
@@ -824,6 +829,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     e.rbar = &rbar[warp - 2];
     e.rphase = 0;
     e.seq = 0;
+    e.tab = nullptr;
+    if constexpr (EPI == kEpiQkvRope && HD == 64) {
+      // the table is an input of the step; every epilogue warp takes a share
+      const float4 *src = reinterpret_cast<const float4 *>(p.rope);
+      for (int i = static_cast<int>(threadIdx.x) - 64; i < 16 * 64; i += kEpiWarps * 32) sTab[i] = src[i];
+      asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");   // the epilogue warps only
+      e.tab = sTab;
+    }
     const bool resid_tma = EPI == kEpiResidual && (p.epi_tma & kTmaResid);
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = first_tile; tile < num_tiles; tile += tile_step) {
