@@ -22,6 +22,7 @@ import glob
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -129,10 +130,14 @@ class ClockSampler:
 
 
 def src_digest():
+    """Digest of the kernel sources with // comments and blank lines removed (an
+    edit of a comment does not change what the captured kernels execute)."""
     h = hashlib.sha256()
     for p in sorted(glob.glob(os.path.join(ROOT, "llama_decoder_forward_gb300", "csrc", "*"))):
-        with open(p, "rb") as f:
-            h.update(os.path.basename(p).encode() + f.read())
+        with open(p, encoding="utf-8") as f:
+            lines = [re.sub(r"//.*$", "", ln).rstrip() for ln in f.read().splitlines()]
+        code = "\n".join(ln for ln in lines if ln)
+        h.update(os.path.basename(p).encode() + code.encode())
     return h.hexdigest()[:16]
 
 

@@ -4,22 +4,26 @@
 // cached ones, and with a single new token no causal mask applies; section 7
 // generate slices the RoPE rows at past_len).
 //
-// Per layer: QKV GEMM (rstd, RoPE at cache_len[b], k/v written to k_new/v_new)
-// -> split-K decode attention over cache_len[b] cached keys plus the new key
-// -> O GEMM + residual -> gate/up GEMM + SwiGLU -> down GEMM + residual.
-// Then the tied head.  The GEMMs are the tcgen05 kernel of gemm.cu with M = B.
+// Per layer: QKV projection (rstd, RoPE at cache_len[b], k/v written to
+// k_new/v_new) -> decode attention over cache_len[b] cached keys plus the new
+// key -> O projection + residual -> gate/up + SwiGLU -> down + residual.  Then
+// the tied head.  For batches of at most 64 rows the projections run on the
+// narrow-unit kernel of decode_gemm.cu, otherwise on the tcgen05 GEMM of
+// gemm.cu with M = B; every launch is a programmatic dependent of the one
+// before (weights and cache chunks are requested before the wait).
 //
-// Decode attention is bound by HBM bandwidth (it streams the cache).  One CTA
-// owns (sequence b, kv head, a chunk of kChunk keys) and all g query heads of
-// that kv head, so each cached key/value is read once for the whole group.
-// One thread fetches the chunk's K and V rows with two bulk copies (the TMA
-// engine) into shared memory, so the whole chunk is in flight at once while
-// other CTAs on the SM compute.  Keys are then spread over lane groups of hd/8
-// lanes (16-byte reads, 8 dims per lane); each lane group takes 4 keys per
-// step, reduces the q.k partial dots with shuffles and updates an online
-// softmax in the exp2 domain.  Partial (max, sum, output) triples are merged inside the
-// warp, then across warps in shared memory, then across chunks by the last
-// CTA of the (b, kv head) pair (an atomic arrival counter, no waiting).
+// Decode attention is bound by HBM bandwidth (it streams the cache) and reads
+// each cached key/value once for all g query heads of its kv head.  For head
+// dim 64 and up to kDecMaxB sequences it is a persistent kernel (one CTA per
+// SM streaming a contiguous range of (sequence, kv head, 256-key chunk)
+// items through a TMA ring, tensor cores for the dot products, merge warps for
+// the softmax states; see decode_attn_persist_kernel).  The per-chunk kernels
+// below it serve larger batches (decode_attn_mma_kernel, one CTA per chunk)
+// and head dim 128 (decode_attn_kernel on CUDA cores: lane groups of hd/8
+// lanes take 8 dims each, 16-byte reads, shuffle-reduced dot products and an
+// online softmax in the exp2 domain); their chunks' (max, sum, output)
+// triples are merged by the last CTA of each (sequence, kv head) (an atomic
+// arrival counter, no waiting).
 #include <math.h>
 
 #include "decode.cuh"
