@@ -238,7 +238,7 @@ enum {
   SMOL_K_GATEUP = 5,     /* RMSNorm + gate/up GEMM + SwiGLU               */
   SMOL_K_DOWN = 6,       /* down GEMM + residual                          */
   SMOL_K_HEAD = 7,       /* final RMSNorm + tied lm_head GEMM             */
-  SMOL_K_DEC_ATTN = 8,   /* split-K decode attention                      */
+  SMOL_K_DEC_ATTN = 8,   /* decode attention over the KV cache            */
   SMOL_K_OTHER = 9,      /* packing and bookkeeping kernels               */
   SMOL_K_COUNT = 10
 };
