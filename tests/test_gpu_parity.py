@@ -201,3 +201,17 @@ def test_decode_head_dim_128(S):
         hidden=2048, n_heads=16, n_kv_heads=4, head_dim=128, intermediate=11008, n_layers=1,
         vocab=512, s_max=300, rms_eps=1e-6, rope_theta=1e6, w_std=0.02)
     run_decode_case(S, wl, [0, 129, 300], seed=7)
+
+
+def test_decode_single_sequence_long_cache(S):
+    # one sequence, 16 chunks per kv head: the persistent attention spreads the
+    # 48 chunks over as many CTAs, so each (sequence, kv head) is merged from
+    # up to 16 partials; most CTAs get no work at all
+    wl = W["smollm2_decode_b64_cache4096"].scaled(n_layers=1, s_max=4096, vocab=512)
+    run_decode_case(S, wl, [4095], seed=8)
+
+
+def test_decode_empty_caches(S):
+    # no cached keys: attention over the new token alone
+    wl = W["smollm2_decode_b64_cache4096"].scaled(n_layers=2, s_max=64, vocab=512)
+    run_decode_case(S, wl, [0, 0, 1], seed=9)
