@@ -15,7 +15,10 @@ Sources (web pages describing the method, cited by title and section):
        sections 1 Config, 2 RMSNorm, 3 RoPE, 4 Attention, 5 MLP (SwiGLU),
        6 Transformer Block, 7 Top-level SmolLM2-135M, 8 Quick self-test.
   [M3] "SmolLM3" (nnterp encyclopedia): "The block, in order",
-       "Grouped-query attention", "The readout, the embeddings and the tokenizer".
+       "Every fourth block has no rotary", "On a NoPE block the queries and
+       keys are the projections", "Grouped-query attention", "A sliding window
+       the 3B checkpoints leave off", "The readout, the embeddings and the
+       tokenizer".
   [M4] "model.py" - complete SmolLM2-135M implementation (abi96062):
        module docstring (parameter total), SmolLM2Model.forward.
   [M5] "components.py" (abi96062): RMSNorm, RotaryEmbedding,
@@ -33,6 +36,15 @@ design notes):
     an attention output of exactly 0.
   * Left padding: position id of token t of sequence b is t - valid_start[b];
     padding rows take position 0 (their values never reach a valid row).
+  * NoPE blocks ([M3] "Every fourth block has no rotary"): a per-block flag
+    list with the meaning of the SmolLM3 config's no_rope_layers (1 = the
+    block rotates q and k, 0 = it does not); absent = every block rotates.
+  * Sliding window ([M3] "A sliding window the 3B checkpoints leave off"
+    names the setting, not its bounds): a window of w on a block lets query t
+    see the w most recent keys, its own included, i.e. keys j with
+    t - w < j <= t, on top of the causal and padding masks; 0 = no window.
+    In decode the new token at position L sees cached slots j >= L - w + 1
+    plus itself.
   * Decode: the cache holds post-RoPE keys (stored "after RoPE, before GQA
     expansion" in [M1] section 4); only the new token's q and k are rotated,
     at position cache_len[b]; with a single new token no causal mask applies
@@ -45,7 +57,7 @@ the parameter total printed in [M4]).
 from __future__ import annotations
 
 from dataclasses import dataclass
-from typing import Dict, List, Optional
+from typing import Dict, List, Optional, Tuple
 
 import numpy as np
 
@@ -66,6 +78,20 @@ class Config:
     max_pos: int
     rms_eps: float
     rope_theta: float
+    # [M3] "Every fourth block has no rotary": one flag per block, 1 where the
+    # block applies the rotary and 0 on a NoPE block; None = rotary everywhere
+    no_rope_layers: Optional[Tuple[int, ...]] = None
+    # [M3] "A sliding window ...": per block, 0 = full causal attention, w > 0 =
+    # query t sees keys t - w < j <= t; None = no window on any block
+    sliding_window: Optional[Tuple[int, ...]] = None
+
+
+def block_kind(cfg: Config, layer: int) -> Tuple[bool, int]:
+    """(applies the rotary, window) of block ``layer`` ([M3] "Every fourth
+    block has no rotary", "A sliding window the 3B checkpoints leave off")."""
+    rope = True if cfg.no_rope_layers is None else bool(cfg.no_rope_layers[layer])
+    window = 0 if cfg.sliding_window is None else int(cfg.sliding_window[layer])
+    return rope, window
 
 
 SMOLLM2_135M = Config(hidden=576, n_heads=9, n_kv_heads=3, head_dim=64,
@@ -157,14 +183,16 @@ def positions(B: int, T: int, valid_start=None) -> np.ndarray:
     return np.maximum(t - vs, 0)
 
 
-def gqa_attention(q, k, v, valid_start=None) -> np.ndarray:
+def gqa_attention(q, k, v, valid_start=None, window: int = 0) -> np.ndarray:
     """Causal grouped-query softmax attention.
 
     q: [B, H, T, hd]; k, v: [B, KV, S, hd] with S == T (prefill).
     o[b,h,t] = sum_{j valid, j<=t} softmax_j(q[b,h,t].k[b,h//g,j] / sqrt(hd)) v[b,h//g,j]
-    A row with no valid key returns 0.
+    A row with no valid key returns 0.  With window w > 0 a key is also
+    masked when j <= t - w.
     [M1] section 4 (scores / sqrt(head_dim), triu(1) causal mask, additive
-    padding mask, softmax, probs @ v); [M3] "Grouped-query attention".
+    padding mask, softmax, probs @ v); [M3] "Grouped-query attention" and
+    "A sliding window the 3B checkpoints leave off".
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, H, T, hd = q.shape
@@ -176,6 +204,8 @@ def gqa_attention(q, k, v, valid_start=None) -> np.ndarray:
     for b in range(B):
         vs = 0 if valid_start is None else int(valid_start[b])
         masked = (j_idx > t_idx) | (j_idx < vs)
+        if window > 0:
+            masked = masked | (j_idx <= t_idx - window)
         for h in range(H):
             kvh = h // g
             s = np.matmul(q[b, h], k[b, kvh].T) / np.sqrt(F64(hd))
@@ -207,11 +237,14 @@ class BlockWeights:
 
 
 def block_forward(cfg: Config, w: BlockWeights, x, valid_start=None,
-                  taps: Optional[Dict[str, np.ndarray]] = None) -> np.ndarray:
-    """Pre-norm decoder block on x [B, T, d].
+                  taps: Optional[Dict[str, np.ndarray]] = None, layer: int = 0) -> np.ndarray:
+    """Pre-norm decoder block on x [B, T, d]; ``layer`` selects the block's
+    NoPE flag and window from cfg.
 
     h   = x + O(attn(RoPE(Q, K), V)) with Q, K, V projections of RMSNorm1(x)
     out = h + Down(SiLU(Gate(RMSNorm2(h))) * Up(RMSNorm2(h)))
+    On a NoPE block Q and K enter attention unrotated ([M3] "On a NoPE block
+    the queries and keys are the projections").
     [M1] section 6 SmolBlock; [M3] "The block, in order"; [M5] TransformerBlock.
     ``taps`` (optional) receives the named intermediates used by [M3].
     """
@@ -224,9 +257,11 @@ def block_forward(cfg: Config, w: BlockWeights, x, valid_start=None,
     q = linear(n, w.wq).reshape(B, T, H, hd).transpose(0, 2, 1, 3)
     k = linear(n, w.wk).reshape(B, T, KV, hd).transpose(0, 2, 1, 3)
     v = linear(n, w.wv).reshape(B, T, KV, hd).transpose(0, 2, 1, 3)
-    q = apply_rope(q, pos[:, None, :], cfg.rope_theta)
-    k = apply_rope(k, pos[:, None, :], cfg.rope_theta)
-    o = gqa_attention(q, k, v, valid_start)
+    rope, window = block_kind(cfg, layer)
+    if rope:
+        q = apply_rope(q, pos[:, None, :], cfg.rope_theta)
+        k = apply_rope(k, pos[:, None, :], cfg.rope_theta)
+    o = gqa_attention(q, k, v, valid_start, window)
     o_tok = o.transpose(0, 2, 1, 3).reshape(B, T, H * hd)
     attn_out = linear(o_tok, w.wo)
     h = x + attn_out
@@ -264,8 +299,8 @@ def model_forward(cfg: Config, layers: List[BlockWeights], embed, final_norm, id
     if T > cfg.max_pos:
         raise ValueError("sequence longer than max_position_embeddings")
     x = _f64(embed)[ids]
-    for w in layers:
-        x = block_forward(cfg, w, x, valid_start)
+    for l, w in enumerate(layers):
+        x = block_forward(cfg, w, x, valid_start, layer=l)
     if taps is not None:
         taps["final_norm_output"] = rms_norm(x, final_norm, cfg.rms_eps)
     logits = lm_head(cfg, x, final_norm, embed)
@@ -282,9 +317,11 @@ def decode_step(cfg: Config, layers: List[BlockWeights], embed, final_norm, ids,
     keys and values in slots [0, cache_len[b]).  The new token sits at position
     cache_len[b]; it attends over the cached entries plus its own key/value,
     with no further mask.  Returns (logits [B, V], k_new [L, B, KV, hd],
-    v_new [L, B, KV, hd]); k_new is post-RoPE.
+    v_new [L, B, KV, hd]); k_new is post-RoPE (unrotated on a NoPE block).
+    A block with window w attends over the cached slots j >= cache_len[b] - w + 1
+    only.
     [M1] section 4 (cache concat, ``past_key_value`` branch) and section 7
-    (``generate``: RoPE rows sliced at past_len).
+    (``generate``: RoPE rows sliced at past_len); [M3] NoPE blocks and windows.
     """
     ids = np.asarray(ids)
     cache_len = np.asarray(cache_len)
@@ -299,18 +336,23 @@ def decode_step(cfg: Config, layers: List[BlockWeights], embed, final_norm, ids,
     v_new = np.zeros((L, B, KV, hd))
     for l, w in enumerate(layers):
         n = rms_norm(x, w.attn_norm, cfg.rms_eps)
+        rope, window = block_kind(cfg, l)
         pos = cache_len[:, None]                           # [B, 1] broadcast over heads
-        q = apply_rope(linear(n, w.wq).reshape(B, H, hd), pos, cfg.rope_theta)
-        k = apply_rope(linear(n, w.wk).reshape(B, KV, hd), pos, cfg.rope_theta)
+        q = linear(n, w.wq).reshape(B, H, hd)
+        k = linear(n, w.wk).reshape(B, KV, hd)
+        if rope:
+            q = apply_rope(q, pos, cfg.rope_theta)
+            k = apply_rope(k, pos, cfg.rope_theta)
         v = linear(n, w.wv).reshape(B, KV, hd)
         k_new[l], v_new[l] = k, v
         o = np.zeros((B, H, hd))
         for b in range(B):
             Lb = int(cache_len[b])
+            first = max(0, Lb - window + 1) if window > 0 else 0
             for h in range(H):
                 kvh = h // g
-                keys = np.concatenate([_f64(k_cache[l, b, kvh, :Lb]), k[b, kvh][None]], axis=0)
-                vals = np.concatenate([_f64(v_cache[l, b, kvh, :Lb]), v[b, kvh][None]], axis=0)
+                keys = np.concatenate([_f64(k_cache[l, b, kvh, first:Lb]), k[b, kvh][None]], axis=0)
+                vals = np.concatenate([_f64(v_cache[l, b, kvh, first:Lb]), v[b, kvh][None]], axis=0)
                 s = np.matmul(keys, q[b, h]) / np.sqrt(F64(hd))
                 e = np.exp(s - np.max(s))
                 o[b, h] = np.matmul(e / np.sum(e), vals)

@@ -39,8 +39,10 @@ def silu(z):
     return z / (1.0 + math.exp(-z))
 
 
-def block(cfg, w, x, valid_start=None):
-    """x: [B][T][d] nested lists; w: dict of nested lists."""
+def block(cfg, w, x, valid_start=None, rope=True, window=0):
+    """x: [B][T][d] nested lists; w: dict of nested lists.  rope=False leaves
+    q and k unrotated (a NoPE block); window > 0 keeps only the `window` most
+    recent keys of each query, its own included."""
     H, KV, hd = cfg.n_heads, cfg.n_kv_heads, cfg.head_dim
     B, T = len(x), len(x[0])
     out = []
@@ -53,15 +55,16 @@ def block(cfg, w, x, valid_start=None):
             q = matvec(w["wq"], n)
             k = matvec(w["wk"], n)
             v = matvec(w["wv"], n)
-            qs.append([rotate(q[h * hd:(h + 1) * hd], pos, cfg.rope_theta) for h in range(H)])
-            ks.append([rotate(k[h * hd:(h + 1) * hd], pos, cfg.rope_theta) for h in range(KV)])
+            rot = (lambda u: rotate(u, pos, cfg.rope_theta)) if rope else (lambda u: list(u))
+            qs.append([rot(q[h * hd:(h + 1) * hd]) for h in range(H)])
+            ks.append([rot(k[h * hd:(h + 1) * hd]) for h in range(KV)])
             vs_.append([v[h * hd:(h + 1) * hd] for h in range(KV)])
         rows = []
         for t in range(T):
             o = []
             for h in range(H):
                 kvh = h * KV // H
-                keys = [j for j in range(T) if vs <= j <= t]
+                keys = [j for j in range(T) if vs <= j <= t and (window == 0 or t - j < window)]
                 if not keys:
                     o.extend([0.0] * hd)
                     continue
@@ -82,10 +85,12 @@ def block(cfg, w, x, valid_start=None):
     return out
 
 
-def model(cfg, layers, embed, final_norm, ids):
+def model(cfg, layers, embed, final_norm, ids, kinds=None):
+    """kinds: optional list of (rope, window) per layer."""
     x = [[list(embed[i]) for i in seq] for seq in ids]
-    for w in layers:
-        x = block(cfg, w, x)
+    for l, w in enumerate(layers):
+        rope, window = kinds[l] if kinds else (True, 0)
+        x = block(cfg, w, x, rope=rope, window=window)
     logits = []
     for seq in x:
         logits.append([matvec(embed, rmsnorm(row, final_norm, cfg.rms_eps)) for row in seq])

@@ -335,9 +335,9 @@ def _prefill_cache(cfg, layers, embed, ids):
     """Post-RoPE K and V of every layer for a prefill of ids [B, T]."""
     x = embed[ids]
     ks, vs = [], []
-    for w in layers:
+    for l, w in enumerate(layers):
         taps = {}
-        x = O.block_forward(cfg, w, x, taps=taps)
+        x = O.block_forward(cfg, w, x, taps=taps, layer=l)
         ks.append(taps["attention_keys"])
         vs.append(taps["attention_values"])
     return np.stack(ks), np.stack(vs)   # [L, B, KV, T, hd]
@@ -361,6 +361,173 @@ def test_decode_matches_last_row_of_prefill():
         v_cache[:, b, :, :L] = v[:, 0]
         k_cache[:, b, :, L:] = 99.0        # slots past the length must not be read
         v_cache[:, b, :, L:] = -99.0
+    ids = np.array([s[-1] for s in seqs])
+    logits, k_new, v_new = O.decode_step(cfg, layers, embed, fnorm, ids, lens, k_cache, v_cache)
+    for b, L in enumerate(lens):
+        full = O.model_forward(cfg, layers, embed, fnorm, seqs[b][None])
+        np.testing.assert_allclose(logits[b], full[0, -1], rtol=1e-11, atol=1e-12)
+        k, v = _prefill_cache(cfg, layers, embed, seqs[b][None])
+        np.testing.assert_allclose(k_new[:, b], k[:, 0, :, L], rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(v_new[:, b], v[:, 0, :, L], rtol=1e-11, atol=1e-12)
+
+
+# ---------------------------------------------------------------- SmolLM3 variants:
+# NoPE blocks and sliding windows ("SmolLM3", nnterp encyclopedia: "Every fourth
+# block has no rotary", "On a NoPE block the queries and keys are the
+# projections", "A sliding window the 3B checkpoints leave off")
+
+def _with(cfg, **kw):
+    return O.Config(**{**cfg.__dict__, **kw})
+
+
+def test_block_kind_defaults_and_lists():
+    assert O.block_kind(TINY, 0) == (True, 0) and O.block_kind(TINY, 1) == (True, 0)
+    cfg = _with(TINY, no_rope_layers=(1, 0), sliding_window=(0, 128))
+    assert O.block_kind(cfg, 0) == (True, 0)
+    assert O.block_kind(cfg, 1) == (False, 128)
+
+
+def test_nope_and_window_block_vs_bruteforce_loops():
+    rng = np.random.default_rng(21)
+    w = tiny_weights(TINY, rng)
+    x = rng.normal(0, 1, (2, 9, TINY.hidden))
+    wn = {k: nested(a) for k, a in w.items()}
+    for rope, window in ((False, 0), (True, 3), (False, 4), (True, 1)):
+        cfg = _with(TINY, no_rope_layers=(int(rope), 1), sliding_window=(window, 0))
+        for vs in (None, [0, 3]):
+            out = O.block_forward(cfg, as_block(w), x, vs, layer=0)
+            ref = np.array(bf.block(TINY, wn, nested(x), vs, rope=rope, window=window))
+            for b in range(2):
+                v0 = 0 if vs is None else vs[b]
+                np.testing.assert_allclose(out[b, v0:], ref[b, v0:], rtol=1e-11, atol=1e-12)
+
+
+def test_nope_queries_are_the_projections():
+    # on a NoPE block the attention's queries and keys equal the projections split
+    # into heads at every position; on a rotary block only at position 0
+    rng = np.random.default_rng(22)
+    w = tiny_weights(TINY, rng)
+    x = rng.normal(0, 1, (1, 6, TINY.hidden))
+    cfg = _with(TINY, no_rope_layers=(1, 0))
+    t_rot, t_nope = {}, {}
+    O.block_forward(cfg, as_block(w), x, taps=t_rot, layer=0)
+    O.block_forward(cfg, as_block(w), x, taps=t_nope, layer=1)
+    np.testing.assert_array_equal(t_rot["attention_norm_output"], t_nope["attention_norm_output"])
+    raw_q = np.matmul(t_nope["attention_norm_output"], np.asarray(w["wq"]).T)
+    raw_q = raw_q.reshape(1, 6, TINY.n_heads, TINY.head_dim).transpose(0, 2, 1, 3)
+    np.testing.assert_array_equal(t_nope["attention_queries"], raw_q)
+    np.testing.assert_array_equal(t_rot["attention_queries"][:, :, 0], raw_q[:, :, 0])
+    assert not np.allclose(t_rot["attention_queries"][:, :, 1:], raw_q[:, :, 1:])
+
+
+def test_nope_last_row_ignores_the_order_of_earlier_tokens():
+    # without the rotary a score depends on the two tokens' contents alone, so
+    # the last query (which sees every key) is unchanged by permuting the keys
+    # before it; with the rotary it changes
+    cfg = O.Config(hidden=16, n_heads=4, n_kv_heads=2, head_dim=4, intermediate=12, n_layers=2,
+                   vocab=5, max_pos=64, rms_eps=1e-5, rope_theta=10.0, no_rope_layers=(1, 0))
+    rng = np.random.default_rng(23)
+    w = as_block(tiny_weights(cfg, rng))
+    T = 8
+    x = rng.normal(0, 1, (1, T, cfg.hidden))
+    perm = np.concatenate([rng.permutation(T - 1), [T - 1]])
+    xp = x[:, perm]
+    nope = O.block_forward(cfg, w, x, layer=1)[0, -1]
+    nope_p = O.block_forward(cfg, w, xp, layer=1)[0, -1]
+    np.testing.assert_allclose(nope_p, nope, rtol=1e-12, atol=1e-12)
+    rot = O.block_forward(cfg, w, x, layer=0)[0, -1]
+    rot_p = O.block_forward(cfg, w, xp, layer=0)[0, -1]
+    assert np.max(np.abs(rot_p - rot)) > 1e-6
+
+
+def test_window_not_shorter_than_sequence_is_full_causal():
+    rng = np.random.default_rng(24)
+    B, H, KV, T, hd = 2, 6, 2, 11, 4
+    q, k, v = _rand_qkv(B, H, KV, T, hd, rng)
+    full = O.gqa_attention(q, k, v, [0, 4])
+    for wdw in (T, T + 5):
+        np.testing.assert_array_equal(O.gqa_attention(q, k, v, [0, 4], window=wdw), full)
+    assert not np.allclose(O.gqa_attention(q, k, v, [0, 4], window=T - 1), full)
+
+
+def test_window_of_one_returns_own_value():
+    # a single visible key gets softmax weight exactly 1
+    rng = np.random.default_rng(25)
+    B, H, KV, T, hd = 2, 6, 3, 9, 8
+    q, k, v = _rand_qkv(B, H, KV, T, hd, rng)
+    o = O.gqa_attention(q, k, v, window=1)
+    g = H // KV
+    for h in range(H):
+        np.testing.assert_array_equal(o[:, h], v[:, h // g])
+
+
+def test_window_vs_torch_sdpa_band_mask():
+    rng = np.random.default_rng(26)
+    B, H, KV, T, hd = 2, 8, 2, 40, 16
+    q, k, v = _rand_qkv(B, H, KV, T, hd, rng)
+    g = H // KV
+    kt = torch.tensor(k).repeat_interleave(g, dim=1)
+    vt = torch.tensor(v).repeat_interleave(g, dim=1)
+    for wdw in (1, 5, 16, 39):
+        ones = torch.ones(T, T, dtype=torch.bool)
+        band = torch.tril(ones) & ~torch.tril(ones, diagonal=-wdw)
+        ref = F.scaled_dot_product_attention(torch.tensor(q), kt, vt, attn_mask=band).numpy()
+        np.testing.assert_allclose(O.gqa_attention(q, k, v, window=wdw), ref, rtol=1e-11, atol=1e-12)
+
+
+def test_window_locality_of_a_block():
+    # with window w, block output row t depends on input rows t-w+1 .. t only
+    wdw = 3
+    cfg = _with(TINY, sliding_window=(wdw, 0))
+    rng = np.random.default_rng(27)
+    w = as_block(tiny_weights(TINY, rng))
+    x = rng.normal(0, 1, (1, 12, TINY.hidden))
+    base = O.block_forward(cfg, w, x, layer=0)
+    j0 = 4
+    x2 = x.copy()
+    x2[0, j0] += 1.5
+    pert = O.block_forward(cfg, w, x2, layer=0)
+    np.testing.assert_array_equal(pert[0, :j0], base[0, :j0])
+    np.testing.assert_array_equal(pert[0, j0 + wdw:], base[0, j0 + wdw:])
+    for t in range(j0, j0 + wdw):
+        assert not np.allclose(pert[0, t], base[0, t])
+
+
+def test_model_with_nope_and_window_vs_bruteforce_loops():
+    rng = np.random.default_rng(28)
+    cfg = _with(TINY, no_rope_layers=(1, 0), sliding_window=(0, 2))
+    layers_raw = [tiny_weights(TINY, rng) for _ in range(2)]
+    embed = rng.normal(0, 0.5, (TINY.vocab, TINY.hidden))
+    fnorm = 1 + rng.normal(0, 0.1, TINY.hidden)
+    ids = rng.integers(0, TINY.vocab, (2, 5))
+    out = O.model_forward(cfg, [as_block(w) for w in layers_raw], embed, fnorm, ids)
+    ref = np.array(bf.model(TINY, [{k: nested(a) for k, a in w.items()} for w in layers_raw],
+                            nested(embed), nested(fnorm), nested(ids), kinds=[(True, 0), (False, 2)]))
+    np.testing.assert_allclose(out, ref, rtol=1e-11, atol=1e-12)
+
+
+def test_decode_with_nope_and_windows_matches_last_row_of_prefill():
+    cfg = O.Config(hidden=16, n_heads=4, n_kv_heads=2, head_dim=4, intermediate=12, n_layers=3,
+                   vocab=13, max_pos=64, rms_eps=1e-5, rope_theta=1e4,
+                   no_rope_layers=(1, 0, 0), sliding_window=(0, 3, 7))
+    rng = np.random.default_rng(29)
+    layers = [as_block(tiny_weights(cfg, rng)) for _ in range(cfg.n_layers)]
+    embed = rng.normal(0, 0.5, (cfg.vocab, cfg.hidden))
+    fnorm = 1 + rng.normal(0, 0.1, cfg.hidden)
+    lens = [1, 5, 9, 2]
+    S = 12
+    seqs = [rng.integers(0, cfg.vocab, L + 1) for L in lens]
+    k_cache = np.zeros((cfg.n_layers, len(lens), cfg.n_kv_heads, S, cfg.head_dim))
+    v_cache = np.zeros_like(k_cache)
+    for b, L in enumerate(lens):
+        k, v = _prefill_cache(cfg, layers, embed, seqs[b][None, :L])
+        k_cache[:, b, :, :L] = k[:, 0]
+        v_cache[:, b, :, :L] = v[:, 0]
+        k_cache[:, b, :, L:] = 99.0        # slots past the length must not be read
+        v_cache[:, b, :, L:] = -99.0
+    # slots that fall out of layer 1's window (3) must not be read either
+    k_cache[1, 2, :, :9 - 2] = 77.0
+    v_cache[1, 2, :, :9 - 2] = -77.0
     ids = np.array([s[-1] for s in seqs])
     logits, k_new, v_new = O.decode_step(cfg, layers, embed, fnorm, ids, lens, k_cache, v_cache)
     for b, L in enumerate(lens):
