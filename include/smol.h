@@ -54,6 +54,19 @@ typedef struct smol_config {
   int max_pos;         /* max_position_embeddings: RoPE table rows and length guard */
   float rms_eps;       /* RMSNorm epsilon */
   float rope_theta;    /* RoPE base */
+  /* Per-block variants of SmolLM3 ([M3] "Every fourth block has no rotary",
+   * "A sliding window the 3B checkpoints leave off").  Both are HOST arrays
+   * of n_layers entries, indexed by the block's layer index, read during the
+   * call; NULL leaves every block as SmolLM2's.
+   * no_rope_layers[l]: 1 = block l rotates q and k (RoPE), 0 = a NoPE block
+   *                    (q and k enter attention as projected; the k_out/k_new
+   *                    and cache keys of that block are unrotated too).
+   * sliding_window[l]: 0 = full causal attention; w > 0 = query t sees only
+   *                    keys j with t - w < j <= t (its own and the w - 1
+   *                    before it); in decode the new token at position L sees
+   *                    cache slots j >= L - w + 1 and itself. */
+  const int32_t *no_rope_layers;
+  const int32_t *sliding_window;
 } smol_config;
 
 /* One block's weights, device pointers, bf16, nn.Linear layout [out, in]. */

@@ -5,7 +5,9 @@
 // section 4: scores / sqrt(head_dim), triu(1) causal mask plus the additive
 // padding mask, softmax, probs @ v; GQA through repeat_interleave, i.e. query
 // head h reads key/value head h // g, as in the "SmolLM3" page's
-// "Grouped-query attention").  Rows with no visible key produce 0.
+// "Grouped-query attention").  Rows with no visible key produce 0.  With a
+// sliding window w (the "SmolLM3" page, "A sliding window the 3B checkpoints
+// leave off") keys j <= t - w are hidden too.
 //
 // One CTA owns (sequence b, kv head, a block of BQ query tokens) and all g
 // query heads of that kv head: each K/V tile is loaded once into shared memory
@@ -90,7 +92,8 @@ __global__ void __launch_bounds__(512, 1) flash_attn_kernel(const AttnParams p) 
   };
 
   const int last_q = min(q0 + BQ, T) - 1;
-  const int kt_lo = vs / BK;
+  const int W = p.window;                                         // > 0: sliding window
+  const int kt_lo = (W > 0 ? max(vs, q0 - W + 1) : vs) / BK;      // first key any row of the block sees
   const int kt_hi = last_q / BK;
   load_kv(kt_lo, 0);
   cp_async_commit();
@@ -122,8 +125,9 @@ __global__ void __launch_bounds__(512, 1) flash_attn_kernel(const AttnParams p) 
     __syncthreads();
 
     const int k0 = kt * BK;
-    // skip tiles whose keys are all in this warp's future, and warps made only of padding rows
-    if (k0 <= tw_hi && tw_hi >= vs) {
+    // skip tiles whose keys are all in this warp's future or all before its
+    // rows' windows, and warps made only of padding rows
+    if (k0 <= tw_hi && tw_hi >= vs && (W == 0 || k0 + BK - 1 > tw_lo - W)) {
       const f16 *tK = sK + st * BK * HD;
       const f16 *tV = sV + st * BK * HD;
       float s[NT][4];
@@ -143,7 +147,7 @@ __global__ void __launch_bounds__(512, 1) flash_attn_kernel(const AttnParams p) 
         }
       }
       // scale into the exp2 domain and mask
-      const bool need_mask = (k0 + BK - 1 > tw_lo) || (k0 < vs);
+      const bool need_mask = (k0 + BK - 1 > tw_lo) || (k0 < vs) || (W > 0 && k0 <= tw_hi - W);
 #pragma unroll
       for (int i = 0; i < NT; ++i) {
 #pragma unroll
@@ -152,7 +156,7 @@ __global__ void __launch_bounds__(512, 1) flash_attn_kernel(const AttnParams p) 
           if (need_mask) {
             const int j = k0 + i * 8 + ((lane & 3) << 1) + (e & 1);
             const int t = (e < 2) ? t_a : t_b;
-            if (j > t || j < vs) x = -INFINITY;
+            if (j > t || j < vs || (W > 0 && j <= t - W)) x = -INFINITY;
           }
           s[i][e] = x;
         }

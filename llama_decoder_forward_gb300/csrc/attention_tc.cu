@@ -5,6 +5,9 @@
 // section 4: scaled scores, triu(1) causal mask plus the padding mask, softmax,
 // probs @ v; query head h reads key/value head h // g as in the "SmolLM3"
 // page's "Grouped-query attention").  Rows with no visible key produce 0.
+// A block with a sliding window w (the "SmolLM3" page, "A sliding window the
+// 3B checkpoints leave off") also hides keys j <= t - w: the CTA starts at the
+// tile of its first query's window and masks per row.
 //
 // One CTA owns (sequence b, kv head, a tile of 128 query tokens) and the GH
 // query heads of that kv head.  Each K tile [128 keys x 64] and V^T tile
@@ -62,6 +65,7 @@ struct AtParams {
   const int *valid_start;
   int B, T, H, KV, G, GH, n_hsub;
   float scale_log2;
+  int window;               // > 0: query t sees keys j > t - window only
   int *status;
 };
 
@@ -144,7 +148,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int vs = p.valid_start ? min(max(p.valid_start[b], 0), T) : 0;
   const int last_q = min(q0 + kBQ - 1, T - 1);
   const int j_hi = last_q / kBK;
-  const int j_lo = min(vs / kBK, j_hi);          // an all-padding tile still runs one (masked) tile
+  // lowest key any query of the tile sees (padding start; window start of the first query)
+  const int key_lo = p.window > 0 ? max(vs, q0 - p.window + 1) : vs;
+  const int j_lo = min(key_lo / kBK, j_hi);      // an all-padding tile still runs one (masked) tile
   const int ntiles = j_hi - j_lo + 1;
   const int nslots = ntiles * GH;
 
@@ -273,6 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int grp = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;              // query row within the tile
     const int t = q0 + r;
+    const int row_lo = p.window > 0 ? max(vs, t - p.window + 1) : vs;   // this row's first visible key
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float sl2 = p.scale_log2;
     float *red_max = reinterpret_cast<float *>(smem + C::OFF_RED);          // [2][2][128]
@@ -288,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int it = s / GH, h = s - it * GH, sb = s & 1;
       const int k0 = (j_lo + it) * kBK + grp * 64;  // first key of this group's half tile
       const bool ok = alive && __all_sync(0xffffffffu, mbar_wait_bounded(&s_full[sb], (s >> 1) & 1, abort_flag));
-      const bool need_mask = (k0 + 63 > q0) || (k0 < vs);
+      const bool need_mask = (k0 + 63 > q0) || (k0 < vs) || (p.window > 0 && k0 <= last_q - p.window);
       uint32_t sv[64];
       float mx = -INFINITY;
       if (ok) {
@@ -302,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int q = 0; q < 8; ++q) mc[q] = -INFINITY;
         if (need_mask) {
-          const int hi = t - k0, lo = vs - k0;
+          const int hi = t - k0, lo = row_lo - k0;
 #pragma unroll
           for (int e = 0; e < 64; ++e)
             if (e <= hi && e >= lo) mc[e & 7] = fmaxf(mc[e & 7], __uint_as_float(sv[e]));
@@ -354,8 +361,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t pk[32];
       float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // eight partial sums
       if (need_mask) {
-        // keys k0+e visible iff lo <= e <= hi (causal and padding limits)
-        const int hi = t - k0, lo = vs - k0;
+        // keys k0+e visible iff lo <= e <= hi (causal, padding and window limits)
+        const int hi = t - k0, lo = row_lo - k0;
 #pragma unroll
         for (int e = 0; e < 64; e += 2) {
           const float x0 = (e <= hi && e >= lo) ? fmaf(__uint_as_float(sv[e]), sl2, -mu) : -INFINITY;
@@ -457,6 +464,7 @@ cudaError_t launch_gh(const AttnParams &a, const CUtensorMap &tq, const CUtensor
   p.GH = GH;
   p.n_hsub = p.G / GH;
   p.scale_log2 = a.scale_log2;
+  p.window = a.window;
   p.status = a.status;
   dim3 grid((unsigned)(a.B * a.KV * p.n_hsub), (unsigned)cdiv(a.T, kBQ), 1u);
   // as a programmatic dependent: CTAs set up barriers and TMEM while the

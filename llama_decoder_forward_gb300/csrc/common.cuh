@@ -27,6 +27,15 @@ __host__ __device__ constexpr long long cdiv(long long a, long long b) { return 
 // rope_table_rows counts float2 rows of hd/2 entries each.
 __host__ __device__ constexpr long long rope_table_rows(int max_pos) { return 64 + cdiv(max_pos, 64); }
 
+// Per-block variants (SmolLM3): does block `layer` rotate q and k, and its
+// attention window (0 = full causal).  The arrays are host arrays of the config.
+inline bool layer_rotary(const smol_config *c, int layer) {
+  return c->no_rope_layers == nullptr || c->no_rope_layers[layer] != 0;
+}
+inline int layer_window(const smol_config *c, int layer) {
+  return c->sliding_window ? c->sliding_window[layer] : 0;
+}
+
 // ------------------------------------------------------------------ GEMM
 // D[M, N] = A[M, K] * B[N, K]^T on tcgen05 with one of these epilogues.
 enum Epilogue : int {
@@ -59,7 +68,8 @@ struct GemmParams {
   int T_pad;              // row pitch of v_t in elements (T rounded up to a multiple of 8)
   bf16 *k_bf, *v_bf;      // optional bf16 copies of k and v (cache entries), same layout
   int T, H, KV, hd;
-  const float2 *rope;     // [rope_table_rows(max_pos)][hd/2] (cos, sin), two-level
+  const float2 *rope;     // [rope_table_rows(max_pos)][hd/2] (cos, sin), two-level;
+                          // nullptr: q and k are not rotated (a NoPE block)
   const int *valid_start; // [B] or nullptr: position t - valid_start[b]
   const int *pos_add;     // [B] or nullptr: adds clamp(pos_add[b], 0, pos_limit) (decode)
   int pos_limit;
@@ -126,6 +136,7 @@ struct AttnParams {
   const int *valid_start; // [B] or nullptr
   int B, T, H, KV, hd;
   float scale_log2;       // log2(e) / sqrt(hd)
+  int window;             // > 0: query t sees keys j > t - window only (sliding window)
   int pdl;                // tcgen05 kernel: launch as a programmatic dependent of the preceding kernel
 };
 cudaError_t launch_flash_attention(const AttnParams &p, cudaStream_t stream);

@@ -7,7 +7,11 @@
 // Per layer: QKV projection (rstd, RoPE at cache_len[b], k/v written to
 // k_new/v_new) -> decode attention over cache_len[b] cached keys plus the new
 // key -> O projection + residual -> gate/up + SwiGLU -> down + residual.  Then
-// the tied head.  For batches of at most 64 rows the projections run on the
+// the tied head.  The SmolLM3 per-block variants ("SmolLM3" page: "Every
+// fourth block has no rotary", "A sliding window the 3B checkpoints leave
+// off"): a NoPE block skips the rotation; a block with window w attends over
+// the cache slots [cache_len[b] - w + 1, cache_len[b]) and the new key, each
+// kernel shifting its slice of the cache by the first visible slot.  For batches of at most 64 rows the projections run on the
 // narrow-unit kernel of decode_gemm.cu, otherwise on the tcgen05 GEMM of
 // gemm.cu with M = B; every launch is a programmatic dependent of the one
 // before (weights and cache chunks are requested before the wait).
@@ -66,6 +70,12 @@ static DecWs dec_ws(const smol_config *c, int B) {
 
 size_t decode_ws_bytes(const smol_config *cfg, int B) { return dec_ws(cfg, B).total; }
 
+// The cache slots a new token at position Lb (already clamped) attends over:
+// [first, Lb), plus its own key.  A window w keeps the w - 1 slots before it.
+__device__ __forceinline__ int dec_first_slot(int Lb, int window) {
+  return window > 0 ? max(0, Lb - window + 1) : 0;
+}
+
 struct DecAttnParams {
   const f16 *q;             // [B, H, hd] (already rotated)
   const bf16 *k_cache, *v_cache;   // this layer: [B, KV, S_max, hd]
@@ -76,6 +86,7 @@ struct DecAttnParams {
   int *counters;            // [B, KV], zero between layers
   int B, H, KV, S_max, max_pos, max_splits;
   float scale_log2;
+  int window;               // > 0: only cache slots j >= cache_len - window + 1 are read
   int *status;              // workspace status word (bounded wait)
   int layer;                // layer index (row offset into the whole-cache tensor maps)
 };
@@ -209,6 +220,8 @@ __global__ void __launch_bounds__(128) decode_attn_mma_kernel(const __grid_const
   int Lb = p.cache_len[b];
   const int lmax = min(p.S_max, p.max_pos - 1);
   Lb = Lb < 0 ? 0 : (Lb > lmax ? lmax : Lb);
+  const int first = dec_first_slot(Lb, p.window);   // keys below are outside the window
+  Lb -= first;                                      // from here on: visible cached keys
   const int n_keys = Lb + 1;
   const int nsplit = (n_keys + kChunk - 1) / kChunk;
   if (split >= nsplit) return;
@@ -224,7 +237,7 @@ __global__ void __launch_bounds__(128) decode_attn_mma_kernel(const __grid_const
   if (threadIdx.x == 0) {
     // the cache is an input of the step, not written by any kernel of it: its
     // chunk is requested before waiting for the preceding kernel
-    const int y = static_cast<int>(((long long)p.layer * p.B + b) * p.KV + kvh) * p.S_max + k_begin;
+    const int y = static_cast<int>(((long long)p.layer * p.B + b) * p.KV + kvh) * p.S_max + first + k_begin;
     mbar_arrive_expect_tx(kv_bar, 2 * kChunk * 128);
     tma_load_2d(sK, &tmK, kv_bar, 0, y);
     tma_load_2d(sV, &tmV, kv_bar, 0, y);
@@ -424,6 +437,7 @@ __global__ void __launch_bounds__((kPersistWarps + 3) * 32, 1) decode_attn_persi
       const int bb = b0 + lane;
       int Lb = bb < p.B ? p.cache_len[bb] : 0;
       Lb = Lb < 0 ? 0 : (Lb > lmax ? lmax : Lb);
+      Lb -= dec_first_slot(Lb, p.window);          // visible cached keys
       const int n = bb < p.B ? (Lb + 1 + kChunk - 1) / kChunk : 0;
       int v = n;
 #pragma unroll
@@ -495,7 +509,14 @@ __global__ void __launch_bounds__((kPersistWarps + 3) * 32, 1) decode_attn_persi
           ok = false;
           break;
         }
-        const int y = static_cast<int>(((long long)p.layer * p.B + b) * p.KV + kvh) * p.S_max + ch * kChunk;
+        int first = 0;                              // first slot inside the window
+        if (p.window > 0) {
+          int Lf = p.cache_len[b];
+          Lf = Lf < 0 ? 0 : (Lf > lmax ? lmax : Lf);
+          first = Lf - lens[b];
+        }
+        const int y = static_cast<int>(((long long)p.layer * p.B + b) * p.KV + kvh) * p.S_max + first +
+                      ch * kChunk;
         mbar_arrive_expect_tx(&full[stage], STAGE);
         tma_load_2d(dsm + stage * STAGE, &tmK, &full[stage], 0, y);
         tma_load_2d(dsm + stage * STAGE + kChunk * 128, &tmV, &full[stage], 0, y);
@@ -826,6 +847,8 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_attn_kernel(const DecAt
   int Lb = p.cache_len[b];
   const int lmax = min(p.S_max, p.max_pos - 1);
   Lb = Lb < 0 ? 0 : (Lb > lmax ? lmax : Lb);
+  const int first = dec_first_slot(Lb, p.window);   // keys below are outside the window
+  Lb -= first;                                      // from here on: visible cached keys
   const int n_keys = Lb + 1;                       // cached keys + the new one
   const int nsplit = (n_keys + kChunk - 1) / kChunk;
   if (split >= nsplit) return;
@@ -860,8 +883,8 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_attn_kernel(const DecAt
   }
 
   const long long row = (long long)b * p.KV + kvh;
-  const bf16 *kc = p.k_cache + row * p.S_max * HD;
-  const bf16 *vc = p.v_cache + row * p.S_max * HD;
+  const bf16 *kc = p.k_cache + (row * p.S_max + first) * HD;
+  const bf16 *vc = p.v_cache + (row * p.S_max + first) * HD;
   const bf16 *kn = p.k_new + row * HD;
   const bf16 *vn = p.v_new + row * HD;
 
@@ -1143,7 +1166,7 @@ cudaError_t run_decode(const DecodeArgs &a, void *ws, int sms, cudaStream_t st, 
     p.M = B; p.N = (H + 2 * KV) * hd; p.K = d;
     p.ssq_in = ssq_a; p.inv_dim = 1.0f / d; p.eps = c.rms_eps; p.ssq_zero = ssq_b;
     p.q = q; p.k_bf = kn; p.v_bf = vn; p.T = 1; p.H = H; p.KV = KV; p.hd = hd;
-    p.rope = a.rope; p.valid_start = nullptr; p.pos_add = a.cache_len; p.pos_limit = min(a.S_max, c.max_pos - 1);
+    p.rope = layer_rotary(&c, l) ? a.rope : nullptr; p.valid_start = nullptr; p.pos_add = a.cache_len; p.pos_limit = min(a.S_max, c.max_pos - 1);
     p.max_pos = c.max_pos; p.status = status; p.pdl = 1;
     DEC_LAUNCH_K(SMOL_K_QKV, dec_gemm(kEpiQkvRope, hd, x, lb + a.off_qkv, p, sms, st));
 
@@ -1158,6 +1181,7 @@ cudaError_t run_decode(const DecodeArgs &a, void *ws, int sms, cudaStream_t st, 
     ap.counters = counters;
     ap.B = B; ap.H = H; ap.KV = KV; ap.S_max = a.S_max; ap.max_pos = c.max_pos;
     ap.max_splits = W.max_splits; ap.scale_log2 = sl2; ap.status = status;
+    ap.window = layer_window(&c, l);
     const int lmax = min(a.S_max, c.max_pos - 1);
     dim3 grid((unsigned)cdiv(lmax + 1, kChunk), (unsigned)KV, (unsigned)B);
     ap.layer = l;

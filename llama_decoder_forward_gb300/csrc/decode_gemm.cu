@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   float c0 = 1.f, s0 = 0.f, c1 = 1.f, s1 = 0.f;
   if constexpr (EPI == kEpiQkvRope) {
     const int row = threadIdx.x >> 2, c = (threadIdx.x & 3) * 2;
-    if (row < p.M && (u >> 2) < p.H + p.KV) {
+    if (p.rope && row < p.M && (u >> 2) < p.H + p.KV) {   // no table: a NoPE block
       int pos = 0;
       if (p.pos_add) {
         const int pa = p.pos_add[row];                  // one token per sequence
@@ -337,7 +337,7 @@ bool skinny_gemm_supported(int epi, const GemmParams &p) {
            p.N % (nt * 8) == 0 && p.ldo % 4 == 0;
   if (epi == kEpiSwiglu) return p.out && p.out_is_f16 && p.N % 128 == 0 && p.ldo % 4 == 0;
   if (epi == kEpiQkvRope)
-    return p.hd == 64 && p.T == 1 && p.q && p.rope && !p.v_t && !p.valid_start &&
+    return p.hd == 64 && p.T == 1 && p.q && !p.v_t && !p.valid_start &&
            p.N == (p.H + 2 * p.KV) * 64;
   return false;
 }

@@ -469,8 +469,10 @@ __device__ __forceinline__ void epi_qkv_rope(const GemmParams &p, EpiCtx &e) {
   pos = pos < 0 ? 0 : (pos >= p.max_pos ? p.max_pos - 1 : pos);
   // entry (j, pos & 63) of the fine part and (j, pos >> 6) of the coarse part
   const int n_coarse = static_cast<int>(cdiv(p.max_pos, 64));
-  const float4 *fine4 = (HD == 64 && e.tab ? e.tab : reinterpret_cast<const float4 *>(p.rope)) + (pos & 63);
-  const float4 *coarse4 = reinterpret_cast<const float4 *>(p.rope) + (HD / 4) * 64 + (pos >> 6);
+  const bool rotary = p.rope != nullptr;          // launch-uniform; false on a NoPE block
+  const float4 *tab = rotary ? reinterpret_cast<const float4 *>(p.rope) : nullptr;
+  const float4 *fine4 = rotary ? (HD == 64 && e.tab ? e.tab : tab) + (pos & 63) : nullptr;
+  const float4 *coarse4 = rotary ? tab + (HD / 4) * 64 + (pos >> 6) : nullptr;
   // element offsets of (b, head 0, t, 0) in [B, H, T, hd] and [B, KV, T, hd]
   const long long q_row = ((long long)b * p.H * p.T + t) * HD;
   const long long kv_row = ((long long)b * p.KV * p.T + t) * HD;
@@ -500,19 +502,27 @@ __device__ __forceinline__ void epi_qkv_rope(const GemmParams &p, EpiCtx &e) {
       tmem_ld32(tcol + i0, x1);
       tmem_ld32(tcol + HD / 2 + i0, x2);
       tmem_ld_wait();
+      if (rotary) {
 #pragma unroll
-      for (int k = 0; k < 32; k += 2) {
-        const int jj = (i0 + k) >> 1;             // pairs i0+k and i0+k+1
-        const float4 f = fine4[jj * 64];          // (cos, sin) of b*f
-        const float4 g = coarse4[jj * n_coarse];  // (cos, sin) of 64*a*f
-        const float c0 = g.x * f.x - g.y * f.y, s0 = g.y * f.x + g.x * f.y;
-        const float c1 = g.z * f.z - g.w * f.w, s1 = g.w * f.z + g.z * f.w;
-        const float a0 = __uint_as_float(x1[k]) * rs, b0 = __uint_as_float(x2[k]) * rs;
-        const float a1 = __uint_as_float(x1[k + 1]) * rs, b1 = __uint_as_float(x2[k + 1]) * rs;
-        y1[k] = a0 * c0 - b0 * s0;
-        y2[k] = a0 * s0 + b0 * c0;
-        y1[k + 1] = a1 * c1 - b1 * s1;
-        y2[k + 1] = a1 * s1 + b1 * c1;
+        for (int k = 0; k < 32; k += 2) {
+          const int jj = (i0 + k) >> 1;           // pairs i0+k and i0+k+1
+          const float4 f = fine4[jj * 64];        // (cos, sin) of b*f
+          const float4 g = coarse4[jj * n_coarse];  // (cos, sin) of 64*a*f
+          const float c0 = g.x * f.x - g.y * f.y, s0 = g.y * f.x + g.x * f.y;
+          const float c1 = g.z * f.z - g.w * f.w, s1 = g.w * f.z + g.z * f.w;
+          const float a0 = __uint_as_float(x1[k]) * rs, b0 = __uint_as_float(x2[k]) * rs;
+          const float a1 = __uint_as_float(x1[k + 1]) * rs, b1 = __uint_as_float(x2[k + 1]) * rs;
+          y1[k] = a0 * c0 - b0 * s0;
+          y2[k] = a0 * s0 + b0 * c0;
+          y1[k + 1] = a1 * c1 - b1 * s1;
+          y2[k + 1] = a1 * s1 + b1 * c1;
+        }
+      } else {                                    // a NoPE block: the scaled projections
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          y1[k] = __uint_as_float(x1[k]) * rs;
+          y2[k] = __uint_as_float(x2[k]) * rs;
+        }
       }
       seg1 = i0;
       seg2 = HD / 2 + i0;
@@ -832,10 +842,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     e.tab = nullptr;
     if constexpr (EPI == kEpiQkvRope && HD == 64) {
       // the table is an input of the step; every epilogue warp takes a share
-      const float4 *src = reinterpret_cast<const float4 *>(p.rope);
-      for (int i = static_cast<int>(threadIdx.x) - 64; i < 16 * 64; i += kEpiWarps * 32) sTab[i] = src[i];
-      asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");   // the epilogue warps only
-      e.tab = sTab;
+      // (no table on a NoPE block)
+      if (p.rope) {
+        const float4 *src = reinterpret_cast<const float4 *>(p.rope);
+        for (int i = static_cast<int>(threadIdx.x) - 64; i < 16 * 64; i += kEpiWarps * 32) sTab[i] = src[i];
+        asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");   // the epilogue warps only
+        e.tab = sTab;
+      }
     }
     const bool resid_tma = EPI == kEpiResidual && (p.epi_tma & kTmaResid);
     uint32_t acc = 0, acc_phase = 0;

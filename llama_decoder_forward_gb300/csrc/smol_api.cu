@@ -91,6 +91,10 @@ int check_cfg(const smol_config *c) {
   if (c->n_heads % c->n_kv_heads) return SMOL_ERR_UNSUPPORTED_SHAPE;
   if (c->n_heads / c->n_kv_heads > 8) return SMOL_ERR_UNSUPPORTED_SHAPE;
   if (c->hidden % 64 || c->intermediate % 64 || c->vocab % 64) return SMOL_ERR_UNSUPPORTED_SHAPE;
+  for (int l = 0; l < c->n_layers; ++l) {
+    if (c->no_rope_layers && c->no_rope_layers[l] != 0 && c->no_rope_layers[l] != 1) return SMOL_ERR_INVALID_ARG;
+    if (c->sliding_window && c->sliding_window[l] < 0) return SMOL_ERR_INVALID_ARG;
+  }
   return SMOL_OK;
 }
 
@@ -194,7 +198,10 @@ int run_block(const smol_config *c, const void *packed, int layer, const BlockIO
     p.v = v;
   }
   p.T = T; p.H = H; p.KV = KV; p.hd = hd;
-  p.rope = reinterpret_cast<const float2 *>(static_cast<const uint8_t *>(packed) + PL.rope_off);
+  // a NoPE block passes no table: the epilogue then leaves q and k unrotated
+  p.rope = layer_rotary(c, layer)
+               ? reinterpret_cast<const float2 *>(static_cast<const uint8_t *>(packed) + PL.rope_off)
+               : nullptr;
   p.valid_start = valid_start; p.max_pos = c->max_pos; p.status = status;
   // every kernel of the block is a programmatic dependent of the one before
   // (each waits for it with griddepcontrol.wait before touching its data)
@@ -206,6 +213,7 @@ int run_block(const smol_config *c, const void *packed, int layer, const BlockIO
   ap.q = q; ap.k = k; ap.v = v; ap.o = o; ap.valid_start = valid_start;
   ap.B = B; ap.T = T; ap.H = H; ap.KV = KV; ap.hd = hd;
   ap.scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
+  ap.window = layer_window(c, layer);
   ap.status = status;
   ap.pdl = 1;
   if (tc_attn) {

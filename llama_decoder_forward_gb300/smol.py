@@ -31,9 +31,12 @@ ACT_BF16, ACT_F32 = 0, 1
 
 
 class Config(ctypes.Structure):
+    # no_rope_layers / sliding_window: host int32 arrays of n_layers entries or
+    # NULL (assigning a ctypes array to the field keeps it alive with the struct)
     _fields_ = [("hidden", c_int), ("n_heads", c_int), ("n_kv_heads", c_int), ("head_dim", c_int),
                 ("intermediate", c_int), ("n_layers", c_int), ("vocab", c_int), ("max_pos", c_int),
-                ("rms_eps", c_float), ("rope_theta", c_float)]
+                ("rms_eps", c_float), ("rope_theta", c_float),
+                ("no_rope_layers", POINTER(ctypes.c_int32)), ("sliding_window", POINTER(ctypes.c_int32))]
 
 
 class BlockWeights(ctypes.Structure):
@@ -96,16 +99,35 @@ def _check(code: int, where: str) -> None:
         raise SmolError(code, where)
 
 
+def _i32_array(vals, n_layers: int, name: str):
+    if vals is None:
+        return None
+    vals = [int(v) for v in vals]
+    if len(vals) != n_layers:
+        raise ValueError(f"{name} needs one entry per layer ({n_layers}), got {len(vals)}")
+    return (ctypes.c_int32 * n_layers)(*vals)
+
+
 def make_config(hidden, n_heads, n_kv_heads, head_dim, intermediate, n_layers, vocab, max_pos,
-                rms_eps, rope_theta) -> Config:
-    return Config(hidden, n_heads, n_kv_heads, head_dim, intermediate, n_layers, vocab, max_pos,
-                  rms_eps, rope_theta)
+                rms_eps, rope_theta, no_rope_layers=None, sliding_window=None) -> Config:
+    """no_rope_layers: per layer 1 = RoPE, 0 = NoPE block (None: RoPE everywhere);
+    sliding_window: per layer 0 = full causal, w > 0 = window of w keys (None: none)."""
+    cfg = Config(hidden, n_heads, n_kv_heads, head_dim, intermediate, n_layers, vocab, max_pos,
+                 rms_eps, rope_theta)
+    nr = _i32_array(no_rope_layers, n_layers, "no_rope_layers")
+    sw = _i32_array(sliding_window, n_layers, "sliding_window")
+    if nr is not None:
+        cfg.no_rope_layers = nr
+    if sw is not None:
+        cfg.sliding_window = sw
+    return cfg
 
 
 def config_of(wl) -> Config:
     """Config from a synth.Workload (same field names)."""
     return make_config(wl.hidden, wl.n_heads, wl.n_kv_heads, wl.head_dim, wl.intermediate,
-                       wl.n_layers, wl.vocab, wl.max_pos, wl.rms_eps, wl.rope_theta)
+                       wl.n_layers, wl.vocab, wl.max_pos, wl.rms_eps, wl.rope_theta,
+                       getattr(wl, "no_rope_layers", None), getattr(wl, "sliding_window", None))
 
 
 def _p(t: Optional[torch.Tensor]):

@@ -44,6 +44,8 @@ class Workload:
     w_std: float
     len_range: Optional[Tuple[int, int]] = None   # inclusive; left-pad lengths or cache lengths
     s_max: int = 0                 # decode cache slots per (layer, seq, kv head)
+    no_rope_layers: Optional[Tuple[int, ...]] = None   # per layer: 1 RoPE, 0 NoPE (SmolLM3)
+    sliding_window: Optional[Tuple[int, ...]] = None   # per layer: 0 full causal, w > 0 window
 
     def scaled(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)

@@ -22,7 +22,8 @@ def oracle_config(wl: synth.Workload, n_layers=None) -> O.Config:
     return O.Config(hidden=wl.hidden, n_heads=wl.n_heads, n_kv_heads=wl.n_kv_heads,
                     head_dim=wl.head_dim, intermediate=wl.intermediate,
                     n_layers=n_layers if n_layers is not None else wl.n_layers,
-                    vocab=wl.vocab, max_pos=wl.max_pos, rms_eps=wl.rms_eps, rope_theta=wl.rope_theta)
+                    vocab=wl.vocab, max_pos=wl.max_pos, rms_eps=wl.rms_eps, rope_theta=wl.rope_theta,
+                    no_rope_layers=wl.no_rope_layers, sliding_window=wl.sliding_window)
 
 
 def np32(t: torch.Tensor) -> np.ndarray:

@@ -80,6 +80,23 @@ def test_config_validation(smol, kw, code):
         assert rc == code
 
 
+def test_per_block_variant_arrays(smol):
+    # SmolLM3 NoPE flags must be 0 or 1 and windows non-negative; the arrays
+    # have one entry per layer (the binding checks the length)
+    n = 30
+    ok = _cfg(smol, no_rope_layers=[1, 1, 1, 0] * 7 + [1, 1], sliding_window=[0, 128] * 15)
+    assert smol.packed_bytes(ok, n, True) == smol.packed_bytes(_cfg(smol), n, True)
+    assert smol.workspace_bytes(ok, smol.OP_DECODE, 64, 1) == smol.workspace_bytes(_cfg(smol), smol.OP_DECODE, 64, 1)
+    assert smol.packed_bytes(_cfg(smol, no_rope_layers=[1] * 29 + [2]), n, True) == 0
+    assert smol.packed_bytes(_cfg(smol, sliding_window=[0] * 29 + [-1]), n, True) == 0
+    with pytest.raises(ValueError):
+        _cfg(smol, sliding_window=[0] * 29)
+    f = ctypes.c_void_p(0x10000)
+    bad = _cfg(smol, sliding_window=[-5] + [0] * 29)
+    assert smol.raw.smol_block_forward(ctypes.byref(bad), f, 0, f, f, 0, 1, 8, None, None, None, f,
+                                       1 << 40, None) == -1
+
+
 def test_argument_errors_return_before_any_launch(smol):
     cfg = _cfg(smol)
     f = ctypes.c_void_p(0x10000)

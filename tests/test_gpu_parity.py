@@ -22,10 +22,11 @@ def S():
     return smol
 
 
-def run_block_case(S, wl, seed=0, check_kv=True, act=torch.float32, x_scale=1.0):
-    """One block through the C ABI vs the oracle.  act is the residual-stream
-    type of x/out (fp32: the stated bar; bf16: the bar plus the output's own
-    rounding).  k/v are bf16 cache entries, checked like bf16 outputs."""
+def run_block_case(S, wl, seed=0, check_kv=True, act=torch.float32, x_scale=1.0, layer=0):
+    """Block `layer` of the workload through the C ABI vs the oracle.  act is
+    the residual-stream type of x/out (fp32: the stated bar; bf16: the bar plus
+    the output's own rounding).  k/v are bf16 cache entries, checked like bf16
+    outputs."""
     inp = synth.generate(wl, seed=seed)
     if x_scale != 1.0:
         inp.x = (inp.x.float() * x_scale).to(torch.bfloat16)
@@ -37,12 +38,13 @@ def run_block_case(S, wl, seed=0, check_kv=True, act=torch.float32, x_scale=1.0)
     out = torch.empty_like(x)
     k_out = torch.empty(wl.B, wl.n_kv_heads, wl.T, wl.head_dim, dtype=torch.bfloat16, device="cuda")
     v_out = torch.empty_like(k_out)
-    S.block_forward(cfg, packed, 0, x, out, ws, valid_start=dev.valid_start, k_out=k_out, v_out=v_out)
+    S.block_forward(cfg, packed, layer, x, out, ws, valid_start=dev.valid_start, k_out=k_out, v_out=v_out)
     assert S.workspace_status(ws) == S.OK
     torch.cuda.synchronize()
     taps = {}
     vs = None if inp.valid_start is None else inp.valid_start.numpy()
-    ref = O.block_forward(oracle_config(wl, 1), oracle_layers(inp, 1)[0], np32(inp.x), vs, taps=taps)
+    ref = O.block_forward(oracle_config(wl), oracle_layers(inp)[layer], np32(inp.x), vs, taps=taps,
+                          layer=layer)
     got = out.float().cpu().numpy()
     assert np.all(np.isfinite(got))
     rows = np.ones((wl.B, wl.T), dtype=bool)
@@ -215,3 +217,63 @@ def test_decode_empty_caches(S):
     # no cached keys: attention over the new token alone
     wl = W["smollm2_decode_b64_cache4096"].scaled(n_layers=2, s_max=64, vocab=512)
     run_decode_case(S, wl, [0, 0, 1], seed=9)
+
+
+# ---------------------------------------------------------------- SmolLM3 per-block variants
+# NoPE blocks and sliding windows ("SmolLM3" page: "Every fourth block has no
+# rotary", "A sliding window the 3B checkpoints leave off")
+
+@pytest.mark.parametrize("rope,window", [(0, 0), (1, 100), (0, 128), (1, 1), (1, 257), (0, 385)])
+def test_block_nope_window_tc_attention(S, rope, window):
+    # head dim 64, groups of 3: the tcgen05 attention; windows below, at and
+    # across the 128-key tiles, and one as long as the sequence
+    wl = W["smollm2_block_b1_t128"].scaled(B=2, T=385, n_layers=2, no_rope_layers=(1, rope),
+                                           sliding_window=(0, window))
+    run_block_case(S, wl, seed=40 + window, layer=1)
+
+
+def test_block_window_left_padded(S):
+    wl = W["slm125m_block_leftpad_b16_t1024"].scaled(B=4, T=300, len_range=(1, 300), n_layers=1,
+                                                     sliding_window=(70,))
+    run_block_case(S, wl, seed=41, act=torch.bfloat16)
+
+
+def test_block_smollm3_nope_window_head_dim_128(S):
+    # head dim 128: the mma.sync flash attention
+    wl = W["smollm3_4blocks_b4_t4096"].scaled(B=2, T=150, n_layers=2, no_rope_layers=(1, 0),
+                                              sliding_window=(0, 37))
+    run_block_case(S, wl, seed=42, layer=1)
+
+
+def test_model_nope_and_window_layers(S):
+    # the two-block layout of the SmolLM3 page's small checkpoint: block 1 is a
+    # NoPE block with a window
+    wl = W["smollm2_model_b8_t2048"].scaled(B=2, T=200, n_layers=2, vocab=1024,
+                                            no_rope_layers=(1, 0), sliding_window=(0, 128))
+    run_model_case(S, wl, seed=43)
+
+
+def test_decode_nope_and_window_layers(S):
+    # persistent decode attention: lengths below, at and above the windows, and
+    # windows that start inside a 256-key chunk
+    wl = W["smollm2_decode_b64_cache4096"].scaled(n_layers=3, s_max=700, vocab=512,
+                                                  no_rope_layers=(1, 0, 1),
+                                                  sliding_window=(0, 128, 300))
+    run_decode_case(S, wl, [0, 1, 127, 128, 129, 299, 300, 301, 700, 555], seed=44)
+
+
+def test_decode_window_head_dim_128(S):
+    wl = W["smollm2_decode_b64_cache4096"].scaled(
+        hidden=2048, n_heads=16, n_kv_heads=4, head_dim=128, intermediate=11008, n_layers=2,
+        vocab=512, s_max=300, rms_eps=1e-6, rope_theta=1e6, w_std=0.02,
+        no_rope_layers=(0, 1), sliding_window=(128, 0))
+    run_decode_case(S, wl, [0, 129, 300, 64], seed=45)
+
+
+def test_decode_batch_beyond_persistent_limit(S):
+    # more than 2048 sequences: the per-chunk tensor-core decode attention
+    # (one CTA per (chunk, kv head, sequence)), with and without a window
+    wl = W["smollm2_decode_b64_cache4096"].scaled(n_layers=2, s_max=96, vocab=512,
+                                                  sliding_window=(0, 60))
+    lengths = [int(v) for v in np.random.default_rng(46).integers(0, 97, size=2100)]
+    run_decode_case(S, wl, lengths, seed=46)
