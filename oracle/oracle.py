@@ -45,6 +45,12 @@ design notes):
     t - w < j <= t, on top of the causal and padding masks; 0 = no window.
     In decode the new token at position L sees cached slots j >= L - w + 1
     plus itself.
+  * Next-token choice ([M1] section 7 generate; [M4] generate): greedy is the
+    first index of the row maximum; the multinomial draw is the inverse CDF
+    in vocabulary order of a uniform number u in [0, 1) that the caller
+    passes in (the pages call torch.multinomial, whose internal method they
+    do not give); the top-p sort puts equal logits in ascending index order
+    (the pages' torch.sort leaves their order open).
   * Decode: the cache holds post-RoPE keys (stored "after RoPE, before GQA
     expansion" in [M1] section 4); only the new token's q and k are rotated,
     at position cache_len[b]; with a single new token no causal mask applies
@@ -360,3 +366,58 @@ def decode_step(cfg: Config, layers: List[BlockWeights], embed, final_norm, ids,
         m = rms_norm(x, w.mlp_norm, cfg.rms_eps)
         x = x + linear(silu(linear(m, w.wgate)) * linear(m, w.wup), w.wdown)
     return lm_head(cfg, x, final_norm, embed), k_new, v_new
+
+
+def _softmax_1d(z) -> np.ndarray:
+    """softmax over a 1-D array in which -inf entries get probability 0."""
+    z = _f64(z)
+    m = np.max(z)
+    e = np.exp(z - m)
+    return e / np.sum(e)
+
+
+def sample_next(logits, temperature: float = 1.0, top_k: Optional[int] = None,
+                top_p: Optional[float] = None, u=None, do_sample: bool = True) -> np.ndarray:
+    """Next token of each row of logits [B, V], as the pages' ``generate`` picks it.
+
+    [M1] section 7 generate and [M4] generate, step by step:
+      1. greedy when do_sample is false or temperature is 0 (here: <= 0):
+         argmax of the row, the first index among equal maxima;
+      2. z = logits / temperature;
+      3. top_k > 0: entries with z below the k-th largest z (k clipped to V)
+         are set to -inf, so values equal to the k-th stay;
+      4. top_p < 1: sort z descending (equal values by ascending index), take
+         the cumulative softmax probabilities, remove sorted positions whose
+         cumulative probability exceeds top_p after shifting that flag one
+         place right (the first position is never removed);
+      5. probs = softmax(z); the token is the first index i with
+         sum_{j <= i} probs[j] > u[b] (inverse CDF in vocabulary order).
+    Returns int64 [B].
+    """
+    logits = _f64(logits)
+    B, V = logits.shape
+    out = np.zeros(B, dtype=np.int64)
+    for b in range(B):
+        row = logits[b]
+        if not do_sample or temperature <= 0:
+            out[b] = int(np.argmax(row))
+            continue
+        z = row / F64(temperature)
+        if top_k is not None and top_k > 0:
+            k = min(int(top_k), V)
+            kth = np.sort(z)[::-1][k - 1]
+            z = np.where(z < kth, -np.inf, z)
+        if top_p is not None and top_p < 1.0:
+            order = np.argsort(-z, kind="stable")
+            cum = np.cumsum(_softmax_1d(z[order]))
+            remove = cum > top_p
+            remove[1:] = remove[:-1].copy()
+            remove[0] = False
+            z = z.copy()
+            z[order[remove]] = -np.inf
+        probs = _softmax_1d(z)
+        cdf = np.cumsum(probs)
+        i = int(np.searchsorted(cdf, F64(u[b]), side="right"))
+        last = int(np.nonzero(probs > 0)[0][-1])
+        out[b] = min(i, last)                  # u within rounding of 1: the last token
+    return out

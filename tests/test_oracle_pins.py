@@ -536,3 +536,86 @@ def test_decode_with_nope_and_windows_matches_last_row_of_prefill():
         k, v = _prefill_cache(cfg, layers, embed, seqs[b][None])
         np.testing.assert_allclose(k_new[:, b], k[:, 0, :, L], rtol=1e-11, atol=1e-12)
         np.testing.assert_allclose(v_new[:, b], v[:, 0, :, L], rtol=1e-11, atol=1e-12)
+
+
+# ---------------------------------------------------------------- next-token choice
+# ("model.py" (SmolLM2-135M) section 7 generate; the abi96062 model.py generate)
+
+def _sm(vals):
+    e = [math.exp(v) for v in vals]
+    return [x / sum(e) for x in e]
+
+
+def test_sample_greedy_first_maximum():
+    row = np.array([[1.0, 5.0, 5.0, 2.0]])
+    for kw in (dict(do_sample=False), dict(temperature=0.0)):
+        assert O.sample_next(row, u=[0.99], **kw)[0] == 1
+
+
+def test_sample_top_p_hand_example():
+    # softmax([3,2,1,0]) = (0.6439, 0.2369, 0.0871, 0.0321): top_p 0.7 keeps
+    # tokens 0 and 1 (the token that crosses 0.7 stays), top_p 0.5 token 0 only
+    row = np.array([[3.0, 2.0, 1.0, 0.0]])
+    p = _sm([3.0, 2.0, 1.0, 0.0])
+    assert p[0] <= 0.7 < p[0] + p[1]
+    p0 = math.exp(3.0) / (math.exp(3.0) + math.exp(2.0))        # renormalised over {0, 1}
+    assert O.sample_next(row, top_p=0.7, u=[p0 - 1e-9])[0] == 0
+    assert O.sample_next(row, top_p=0.7, u=[p0 + 1e-9])[0] == 1
+    assert O.sample_next(row, top_p=0.7, u=[0.999999])[0] == 1
+    for u in (0.0, 0.5, 0.999999):
+        assert O.sample_next(row, top_p=0.5, u=[u])[0] == 0
+
+
+def test_sample_top_p_applies_after_top_k():
+    # top_k 2 first: softmax over {3, 2} gives token 0 probability 0.7311 > 0.7,
+    # so top_p 0.7 then keeps token 0 alone; without top_k it keeps 0 and 1
+    row = np.array([[3.0, 2.0, 1.0, 0.0]])
+    assert O.sample_next(row, top_k=2, top_p=0.7, u=[0.9])[0] == 0
+    assert O.sample_next(row, top_p=0.7, u=[0.9])[0] == 1
+
+
+def test_sample_top_k_keeps_ties_with_the_kth():
+    row = np.array([[4.0, 4.0, 4.0, 1.0]])
+    # three equal survivors, probability 1/3 each; token 3 is never drawn
+    assert [O.sample_next(row, top_k=2, u=[u])[0] for u in (0.1, 0.5, 0.9, 0.9999)] == [0, 1, 2, 2]
+    # top_k 1 keeps the maximum (and values equal to it)
+    rng = np.random.default_rng(30)
+    rows = rng.normal(0, 2, (20, 50))
+    us = rng.random(20)
+    np.testing.assert_array_equal(O.sample_next(rows, top_k=1, u=us), np.argmax(rows, axis=1))
+
+
+def test_sample_top_p_ties_in_index_order():
+    row = np.array([[2.0, 2.0, 2.0, 2.0]])
+    # cumulative 0.25, 0.5, ...: top_p 0.3 keeps the first two sorted, i.e. indices 0 and 1
+    assert O.sample_next(row, top_p=0.3, u=[0.6])[0] == 1
+    assert O.sample_next(row, top_p=0.3, u=[0.4])[0] == 0
+    # a tiny top_p keeps only the first sorted entry: the lowest index of the maximum
+    row2 = np.array([[1.0, 5.0, 5.0, 2.0]])
+    assert O.sample_next(row2, top_p=1e-9, u=[0.99])[0] == 1
+
+
+def test_sample_inverse_cdf_frequencies_match_softmax():
+    # u on a uniform grid of N points: token i is drawn for the points in
+    # [cdf_{i-1}, cdf_i), so its count is N * softmax_i to within one point
+    rng = np.random.default_rng(31)
+    vals = rng.normal(0, 1.5, 6)
+    temp = 0.8
+    N = 20000
+    us = (np.arange(N) + 0.5) / N
+    toks = O.sample_next(np.repeat(vals[None], N, axis=0), temperature=temp, u=us)
+    counts = np.bincount(toks, minlength=6)
+    expect = np.array(_sm(list(vals / temp))) * N
+    assert np.all(np.abs(counts - expect) <= 1.0 + 1e-9)
+    # and the draw is monotone in u (vocabulary order)
+    assert np.all(np.diff(toks) >= 0)
+
+
+def test_sample_temperature_is_a_logit_scale():
+    # dividing by 0.5 is multiplying by 2 exactly: the same draws as logits * 2 at temperature 1
+    rng = np.random.default_rng(32)
+    rows = rng.normal(0, 1, (30, 40))
+    us = rng.random(30)
+    for kw in (dict(), dict(top_k=7), dict(top_p=0.8), dict(top_k=9, top_p=0.6)):
+        np.testing.assert_array_equal(O.sample_next(rows, temperature=0.5, u=us, **kw),
+                                      O.sample_next(rows * 2.0, temperature=1.0, u=us, **kw))
