@@ -130,11 +130,18 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(rows)}
 
 
+# Translation units that hold none of the kernels whose DRAM traffic is recorded
+# (the next-token choice kernel): they cannot change what those kernels do.
+DIGEST_EXCLUDE = ("sample.cu",)
+
+
 def src_digest():
     """Digest of the kernel sources with // comments and blank lines removed (an
     edit of a comment does not change what the captured kernels execute)."""
     h = hashlib.sha256()
     for p in sorted(glob.glob(os.path.join(ROOT, "llama_decoder_forward_gb300", "csrc", "*"))):
+        if os.path.basename(p) in DIGEST_EXCLUDE:
+            continue
         with open(p, encoding="utf-8") as f:
             lines = [re.sub(r"//.*$", "", ln).rstrip() for ln in f.read().splitlines()]
         code = "\n".join(ln for ln in lines if ln)
@@ -411,6 +418,19 @@ def run_decode(S, args, rank, world, peaks, peaks_src):
     step_bytes, attn_bytes = decode_bytes(wl, lengths)
     hbm = peaks["hbm_gbs"]
     ach = attn_bytes / (att_ms / 1e3) / 1e9 if att_ms else None
+    # next-token choice on the step's logits (not part of the step timed above)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(200 + rank)
+    uniform = torch.rand(B, generator=gen, device="cuda")
+    next_ids = torch.empty(B, dtype=torch.int32, device="cuda")
+    smp_kw = dict(temperature=0.8, top_k=50, top_p=0.9)
+
+    def choose():
+        S.sample(logits, next_ids, uniform, **smp_kw)
+
+    for _ in range(3):
+        choose()
+    smp_ms = max_over_ranks(time_steps(choose, args.steps, world), world)
     return {
         "workload": f"{wl.name}: SmolLM2-135M decode step, {L} blocks, batch {B}, cache lengths uniform "
                     f"in [{wl.len_range[0]}, {wl.len_range[1]}], cache [{L},{B},{KV},{wl.s_max},{hd}] bf16",
@@ -427,6 +447,9 @@ def run_decode(S, args, rank, world, peaks, peaks_src):
                      "mean_launch_ms": round(att_ms, 5) if att_ms else None, "launches_timed": att_n,
                      "peak_source": f"{peaks_src} copy bandwidth"},
         "kernel_ms_per_step": {k: round(v, 4) for k, v in sorted(tot.items(), key=lambda kv: -kv[1])},
+        "next_token_choice": {"ms_per_call": round(smp_ms, 4), "rows": B, "vocab": wl.vocab,
+                              "config": "temperature 0.8, top_k 50, top_p 0.9, uniform from the caller",
+                              "launches": 1, "logits_bytes": B * wl.vocab * 2},
     }
 
 

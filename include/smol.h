@@ -230,6 +230,29 @@ int smol_decode_step_noalloc(const smol_config *cfg, const void *packed, const i
                              const void *v_cache, int S_max, void *k_new, void *v_new,
                              void *logits, void *stream);
 
+/* ---------------------------------------------------------------------------
+ * smol_sample: the next token of each row of logits, chosen the way the pages'
+ * generate loop chooses it ([M1] section 7 generate; [M4] generate).
+ *   Greedy when do_sample == 0 or temperature <= 0: the first index of the row
+ *   maximum.  Otherwise, with z = logits / temperature:
+ *     top_k > 0   tokens whose z is below the k-th largest z are removed
+ *                 (values equal to the k-th stay; top_k >= V removes nothing);
+ *     top_p < 1   in descending z order (equal values by ascending index), the
+ *                 tokens after the first one at which the cumulative softmax
+ *                 probability of the top-k survivors exceeds top_p are removed;
+ *     the draw    the first index i, in vocabulary order, at which the
+ *                 cumulative probability of the survivors exceeds uniform[b]
+ *                 (the inverse CDF; the pages call a multinomial sampler).
+ *   logits      device bf16 [B, ld], rows of V finite values (ld >= V elements).
+ *   uniform     device fp32 [B], each in [0, 1): the caller's random numbers
+ *               (unused, may be NULL, when greedy).
+ *   next        device int32 [B] output.
+ * One kernel launch on `stream`, no workspace.  SMOL_ERR_INVALID_ARG for a NULL
+ * pointer, B < 1, V < 1, ld < V, or a NaN temperature/top_p.
+ * ------------------------------------------------------------------------- */
+int smol_sample(const void *logits, int B, int V, long long ld, float temperature, int top_k,
+                float top_p, int do_sample, const float *uniform, int32_t *next, void *stream);
+
 /* Reads (synchronising `stream`) and clears the workspace status word written
  * by kernels whose bounded waits gave up.  Returns SMOL_OK, SMOL_ERR_TIMEOUT
  * or SMOL_ERR_CUDA.  Not meant for the hot path. */
@@ -253,7 +276,8 @@ enum {
   SMOL_K_HEAD = 7,       /* final RMSNorm + tied lm_head GEMM             */
   SMOL_K_DEC_ATTN = 8,   /* decode attention over the KV cache            */
   SMOL_K_OTHER = 9,      /* packing and bookkeeping kernels               */
-  SMOL_K_COUNT = 10
+  SMOL_K_SAMPLE = 10,    /* next-token choice (smol_sample)               */
+  SMOL_K_COUNT = 11
 };
 /* From now on (this host thread), every launch whose kind bit is set in
  * `kind_mask` is bracketed by CUDA events on its stream, up to `capacity`

@@ -144,6 +144,11 @@ cudaError_t launch_flash_attention(const AttnParams &p, cudaStream_t stream);
 bool attention_tc_supported(int hd, int H, int KV);
 cudaError_t launch_attention_tc(const AttnParams &p, cudaStream_t stream);
 
+// ------------------------------------------------------------------ next-token choice
+// One CTA per row of bf16 logits [B][ld]; see sample.cu.
+cudaError_t launch_sample(const void *logits, long long ld, int B, int V, float temperature, int top_k,
+                          float top_p, int do_sample, const float *uniform, int *next, cudaStream_t st);
+
 // ------------------------------------------------------------------ small kernels
 cudaError_t launch_embed_rows(const int *ids, const bf16 *embed, int vocab, int d, long long rows,
                               f16 *x16, float *x_f32, float *ssq, cudaStream_t stream);

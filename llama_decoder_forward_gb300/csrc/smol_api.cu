@@ -456,6 +456,24 @@ SMOL_API int smol_decode_step(const smol_config *cfg, const void *packed, const 
   return SMOL_OK;
 }
 
+SMOL_API int smol_sample(const void *logits, int B, int V, long long ld, float temperature, int top_k,
+                         float top_p, int do_sample, const float *uniform, int32_t *next, void *stream) {
+  g_launches = 0;
+  const bool greedy = !do_sample || !(temperature > 0.f);
+  if (!logits || !next || (!greedy && !uniform)) return SMOL_ERR_INVALID_ARG;
+  if (B < 1 || V < 1 || ld < V || temperature != temperature || top_p != top_p) return SMOL_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(logits) & 1u) || (reinterpret_cast<uintptr_t>(next) & 3u) ||
+      (reinterpret_cast<uintptr_t>(uniform) & 3u))
+    return SMOL_ERR_MISALIGNED;
+  int sms = 0;
+  int rc = device_sms(&sms);
+  if (rc != SMOL_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  LAUNCH_K(SMOL_K_SAMPLE, st, launch_sample(logits, ld, B, V, temperature, top_k, top_p, do_sample, uniform,
+                                            reinterpret_cast<int *>(next), st));
+  return SMOL_OK;
+}
+
 SMOL_API int smol_workspace_status(void *ws, void *stream) {
   if (!ws) return SMOL_ERR_INVALID_ARG;
   int h = 0;

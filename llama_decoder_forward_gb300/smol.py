@@ -64,14 +64,18 @@ _SIGS = {
     "smol_status_string": (ctypes.c_char_p, [c_int]),
     "smol_decode_step_noalloc": (c_int, [_CFG, c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p,
                                          c_int, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "smol_sample": (c_int, [c_void_p, c_int, c_int, ctypes.c_longlong, c_float, c_int, c_float, c_int,
+                            c_void_p, c_void_p, c_void_p]),
     "smol_profile_begin": (c_int, [ctypes.c_uint, c_int]),
     "smol_profile_end": (c_int, [POINTER(c_int), POINTER(c_float), c_int]),
 }
 
 # kernel kinds of smol_profile_begin (SMOL_K_*)
 KERNEL_KINDS = ("embed", "rowstats", "qkv_gemm_rope", "flash_attention", "o_gemm_residual",
-                "gateup_gemm_swiglu", "down_gemm_residual", "lm_head_gemm", "decode_attention", "other")
-K_EMBED, K_ROWSTATS, K_QKV, K_ATTN, K_OPROJ, K_GATEUP, K_DOWN, K_HEAD, K_DEC_ATTN, K_OTHER = range(10)
+                "gateup_gemm_swiglu", "down_gemm_residual", "lm_head_gemm", "decode_attention", "other",
+                "sample")
+(K_EMBED, K_ROWSTATS, K_QKV, K_ATTN, K_OPROJ, K_GATEUP, K_DOWN, K_HEAD, K_DEC_ATTN, K_OTHER,
+ K_SAMPLE) = range(11)
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
     _fn.restype = _res
@@ -239,6 +243,22 @@ def decode_step_noalloc(cfg: Config, packed: torch.Tensor, ids: torch.Tensor, ca
     _check(_lib.smol_decode_step_noalloc(ctypes.byref(cfg), _p(packed), _p(ids), _p(cache_len), B,
                                          _p(k_cache), _p(v_cache), S_max, _p(k_new), _p(v_new),
                                          _p(logits), _stream(stream)), "smol_decode_step_noalloc")
+
+
+def sample(logits: torch.Tensor, next_ids: torch.Tensor, uniform: Optional[torch.Tensor] = None,
+           temperature: float = 1.0, top_k: int = 0, top_p: float = 1.0, do_sample: bool = True,
+           stream=None) -> None:
+    """Next token of each row of logits [B, V] (bf16, rows may be strided) into
+    next_ids [B] (int32); uniform [B] fp32 in [0, 1) unless greedy."""
+    if logits.dim() != 2 or logits.dtype != torch.bfloat16 or not logits.is_cuda or logits.stride(1) != 1:
+        raise ValueError("logits must be a CUDA bf16 [B, V] tensor with unit column stride")
+    B, V = logits.shape
+    _dev(next_ids, torch.int32, "next_ids")
+    if uniform is not None:
+        _dev(uniform, torch.float32, "uniform")
+    _check(_lib.smol_sample(_p(logits), B, V, logits.stride(0), float(temperature), int(top_k),
+                            float(top_p), int(bool(do_sample)), _p(uniform), _p(next_ids),
+                            _stream(stream)), "smol_sample")
 
 
 def workspace_status(ws: torch.Tensor, stream=None) -> int:

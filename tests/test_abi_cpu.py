@@ -97,6 +97,23 @@ def test_per_block_variant_arrays(smol):
                                        1 << 40, None) == -1
 
 
+def test_sample_argument_errors(smol):
+    f = ctypes.c_void_p(0x10000)
+    smp = smol.raw.smol_sample
+    nan = float("nan")
+    assert smp(None, 4, 100, 100, 1.0, 0, 1.0, 1, f, f, None) == -1          # logits
+    assert smp(f, 4, 100, 100, 1.0, 0, 1.0, 1, None, f, None) == -1          # uniform when sampling
+    assert smp(f, 4, 100, 100, 1.0, 0, 1.0, 1, f, None, None) == -1          # next
+    assert smp(f, 0, 100, 100, 1.0, 0, 1.0, 1, f, f, None) == -1             # B
+    assert smp(f, 4, 0, 100, 1.0, 0, 1.0, 1, f, f, None) == -1               # V
+    assert smp(f, 4, 100, 99, 1.0, 0, 1.0, 1, f, f, None) == -1              # ld < V
+    assert smp(f, 4, 100, 100, nan, 0, 1.0, 1, f, f, None) == -1             # temperature
+    assert smp(f, 4, 100, 100, 1.0, 0, nan, 1, f, f, None) == -1             # top_p
+    assert smp(ctypes.c_void_p(0x10001), 4, 100, 100, 1.0, 0, 1.0, 1, f, f, None) == -3
+    assert smp(f, 4, 100, 100, 1.0, 0, 1.0, 1, f, ctypes.c_void_p(0x10002), None) == -3
+    assert smol.last_launch_count() == 0
+
+
 def test_argument_errors_return_before_any_launch(smol):
     cfg = _cfg(smol)
     f = ctypes.c_void_p(0x10000)

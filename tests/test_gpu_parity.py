@@ -277,3 +277,101 @@ def test_decode_batch_beyond_persistent_limit(S):
                                                   sliding_window=(0, 60))
     lengths = [int(v) for v in np.random.default_rng(46).integers(0, 97, size=2100)]
     run_decode_case(S, wl, lengths, seed=46)
+
+
+# ---------------------------------------------------------------- next-token choice
+# ("model.py" (SmolLM2-135M) section 7 generate; the abi96062 model.py generate)
+
+def _oracle_choices(rows, u, **kw):
+    """The oracle's tokens, and the tokens it gives when u or top_p move by 1e-6
+    (a fp32 kernel may land either way that close to a boundary)."""
+    base = O.sample_next(rows, u=u, **kw)
+    alts = [base]
+    for du in (-1e-6, 1e-6):
+        alts.append(O.sample_next(rows, u=np.clip(u + du, 0.0, 1.0 - 1e-12), **kw))
+    tp = kw.get("top_p")
+    if tp is not None and tp < 1.0:
+        for dp in (-1e-6, 1e-6):
+            alts.append(O.sample_next(rows, u=u, **{**kw, "top_p": tp + dp}))
+    return base, np.stack(alts)
+
+
+def _check_sample(S, logits_bf16, u, **kw):
+    B = logits_bf16.shape[0]
+    dev = logits_bf16.cuda()
+    nxt = torch.full((B,), -1, dtype=torch.int32, device="cuda")
+    S.sample(dev, nxt, u.cuda(), **kw)
+    torch.cuda.synchronize()
+    got = nxt.cpu().numpy().astype(np.int64)
+    rows = logits_bf16.float().numpy().astype(np.float64)
+    okw = {k: v for k, v in kw.items() if k in ("temperature", "top_k", "top_p", "do_sample")}
+    for k in ("temperature", "top_p"):            # the kernel takes them as fp32
+        if k in okw:
+            okw[k] = float(np.float32(okw[k]))
+    base, alts = _oracle_choices(rows, u.numpy().astype(np.float64), **okw)
+    decisive = np.all(alts == base[None], axis=0)
+    assert np.all(got[decisive] == base[decisive]), (kw, np.nonzero(got[decisive] != base[decisive]))
+    assert np.all(np.any(alts == got[None], axis=0)), kw
+    return int(decisive.sum())
+
+
+@pytest.mark.parametrize("kw", [
+    dict(do_sample=False), dict(temperature=0.0), dict(temperature=1.0),
+    dict(temperature=0.7, top_k=50), dict(temperature=1.0, top_p=0.9),
+    dict(temperature=0.8, top_k=40, top_p=0.5), dict(temperature=1.3, top_k=1),
+    dict(temperature=1.0, top_p=1e-6), dict(temperature=0.6, top_k=49152, top_p=0.95)])
+@pytest.mark.parametrize("dist", ["normal", "ties"])
+def test_sample_matches_oracle(S, kw, dist):
+    B, V = 32, 49152
+    g = torch.Generator().manual_seed(50 + (dist == "ties"))
+    x = torch.randn(B, V, generator=g)
+    # "ties": whole-number logits, thousands of equal values per row
+    logits = ((x * 3.0) if dist == "normal" else torch.round(x * 2.0)).to(torch.bfloat16)
+    u = torch.rand(B, generator=g)
+    n = _check_sample(S, logits, u, **kw)
+    assert n >= B // 2                            # most draws are nowhere near a boundary
+
+
+def test_sample_smollm3_vocab_strided_rows(S):
+    # the SmolLM3 vocabulary (128256) and rows with a pitch beyond V
+    B, V, ld = 4, 128256, 128256 + 64
+    g = torch.Generator().manual_seed(52)
+    buf = (torch.randn(B, ld, generator=g) * 2.0).to(torch.bfloat16)
+    u = torch.rand(B, generator=g)
+    logits = buf.cuda()[:, :V]
+    nxt = torch.empty(B, dtype=torch.int32, device="cuda")
+    S.sample(logits, nxt, u.cuda(), temperature=0.9, top_k=100, top_p=0.8)
+    torch.cuda.synchronize()
+    rows = buf[:, :V].float().numpy().astype(np.float64)
+    base, alts = _oracle_choices(rows, u.numpy().astype(np.float64), temperature=float(np.float32(0.9)),
+                                 top_k=100, top_p=float(np.float32(0.8)))
+    got = nxt.cpu().numpy()
+    assert np.all(np.any(alts == got[None], axis=0))
+
+
+def test_sample_degenerate_rows(S):
+    # one-token vocabulary; all-equal rows (greedy takes index 0, the draw is uniform)
+    one = torch.tensor([[1.5], [-2.0]], dtype=torch.bfloat16)
+    for kw in (dict(do_sample=False), dict(temperature=1.0, top_p=0.5, top_k=3)):
+        assert _check_sample(S, one, torch.tensor([0.3, 0.99]), **kw) == 2
+    flat = torch.zeros(3, 1000, dtype=torch.bfloat16)
+    _check_sample(S, flat, torch.tensor([0.0, 0.5004, 0.99999]), temperature=1.0)
+    _check_sample(S, flat, torch.tensor([0.0, 0.5, 0.99999]), do_sample=False)
+    _check_sample(S, flat, torch.tensor([0.1, 0.6, 0.99999]), temperature=1.0, top_p=0.3)
+
+
+def test_sample_after_decode_step(S):
+    # the decode step's logits feed the choice directly (no host round trip)
+    wl = W["smollm2_decode_b64_cache4096"].scaled(n_layers=2, s_max=128, vocab=4096, B=5)
+    inp = synth.generate(wl, seed=53)
+    inp.lengths = torch.tensor([0, 5, 64, 100, 128], dtype=torch.int32)
+    dev = to_device(inp)
+    cfg = S.config_of(wl)
+    packed = S.prepare_weights(cfg, dev.layers, dev.embed, dev.final_norm)
+    ws = S.alloc_workspace(cfg, S.OP_DECODE, wl.B, 1)
+    k_new = torch.empty(2, 5, 3, 64, dtype=torch.bfloat16, device="cuda")
+    v_new = torch.empty_like(k_new)
+    logits = torch.empty(5, 4096, dtype=torch.bfloat16, device="cuda")
+    S.decode_step(cfg, packed, dev.ids, dev.lengths, dev.k_cache, dev.v_cache, k_new, v_new, logits, ws)
+    u = torch.tensor([0.1, 0.3, 0.5, 0.7, 0.9])
+    _check_sample(S, logits.cpu(), u, temperature=0.8, top_k=20, top_p=0.9)
