@@ -45,6 +45,17 @@ design notes):
     t - w < j <= t, on top of the causal and padding masks; 0 = no window.
     In decode the new token at position L sees cached slots j >= L - w + 1
     plus itself.
+  * Prefill with a past ([M1] sections 4 and 7 with past_key_values and
+    T > 1): the page drops the causal mask whenever a past exists, which
+    would let a new token see the ones after it; the reading taken is the
+    causal mask offset by the past: new token t of sequence b sits at
+    position cache_len[b] + t and sees the cached slots [0, cache_len[b])
+    and the new tokens 0 .. t (window limits as above).  Cache lengths are
+    per sequence, as in decode.
+  * Additive attention mask ([M1] section 4, attention_mask of 0 / -inf over
+    the keys): a key j of sequence b is hidden iff the mask is -inf there,
+    on top of the causal mask; positions stay 0 .. T-1 (the page derives no
+    positions from it); a row with no visible key gets attention output 0.
   * Next-token choice ([M1] section 7 generate; [M4] generate): greedy is the
     first index of the row maximum; the multinomial draw is the inverse CDF
     in vocabulary order of a uniform number u in [0, 1) that the caller
@@ -189,13 +200,14 @@ def positions(B: int, T: int, valid_start=None) -> np.ndarray:
     return np.maximum(t - vs, 0)
 
 
-def gqa_attention(q, k, v, valid_start=None, window: int = 0) -> np.ndarray:
+def gqa_attention(q, k, v, valid_start=None, window: int = 0, key_mask=None) -> np.ndarray:
     """Causal grouped-query softmax attention.
 
     q: [B, H, T, hd]; k, v: [B, KV, S, hd] with S == T (prefill).
     o[b,h,t] = sum_{j valid, j<=t} softmax_j(q[b,h,t].k[b,h//g,j] / sqrt(hd)) v[b,h//g,j]
     A row with no valid key returns 0.  With window w > 0 a key is also
-    masked when j <= t - w.
+    masked when j <= t - w.  key_mask [B, S] (optional, bool, True = visible)
+    hides the keys where it is False ([M1] section 4 attention_mask).
     [M1] section 4 (scores / sqrt(head_dim), triu(1) causal mask, additive
     padding mask, softmax, probs @ v); [M3] "Grouped-query attention" and
     "A sliding window the 3B checkpoints leave off".
@@ -212,6 +224,8 @@ def gqa_attention(q, k, v, valid_start=None, window: int = 0) -> np.ndarray:
         masked = (j_idx > t_idx) | (j_idx < vs)
         if window > 0:
             masked = masked | (j_idx <= t_idx - window)
+        if key_mask is not None:
+            masked = masked | ~np.asarray(key_mask[b], dtype=bool)[None, :]
         for h in range(H):
             kvh = h // g
             s = np.matmul(q[b, h], k[b, kvh].T) / np.sqrt(F64(hd))
@@ -243,7 +257,8 @@ class BlockWeights:
 
 
 def block_forward(cfg: Config, w: BlockWeights, x, valid_start=None,
-                  taps: Optional[Dict[str, np.ndarray]] = None, layer: int = 0) -> np.ndarray:
+                  taps: Optional[Dict[str, np.ndarray]] = None, layer: int = 0,
+                  key_mask=None) -> np.ndarray:
     """Pre-norm decoder block on x [B, T, d]; ``layer`` selects the block's
     NoPE flag and window from cfg.
 
@@ -253,6 +268,8 @@ def block_forward(cfg: Config, w: BlockWeights, x, valid_start=None,
     the queries and keys are the projections").
     [M1] section 6 SmolBlock; [M3] "The block, in order"; [M5] TransformerBlock.
     ``taps`` (optional) receives the named intermediates used by [M3].
+    ``key_mask`` [B, T] (optional, True = visible) is the additive 0 / -inf
+    attention_mask of [M1] section 4 in boolean form.
     """
     x = _f64(x)
     B, T, d = x.shape
@@ -267,7 +284,7 @@ def block_forward(cfg: Config, w: BlockWeights, x, valid_start=None,
     if rope:
         q = apply_rope(q, pos[:, None, :], cfg.rope_theta)
         k = apply_rope(k, pos[:, None, :], cfg.rope_theta)
-    o = gqa_attention(q, k, v, valid_start, window)
+    o = gqa_attention(q, k, v, valid_start, window, key_mask)
     o_tok = o.transpose(0, 2, 1, 3).reshape(B, T, H * hd)
     attn_out = linear(o_tok, w.wo)
     h = x + attn_out
@@ -294,7 +311,8 @@ def lm_head(cfg: Config, x, final_norm, embed) -> np.ndarray:
 
 
 def model_forward(cfg: Config, layers: List[BlockWeights], embed, final_norm, ids,
-                  valid_start=None, taps: Optional[Dict[str, np.ndarray]] = None) -> np.ndarray:
+                  valid_start=None, taps: Optional[Dict[str, np.ndarray]] = None,
+                  key_mask=None) -> np.ndarray:
     """Embedding -> L blocks -> final norm -> tied head; logits [B, T, V].
 
     [M1] section 7 SmolLM2.forward (including its max-position assertion);
@@ -306,7 +324,7 @@ def model_forward(cfg: Config, layers: List[BlockWeights], embed, final_norm, id
         raise ValueError("sequence longer than max_position_embeddings")
     x = _f64(embed)[ids]
     for l, w in enumerate(layers):
-        x = block_forward(cfg, w, x, valid_start, layer=l)
+        x = block_forward(cfg, w, x, valid_start, layer=l, key_mask=key_mask)
     if taps is not None:
         taps["final_norm_output"] = rms_norm(x, final_norm, cfg.rms_eps)
     logits = lm_head(cfg, x, final_norm, embed)
@@ -363,6 +381,64 @@ def decode_step(cfg: Config, layers: List[BlockWeights], embed, final_norm, ids,
                 e = np.exp(s - np.max(s))
                 o[b, h] = np.matmul(e / np.sum(e), vals)
         x = x + linear(o.reshape(B, H * hd), w.wo)
+        m = rms_norm(x, w.mlp_norm, cfg.rms_eps)
+        x = x + linear(silu(linear(m, w.wgate)) * linear(m, w.wup), w.wdown)
+    return lm_head(cfg, x, final_norm, embed), k_new, v_new
+
+
+def prefill_with_cache(cfg: Config, layers: List[BlockWeights], embed, final_norm, ids,
+                       cache_len, k_cache, v_cache):
+    """T new tokens per sequence on top of a KV cache (chunked prefill).
+
+    ids [B, T]; cache_len [B]; k_cache, v_cache [L, B, KV, S, hd] holding
+    post-RoPE keys and values in slots [0, cache_len[b]).  New token t of
+    sequence b sits at position cache_len[b] + t and attends over the cached
+    slots (those inside its block's window) and the new tokens 0 .. t.
+    Returns (logits [B, T, V], k_new [L, B, KV, T, hd], v_new [L, B, KV, T, hd]),
+    k_new post-RoPE (unrotated on a NoPE block): what a caller appends.
+    [M1] section 4 (cache concat; the causal mask offset by the past, see the
+    readings above) and section 7 (RoPE rows sliced at past_len).
+    """
+    ids = np.asarray(ids)
+    cache_len = np.asarray(cache_len)
+    B, T = ids.shape
+    H, KV, hd = cfg.n_heads, cfg.n_kv_heads, cfg.head_dim
+    g = H // KV
+    L = len(layers)
+    if np.any(cache_len + T > cfg.max_pos):
+        raise ValueError("cache_len + T exceeds max_position_embeddings")
+    x = _f64(embed)[ids]                                   # [B, T, d]
+    k_new = np.zeros((L, B, KV, T, hd))
+    v_new = np.zeros((L, B, KV, T, hd))
+    t_idx = np.arange(T)
+    for l, w in enumerate(layers):
+        rope, window = block_kind(cfg, l)
+        n = rms_norm(x, w.attn_norm, cfg.rms_eps)
+        q = linear(n, w.wq).reshape(B, T, H, hd).transpose(0, 2, 1, 3)
+        k = linear(n, w.wk).reshape(B, T, KV, hd).transpose(0, 2, 1, 3)
+        v = linear(n, w.wv).reshape(B, T, KV, hd).transpose(0, 2, 1, 3)
+        if rope:
+            pos = (cache_len[:, None] + t_idx[None, :])[:, None, :]   # [B, 1, T]
+            q = apply_rope(q, pos, cfg.rope_theta)
+            k = apply_rope(k, pos, cfg.rope_theta)
+        k_new[l], v_new[l] = k, v
+        o = np.zeros((B, H, T, hd))
+        for b in range(B):
+            Lb = int(cache_len[b])
+            keys_all = np.concatenate([_f64(k_cache[l, b, :, :Lb]), k[b]], axis=1)   # [KV, Lb+T, hd]
+            vals_all = np.concatenate([_f64(v_cache[l, b, :, :Lb]), v[b]], axis=1)
+            j_pos = np.arange(Lb + T)[None, :]             # key positions
+            q_pos = (Lb + t_idx)[:, None]                  # query positions
+            masked = j_pos > q_pos
+            if window > 0:
+                masked = masked | (j_pos <= q_pos - window)
+            for h in range(H):
+                kvh = h // g
+                sc = np.matmul(q[b, h], keys_all[kvh].T) / np.sqrt(F64(hd))
+                sc = np.where(masked, -np.inf, sc)
+                e = np.exp(sc - np.max(sc, axis=-1, keepdims=True))
+                o[b, h] = np.matmul(e / np.sum(e, axis=-1, keepdims=True), vals_all[kvh])
+        x = x + linear(o.transpose(0, 2, 1, 3).reshape(B, T, H * hd), w.wo)
         m = rms_norm(x, w.mlp_norm, cfg.rms_eps)
         x = x + linear(silu(linear(m, w.wgate)) * linear(m, w.wup), w.wdown)
     return lm_head(cfg, x, final_norm, embed), k_new, v_new

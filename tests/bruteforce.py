@@ -39,10 +39,11 @@ def silu(z):
     return z / (1.0 + math.exp(-z))
 
 
-def block(cfg, w, x, valid_start=None, rope=True, window=0):
+def block(cfg, w, x, valid_start=None, rope=True, window=0, key_mask=None):
     """x: [B][T][d] nested lists; w: dict of nested lists.  rope=False leaves
     q and k unrotated (a NoPE block); window > 0 keeps only the `window` most
-    recent keys of each query, its own included."""
+    recent keys of each query, its own included; key_mask[b][j] false hides
+    key j of sequence b."""
     H, KV, hd = cfg.n_heads, cfg.n_kv_heads, cfg.head_dim
     B, T = len(x), len(x[0])
     out = []
@@ -64,7 +65,8 @@ def block(cfg, w, x, valid_start=None, rope=True, window=0):
             o = []
             for h in range(H):
                 kvh = h * KV // H
-                keys = [j for j in range(T) if vs <= j <= t and (window == 0 or t - j < window)]
+                keys = [j for j in range(T) if vs <= j <= t and (window == 0 or t - j < window)
+                        and (key_mask is None or key_mask[b][j])]
                 if not keys:
                     o.extend([0.0] * hd)
                     continue

@@ -619,3 +619,139 @@ def test_sample_temperature_is_a_logit_scale():
     for kw in (dict(), dict(top_k=7), dict(top_p=0.8), dict(top_k=9, top_p=0.6)):
         np.testing.assert_array_equal(O.sample_next(rows, temperature=0.5, u=us, **kw),
                                       O.sample_next(rows * 2.0, temperature=1.0, u=us, **kw))
+
+
+# ---------------------------------------------------------------- prefill on top of a cache
+# ("model.py" (SmolLM2-135M) section 4 with past_key_value and section 7: the
+# causal mask offset by the past, RoPE rows sliced at the past length)
+
+def _chunk_cfg(**kw):
+    return O.Config(hidden=16, n_heads=4, n_kv_heads=2, head_dim=4, intermediate=12, n_layers=3,
+                    vocab=13, max_pos=64, rms_eps=1e-5, rope_theta=1e4, **kw)
+
+
+def _cache_from(cfg, layers, embed, seqs, S):
+    """Caches [L, B, KV, S, hd] filled by full prefills of each sequence;
+    slots past each length hold poison that must never be read."""
+    k_cache = np.full((cfg.n_layers, len(seqs), cfg.n_kv_heads, S, cfg.head_dim), 99.0)
+    v_cache = np.full_like(k_cache, -99.0)
+    for b, sq in enumerate(seqs):
+        if len(sq):
+            k, v = _prefill_cache(cfg, layers, embed, np.asarray(sq)[None])
+            k_cache[:, b, :, :len(sq)] = k[:, 0]
+            v_cache[:, b, :, :len(sq)] = v[:, 0]
+    return k_cache, v_cache
+
+
+@pytest.mark.parametrize("kinds", [dict(), dict(no_rope_layers=(1, 0, 1), sliding_window=(0, 3, 5))])
+def test_chunked_prefill_equals_full_prefill(kinds):
+    cfg = _chunk_cfg(**kinds)
+    rng = np.random.default_rng(33)
+    layers = [as_block(tiny_weights(cfg, rng)) for _ in range(cfg.n_layers)]
+    embed = rng.normal(0, 0.5, (cfg.vocab, cfg.hidden))
+    fnorm = 1 + rng.normal(0, 0.1, cfg.hidden)
+    T, past = 4, [0, 3, 7]
+    seqs = [rng.integers(0, cfg.vocab, p + T) for p in past]
+    k_cache, v_cache = _cache_from(cfg, layers, embed, [s[:p] for s, p in zip(seqs, past)], 12)
+    new_ids = np.stack([s[p:] for s, p in zip(seqs, past)])
+    logits, k_new, v_new = O.prefill_with_cache(cfg, layers, embed, fnorm, new_ids, past, k_cache, v_cache)
+    for b, p in enumerate(past):
+        full = O.model_forward(cfg, layers, embed, fnorm, seqs[b][None])
+        np.testing.assert_allclose(logits[b], full[0, p:], rtol=1e-11, atol=1e-12)
+        k, v = _prefill_cache(cfg, layers, embed, seqs[b][None])
+        np.testing.assert_allclose(k_new[:, b], k[:, 0, :, p:], rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(v_new[:, b], v[:, 0, :, p:], rtol=1e-11, atol=1e-12)
+
+
+def test_three_chained_chunks_equal_one_prefill():
+    cfg = _chunk_cfg(sliding_window=(0, 4, 0))
+    rng = np.random.default_rng(34)
+    layers = [as_block(tiny_weights(cfg, rng)) for _ in range(cfg.n_layers)]
+    embed = rng.normal(0, 0.5, (cfg.vocab, cfg.hidden))
+    fnorm = 1 + rng.normal(0, 0.1, cfg.hidden)
+    ids = rng.integers(0, cfg.vocab, (2, 9))
+    S = 9
+    k_cache = np.zeros((cfg.n_layers, 2, cfg.n_kv_heads, S, cfg.head_dim))
+    v_cache = np.zeros_like(k_cache)
+    outs, at = [], 0
+    for T in (2, 4, 3):
+        lg, kn, vn = O.prefill_with_cache(cfg, layers, embed, fnorm, ids[:, at:at + T], [at, at],
+                                          k_cache, v_cache)
+        k_cache[:, :, :, at:at + T] = kn                 # the caller appends
+        v_cache[:, :, :, at:at + T] = vn
+        outs.append(lg)
+        at += T
+    full = O.model_forward(cfg, layers, embed, fnorm, ids)
+    np.testing.assert_allclose(np.concatenate(outs, axis=1), full, rtol=1e-11, atol=1e-12)
+
+
+def test_prefill_of_one_token_is_the_decode_step():
+    cfg = _chunk_cfg(no_rope_layers=(0, 1, 1), sliding_window=(2, 0, 6))
+    rng = np.random.default_rng(35)
+    layers = [as_block(tiny_weights(cfg, rng)) for _ in range(cfg.n_layers)]
+    embed = rng.normal(0, 0.5, (cfg.vocab, cfg.hidden))
+    fnorm = 1 + rng.normal(0, 0.1, cfg.hidden)
+    lens = np.array([0, 4, 11])
+    k_cache = rng.normal(0, 1, (cfg.n_layers, 3, cfg.n_kv_heads, 11, cfg.head_dim))
+    v_cache = rng.normal(0, 1, k_cache.shape)
+    ids = rng.integers(0, cfg.vocab, 3)
+    lg, kn, vn = O.prefill_with_cache(cfg, layers, embed, fnorm, ids[:, None], lens, k_cache, v_cache)
+    dl, dk, dv = O.decode_step(cfg, layers, embed, fnorm, ids, lens, k_cache, v_cache)
+    np.testing.assert_allclose(lg[:, 0], dl, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(kn[:, :, :, 0], dk, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(vn[:, :, :, 0], dv, rtol=1e-12, atol=1e-13)
+
+
+def test_prefill_on_empty_caches_is_the_model_forward():
+    cfg = _chunk_cfg()
+    rng = np.random.default_rng(36)
+    layers = [as_block(tiny_weights(cfg, rng)) for _ in range(cfg.n_layers)]
+    embed = rng.normal(0, 0.5, (cfg.vocab, cfg.hidden))
+    fnorm = 1 + rng.normal(0, 0.1, cfg.hidden)
+    ids = rng.integers(0, cfg.vocab, (2, 6))
+    cache = np.full((cfg.n_layers, 2, cfg.n_kv_heads, 4, cfg.head_dim), 55.0)   # never read
+    lg, _, _ = O.prefill_with_cache(cfg, layers, embed, fnorm, ids, [0, 0], cache, cache)
+    np.testing.assert_allclose(lg, O.model_forward(cfg, layers, embed, fnorm, ids), rtol=1e-12, atol=1e-13)
+
+
+# ---------------------------------------------------------------- additive key mask
+# ("model.py" (SmolLM2-135M) section 4: attention_mask of 0 / -inf added to the scores)
+
+def test_key_mask_of_left_padding_is_valid_start():
+    rng = np.random.default_rng(37)
+    B, H, KV, T, hd = 3, 6, 2, 10, 4
+    q, k, v = _rand_qkv(B, H, KV, T, hd, rng)
+    vs = [0, 4, 10]
+    mask = np.arange(T)[None, :] >= np.array(vs)[:, None]
+    np.testing.assert_array_equal(O.gqa_attention(q, k, v, key_mask=mask), O.gqa_attention(q, k, v, vs))
+    np.testing.assert_array_equal(O.gqa_attention(q, k, v, key_mask=np.ones((B, T), bool)),
+                                  O.gqa_attention(q, k, v))
+
+
+def test_key_mask_vs_torch_sdpa_boolean_mask():
+    rng = np.random.default_rng(38)
+    B, H, KV, T, hd = 2, 8, 2, 24, 16
+    q, k, v = _rand_qkv(B, H, KV, T, hd, rng)
+    mask = rng.random((B, T)) < 0.6
+    mask[:, 0] = True                                 # every row keeps its first key
+    g = H // KV
+    kt = torch.tensor(k).repeat_interleave(g, dim=1)
+    vt = torch.tensor(v).repeat_interleave(g, dim=1)
+    allowed = torch.tril(torch.ones(T, T, dtype=torch.bool))[None, None] & torch.tensor(mask)[:, None, None, :]
+    ref = F.scaled_dot_product_attention(torch.tensor(q), kt, vt, attn_mask=allowed).numpy()
+    np.testing.assert_allclose(O.gqa_attention(q, k, v, key_mask=mask), ref, rtol=1e-11, atol=1e-12)
+    # a row whose visible keys are all masked out gets 0
+    m2 = mask.copy()
+    m2[0, :3] = False
+    o = O.gqa_attention(q, k, v, key_mask=m2)
+    np.testing.assert_array_equal(o[0, :, :3], 0.0)
+
+
+def test_key_mask_block_vs_bruteforce_loops():
+    rng = np.random.default_rng(39)
+    w = tiny_weights(TINY, rng)
+    x = rng.normal(0, 1, (2, 7, TINY.hidden))
+    mask = np.array([[1, 0, 1, 1, 0, 1, 1], [0, 0, 1, 1, 1, 0, 1]], dtype=bool)
+    out = O.block_forward(TINY, as_block(w), x, key_mask=mask)
+    ref = np.array(bf.block(TINY, {k: nested(a) for k, a in w.items()}, nested(x), key_mask=mask.tolist()))
+    np.testing.assert_allclose(out, ref, rtol=1e-11, atol=1e-12)
