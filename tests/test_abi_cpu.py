@@ -35,6 +35,35 @@ def test_no_unexpected_exports(smol):
     assert ours == set(smol.declared_symbols())
 
 
+def _prototypes(text):
+    """name -> list of parameter declarations of every smol_* prototype in the header."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    out = {}
+    for m in re.finditer(r"(smol_\w+)\s*\(([^;{]*?)\)\s*;", text):
+        args = " ".join(m.group(2).split())
+        out[m.group(1)] = [] if args in ("", "void") else [a.strip() for a in args.split(",")]
+    return out
+
+
+def test_binding_matches_header_prototypes(smol):
+    # every function the binding declares has the header's arity, and pointer
+    # parameters are marshalled as pointers, integers as integers, floats as floats
+    protos = _prototypes(open(smol.HEADER_PATH).read())
+    ints = (ctypes.c_int, ctypes.c_uint, ctypes.c_size_t, ctypes.c_longlong)
+    for name, (_, argtypes) in smol._SIGS.items():
+        assert name in protos, name
+        decl = protos[name]
+        assert len(decl) == len(argtypes), (name, decl, argtypes)
+        for d, t in zip(decl, argtypes):
+            if "*" in d:
+                assert t is ctypes.c_void_p or hasattr(t, "contents") or t is ctypes.c_char_p, (name, d, t)
+            elif d.startswith("float"):
+                assert t is ctypes.c_float, (name, d, t)
+            else:
+                assert t in ints, (name, d, t)
+    assert set(protos) == set(smol._SIGS)
+
+
 def _cfg(smol, **kw):
     base = dict(hidden=576, n_heads=9, n_kv_heads=3, head_dim=64, intermediate=1536, n_layers=30,
                 vocab=49152, max_pos=8192, rms_eps=1e-5, rope_theta=1e5)
