@@ -239,7 +239,8 @@ int smol_decode_step_noalloc(const smol_config *cfg, const void *packed, const i
  *                 (values equal to the k-th stay; top_k >= V removes nothing);
  *     top_p < 1   in descending z order (equal values by ascending index), the
  *                 tokens after the first one at which the cumulative softmax
- *                 probability of the top-k survivors exceeds top_p are removed;
+ *                 probability of the top-k survivors exceeds top_p are removed
+ *                 (top_p <= 0: only the first token in that order survives);
  *     the draw    the first index i, in vocabulary order, at which the
  *                 cumulative probability of the survivors exceeds uniform[b]
  *                 (the inverse CDF; the pages call a multinomial sampler).

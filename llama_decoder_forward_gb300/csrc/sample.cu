@@ -337,7 +337,7 @@ cudaError_t launch_sample(const void *logits, long long ld, int B, int V, float 
   p.V = V;
   p.temperature = temperature;
   p.top_k = top_k;
-  p.top_p = top_p;
+  p.top_p = top_p > 0.f ? top_p : 0.f;   // top_p <= 0 keeps the first token in descending order, as 0 does
   p.do_sample = do_sample;
   p.uniform = uniform;
   p.next = next;

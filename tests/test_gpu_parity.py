@@ -319,7 +319,8 @@ def _check_sample(S, logits_bf16, u, **kw):
     dict(do_sample=False), dict(temperature=0.0), dict(temperature=1.0),
     dict(temperature=0.7, top_k=50), dict(temperature=1.0, top_p=0.9),
     dict(temperature=0.8, top_k=40, top_p=0.5), dict(temperature=1.3, top_k=1),
-    dict(temperature=1.0, top_p=1e-6), dict(temperature=0.6, top_k=49152, top_p=0.95)])
+    dict(temperature=1.0, top_p=1e-6), dict(temperature=0.6, top_k=49152, top_p=0.95),
+    dict(temperature=1.0, top_p=0.0), dict(temperature=0.9, top_k=30, top_p=-0.5)])
 @pytest.mark.parametrize("dist", ["normal", "ties"])
 def test_sample_matches_oracle(S, kw, dist):
     B, V = 32, 49152

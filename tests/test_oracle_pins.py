@@ -590,9 +590,10 @@ def test_sample_top_p_ties_in_index_order():
     # cumulative 0.25, 0.5, ...: top_p 0.3 keeps the first two sorted, i.e. indices 0 and 1
     assert O.sample_next(row, top_p=0.3, u=[0.6])[0] == 1
     assert O.sample_next(row, top_p=0.3, u=[0.4])[0] == 0
-    # a tiny top_p keeps only the first sorted entry: the lowest index of the maximum
+    # a tiny, zero or negative top_p keeps only the first sorted entry: the lowest index of the maximum
     row2 = np.array([[1.0, 5.0, 5.0, 2.0]])
-    assert O.sample_next(row2, top_p=1e-9, u=[0.99])[0] == 1
+    for tp in (1e-9, 0.0, -0.5):
+        assert O.sample_next(row2, top_p=tp, u=[0.99])[0] == 1
 
 
 def test_sample_inverse_cdf_frequencies_match_softmax():
