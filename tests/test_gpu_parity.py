@@ -75,7 +75,8 @@ def test_block_small_residual_input(S):
     run_block_case(S, W["smollm2_block_b1_t128"].scaled(B=2, T=96), x_scale=0.0417)
 
 
-@pytest.mark.parametrize("B,T", [(2, 200), (1, 1), (3, 67), (1, 385)])
+@pytest.mark.parametrize("B,T", [(2, 200), (1, 1), (3, 67), (1, 385), (1, 2), (2, 3), (1, 65), (2, 127),
+                                 (1, 129)])
 def test_block_smollm2_ragged(S, B, T):
     run_block_case(S, W["smollm2_block_b1_t128"].scaled(B=B, T=T), seed=B * 1000 + T)
 
