@@ -167,6 +167,21 @@ int smol_block_forward(const smol_config *cfg, const void *packed, int layer,
                        void *k_out, void *v_out, void *ws, size_t ws_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * smol_block_forward_masked: smol_block_forward with a key mask in place of
+ * left padding: the additive attention_mask of [M1] section 4 (0 where a key
+ * may be attended, -inf where not), given as bytes.
+ *   key_mask  device uint8 [B, T], required: key j of sequence b is visible
+ *             iff key_mask[b*T + j] != 0, on top of the causal mask.  Position
+ *             ids stay t (the page derives none from the mask).  A query row
+ *             that sees no key gets an attention output of 0.
+ * All other arguments as in smol_block_forward.
+ * ------------------------------------------------------------------------- */
+int smol_block_forward_masked(const smol_config *cfg, const void *packed, int layer,
+                              const void *x, void *out, int act_dtype, int B, int T,
+                              const uint8_t *key_mask, void *k_out, void *v_out, void *ws,
+                              size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
  * smol_model_forward: embedding -> cfg->n_layers blocks -> final RMSNorm ->
  * tied lm_head ([M1] section 7 SmolLM2.forward; [M4] SmolLM2Model.forward).
  *   ids          device int32 [B, T], each in [0, V) (out-of-range ids are
@@ -179,6 +194,37 @@ int smol_block_forward(const smol_config *cfg, const void *packed, int layer,
 int smol_model_forward(const smol_config *cfg, const void *packed, const int32_t *ids,
                        int B, int T, const int32_t *valid_start, void *logits,
                        void *ws, size_t ws_bytes, void *stream);
+
+/* smol_model_forward with the key mask of smol_block_forward_masked (device
+ * uint8 [B, T], required) in place of valid_start; every block uses it. */
+int smol_model_forward_masked(const smol_config *cfg, const void *packed, const int32_t *ids,
+                              int B, int T, const uint8_t *key_mask, void *logits,
+                              void *ws, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * smol_prefill_with_cache: T new tokens per sequence on top of a KV cache
+ * (chunked prefill; [M1] section 4 with past_key_value and T > 1, section 7
+ * with past_key_values).  New token t of sequence b sits at position
+ * cache_len[b] + t and attends over its cache_len[b] cached entries and the
+ * new tokens 0 .. t (the causal mask offset by the past; the page's model.py
+ * drops the mask whenever a past exists, which would let a token see later
+ * ones).  Per-block NoPE flags and windows apply as in the other calls.
+ *   ids        device int32 [B, T].
+ *   cache_len  device int32 [B], each in [0, min(S_max, max_pos - T)]
+ *              (clamped into that range on the device).
+ *   k_cache, v_cache  device [L, B, KV, S_max, hd] bf16, post-RoPE keys; read only.
+ *   k_new, v_new      device [L, B, KV, T, hd] bf16 outputs: the new tokens'
+ *              post-RoPE keys and values per layer, for the caller to append
+ *              at slots cache_len[b] .. cache_len[b] + T - 1.
+ *   logits     device [B, T, V] bf16.
+ *   ws         >= smol_prefill_cache_workspace_bytes(cfg, B, T, S_max) bytes.
+ * Supported: head_dim 64 (SMOL_ERR_UNSUPPORTED_SHAPE otherwise); T < max_pos.
+ * ------------------------------------------------------------------------- */
+size_t smol_prefill_cache_workspace_bytes(const smol_config *cfg, int B, int T, int S_max);
+int smol_prefill_with_cache(const smol_config *cfg, const void *packed, const int32_t *ids, int B,
+                            int T, const int32_t *cache_len, const void *k_cache,
+                            const void *v_cache, int S_max, void *k_new, void *v_new,
+                            void *logits, void *ws, size_t ws_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------
  * smol_decode_step: one new token per sequence with a KV cache
@@ -215,20 +261,33 @@ int smol_decode_step(const smol_config *cfg, const void *packed, const int32_t *
  *   Scratch: a fixed 8 MiB device array inside the library (every GPU that
  *   loads the library holds one until the process exits).  Calls for which
  *   smol_workspace_bytes(cfg, SMOL_OP_DECODE, B, 1) exceeds 8 MiB return
- *   SMOL_ERR_WORKSPACE and launch nothing (SmolLM2-135M needs about 3.2 MiB
+ *   SMOL_ERR_WORKSPACE and launch nothing (SmolLM2-135M needs about 5.1 MiB
  *   at B = 64).
- *   The first call on a device looks up the array's device address (a host
- *   call, cudaGetSymbolAddress); make that first call before any stream
- *   capture on the device.  Nothing is allocated or freed, ever.
+ *   Each call made outside stream capture looks up the array's device address
+ *   (a host call, cudaGetSymbolAddress, with the device current), so the
+ *   first call on a device must come before any stream capture on it; a call
+ *   made while `stream` is capturing reuses the address of the last uncaptured
+ *   call on that device (SMOL_ERR_INVALID_ARG if there was none).  Nothing is
+ *   allocated or freed, ever.
  *   All calls share the one array: calls whose work overlaps on the GPU
  *   (different streams, or different host threads) race on it and give
  *   wrong results; serialise them.  Each call clears what must start at
  *   zero, so back-to-back calls on one stream are safe.
+ *   The array's first word is the status word of these calls' bounded waits:
+ *   read it with smol_decode_noalloc_status.
  * ------------------------------------------------------------------------- */
 int smol_decode_step_noalloc(const smol_config *cfg, const void *packed, const int32_t *ids,
                              const int32_t *cache_len, int B, const void *k_cache,
                              const void *v_cache, int S_max, void *k_new, void *v_new,
                              void *logits, void *stream);
+
+/* Reads (synchronising `stream`) and clears the status word that
+ * smol_decode_step_noalloc's kernels write into the library's scratch array on
+ * the current device: SMOL_OK, SMOL_ERR_TIMEOUT (a bounded wait gave up since
+ * the last read; the outputs of that call are not valid) or SMOL_ERR_CUDA.
+ * No counterpart on the pages.  Not meant for the hot path, nor for use while
+ * `stream` is capturing. */
+int smol_decode_noalloc_status(void *stream);
 
 /* ---------------------------------------------------------------------------
  * smol_sample: the next token of each row of logits, chosen the way the pages'

@@ -7,7 +7,8 @@
 // head h reads key/value head h // g, as in the "SmolLM3" page's
 // "Grouped-query attention").  Rows with no visible key produce 0.  With a
 // sliding window w (the "SmolLM3" page, "A sliding window the 3B checkpoints
-// leave off") keys j <= t - w are hidden too.
+// leave off") keys j <= t - w are hidden too, and so are the keys an optional
+// key mask (the additive attention_mask of section 4, as bytes) marks 0.
 //
 // One CTA owns (sequence b, kv head, a block of BQ query tokens) and all g
 // query heads of that kv head: each K/V tile is loaded once into shared memory
@@ -93,6 +94,7 @@ __global__ void __launch_bounds__(512, 1) flash_attn_kernel(const AttnParams p) 
 
   const int last_q = min(q0 + BQ, T) - 1;
   const int W = p.window;                                         // > 0: sliding window
+  const uint8_t *kmask = p.key_mask ? p.key_mask + (long long)b * T : nullptr;   // 0 = key hidden
   const int kt_lo = (W > 0 ? max(vs, q0 - W + 1) : vs) / BK;      // first key any row of the block sees
   const int kt_hi = last_q / BK;
   load_kv(kt_lo, 0);
@@ -147,7 +149,7 @@ __global__ void __launch_bounds__(512, 1) flash_attn_kernel(const AttnParams p) 
         }
       }
       // scale into the exp2 domain and mask
-      const bool need_mask = (k0 + BK - 1 > tw_lo) || (k0 < vs) || (W > 0 && k0 <= tw_hi - W);
+      const bool need_mask = (k0 + BK - 1 > tw_lo) || (k0 < vs) || (W > 0 && k0 <= tw_hi - W) || kmask != nullptr;
 #pragma unroll
       for (int i = 0; i < NT; ++i) {
 #pragma unroll
@@ -156,7 +158,7 @@ __global__ void __launch_bounds__(512, 1) flash_attn_kernel(const AttnParams p) 
           if (need_mask) {
             const int j = k0 + i * 8 + ((lane & 3) << 1) + (e & 1);
             const int t = (e < 2) ? t_a : t_b;
-            if (j > t || j < vs || (W > 0 && j <= t - W)) x = -INFINITY;
+            if (j > t || j < vs || (W > 0 && j <= t - W) || (kmask && (j >= T || !kmask[j]))) x = -INFINITY;
           }
           s[i][e] = x;
         }

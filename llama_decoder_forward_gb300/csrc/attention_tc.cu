@@ -7,7 +7,9 @@
 // page's "Grouped-query attention").  Rows with no visible key produce 0.
 // A block with a sliding window w (the "SmolLM3" page, "A sliding window the
 // 3B checkpoints leave off") also hides keys j <= t - w: the CTA starts at the
-// tile of its first query's window and masks per row.
+// tile of its first query's window and masks per row.  An optional key mask
+// (the additive 0 / -inf attention_mask of "model.py" section 4, as bytes)
+// hides further keys; every tile then takes the masked path.
 //
 // One CTA owns (sequence b, kv head, a tile of 128 query tokens) and the GH
 // query heads of that kv head.  Each K tile [128 keys x 64] and V^T tile
@@ -66,6 +68,8 @@ struct AtParams {
   int B, T, H, KV, G, GH, n_hsub;
   float scale_log2;
   int window;               // > 0: query t sees keys j > t - window only
+  const uint8_t *key_mask;  // [B, T] or nullptr: key j of sequence b hidden where 0
+  int Tk, q_off;            // keys per sequence; key index of query 0
   int *status;
 };
 
@@ -110,7 +114,9 @@ __device__ __forceinline__ void at_status(int *status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
 
-template <int GH>
+// KM: the launch carries a key mask (a separate instantiation, so the
+// unmasked kernel is exactly the code without it).
+template <int GH, bool KM>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmVt, const __grid_constant__ CUtensorMap tmO,
@@ -145,11 +151,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kvh = (blockIdx.x - b * groups) / p.n_hsub;
   const int hsub = blockIdx.x - b * groups - kvh * p.n_hsub;
   const int h_first = kvh * p.G + hsub * GH;
-  const int vs = p.valid_start ? min(max(p.valid_start[b], 0), T) : 0;
+  const int Tk = p.Tk, qo = p.q_off;              // query t is key qo + t
+  const int vs = p.valid_start ? min(max(p.valid_start[b], 0), Tk) : 0;
   const int last_q = min(q0 + kBQ - 1, T - 1);
-  const int j_hi = last_q / kBK;
+  const int j_hi = (qo + last_q) / kBK;
   // lowest key any query of the tile sees (padding start; window start of the first query)
-  const int key_lo = p.window > 0 ? max(vs, q0 - p.window + 1) : vs;
+  const int key_lo = p.window > 0 ? max(vs, qo + q0 - p.window + 1) : vs;
   const int j_lo = min(key_lo / kBK, j_hi);      // an all-padding tile still runs one (masked) tile
   const int ntiles = j_hi - j_lo + 1;
   const int nslots = ntiles * GH;
@@ -199,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         mbar_arrive_expect_tx(&kv_full[st], C::K_BYTES + C::VT_BYTES);
-        tma_load_2d(sK + st * C::K_BYTES, &tmK, &kv_full[st], 0, (b * p.KV + kvh) * T + j * kBK);
+        tma_load_2d(sK + st * C::K_BYTES, &tmK, &kv_full[st], 0, (b * p.KV + kvh) * Tk + j * kBK);
         tma_load_2d(sVt + st * C::VT_BYTES, &tmVt, &kv_full[st], j * kBK, (b * p.KV + kvh) * kHD);
         tma_load_2d(sVt + st * C::VT_BYTES + C::VT_SUB, &tmVt, &kv_full[st], j * kBK + 64,
                     (b * p.KV + kvh) * kHD);
@@ -279,7 +286,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int grp = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;              // query row within the tile
     const int t = q0 + r;
-    const int row_lo = p.window > 0 ? max(vs, t - p.window + 1) : vs;   // this row's first visible key
+    const int tk = qo + t;                          // this row's own key index
+    const int row_lo = p.window > 0 ? max(vs, tk - p.window + 1) : vs;   // this row's first visible key
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float sl2 = p.scale_log2;
     float *red_max = reinterpret_cast<float *>(smem + C::OFF_RED);          // [2][2][128]
@@ -291,11 +299,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       l[h] = 0.f;
     }
     bool alive = true;
+    // visibility of this group's 64 keys under the caller's key mask (bit e =
+    // key k0 + e), read once per key tile and shared by its GH head slots
+    unsigned long long vis = ~0ull;
+    int vis_it = -1;
+    const uint8_t *kmask = KM ? p.key_mask + (long long)b * T : nullptr;
     for (int s = 0; s < nslots; ++s) {
       const int it = s / GH, h = s - it * GH, sb = s & 1;
       const int k0 = (j_lo + it) * kBK + grp * 64;  // first key of this group's half tile
+      if (KM && it != vis_it) {
+        vis = 0ull;
+#pragma unroll 8
+        for (int e = 0; e < 64; ++e)
+          if (k0 + e < T && __ldg(kmask + k0 + e)) vis |= 1ull << e;
+        vis_it = it;
+      }
       const bool ok = alive && __all_sync(0xffffffffu, mbar_wait_bounded(&s_full[sb], (s >> 1) & 1, abort_flag));
-      const bool need_mask = (k0 + 63 > q0) || (k0 < vs) || (p.window > 0 && k0 <= last_q - p.window);
+      const bool need_mask = KM || (k0 + 63 > qo + q0) || (k0 < vs) || (p.window > 0 && k0 <= qo + last_q - p.window);
       uint32_t sv[64];
       float mx = -INFINITY;
       if (ok) {
@@ -309,10 +329,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int q = 0; q < 8; ++q) mc[q] = -INFINITY;
         if (need_mask) {
-          const int hi = t - k0, lo = row_lo - k0;
+          const int hi = tk - k0, lo = row_lo - k0;
 #pragma unroll
           for (int e = 0; e < 64; ++e)
-            if (e <= hi && e >= lo) mc[e & 7] = fmaxf(mc[e & 7], __uint_as_float(sv[e]));
+            if (e <= hi && e >= lo && (!KM || ((vis >> e) & 1ull))) mc[e & 7] = fmaxf(mc[e & 7], __uint_as_float(sv[e]));
         } else {
 #pragma unroll
           for (int e = 0; e < 64; e += 2)
@@ -362,11 +382,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // eight partial sums
       if (need_mask) {
         // keys k0+e visible iff lo <= e <= hi (causal, padding and window limits)
-        const int hi = t - k0, lo = row_lo - k0;
+        const int hi = tk - k0, lo = row_lo - k0;
 #pragma unroll
         for (int e = 0; e < 64; e += 2) {
-          const float x0 = (e <= hi && e >= lo) ? fmaf(__uint_as_float(sv[e]), sl2, -mu) : -INFINITY;
-          const float x1 = (e + 1 <= hi && e + 1 >= lo) ? fmaf(__uint_as_float(sv[e + 1]), sl2, -mu) : -INFINITY;
+          const float x0 = (e <= hi && e >= lo && (!KM || ((vis >> e) & 1ull)))
+                               ? fmaf(__uint_as_float(sv[e]), sl2, -mu)
+                               : -INFINITY;
+          const float x1 = (e + 1 <= hi && e + 1 >= lo && (!KM || ((vis >> (e + 1)) & 1ull)))
+                               ? fmaf(__uint_as_float(sv[e + 1]), sl2, -mu)
+                               : -INFINITY;
           const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
           ps[e & 7] += p0;
           ps[(e + 1) & 7] += p1;
@@ -449,11 +473,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int GH>
-cudaError_t launch_gh(const AttnParams &a, const CUtensorMap &tq, const CUtensorMap &tk,
+template <int GH, bool KM>
+cudaError_t launch_ghk(const AttnParams &a, const CUtensorMap &tq, const CUtensorMap &tk,
                       const CUtensorMap &tv, const CUtensorMap &to, cudaStream_t st) {
   using C = AtCfg<GH>;
-  auto kern = attn_tc_kernel<GH>;
+  auto kern = attn_tc_kernel<GH, KM>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   AtParams p{};
@@ -465,6 +489,9 @@ cudaError_t launch_gh(const AttnParams &a, const CUtensorMap &tq, const CUtensor
   p.n_hsub = p.G / GH;
   p.scale_log2 = a.scale_log2;
   p.window = a.window;
+  p.key_mask = a.key_mask;
+  p.Tk = a.Tk > 0 ? a.Tk : a.T;
+  p.q_off = a.q_off;
   p.status = a.status;
   dim3 grid((unsigned)(a.B * a.KV * p.n_hsub), (unsigned)cdiv(a.T, kBQ), 1u);
   // as a programmatic dependent: CTAs set up barriers and TMEM while the
@@ -482,6 +509,12 @@ cudaError_t launch_gh(const AttnParams &a, const CUtensorMap &tq, const CUtensor
   return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, to, p);
 }
 
+template <int GH>
+cudaError_t launch_gh(const AttnParams &a, const CUtensorMap &tq, const CUtensorMap &tk,
+                      const CUtensorMap &tv, const CUtensorMap &to, cudaStream_t st) {
+  return a.key_mask ? launch_ghk<GH, true>(a, tq, tk, tv, to, st) : launch_ghk<GH, false>(a, tq, tk, tv, to, st);
+}
+
 }  // namespace
 
 bool attention_tc_supported(int hd, int H, int KV) {
@@ -493,9 +526,11 @@ cudaError_t launch_attention_tc(const AttnParams &a, cudaStream_t st) {
   if (!attention_tc_supported(a.hd, a.H, a.KV) || a.v_t == nullptr) return cudaErrorInvalidConfiguration;
   CUtensorMap tq, tk, tv, to;
   if (!make_tmap_f16(&tq, a.q, (uint64_t)a.B * a.H * a.T, kHD, kHD, kBQ)) return cudaErrorInvalidValue;
-  if (!make_tmap_f16(&tk, a.k, (uint64_t)a.B * a.KV * a.T, kHD, kHD, kBK)) return cudaErrorInvalidValue;
-  // V^T: rows are (b, kv head, dim), columns are keys; columns >= T read as zero
-  if (!make_tmap_f16(&tv, a.v_t, (uint64_t)a.B * a.KV * kHD, a.T, a.T_pad, kHD)) return cudaErrorInvalidValue;
+  const int Tk = a.Tk > 0 ? a.Tk : a.T;
+  if (Tk < a.T || a.q_off < 0 || a.q_off + a.T > Tk) return cudaErrorInvalidValue;
+  if (!make_tmap_f16(&tk, a.k, (uint64_t)a.B * a.KV * Tk, kHD, kHD, kBK)) return cudaErrorInvalidValue;
+  // V^T: rows are (b, kv head, dim), columns are keys; columns >= Tk read as zero
+  if (!make_tmap_f16(&tv, a.v_t, (uint64_t)a.B * a.KV * kHD, Tk, a.T_pad, kHD)) return cudaErrorInvalidValue;
   // output rows [B*T, H*hd]: a softmax warp's 32 rows x 32 columns per box
   if (!make_tmap_2d(&to, a.o, (uint64_t)a.B * a.T, (uint64_t)a.H * kHD, (uint64_t)a.H * kHD, 32, 32, false))
     return cudaErrorInvalidValue;

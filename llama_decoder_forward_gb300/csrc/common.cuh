@@ -137,6 +137,9 @@ struct AttnParams {
   int B, T, H, KV, hd;
   float scale_log2;       // log2(e) / sqrt(hd)
   int window;             // > 0: query t sees keys j > t - window only (sliding window)
+  const uint8_t *key_mask; // [B, T] or nullptr: key j of sequence b hidden where 0
+  int Tk;                 // keys per sequence (k: [B, KV, Tk, hd], v_t pitch T_pad >= Tk); 0: T
+  int q_off;              // key index of query 0 (queries are the last T of Tk keys); 0 with Tk = T
   int pdl;                // tcgen05 kernel: launch as a programmatic dependent of the preceding kernel
 };
 cudaError_t launch_flash_attention(const AttnParams &p, cudaStream_t stream);
@@ -161,5 +164,10 @@ cudaError_t launch_scale_cols_copy(const bf16 *src, const bf16 *norm_w, long lon
 cudaError_t launch_interleave_gate_up(const bf16 *wg, const bf16 *wu, const bf16 *norm_w, int I,
                                       int d, f16 *dst, cudaStream_t stream);
 cudaError_t launch_rope_table(int max_pos, int hd, float theta, float2 *table, cudaStream_t stream);
+// One layer's cached keys/values plus the T new ones as left-padded f16 sequences of Tk
+// keys (hd 64): K [B, KV, Tk, 64], V^T [B, KV, 64, Tk_pad]; vs[b] = first visible slot.
+cudaError_t launch_gather_cache_kv(const bf16 *kc, const bf16 *vc, int S_max, const int *cache_len, int lmax,
+                                   const f16 *kn, const f16 *vtn, int T_pad, int B, int KV, int T, int Tk,
+                                   int Tk_pad, f16 *Kc, f16 *Vtc, int *vs, cudaStream_t stream);
 
 }  // namespace smol

@@ -53,6 +53,7 @@ PackLayout pack_layout(const smol_config *c, int n_layers, int with_embed) {
 
 struct WsLayout {
   size_t status, x, h, q, k, v, o, a, ssq_a, ssq_b;
+  size_t kc, vtc, vs;        // prefill on top of a cache only
   size_t total;
 };
 
@@ -76,6 +77,23 @@ WsLayout ws_layout(const smol_config *c, int B, int T) {
   W.a = o; o = align_up(o + M * I * 2, 1024);
   W.ssq_a = o; o = align_up(o + M * 4, 1024);
   W.ssq_b = o; o = align_up(o + M * 4, 1024);
+  W.total = o;
+  return W;
+}
+
+// Cache lengths accepted by prefill on top of a cache: positions L + t stay
+// below max_pos and the cached rows fit the S_max slots.
+int cache_lmax(const smol_config *c, int T, int S_max) { return min(S_max, c->max_pos - T); }
+
+// The block workspace plus one layer's left-padded keys/values over Tk = lmax + T.
+WsLayout ws_layout_cache(const smol_config *c, int B, int T, int S_max) {
+  WsLayout W = ws_layout(c, B, T);
+  const long long Tk = (long long)cache_lmax(c, T, S_max) + T;
+  const size_t KV = c->n_kv_heads, hd = c->head_dim;
+  size_t o = W.total;
+  W.kc = o; o = align_up(o + (size_t)B * KV * Tk * hd * 2, 1024);
+  W.vtc = o; o = align_up(o + (size_t)B * KV * hd * t_pad((int)Tk) * 2, 1024);
+  W.vs = o; o = align_up(o + (size_t)B * 4, 1024);
   W.total = o;
   return W;
 }
@@ -169,8 +187,17 @@ struct BlockIO {
 // One decoder block on M = B*T rows.  ssq_a holds the per-row sum of squares
 // of the input; the output's sum of squares is accumulated into ssq_a (which
 // is cleared in between).  The block-internal residual h is kept in f16.
+// Prefill on top of a KV cache: this layer's cache slices and where the
+// gathered keys go.
+struct CacheCtx {
+  const bf16 *k_cache, *v_cache;   // this layer: [B, KV, S_max, hd]
+  const int32_t *cache_len;        // [B] device
+  int S_max, lmax;
+};
+
 int run_block(const smol_config *c, const void *packed, int layer, const BlockIO &io, int B, int T,
-              const int32_t *valid_start, const WsLayout &W, uint8_t *ws, int sms, cudaStream_t st) {
+              const int32_t *valid_start, const uint8_t *key_mask, const WsLayout &W, uint8_t *ws, int sms,
+              cudaStream_t st, const CacheCtx *cc = nullptr) {
   const long long M = (long long)B * T;
   const int d = c->hidden, H = c->n_heads, KV = c->n_kv_heads, hd = c->head_dim, I = c->intermediate;
   const LayerPtrs lp = layer_ptrs(c, packed, layer);
@@ -203,6 +230,10 @@ int run_block(const smol_config *c, const void *packed, int layer, const BlockIO
                ? reinterpret_cast<const float2 *>(static_cast<const uint8_t *>(packed) + PL.rope_off)
                : nullptr;
   p.valid_start = valid_start; p.max_pos = c->max_pos; p.status = status;
+  if (cc) {                        // new token t of sequence b sits at position cache_len[b] + t
+    p.pos_add = cc->cache_len;
+    p.pos_limit = cc->lmax;
+  }
   // every kernel of the block is a programmatic dependent of the one before
   // (each waits for it with griddepcontrol.wait before touching its data)
   p.pdl = 1;
@@ -214,9 +245,28 @@ int run_block(const smol_config *c, const void *packed, int layer, const BlockIO
   ap.B = B; ap.T = T; ap.H = H; ap.KV = KV; ap.hd = hd;
   ap.scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
   ap.window = layer_window(c, layer);
+  ap.key_mask = key_mask;
   ap.status = status;
   ap.pdl = 1;
-  if (tc_attn) {
+  if (cc) {
+    // the cached slice and the new keys as one left-padded sequence of Tk keys;
+    // the queries are its last T
+    const int Tk = cc->lmax + T;
+    f16 *kc = reinterpret_cast<f16 *>(ws + W.kc);
+    f16 *vtc = reinterpret_cast<f16 *>(ws + W.vtc);
+    int *vsb = reinterpret_cast<int *>(ws + W.vs);
+    LAUNCH(launch_gather_cache_kv(cc->k_cache, cc->v_cache, cc->S_max, cc->cache_len, cc->lmax, k, v,
+                                  (int)t_pad(T), B, KV, T, Tk, (int)t_pad(Tk), kc, vtc, vsb, st));
+    ap.k = kc;
+    ap.v = nullptr;
+    ap.v_t = vtc;
+    ap.T_pad = (int)t_pad(Tk);
+    ap.Tk = Tk;
+    ap.q_off = Tk - T;
+    ap.valid_start = vsb;
+    ap.pdl = 0;                    // the gather kernel in between is not a programmatic launch
+    LAUNCH_K(SMOL_K_ATTN, st, launch_attention_tc(ap, st));
+  } else if (tc_attn) {
     ap.v = nullptr;
     ap.v_t = v;
     ap.T_pad = (int)t_pad(T);
@@ -321,9 +371,11 @@ SMOL_API size_t smol_workspace_bytes(const smol_config *cfg, int op, int B, int 
   return ws_layout(cfg, B, T).total;
 }
 
-SMOL_API int smol_block_forward(const smol_config *cfg, const void *packed, int layer, const void *x,
-                                void *out, int act_dtype, int B, int T, const int32_t *valid_start,
-                                void *k_out, void *v_out, void *ws, size_t ws_bytes, void *stream) {
+namespace {
+
+int block_forward_impl(const smol_config *cfg, const void *packed, int layer, const void *x, void *out,
+                       int act_dtype, int B, int T, const int32_t *valid_start, const uint8_t *key_mask,
+                       void *k_out, void *v_out, void *ws, size_t ws_bytes, void *stream) {
   g_launches = 0;
   int rc = check_cfg(cfg);
   if (rc) return rc;
@@ -359,12 +411,12 @@ SMOL_API int smol_block_forward(const smol_config *cfg, const void *packed, int 
     io.out16 = out;
     io.out16_is_f16 = 0;
   }
-  return run_block(cfg, packed, layer, io, B, T, valid_start, W, wsb, sms, st);
+  return run_block(cfg, packed, layer, io, B, T, valid_start, key_mask, W, wsb, sms, st);
 }
 
-SMOL_API int smol_model_forward(const smol_config *cfg, const void *packed, const int32_t *ids, int B,
-                                int T, const int32_t *valid_start, void *logits, void *ws,
-                                size_t ws_bytes, void *stream) {
+int model_forward_impl(const smol_config *cfg, const void *packed, const int32_t *ids, int B, int T,
+                       const int32_t *valid_start, const uint8_t *key_mask, void *logits, void *ws,
+                       size_t ws_bytes, void *stream) {
   g_launches = 0;
   int rc = check_cfg(cfg);
   if (rc) return rc;
@@ -396,7 +448,7 @@ SMOL_API int smol_model_forward(const smol_config *cfg, const void *packed, cons
   io.out16 = x;
   io.out16_is_f16 = 1;
   for (int l = 0; l < cfg->n_layers; ++l) {
-    rc = run_block(cfg, packed, l, io, B, T, valid_start, W, wsb, sms, st);
+    rc = run_block(cfg, packed, l, io, B, T, valid_start, key_mask, W, wsb, sms, st);
     if (rc) return rc;
   }
   GemmParams p{};
@@ -408,6 +460,42 @@ SMOL_API int smol_model_forward(const smol_config *cfg, const void *packed, cons
   LAUNCH_K(SMOL_K_HEAD, st, launch_gemm(kEpiScale, gemm_pick_bn(kEpiScale, cfg->vocab, cfg->head_dim), x,
                      pk + L.head_off, p, sms, st));
   return SMOL_OK;
+}
+
+}  // namespace
+
+SMOL_API int smol_block_forward(const smol_config *cfg, const void *packed, int layer, const void *x,
+                                void *out, int act_dtype, int B, int T, const int32_t *valid_start,
+                                void *k_out, void *v_out, void *ws, size_t ws_bytes, void *stream) {
+  return block_forward_impl(cfg, packed, layer, x, out, act_dtype, B, T, valid_start, nullptr, k_out, v_out,
+                            ws, ws_bytes, stream);
+}
+
+SMOL_API int smol_block_forward_masked(const smol_config *cfg, const void *packed, int layer, const void *x,
+                                       void *out, int act_dtype, int B, int T, const uint8_t *key_mask,
+                                       void *k_out, void *v_out, void *ws, size_t ws_bytes, void *stream) {
+  if (!key_mask) {
+    g_launches = 0;
+    return SMOL_ERR_INVALID_ARG;
+  }
+  return block_forward_impl(cfg, packed, layer, x, out, act_dtype, B, T, nullptr, key_mask, k_out, v_out,
+                            ws, ws_bytes, stream);
+}
+
+SMOL_API int smol_model_forward(const smol_config *cfg, const void *packed, const int32_t *ids, int B,
+                                int T, const int32_t *valid_start, void *logits, void *ws,
+                                size_t ws_bytes, void *stream) {
+  return model_forward_impl(cfg, packed, ids, B, T, valid_start, nullptr, logits, ws, ws_bytes, stream);
+}
+
+SMOL_API int smol_model_forward_masked(const smol_config *cfg, const void *packed, const int32_t *ids, int B,
+                                       int T, const uint8_t *key_mask, void *logits, void *ws,
+                                       size_t ws_bytes, void *stream) {
+  if (!key_mask) {
+    g_launches = 0;
+    return SMOL_ERR_INVALID_ARG;
+  }
+  return model_forward_impl(cfg, packed, ids, B, T, nullptr, key_mask, logits, ws, ws_bytes, stream);
 }
 
 SMOL_API int smol_decode_step(const smol_config *cfg, const void *packed, const int32_t *ids,
@@ -453,6 +541,69 @@ SMOL_API int smol_decode_step(const smol_config *cfg, const void *packed, const 
   cudaError_t e = run_decode(a, ws, sms, static_cast<cudaStream_t>(stream), &n);
   g_launches = n;
   if (e != cudaSuccess) return cuda_fail(e);
+  return SMOL_OK;
+}
+
+SMOL_API size_t smol_prefill_cache_workspace_bytes(const smol_config *cfg, int B, int T, int S_max) {
+  if (check_cfg(cfg) != SMOL_OK || B <= 0 || T <= 0 || S_max <= 0 || T >= cfg->max_pos) return 0;
+  if (!attention_tc_supported(cfg->head_dim, cfg->n_heads, cfg->n_kv_heads)) return 0;
+  return ws_layout_cache(cfg, B, T, S_max).total;
+}
+
+SMOL_API int smol_prefill_with_cache(const smol_config *cfg, const void *packed, const int32_t *ids, int B, int T,
+                                     const int32_t *cache_len, const void *k_cache, const void *v_cache,
+                                     int S_max, void *k_new, void *v_new, void *logits, void *ws,
+                                     size_t ws_bytes, void *stream) {
+  g_launches = 0;
+  int rc = check_cfg(cfg);
+  if (rc) return rc;
+  if (!packed || !ids || !cache_len || !k_cache || !v_cache || !k_new || !v_new || !logits || !ws || B <= 0 ||
+      T <= 0 || S_max <= 0 || cfg->vocab <= 0)
+    return SMOL_ERR_INVALID_ARG;
+  if (!attention_tc_supported(cfg->head_dim, cfg->n_heads, cfg->n_kv_heads)) return SMOL_ERR_UNSUPPORTED_SHAPE;
+  if ((long long)B * T > 0x7fffffffLL) return SMOL_ERR_UNSUPPORTED_SHAPE;
+  if (T >= cfg->max_pos) return SMOL_ERR_TOO_LONG;
+  if (!aligned16(packed) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) ||
+      !aligned16(v_new) || !aligned16(logits) || !aligned16(ws) || (reinterpret_cast<uintptr_t>(ids) & 3u) ||
+      (reinterpret_cast<uintptr_t>(cache_len) & 3u))
+    return SMOL_ERR_MISALIGNED;
+  const WsLayout W = ws_layout_cache(cfg, B, T, S_max);
+  if (ws_bytes < W.total) return SMOL_ERR_WORKSPACE;
+  int sms;
+  if ((rc = device_sms(&sms))) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t *wsb = static_cast<uint8_t *>(ws);
+  const long long M = (long long)B * T;
+  const PackLayout L = pack_layout(cfg, cfg->n_layers, 1);
+  const uint8_t *pk = static_cast<const uint8_t *>(packed);
+  f16 *x = reinterpret_cast<f16 *>(wsb + W.x);
+  float *ssq_a = reinterpret_cast<float *>(wsb + W.ssq_a);
+  LAUNCH_K(SMOL_K_EMBED, st, launch_embed_rows(ids, reinterpret_cast<const bf16 *>(pk + L.embed_off), cfg->vocab,
+                           cfg->hidden, M, x, nullptr, ssq_a, st));
+  const size_t layer_cache = (size_t)B * cfg->n_kv_heads * S_max * cfg->head_dim;
+  const size_t layer_new = (size_t)B * cfg->n_kv_heads * T * cfg->head_dim;
+  for (int l = 0; l < cfg->n_layers; ++l) {
+    BlockIO io{};
+    io.x16 = x;
+    io.resid_f16 = x;
+    io.out16 = x;
+    io.out16_is_f16 = 1;
+    io.k_bf = static_cast<bf16 *>(k_new) + l * layer_new;
+    io.v_bf = static_cast<bf16 *>(v_new) + l * layer_new;
+    CacheCtx cc{static_cast<const bf16 *>(k_cache) + l * layer_cache,
+                static_cast<const bf16 *>(v_cache) + l * layer_cache, cache_len, S_max,
+                cache_lmax(cfg, T, S_max)};
+    rc = run_block(cfg, packed, l, io, B, T, nullptr, nullptr, W, wsb, sms, st, &cc);
+    if (rc) return rc;
+  }
+  GemmParams p{};
+  p.M = (int)M; p.N = cfg->vocab; p.K = cfg->hidden;
+  p.out = logits; p.out_is_f16 = 0; p.ldo = cfg->vocab;
+  p.ssq_in = ssq_a; p.inv_dim = 1.0f / cfg->hidden; p.eps = cfg->rms_eps;
+  p.status = reinterpret_cast<int *>(wsb + W.status);
+  p.pdl = 1;
+  LAUNCH_K(SMOL_K_HEAD, st, launch_gemm(kEpiScale, gemm_pick_bn(kEpiScale, cfg->vocab, cfg->head_dim), x,
+                     pk + L.head_off, p, sms, st));
   return SMOL_OK;
 }
 

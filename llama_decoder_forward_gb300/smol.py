@@ -57,6 +57,10 @@ _SIGS = {
                                    c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "smol_model_forward": (c_int, [_CFG, c_void_p, c_void_p, c_int, c_int, c_void_p, c_void_p,
                                    c_void_p, c_size_t, c_void_p]),
+    "smol_block_forward_masked": (c_int, [_CFG, c_void_p, c_int, c_void_p, c_void_p, c_int, c_int, c_int,
+                                          c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "smol_model_forward_masked": (c_int, [_CFG, c_void_p, c_void_p, c_int, c_int, c_void_p, c_void_p,
+                                          c_void_p, c_size_t, c_void_p]),
     "smol_decode_step": (c_int, [_CFG, c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_int,
                                  c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "smol_workspace_status": (c_int, [c_void_p, c_void_p]),
@@ -64,6 +68,10 @@ _SIGS = {
     "smol_status_string": (ctypes.c_char_p, [c_int]),
     "smol_decode_step_noalloc": (c_int, [_CFG, c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p,
                                          c_int, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "smol_decode_noalloc_status": (c_int, [c_void_p]),
+    "smol_prefill_cache_workspace_bytes": (c_size_t, [_CFG, c_int, c_int, c_int]),
+    "smol_prefill_with_cache": (c_int, [_CFG, c_void_p, c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p,
+                                        c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "smol_sample": (c_int, [c_void_p, c_int, c_int, ctypes.c_longlong, c_float, c_int, c_float, c_int,
                             c_void_p, c_void_p, c_void_p]),
     "smol_profile_begin": (c_int, [ctypes.c_uint, c_int]),
@@ -203,6 +211,37 @@ def block_forward(cfg: Config, packed: torch.Tensor, layer: int, x: torch.Tensor
                                    _stream(stream)), "smol_block_forward")
 
 
+def block_forward_masked(cfg: Config, packed: torch.Tensor, layer: int, x: torch.Tensor, out: torch.Tensor,
+                         ws: torch.Tensor, key_mask: torch.Tensor, k_out=None, v_out=None, stream=None) -> None:
+    """block_forward with a key mask (uint8 [B, T], nonzero = visible) in place of left padding."""
+    B, T, _ = x.shape
+    if x.dtype not in (torch.bfloat16, torch.float32) or out.dtype != x.dtype:
+        raise ValueError("x and out must both be bf16 or both fp32")
+    _dev(x, x.dtype, "x")
+    _dev(out, x.dtype, "out")
+    _dev(key_mask, torch.uint8, "key_mask")
+    if tuple(key_mask.shape) != (B, T):
+        raise ValueError("key_mask must be [B, T]")
+    act = ACT_F32 if x.dtype == torch.float32 else ACT_BF16
+    _check(_lib.smol_block_forward_masked(ctypes.byref(cfg), _p(packed), layer, _p(x), _p(out), act, B, T,
+                                          _p(key_mask), _p(k_out), _p(v_out), _p(ws), ws.numel(),
+                                          _stream(stream)), "smol_block_forward_masked")
+
+
+def model_forward_masked(cfg: Config, packed: torch.Tensor, ids: torch.Tensor, logits: torch.Tensor,
+                         ws: torch.Tensor, key_mask: torch.Tensor, stream=None) -> None:
+    """model_forward with a key mask (uint8 [B, T], nonzero = visible) in place of left padding."""
+    B, T = ids.shape
+    _dev(ids, torch.int32, "ids")
+    _dev(logits, torch.bfloat16, "logits")
+    _dev(key_mask, torch.uint8, "key_mask")
+    if tuple(key_mask.shape) != (B, T):
+        raise ValueError("key_mask must be [B, T]")
+    _check(_lib.smol_model_forward_masked(ctypes.byref(cfg), _p(packed), _p(ids), B, T, _p(key_mask),
+                                          _p(logits), _p(ws), ws.numel(), _stream(stream)),
+           "smol_model_forward_masked")
+
+
 def model_forward(cfg: Config, packed: torch.Tensor, ids: torch.Tensor, logits: torch.Tensor,
                   ws: torch.Tensor, valid_start=None, stream=None) -> None:
     B, T = ids.shape
@@ -211,6 +250,29 @@ def model_forward(cfg: Config, packed: torch.Tensor, ids: torch.Tensor, logits: 
     _check(_lib.smol_model_forward(ctypes.byref(cfg), _p(packed), _p(ids), B, T, _p(valid_start),
                                    _p(logits), _p(ws), ws.numel(), _stream(stream)),
            "smol_model_forward")
+
+
+def prefill_cache_workspace(cfg: Config, B: int, T: int, S_max: int, device="cuda") -> torch.Tensor:
+    n = _lib.smol_prefill_cache_workspace_bytes(ctypes.byref(cfg), B, T, S_max)
+    if n == 0:
+        raise SmolError(ERR_UNSUPPORTED_SHAPE, "smol_prefill_cache_workspace_bytes")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def prefill_with_cache(cfg: Config, packed: torch.Tensor, ids: torch.Tensor, cache_len: torch.Tensor,
+                       k_cache: torch.Tensor, v_cache: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                       logits: torch.Tensor, ws: torch.Tensor, stream=None) -> None:
+    """T new tokens per sequence on top of a KV cache (chunked prefill)."""
+    B, T = ids.shape
+    S_max = k_cache.shape[3]
+    _dev(ids, torch.int32, "ids")
+    _dev(cache_len, torch.int32, "cache_len")
+    for name, t in (("k_cache", k_cache), ("v_cache", v_cache), ("k_new", k_new), ("v_new", v_new),
+                    ("logits", logits)):
+        _dev(t, torch.bfloat16, name)
+    _check(_lib.smol_prefill_with_cache(ctypes.byref(cfg), _p(packed), _p(ids), B, T, _p(cache_len),
+                                        _p(k_cache), _p(v_cache), S_max, _p(k_new), _p(v_new), _p(logits),
+                                        _p(ws), ws.numel(), _stream(stream)), "smol_prefill_with_cache")
 
 
 def decode_step(cfg: Config, packed: torch.Tensor, ids: torch.Tensor, cache_len: torch.Tensor,
@@ -259,6 +321,11 @@ def sample(logits: torch.Tensor, next_ids: torch.Tensor, uniform: Optional[torch
     _check(_lib.smol_sample(_p(logits), B, V, logits.stride(0), float(temperature), int(top_k),
                             float(top_p), int(bool(do_sample)), _p(uniform), _p(next_ids),
                             _stream(stream)), "smol_sample")
+
+
+def decode_noalloc_status(stream=None) -> int:
+    """Synchronising read (and reset) of the status word of decode_step_noalloc."""
+    return _lib.smol_decode_noalloc_status(_stream(stream))
 
 
 def workspace_status(ws: torch.Tensor, stream=None) -> int:

@@ -85,6 +85,8 @@ def test_size_queries(smol):
     M = 8 * 2048
     assert ws >= M * (2 * d + 2 * H * hd + 2 * KV * hd + I) * 2 + 2 * M * 4
     assert smol.workspace_bytes(cfg, smol.OP_DECODE, 64, 1) > 0
+    # the decode batch of 64 fits the no-alloc variant's fixed 8 MiB scratch
+    assert smol.workspace_bytes(cfg, smol.OP_DECODE, 64, 1) <= 8 << 20
     assert smol.workspace_bytes(cfg, 99, 8, 2048) == 0
     assert smol.workspace_bytes(_cfg(smol, head_dim=96, hidden=864), smol.OP_BLOCK, 1, 1) == 0
 
@@ -124,6 +126,33 @@ def test_per_block_variant_arrays(smol):
     bad = _cfg(smol, sliding_window=[-5] + [0] * 29)
     assert smol.raw.smol_block_forward(ctypes.byref(bad), f, 0, f, f, 0, 1, 8, None, None, None, f,
                                        1 << 40, None) == -1
+
+
+def test_masked_forward_needs_a_mask(smol):
+    cfg = _cfg(smol)
+    f = ctypes.c_void_p(0x10000)
+    big = 1 << 40
+    assert smol.raw.smol_block_forward_masked(ctypes.byref(cfg), f, 0, f, f, 0, 1, 8, None, None, None, f,
+                                              big, None) == -1
+    assert smol.raw.smol_model_forward_masked(ctypes.byref(cfg), f, f, 1, 8, None, f, f, big, None) == -1
+    assert smol.raw.smol_block_forward_masked(ctypes.byref(cfg), f, 0, f, f, 0, 1, 8193, f, None, None, f,
+                                              big, None) == -4
+
+
+def test_prefill_with_cache_argument_errors(smol):
+    cfg = _cfg(smol)
+    f = ctypes.c_void_p(0x10000)
+    big = 1 << 40
+    pwc = smol.raw.smol_prefill_with_cache
+    assert pwc(ctypes.byref(cfg), f, f, 2, 8, None, f, f, 64, f, f, f, f, big, None) == -1     # cache_len
+    assert pwc(ctypes.byref(cfg), f, f, 2, 8, f, f, f, 0, f, f, f, f, big, None) == -1        # S_max
+    assert pwc(ctypes.byref(cfg), f, f, 2, 8192, f, f, f, 64, f, f, f, f, big, None) == -4    # T >= max_pos
+    assert pwc(ctypes.byref(cfg), f, f, 2, 8, f, f, f, 64, f, f, f, f, 16, None) == -5        # workspace
+    hd128 = _cfg(smol, hidden=1152, head_dim=128)
+    assert pwc(ctypes.byref(hd128), f, f, 2, 8, f, f, f, 64, f, f, f, f, big, None) == -2
+    assert smol.raw.smol_prefill_cache_workspace_bytes(ctypes.byref(cfg), 2, 8, 64) > \
+        smol.workspace_bytes(cfg, smol.OP_MODEL, 2, 8)
+    assert smol.last_launch_count() == 0
 
 
 def test_sample_argument_errors(smol):

@@ -377,3 +377,101 @@ def test_sample_after_decode_step(S):
     S.decode_step(cfg, packed, dev.ids, dev.lengths, dev.k_cache, dev.v_cache, k_new, v_new, logits, ws)
     u = torch.tensor([0.1, 0.3, 0.5, 0.7, 0.9])
     _check_sample(S, logits.cpu(), u, temperature=0.8, top_k=20, top_p=0.9)
+
+
+# ---------------------------------------------------------------- additive key mask
+# ("model.py" (SmolLM2-135M) section 4: attention_mask of 0 / -inf over the keys)
+
+def _key_mask(B, T, seed, keep=0.6):
+    g = torch.Generator().manual_seed(seed)
+    m = (torch.rand(B, T, generator=g) < keep).to(torch.uint8)
+    m[:, 1::97] = 0                                   # hidden keys at tile-crossing strides
+    return m
+
+
+@pytest.mark.parametrize("wl_name,B,T,layer_kw", [
+    ("smollm2_block_b1_t128", 2, 300, dict()),                                   # tcgen05, G = 3
+    ("smollm2_block_b1_t128", 1, 257, dict(sliding_window=(90,))),               # mask + window
+    ("smollm3_4blocks_b4_t4096", 2, 130, dict()),                                # hd 128 flash path
+])
+def test_block_key_mask(S, wl_name, B, T, layer_kw):
+    wl = W[wl_name].scaled(B=B, T=T, n_layers=1, **layer_kw)
+    inp = synth.generate(wl, seed=60 + T)
+    mask = _key_mask(B, T, 61 + T)
+    mask[0, :5] = 0                                   # the first rows of sequence 0 see no key
+    dev = to_device(inp)
+    cfg = S.config_of(wl)
+    packed = S.prepare_weights(cfg, dev.layers)
+    ws = S.alloc_workspace(cfg, S.OP_BLOCK, B, T)
+    x = dev.x.float().contiguous()
+    out = torch.empty_like(x)
+    S.block_forward_masked(cfg, packed, 0, x, out, ws, mask.cuda())
+    assert S.workspace_status(ws) == S.OK
+    torch.cuda.synchronize()
+    ref = O.block_forward(oracle_config(wl), oracle_layers(inp)[0], np32(inp.x), key_mask=mask.numpy().astype(bool))
+    got = out.cpu().numpy()
+    assert np.all(np.isfinite(got))
+    err = rel_max_err(got, ref)
+    print(f"key mask block: rel max err {err:.3e}")
+    assert err <= BLOCK_REL_TOL
+
+
+def test_model_key_mask(S):
+    wl = W["smollm2_model_b8_t2048"].scaled(B=2, T=150, n_layers=2, vocab=1024)
+    inp = synth.generate(wl, seed=62)
+    mask = _key_mask(2, 150, 63)
+    mask[:, 0] = 1
+    dev = to_device(inp)
+    cfg = S.config_of(wl)
+    packed = S.prepare_weights(cfg, dev.layers, dev.embed, dev.final_norm)
+    ws = S.alloc_workspace(cfg, S.OP_MODEL, 2, 150)
+    logits = torch.empty(2, 150, 1024, dtype=torch.bfloat16, device="cuda")
+    S.model_forward_masked(cfg, packed, dev.ids, logits, ws, mask.cuda())
+    assert S.workspace_status(ws) == S.OK
+    ref = O.model_forward(oracle_config(wl), oracle_layers(inp), np32(inp.embed), np32(inp.final_norm),
+                          inp.ids.numpy().astype(np.int64), key_mask=mask.numpy().astype(bool))
+    got = np32(logits)
+    cos, mabs = cosine(got, ref), max_abs(got, ref)
+    print(f"key mask model: cos {cos:.7f} max abs {mabs:.3e}")
+    assert cos >= LOGITS_COS_MIN and mabs <= LOGITS_MAX_ABS, (cos, mabs)
+
+
+# ---------------------------------------------------------------- prefill on top of a cache
+# ("model.py" (SmolLM2-135M) section 4 with past_key_value, section 7 with past_key_values)
+
+def run_prefill_cache_case(S, wl, lengths, T, seed=0):
+    wl = wl.scaled(B=len(lengths))
+    inp = synth.generate(wl, seed=seed)
+    g = torch.Generator().manual_seed(seed + 1)
+    ids = torch.randint(0, wl.vocab, (wl.B, T), generator=g).to(torch.int32)
+    lens = torch.tensor(lengths, dtype=torch.int32)
+    dev = to_device(inp)
+    cfg = S.config_of(wl)
+    packed = S.prepare_weights(cfg, dev.layers, dev.embed, dev.final_norm)
+    ws = S.prefill_cache_workspace(cfg, wl.B, T, wl.s_max)
+    L, B, KV, hd = wl.n_layers, wl.B, wl.n_kv_heads, wl.head_dim
+    k_new = torch.empty(L, B, KV, T, hd, dtype=torch.bfloat16, device="cuda")
+    v_new = torch.empty_like(k_new)
+    logits = torch.empty(B, T, wl.vocab, dtype=torch.bfloat16, device="cuda")
+    S.prefill_with_cache(cfg, packed, ids.cuda(), lens.cuda(), dev.k_cache, dev.v_cache, k_new, v_new, logits, ws)
+    assert S.workspace_status(ws) == S.OK
+    ref, kr, vr = O.prefill_with_cache(oracle_config(wl), oracle_layers(inp), np32(inp.embed), np32(inp.final_norm),
+                                       ids.numpy().astype(np.int64), np.asarray(lengths), np32(inp.k_cache),
+                                       np32(inp.v_cache))
+    got = np32(logits)
+    cos, mabs = cosine(got, ref), max_abs(got, ref)
+    ek, ev = rel_max_err_bf16_out(np32(k_new), kr), rel_max_err_bf16_out(np32(v_new), vr)
+    print(f"prefill with cache: cos {cos:.6f} max abs {mabs:.3e} k {ek:.3e} v {ev:.3e}")
+    assert cos >= LOGITS_COS_MIN and mabs <= LOGITS_MAX_ABS, (cos, mabs)
+    assert ek <= BLOCK_REL_TOL and ev <= BLOCK_REL_TOL, (ek, ev)
+
+
+def test_prefill_with_cache_ragged(S):
+    wl = W["smollm2_decode_b64_cache4096"].scaled(n_layers=2, s_max=300, vocab=512)
+    run_prefill_cache_case(S, wl, [0, 1, 130, 300], T=37, seed=70)
+
+
+def test_prefill_with_cache_long_chunk_nope_window(S):
+    wl = W["smollm2_decode_b64_cache4096"].scaled(n_layers=2, s_max=200, vocab=512, no_rope_layers=(1, 0),
+                                                  sliding_window=(0, 150))
+    run_prefill_cache_case(S, wl, [5, 200], T=260, seed=71)
