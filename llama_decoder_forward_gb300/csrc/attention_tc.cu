@@ -9,25 +9,38 @@
 // 3B checkpoints leave off") also hides keys j <= t - w: the CTA starts at the
 // tile of its first query's window and masks per row.  An optional key mask
 // (the additive 0 / -inf attention_mask of "model.py" section 4, as bytes)
-// hides further keys; every tile then takes the masked path.
+// hides further keys; every tile then takes the masked path.  With a KV cache
+// in front (prefill on top of a cache), query t is key q_off + t of a longer
+// key sequence.
 //
-// One CTA owns (sequence b, kv head, a tile of 128 query tokens) and the GH
-// query heads of that kv head.  Each K tile [128 keys x 64] and V^T tile
-// [64 x 128 keys] is loaded once by TMA into shared memory and serves all GH
-// heads: K/V are never expanded per query head.  Per (kv tile, head):
-//   S = Q_h K^T        tcgen05.mma, M=128 N=128 K=64, fp32 in TMEM (two S buffers,
-//                      so the MMA for the next head runs while this one's softmax does)
-//   P = exp2(S*c - m)  eight softmax warps, one query row per thread per half tile; P is
-//                      written as packed f16 into the S buffer's own TMEM columns
-//   O_h += P V         tcgen05.mma with A (= P) read from TMEM, M=128 N=64 K=128, fp32
-//                      accumulator in TMEM; shared memory only feeds Q, K and V^T
+// One CTA owns (sequence b, kv head, a tile of 128 query tokens) and GH query
+// heads of that kv head.  Each K tile [128 keys x 64] and V^T tile [64 x 128
+// keys] is loaded once by TMA into shared memory and serves all GH heads: K/V
+// are never expanded per query head.  Per (kv tile, head):
+//   S = Q_h K^T        tcgen05.mma, M=128 N=128 K=64, fp32 in TMEM (two S buffers
+//                      taken in turn by the heads)
+//   P = exp2(S*c - m)  a softmax warpgroup, one query row per thread,
+//                      all 128 keys of the tile (no exchange between warps); P is
+//                      written as f16 into the head's shared-memory P buffer, in the
+//                      swizzled K-major layout of an MMA operand, and the S buffer is
+//                      released as soon as it has been read
+//   O_h += P [V | 1]   tcgen05.mma, M=128 N=80 K=128: the 64 value columns plus a
+//                      constant row of ones appended to V^T, so column 64 of the
+//                      accumulator is the row sum of the very f16 P that weights V
+// The tensor pipe is fed by three issuing warps: an issue of tcgen05.mma takes
+// a fixed ~110 cycles of its issuing thread whatever N is (measured), so one
+// thread issuing all twelve small MMAs of a (tile, head) would leave the pipe
+// idle; several warps' MMAs run concurrently.  Warp 1 issues every S MMA, warps
+// 2 and 3 the P V MMAs of the even and odd heads (a head's accumulator is only
+// ever written from one thread, so their order is program order).
 // The running max is updated lazily: O_h is rescaled in TMEM only when a row's
 // max grows by more than 2^8 (otherwise P may exceed 1 by up to 256, exact in
 // the fp32 sums and within f16 range), the FlashAttention-4 idea.
-// Warp 0 issues TMA, warp 1 allocates TMEM and one lane issues every MMA,
-// warps 2..9 (two groups of four, each taking half of every tile's keys) do
-// the softmax and the final normalisation.  All waits are
-// bounded (status word + abort flag, copies and MMAs drained before exit).
+// Warp 0 issues TMA (and, with a key mask, turns the tile's mask bytes into
+// bit words).  Warps 4.. form two softmax warpgroups (one when GH = 1) that
+// take the (tile, head) slots in turn; a head's running row max passes from
+// one to the other through shared memory.  All waits are bounded (status
+// word + abort flag, copies and MMAs drained before exit).
 #include <math.h>
 
 #include "common.cuh"
@@ -40,35 +53,41 @@ namespace {
 constexpr int kBQ = 128;      // query rows per tile (UMMA M)
 constexpr int kBK = 128;      // keys per KV tile
 constexpr int kHD = 64;
-constexpr int kThreads = 320;   // producer, MMA, two softmax warpgroups
+constexpr int kNO = 80;       // accumulator columns per head: 64 value dims, the row sum, 15 zero
+constexpr int kNST = 2;       // K/V stages
+constexpr int kTmemS = 256;   // S buffers at TMEM columns 256 and 384
 
 template <int GH>
 struct AtCfg {
-  static constexpr int Q_BYTES = kBQ * kHD * 2;         // one head: [128][64] f16
+  static constexpr int NG = GH == 1 ? 1 : 2;            // softmax warpgroups, taking the slots in turn
+  static constexpr int THREADS = 128 * (1 + NG);        // one control warpgroup + NG softmax warpgroups
+  static constexpr int Q_BYTES = kBQ * kHD * 2;         // one head: [128 rows][64] f16
   static constexpr int K_BYTES = kBK * kHD * 2;         // [128 keys][64]
-  static constexpr int VT_SUB = kHD * 64 * 2;           // [64 dims][64 keys]
-  static constexpr int VT_BYTES = 2 * VT_SUB;
+  static constexpr int VT_TMA = kHD * 128;              // [64 dims][64 keys], written by TMA
+  static constexpr int VT_SUB = kNO * 128;              // + [16 rows][64 keys]: a row of ones, 15 of zeros
+  static constexpr int VT_BYTES = 2 * VT_SUB;           // keys 0..63 and 64..127 of the tile
+  static constexpr int P_SUB = kBQ * 128;               // [128 rows][64 keys] f16
+  static constexpr int P_BYTES = 2 * P_SUB;             // one head's P, also its output staging
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + GH * Q_BYTES;
-  static constexpr int OFF_VT = OFF_K + 2 * K_BYTES;
-  static constexpr int OFF_RED = OFF_VT + 2 * VT_BYTES;  // [2][2][128] row maxes, [2][4][128] row sums
-  static constexpr int OFF_STG = OFF_RED + (2 * 2 * 128 + 2 * 4 * 128) * 4;   // output staging:
-  static constexpr int STG_WARP = 32 * 32 * 2;          // [head][softmax warp][32 rows][32 f16]
-  static constexpr int OFF_BAR = OFF_STG + GH * 8 * STG_WARP;
-  static constexpr int SMEM = 1024 + OFF_BAR + 256;
-  static constexpr int TMEM_S = 256;                    // S buffers at columns 256 + sb*128;
-                                                        // P (f16) overwrites columns 0..63 of its S
-  static_assert(GH >= 1 && GH * kHD <= 256, "O accumulators must fit below the S buffers");
+  static constexpr int OFF_VT = OFF_K + kNST * K_BYTES;
+  static constexpr int OFF_P = OFF_VT + kNST * VT_BYTES;
+  static constexpr int OFF_MASK = OFF_P + GH * P_BYTES;   // [kNST][4] key-visibility words
+  static constexpr int OFF_MST = OFF_MASK + kNST * 16;  // [GH][128] running row max per head
+  static constexpr int OFF_BAR = OFF_MST + GH * 128 * 4;
+  static constexpr int NBAR = 1 + 2 * kNST + 4 + 3 * GH + 1;
+  static constexpr int SMEM = 1024 + OFF_BAR + NBAR * 8 + 16;
+  static_assert(GH >= 1 && GH * kNO <= kTmemS, "O accumulators must fit below the S buffers");
   static_assert(SMEM <= 232448, "shared memory per CTA");
 };
 
 struct AtParams {
   f16 *o;                   // [B, T, H*hd]
   const int *valid_start;
+  const uint8_t *key_mask;  // [B, T] or nullptr: key j of sequence b hidden where 0
   int B, T, H, KV, G, GH, n_hsub;
   float scale_log2;
   int window;               // > 0: query t sees keys j > t - window only
-  const uint8_t *key_mask;  // [B, T] or nullptr: key j of sequence b hidden where 0
   int Tk, q_off;            // keys per sequence; key index of query 0
   int *status;
 };
@@ -88,19 +107,18 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-// AND of `pred` over the 256 softmax threads (named barrier 1); also a
-// barrier between the two softmax warpgroups.
-__device__ __forceinline__ bool softmax_and(bool pred) {
-  uint32_t out;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, 1, 256, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(out)
-      : "r"((uint32_t)pred)
-      : "memory");
-  return out != 0;
+// (a0, a1) * b + c on the packed two-lane fp32 pipe path (one instruction).
+__device__ __forceinline__ float2 ffma2(float a0, float a1, float b, float c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %4};\n\t"
+      "mov.b64 rc, {%5, %5};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
+  return d;
 }
 
 // max(a, b, c) in one instruction (three-input max of sm_100 and later).
@@ -114,10 +132,8 @@ __device__ __forceinline__ void at_status(int *status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
 
-// KM: the launch carries a key mask (a separate instantiation, so the
-// unmasked kernel is exactly the code without it).
 template <int GH, bool KM>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmVt, const __grid_constant__ CUtensorMap tmO,
                    const AtParams p) {
@@ -128,15 +144,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *sQ = smem + C::OFF_Q;
   uint8_t *sK = smem + C::OFF_K;
   uint8_t *sVt = smem + C::OFF_VT;
+  uint8_t *sP = smem + C::OFF_P;
+  uint32_t *sMask = reinterpret_cast<uint32_t *>(smem + C::OFF_MASK);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
   uint64_t *q_full = bars;
-  uint64_t *kv_full = bars + 1;     // [2]
-  uint64_t *kv_empty = bars + 3;    // [2]
-  uint64_t *s_full = bars + 5;      // [2] S(s) computed
-  uint64_t *s_free = bars + 7;      // [2] PV(s) done: the S/P columns may be overwritten
-  uint64_t *p_full = bars + 9;      // [2] P(s) written into TMEM
-  uint64_t *o_ready = bars + 13;    // [GH]
-  uint64_t *drain = bars + 13 + GH;
+  uint64_t *kv_full = bars + 1;               // [kNST] K and V^T of a tile landed
+  uint64_t *kv_empty = kv_full + kNST;        // [kNST] every head's P V of the tile done (GH commits)
+  uint64_t *s_full = kv_empty + kNST;         // [2] S computed
+  uint64_t *s_free = s_full + 2;              // [2] S read by its softmax warpgroup (128 arrivals)
+  uint64_t *p_full = s_free + 2;              // [GH] P of the head written (128 arrivals)
+  uint64_t *pv_done = p_full + GH;            // [GH] P V of the head done
+  uint64_t *m_ready = pv_done + GH;           // [GH] running max of the head's rows stored (128 arrivals)
+  uint64_t *drain = m_ready + GH;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -163,14 +182,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kNST; ++i) {
       mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 1);
-      mbar_init(&p_full[i], 256);
+      mbar_init(&kv_empty[i], GH);
     }
-    for (int h = 0; h < GH; ++h) mbar_init(&o_ready[h], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 128);
+    }
+    for (int h = 0; h < GH; ++h) {
+      mbar_init(&p_full[h], 128);
+      mbar_init(&pv_done[h], 1);
+      mbar_init(&m_ready[h], 128);
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -179,6 +203,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmVt);
     tma_prefetch_desc(&tmO);
   }
+  // the constant rows under each V^T half tile: row 64 all ones (its product
+  // with P is the row sum of P), rows 65..79 zero; TMA never writes them
+  for (int i = threadIdx.x; i < kNST * 2 * 16 * 8; i += C::THREADS) {
+    const int sub = i >> 7, row = (i >> 3) & 15, ch = i & 7;
+    const uint32_t w = row == 0 ? 0x3c003c00u : 0u;
+    *reinterpret_cast<uint4 *>(sVt + sub * C::VT_SUB + C::VT_TMA + row * 128 + ch * 16) = make_uint4(w, w, w, w);
+  }
+  fence_proxy_async_smem();
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
@@ -190,79 +222,108 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) griddep_launch_dependents();
   if (warp == 0) {
+    // ---------------------------------------------------- TMA producer
+    griddep_wait();                               // q, k and V^T come from the preceding kernel
+    int dummy = 0;
+    long long issued = 0;                         // kv stages issued (for the drain)
+    bool ok = true;
     if (lane == 0) {
-      // ---------------------------------------------------- TMA producer
-      griddep_wait();                             // q, k and V^T come from the preceding kernel
-      int dummy = 0;
-      long long issued = 0;                       // kv stages issued (for the drain)
-      bool ok = true;
       mbar_arrive_expect_tx(q_full, GH * C::Q_BYTES);
       for (int h = 0; h < GH; ++h)
         tma_load_2d(sQ + h * C::Q_BYTES, &tmQ, q_full, 0, ((b * p.H) + h_first + h) * T + q0);
-      for (int it = 0; it < ntiles && ok; ++it) {
-        const int j = j_lo + it, st = it & 1;
-        if (!mbar_wait_bounded(&kv_empty[st], ((it >> 1) & 1) ^ 1, abort_flag)) {
-          ok = false;
-          break;
+    }
+    for (int it = 0; it < ntiles; ++it) {
+      const int j = j_lo + it, st = it % kNST;
+      if (lane == 0) ok = mbar_wait_bounded(&kv_empty[st], ((it / kNST) & 1) ^ 1, abort_flag);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      if constexpr (KM) {
+        // visibility words of the tile's 128 keys (bit e of word w: key j*128 + 32w + e)
+        const uint8_t *km = p.key_mask + (long long)b * T;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const int key = j * kBK + 32 * w + lane;
+          const uint32_t bits = __ballot_sync(0xffffffffu, key < T && km[key] != 0);
+          if (lane == 0) sMask[st * 4 + w] = bits;
         }
-        mbar_arrive_expect_tx(&kv_full[st], C::K_BYTES + C::VT_BYTES);
+        __syncwarp();
+      }
+      if (lane == 0) {
+        // the arrive below releases the mask words to the softmax warps
+        mbar_arrive_expect_tx(&kv_full[st], C::K_BYTES + 2 * C::VT_TMA);
         tma_load_2d(sK + st * C::K_BYTES, &tmK, &kv_full[st], 0, (b * p.KV + kvh) * Tk + j * kBK);
         tma_load_2d(sVt + st * C::VT_BYTES, &tmVt, &kv_full[st], j * kBK, (b * p.KV + kvh) * kHD);
         tma_load_2d(sVt + st * C::VT_BYTES + C::VT_SUB, &tmVt, &kv_full[st], j * kBK + 64,
                     (b * p.KV + kvh) * kHD);
-        ++issued;
       }
+      ++issued;
+    }
+    if (lane == 0) {
       // wait (bounded) until every copy this thread issued has landed
       if (!mbar_wait_bounded(q_full, 0, reinterpret_cast<volatile int *>(&dummy)))
         at_status(p.status, kAtTimeoutDrain);
       if (!ok) {
         at_status(p.status, kAtTimeoutLoad);
         *abort_flag = 1;
-        const long long first = issued > 2 ? issued - 2 : 0;
+        const long long first = issued > kNST ? issued - kNST : 0;
         for (long long i = first; i < issued; ++i)
-          if (!mbar_wait_bounded(&kv_full[i & 1], (uint32_t)((i >> 1) & 1),
+          if (!mbar_wait_bounded(&kv_full[i % kNST], (uint32_t)((i / kNST) & 1),
                                  reinterpret_cast<volatile int *>(&dummy)))
             at_status(p.status, kAtTimeoutDrain);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // ---------------------------------------------------- MMA issuer
+      // ---------------------------------------------------- S = Q_h K^T issuer
       constexpr uint32_t kIdescS = idesc_f16_f32(kBQ, kBK);
-      constexpr uint32_t kIdescO = idesc_f16_f32(kBQ, kHD);
       bool ok = mbar_wait_bounded(q_full, 0, abort_flag), any = false;
-      for (int s = 0; s <= nslots && ok; ++s) {
-        if (s < nslots) {
-          // S(s) = Q_h K_j^T into S buffer s & 1
-          const int it = s / GH, h = s - it * GH, sb = s & 1;
-          if (!mbar_wait_bounded(&s_free[sb], ((s >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
-          if (h == 0 && !mbar_wait_bounded(&kv_full[it & 1], (it >> 1) & 1, abort_flag)) { ok = false; break; }
-          tc_fence_after_sync();
-          const uint64_t a = sdesc_kmajor_sw128(smem_u32(sQ + h * C::Q_BYTES));
-          const uint64_t bk = sdesc_kmajor_sw128(smem_u32(sK + (it & 1) * C::K_BYTES));
+      for (int s = 0; s < nslots && ok; ++s) {
+        const int it = s / GH, h = s - it * GH, sb = s & 1, st = it % kNST;
+        if (!mbar_wait_bounded(&s_free[sb], ((s >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+        if (h == 0 && !mbar_wait_bounded(&kv_full[st], (it / kNST) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after_sync();
+        const uint64_t a = sdesc_kmajor_sw128(smem_u32(sQ + h * C::Q_BYTES));
+        const uint64_t bk = sdesc_kmajor_sw128(smem_u32(sK + st * C::K_BYTES));
 #pragma unroll
-          for (int k = 0; k < kHD / 16; ++k)
-            umma_f16(tmem + C::TMEM_S + sb * kBK, a + 2 * k, bk + 2 * k, kIdescS, k > 0);
-          any = true;
-          umma_commit(&s_full[sb]);
+        for (int k = 0; k < kHD / 16; ++k)
+          umma_f16(tmem + kTmemS + sb * kBK, a + 2 * k, bk + 2 * k, kIdescS, k > 0);
+        any = true;
+        umma_commit(&s_full[sb]);
+      }
+      if (!ok) {
+        at_status(p.status, kAtTimeoutMma);
+        *abort_flag = 1;
+        if (any) {
+          umma_commit(drain);
+          int dummy = 0;
+          if (!mbar_wait_bounded(drain, 0, reinterpret_cast<volatile int *>(&dummy)))
+            at_status(p.status, kAtTimeoutDrain);
         }
-        if (s >= 1) {
-          // O_h += P(s-1) V_j
-          const int ps = s - 1, it = ps / GH, h = ps - it * GH, pb = ps & 1;
-          if (!mbar_wait_bounded(&p_full[pb], (ps >> 1) & 1, abort_flag)) { ok = false; break; }
-          tc_fence_after_sync();
+      }
+    }
+  } else if (warp < 4) {
+    if (lane == 0) {
+      // ---------------------------------------------------- O_h += P_h [V | 1] issuer
+      // warp 2 takes the even heads, warp 3 the odd ones, in slot order
+      constexpr uint32_t kIdescO = idesc_f16_f32(kBQ, kNO);
+      const int par = warp - 2;
+      bool ok = true, any = false;
+      for (int s = 0; s < nslots && ok; ++s) {
+        const int it = s / GH, h = s - it * GH, st = it % kNST;
+        if ((h & 1) != par) continue;
+        if (!mbar_wait_bounded(&p_full[h], it & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after_sync();
 #pragma unroll
-          for (int kb = 0; kb < 2; ++kb) {
-            const uint64_t bv = sdesc_kmajor_sw128(smem_u32(sVt + (it & 1) * C::VT_BYTES + kb * C::VT_SUB));
+        for (int kb = 0; kb < 2; ++kb) {
+          const uint64_t ap = sdesc_kmajor_sw128(smem_u32(sP + h * C::P_BYTES + kb * C::P_SUB));
+          const uint64_t bv = sdesc_kmajor_sw128(smem_u32(sVt + st * C::VT_BYTES + kb * C::VT_SUB));
 #pragma unroll
-            for (int k = 0; k < 4; ++k)   // 16 keys of P = 8 TMEM columns per MMA
-              umma_f16_tmem_a(tmem + h * kHD, tmem + C::TMEM_S + pb * kBK + (kb * 4 + k) * 8, bv + 2 * k,
-                              kIdescO, (it | kb | k) != 0);
-          }
-          umma_commit(&s_free[pb]);
-          umma_commit(&o_ready[h]);
-          if (h == GH - 1) umma_commit(&kv_empty[it & 1]);
+          for (int k = 0; k < 4; ++k)
+            umma_f16(tmem + h * kNO, ap + 2 * k, bv + 2 * k, kIdescO, (it | kb | k) != 0);
         }
+        any = true;
+        umma_commit(&pv_done[h]);
+        umma_commit(&kv_empty[st]);
       }
       if (!ok) {
         at_status(p.status, kAtTimeoutMma);
@@ -277,192 +338,181 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     griddep_wait();                               // o is written below
-    // ---------------------------------------------- softmax: warps 2..5 take keys
-    // 0..63 of every tile (group 0), warps 6..9 keys 64..127 (group 1); one
-    // query row per thread.  The groups exchange partial row maxes in shared
-    // memory at a named-barrier reduction that also ANDs their health, so a
-    // bounded wait that gives up in one group stops both together.
-    const int quarter = warp & 3;
-    const int grp = (warp - 2) >> 2;
+    // ---------------------------------------------- softmax warpgroup g: slots g, g + NG, ...
+    const int g = (warp - 4) >> 2;
+    const int quarter = warp & 3;                   // TMEM lanes 32*quarter .. +31
     const int r = quarter * 32 + lane;              // query row within the tile
     const int t = q0 + r;
     const int tk = qo + t;                          // this row's own key index
     const int row_lo = p.window > 0 ? max(vs, tk - p.window + 1) : vs;   // this row's first visible key
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    float *m_state = reinterpret_cast<float *>(smem + C::OFF_MST);      // [GH][128]
     const float sl2 = p.scale_log2;
-    float *red_max = reinterpret_cast<float *>(smem + C::OFF_RED);          // [2][2][128]
-    float *red_sum = red_max + 2 * 2 * 128;                                   // [2][4][128]
-    float m[GH], l[GH];                             // running max (shared value), partial sums
-#pragma unroll
-    for (int h = 0; h < GH; ++h) {
-      m[h] = -INFINITY;
-      l[h] = 0.f;
-    }
     bool alive = true;
-    // visibility of this group's 64 keys under the caller's key mask (bit e =
-    // key k0 + e), read once per key tile and shared by its GH head slots
-    unsigned long long vis = ~0ull;
-    int vis_it = -1;
-    const uint8_t *kmask = KM ? p.key_mask + (long long)b * T : nullptr;
-    for (int s = 0; s < nslots; ++s) {
-      const int it = s / GH, h = s - it * GH, sb = s & 1;
-      const int k0 = (j_lo + it) * kBK + grp * 64;  // first key of this group's half tile
-      if (KM && it != vis_it) {
-        vis = 0ull;
-#pragma unroll 8
-        for (int e = 0; e < 64; ++e)
-          if (k0 + e < T && __ldg(kmask + k0 + e)) vis |= 1ull << e;
-        vis_it = it;
+    for (int s = g; s < nslots; s += C::NG) {
+      const int it = s / GH, h = s - it * GH, sb = s & 1, st = it % kNST;
+      const int k0 = (j_lo + it) * kBK;             // first key of the tile
+      const bool need_mask =
+          KM || (k0 + kBK - 1 > qo + q0) || (k0 < vs) || (p.window > 0 && k0 <= qo + last_q - p.window);
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&s_full[sb], (s >> 1) & 1, abort_flag))) {
+        alive = false;
+        break;
       }
-      const bool ok = alive && __all_sync(0xffffffffu, mbar_wait_bounded(&s_full[sb], (s >> 1) & 1, abort_flag));
-      const bool need_mask = KM || (k0 + 63 > qo + q0) || (k0 < vs) || (p.window > 0 && k0 <= qo + last_q - p.window);
-      uint32_t sv[64];
-      float mx = -INFINITY;
-      if (ok) {
-        tc_fence_after_sync();
-        const uint32_t s_col = lane_base + C::TMEM_S + sb * kBK + grp * 64;
-        tmem_ld32(s_col, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-        tmem_ld32(s_col + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-        tmem_ld_wait();
-        // eight independent max chains (a single chain is latency-bound)
-        float mc[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) mc[q] = -INFINITY;
-        if (need_mask) {
-          const int hi = tk - k0, lo = row_lo - k0;
-#pragma unroll
-          for (int e = 0; e < 64; ++e)
-            if (e <= hi && e >= lo && (!KM || ((vis >> e) & 1ull))) mc[e & 7] = fmaxf(mc[e & 7], __uint_as_float(sv[e]));
-        } else {
-#pragma unroll
-          for (int e = 0; e < 64; e += 2)
-            mc[(e >> 1) & 7] = fmax3(mc[(e >> 1) & 7], __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
-        }
-        mx = fmaxf(fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3])), fmaxf(fmaxf(mc[4], mc[5]), fmaxf(mc[6], mc[7])));
-      }
-      red_max[((s & 1) * 2 + grp) * 128 + r] = mx;
-      tc_fence_before_sync();                       // both groups' S reads precede any P write
-      alive = softmax_and(ok);
       tc_fence_after_sync();
-      if (!alive) break;
-      float mxa = fmaxf(mx, red_max[((s & 1) * 2 + (grp ^ 1)) * 128 + r]);
-      mxa = (mxa == -INFINITY) ? -INFINITY : mxa * sl2;   // into the exp2 domain
-      float mh = m[h];
-      float alpha = 1.f;
-      const bool resc = (mh != -INFINITY) && (mxa > mh + 8.f);
-      if (resc) {
-        alpha = ex2_approx(mh - mxa);
-        l[h] *= alpha;
-        mh = mxa;
-      } else if (mh == -INFINITY) {
-        mh = mxa;                                   // first visible key(s) of this row
-      }
-      m[h] = mh;
-      if (__any_sync(0xffffffffu, resc)) {
-        // O_h must hold every earlier P V before it is rescaled; each group
-        // rescales its 32 of the head's 64 columns
-        if (__all_sync(0xffffffffu, mbar_wait_bounded(&o_ready[h], (it - 1) & 1, abort_flag))) {
-          tc_fence_after_sync();
-          uint32_t ov[32];
-          tmem_ld32(lane_base + h * kHD + grp * 32, ov);
-          tmem_ld_wait();
+      uint32_t sv[128];
+      const uint32_t s_col = lane_base + kTmemS + sb * kBK;
 #pragma unroll
-          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-          tmem_st32(lane_base + h * kHD + grp * 32, ov);
-          tmem_st_wait();
-        } else {
-          alive = false;
-        }
-      }
-      if (!alive) continue;                         // the next reduction stops both groups
-      const float mu = (mh == -INFINITY) ? 0.f : mh;
-      // p = 2^(s*c - m) as f16, packed two keys per TMEM column into the first
-      // 64 columns of this S buffer (this group's 64 keys -> 32 columns)
-      uint32_t pk[32];
-      float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // eight partial sums
-      if (need_mask) {
-        // keys k0+e visible iff lo <= e <= hi (causal, padding and window limits)
-        const int hi = tk - k0, lo = row_lo - k0;
-#pragma unroll
-        for (int e = 0; e < 64; e += 2) {
-          const float x0 = (e <= hi && e >= lo && (!KM || ((vis >> e) & 1ull)))
-                               ? fmaf(__uint_as_float(sv[e]), sl2, -mu)
-                               : -INFINITY;
-          const float x1 = (e + 1 <= hi && e + 1 >= lo && (!KM || ((vis >> (e + 1)) & 1ull)))
-                               ? fmaf(__uint_as_float(sv[e + 1]), sl2, -mu)
-                               : -INFINITY;
-          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-          ps[e & 7] += p0;
-          ps[(e + 1) & 7] += p1;
-          pk[e >> 1] = pack_f16x2(p0, p1);
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < 64; e += 2) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(sv[e]), sl2, -mu));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(sv[e + 1]), sl2, -mu));
-          ps[e & 7] += p0;
-          ps[(e + 1) & 7] += p1;
-          pk[e >> 1] = pack_f16x2(p0, p1);
-        }
-      }
-      tmem_st32(lane_base + C::TMEM_S + sb * kBK + grp * 32, pk);
-      tmem_st_wait();
-      l[h] += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      for (int c = 0; c < 4; ++c) tmem_ld32(s_col + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sv[32 * c]));
+      tmem_ld_wait();
       tc_fence_before_sync();
-      mbar_arrive(&p_full[sb]);
-    }
-    // ------------------------------------------------ normalise and store
-#pragma unroll
-    for (int h = 0; h < GH; ++h) red_sum[(grp * 4 + h) * 128 + r] = l[h];
-    alive = softmax_and(alive);
-    if (!alive) {
-      if (lane == 0) at_status(p.status, kAtTimeoutSoftmax);
-      *abort_flag = 1;
-    } else {
-      const bool row_ok = t < T;
-      const bool warp_rows_ok = q0 + quarter * 32 + 31 < T;   // all 32 rows of this warp exist
-      const long long ldo = (long long)p.H * kHD;
-#pragma unroll 1
-      for (int h = 0; h < GH; ++h) {
-        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&o_ready[h], (ntiles - 1) & 1, abort_flag))) {
-          if (lane == 0) at_status(p.status, kAtTimeoutSoftmax);
-          *abort_flag = 1;
+      mbar_arrive(&s_free[sb]);                     // the S buffer may be overwritten now
+      uint32_t vis[4] = {~0u, ~0u, ~0u, ~0u};
+      if constexpr (KM) {
+        // the tile's mask words (already published: the S MMA of this tile
+        // waited for the same phase)
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&kv_full[st], (it / kNST) & 1, abort_flag))) {
+          alive = false;
           break;
         }
+#pragma unroll
+        for (int w = 0; w < 4; ++w) vis[w] = sMask[st * 4 + w];
+      }
+      // hidden keys (causal, padding, window and key-mask limits) become -inf
+      // in place, so one code path serves masked and unmasked tiles
+      if (need_mask) {
+        const int hi = tk - k0, lo = row_lo - k0;   // keys k0+e visible iff lo <= e <= hi
+#pragma unroll
+        for (int e = 0; e < kBK; ++e)
+          if (!(e <= hi && e >= lo && ((vis[e >> 5] >> (e & 31)) & 1u))) sv[e] = 0xff800000u;
+      }
+      // row max; eight independent chains
+      float mc[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) mc[q] = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < kBK; e += 2)
+        mc[(e >> 1) & 7] = fmax3(mc[(e >> 1) & 7], __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
+      const float mx = fmaxf(fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3])),
+                             fmaxf(fmaxf(mc[4], mc[5]), fmaxf(mc[6], mc[7])));
+      const float mxa = (mx == -INFINITY) ? -INFINITY : mx * sl2;   // into the exp2 domain
+      // the head's running max (exp2 domain), left by whichever warpgroup took
+      // its previous tile
+      float m = -INFINITY;
+      if (it > 0) {
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&m_ready[h], (it - 1) & 1, abort_flag))) {
+          alive = false;
+          break;
+        }
+        m = m_state[h * 128 + r];
+      }
+      float alpha = 1.f;
+      const bool resc = (m != -INFINITY) && (mxa > m + 8.f);
+      if (resc) {
+        alpha = ex2_approx(m - mxa);
+        m = mxa;
+      } else if (m == -INFINITY) {
+        m = mxa;                                    // first visible key(s) of this row
+      }
+      m_state[h * 128 + r] = m;
+      mbar_arrive(&m_ready[h]);                     // releases the store to the head's next tile
+      // P V of the previous tile must be done: it reads the P buffer, and a
+      // rescale of O must not race its accumulation
+      if (it > 0 &&
+          !__all_sync(0xffffffffu, mbar_wait_bounded(&pv_done[h], (it - 1) & 1, abort_flag))) {
+        alive = false;
+        break;
+      }
+      if (__any_sync(0xffffffffu, resc)) {
+        // O_h (and its row-sum column) *= alpha, sixteen columns at a time
         tc_fence_after_sync();
-        const float lt = red_sum[h * 128 + r] + red_sum[(4 + h) * 128 + r];
-        const float inv = lt > 0.f ? 1.f / lt : 0.f;
-        uint32_t ov[32];
-        tmem_ld32(lane_base + h * kHD + grp * 32, ov);
+        const uint32_t o_col = lane_base + h * kNO;
+#pragma unroll 1
+        for (int c = 0; c < kNO; c += 16) {
+          uint32_t ov[16];
+          tmem_ld16(o_col + c, ov);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+          tmem_st16(o_col + c, ov);
+        }
+        tmem_st_wait();
+      }
+      const float mu = (m == -INFINITY) ? 0.f : m;
+      // p = 2^(s*c - m) as f16, eight keys per 16-byte chunk of the row, in the
+      // 128-byte swizzled layout (chunk c of row r at r*128 + 16*(c ^ (r & 7)))
+      uint8_t *pbuf = sP + h * C::P_BYTES;
+#pragma unroll
+      for (int kb = 0; kb < 2; ++kb) {
+        uint8_t *row_base = pbuf + kb * C::P_SUB + r * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const int e0 = kb * 64 + c * 8;
+          uint32_t pk[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 x = ffma2(__uint_as_float(sv[e0 + 2 * q]), __uint_as_float(sv[e0 + 2 * q + 1]), sl2, -mu);
+            pk[q] = pack_f16x2(ex2_approx(x.x), ex2_approx(x.y));
+          }
+          *reinterpret_cast<uint4 *>(row_base + ((c ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+      }
+      fence_proxy_async_smem();                     // P visible to the tensor core
+      tc_fence_before_sync();                       // and the rescale's TMEM stores ordered before it
+      mbar_arrive(&p_full[h]);
+    }
+    // ------------------------------------------------ normalise and store
+    // each head is finished by the warpgroup that took its last tile
+#pragma unroll 1
+    for (int h = 0; h < GH; ++h) {
+      if (((ntiles - 1) * GH + h) % C::NG != g) continue;
+      if (alive &&
+          !__all_sync(0xffffffffu, mbar_wait_bounded(&pv_done[h], (ntiles - 1) & 1, abort_flag)))
+        alive = false;
+      if (!alive) break;
+      tc_fence_after_sync();
+      uint32_t ov[32], os[16];
+      const uint32_t o_col = lane_base + h * kNO;
+      tmem_ld16(o_col + 64, os);
+      tmem_ld_wait();
+      const float lt = __uint_as_float(os[0]);
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      const bool row_ok = t < T;
+      const bool warp_rows_ok = q0 + quarter * 32 + 31 < T;   // all 32 rows of this warp exist
+      // the warp's 32 rows x 64 columns staged in the head's (now free) P buffer, swizzled
+      uint8_t *stg = sP + h * C::P_BYTES + quarter * 32 * 128;
+      f16 *dst = p.o + ((long long)b * T + t) * ((long long)p.H * kHD) + (long long)(h_first + h) * kHD;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        tmem_ld32(o_col + 32 * half, ov);
         tmem_ld_wait();
-        uint4 w[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const float *f = reinterpret_cast<const float *>(&ov[8 * q]);
-          w[q] = make_uint4(pack_f16x2(f[0] * inv, f[1] * inv), pack_f16x2(f[2] * inv, f[3] * inv),
-                            pack_f16x2(f[4] * inv, f[5] * inv), pack_f16x2(f[6] * inv, f[7] * inv));
+          const uint4 w = make_uint4(pack_f16x2(f[0] * inv, f[1] * inv), pack_f16x2(f[2] * inv, f[3] * inv),
+                                     pack_f16x2(f[4] * inv, f[5] * inv), pack_f16x2(f[6] * inv, f[7] * inv));
+          const int c = half * 4 + q;
+          if (warp_rows_ok)
+            *reinterpret_cast<uint4 *>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) = w;
+          else if (row_ok)
+            *reinterpret_cast<uint4 *>(dst + 8 * c) = w;
         }
-        if (warp_rows_ok) {
-          // the warp's 32 rows x 32 columns go out as one TMA box (a lane per
-          // row would make every store instruction 32 separate row segments)
-          uint8_t *stg = smem + C::OFF_STG + (h * 8 + (warp - 2)) * C::STG_WARP;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4 *>(stg + lane * 64 + q * 16) = w[q];
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&tmO, stg, (h_first + h) * kHD + grp * 32, b * T + q0 + quarter * 32);
-            bulk_commit_group();
-          }
-        } else if (row_ok) {
-          f16 *dst = p.o + ((long long)b * T + t) * ldo + (long long)(h_first + h) * kHD + grp * 32;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4 *>(dst + 8 * q) = w[q];
+      }
+      if (warp_rows_ok) {
+        // one TMA box per warp (a lane per row would make every store
+        // instruction 32 separate row segments)
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tmO, stg, (h_first + h) * kHD, b * T + q0 + quarter * 32);
+          bulk_commit_group();
         }
       }
     }
-    if (lane == 0) bulk_wait_group_read<0>();     // the staging blocks are read before the CTA exits
+    if (!alive) {
+      if (lane == 0) at_status(p.status, kAtTimeoutSoftmax);
+      *abort_flag = 1;
+    }
+    if (lane == 0) bulk_wait_group_read<0>();     // the staging is read before the CTA exits
   }
 
   tc_fence_before_sync();
@@ -475,21 +525,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int GH, bool KM>
 cudaError_t launch_ghk(const AttnParams &a, const CUtensorMap &tq, const CUtensorMap &tk,
-                      const CUtensorMap &tv, const CUtensorMap &to, cudaStream_t st) {
+                       const CUtensorMap &tv, const CUtensorMap &to, cudaStream_t st) {
   using C = AtCfg<GH>;
   auto kern = attn_tc_kernel<GH, KM>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t e = ensure_smem_attr<attn_tc_kernel<GH, KM>>(C::SMEM);
   if (e != cudaSuccess) return e;
   AtParams p{};
   p.o = a.o;
   p.valid_start = a.valid_start;
+  p.key_mask = a.key_mask;
   p.B = a.B; p.T = a.T; p.H = a.H; p.KV = a.KV;
   p.G = a.H / a.KV;
   p.GH = GH;
   p.n_hsub = p.G / GH;
   p.scale_log2 = a.scale_log2;
   p.window = a.window;
-  p.key_mask = a.key_mask;
   p.Tk = a.Tk > 0 ? a.Tk : a.T;
   p.q_off = a.q_off;
   p.status = a.status;
@@ -501,7 +551,7 @@ cudaError_t launch_ghk(const AttnParams &a, const CUtensorMap &tq, const CUtenso
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(C::THREADS);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = st;
   cfg.attrs = attr;
@@ -525,23 +575,24 @@ bool attention_tc_supported(int hd, int H, int KV) {
 cudaError_t launch_attention_tc(const AttnParams &a, cudaStream_t st) {
   if (!attention_tc_supported(a.hd, a.H, a.KV) || a.v_t == nullptr) return cudaErrorInvalidConfiguration;
   CUtensorMap tq, tk, tv, to;
-  if (!make_tmap_f16(&tq, a.q, (uint64_t)a.B * a.H * a.T, kHD, kHD, kBQ)) return cudaErrorInvalidValue;
+  if (!get_tmap_f16(&tq, a.q, (uint64_t)a.B * a.H * a.T, kHD, kHD, kBQ)) return cudaErrorInvalidValue;
   const int Tk = a.Tk > 0 ? a.Tk : a.T;
   if (Tk < a.T || a.q_off < 0 || a.q_off + a.T > Tk) return cudaErrorInvalidValue;
-  if (!make_tmap_f16(&tk, a.k, (uint64_t)a.B * a.KV * Tk, kHD, kHD, kBK)) return cudaErrorInvalidValue;
+  if (a.key_mask && Tk != a.T) return cudaErrorInvalidValue;
+  if (!get_tmap_f16(&tk, a.k, (uint64_t)a.B * a.KV * Tk, kHD, kHD, kBK)) return cudaErrorInvalidValue;
   // V^T: rows are (b, kv head, dim), columns are keys; columns >= Tk read as zero
-  if (!make_tmap_f16(&tv, a.v_t, (uint64_t)a.B * a.KV * kHD, Tk, a.T_pad, kHD)) return cudaErrorInvalidValue;
-  // output rows [B*T, H*hd]: a softmax warp's 32 rows x 32 columns per box
-  if (!make_tmap_2d(&to, a.o, (uint64_t)a.B * a.T, (uint64_t)a.H * kHD, (uint64_t)a.H * kHD, 32, 32, false))
+  if (!get_tmap_f16(&tv, a.v_t, (uint64_t)a.B * a.KV * kHD, Tk, a.T_pad, kHD)) return cudaErrorInvalidValue;
+  // output rows [B*T, H*hd]: a softmax warp's 32 rows x 64 columns per box, swizzled
+  if (!get_tmap_2d(&to, a.o, (uint64_t)a.B * a.T, (uint64_t)a.H * kHD, (uint64_t)a.H * kHD, 64, 32, true))
     return cudaErrorInvalidValue;
   const int G = a.H / a.KV;
   switch (G) {
     case 1: return launch_gh<1>(a, tq, tk, tv, to, st);
     case 2: return launch_gh<2>(a, tq, tk, tv, to, st);
     case 3: return launch_gh<3>(a, tq, tk, tv, to, st);
-    case 4: return launch_gh<4>(a, tq, tk, tv, to, st);
+    case 4: return launch_gh<2>(a, tq, tk, tv, to, st);   // two CTAs per group of four
     case 6: return launch_gh<3>(a, tq, tk, tv, to, st);   // two CTAs per group of six
-    case 8: return launch_gh<4>(a, tq, tk, tv, to, st);
+    case 8: return launch_gh<2>(a, tq, tk, tv, to, st);   // four CTAs per group of eight
   }
   return cudaErrorInvalidConfiguration;
 }

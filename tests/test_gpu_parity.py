@@ -81,6 +81,16 @@ def test_block_smollm2_ragged(S, B, T):
     run_block_case(S, W["smollm2_block_b1_t128"].scaled(B=B, T=T), seed=B * 1000 + T)
 
 
+@pytest.mark.parametrize("H,KV", [(4, 4), (4, 2), (4, 1), (6, 1)])
+def test_block_group_sizes(S, H, KV):
+    # query heads per kv head 1, 2, 4 and 6: one CTA per group of 1 or 2 heads
+    # (one softmax warpgroup, or two taking the slots in turn) and groups split
+    # over several CTAs
+    wl = W["smollm2_block_b1_t128"].scaled(B=2, T=300, hidden=64 * H, n_heads=H, n_kv_heads=KV,
+                                           intermediate=512)
+    run_block_case(S, wl, seed=40 + H * 10 + KV)
+
+
 def test_block_smollm3_shape(S):
     run_block_case(S, W["smollm3_4blocks_b4_t4096"].scaled(B=1, T=160, n_layers=1))
 
