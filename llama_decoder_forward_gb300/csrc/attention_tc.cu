@@ -31,8 +31,7 @@
 // a fixed ~110 cycles of its issuing thread whatever N is (measured), so one
 // thread issuing all twelve small MMAs of a (tile, head) would leave the pipe
 // idle; several warps' MMAs run concurrently.  Warp 1 issues every S MMA, warps
-// 2 and 3 the P V MMAs of the even and odd heads (a head's accumulator is only
-// ever written from one thread, so their order is program order).
+// 2 and 3 the P V MMAs of alternate (tile, head) slots.
 // The running max is updated lazily: O_h is rescaled in TMEM only when a row's
 // max grows by more than 2^8 (otherwise P may exceed 1 by up to 256, exact in
 // the fp32 sums and within f16 range), the FlashAttention-4 idea.
@@ -75,7 +74,7 @@ struct AtCfg {
   static constexpr int OFF_MASK = OFF_P + GH * P_BYTES;   // [kNST][4] key-visibility words
   static constexpr int OFF_MST = OFF_MASK + kNST * 16;  // [GH][128] running row max per head
   static constexpr int OFF_BAR = OFF_MST + GH * 128 * 4;
-  static constexpr int NBAR = 1 + 2 * kNST + 4 + 3 * GH + 1;
+  static constexpr int NBAR = 1 + 4 * kNST + 4 + 4 * GH + 1;
   static constexpr int SMEM = 1024 + OFF_BAR + NBAR * 8 + 16;
   static_assert(GH >= 1 && GH * kNO <= kTmemS, "O accumulators must fit below the S buffers");
   static_assert(SMEM <= 232448, "shared memory per CTA");
@@ -148,12 +147,18 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
   uint32_t *sMask = reinterpret_cast<uint32_t *>(smem + C::OFF_MASK);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
   uint64_t *q_full = bars;
-  uint64_t *kv_full = bars + 1;               // [kNST] K and V^T of a tile landed
-  uint64_t *kv_empty = kv_full + kNST;        // [kNST] every head's P V of the tile done (GH commits)
-  uint64_t *s_full = kv_empty + kNST;         // [2] S computed
+  uint64_t *k_full = bars + 1;                // [kNST] K of a tile landed
+  uint64_t *k_empty = k_full + kNST;          // [kNST] every head's S of the tile done
+  uint64_t *v_full = k_empty + kNST;          // [kNST] V^T of a tile (and its key-mask words) landed
+  uint64_t *v_empty = v_full + kNST;          // [kNST] every head's P V of the tile done (GH commits)
+  uint64_t *s_full = v_empty + kNST;          // [2] S computed
   uint64_t *s_free = s_full + 2;              // [2] S read by its softmax warpgroup (128 arrivals)
-  uint64_t *p_full = s_free + 2;              // [GH] P of the head written (128 arrivals)
-  uint64_t *pv_done = p_full + GH;            // [GH] P V of the head done
+  // [GH][2] P of the head written for tiles of even / odd index (128 arrivals).
+  // Split by tile parity so that each barrier has one waiter that sees every
+  // phase: a P V warp takes a given head only every other tile, and a parity
+  // wait two phases behind would pass early.
+  uint64_t *p_full = s_free + 2;
+  uint64_t *pv_done = p_full + 2 * GH;        // [GH] P V of the head done
   uint64_t *m_ready = pv_done + GH;           // [GH] running max of the head's rows stored (128 arrivals)
   uint64_t *drain = m_ready + GH;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
@@ -183,15 +188,18 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int i = 0; i < kNST; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], GH);
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], GH);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], 128);
     }
     for (int h = 0; h < GH; ++h) {
-      mbar_init(&p_full[h], 128);
+      mbar_init(&p_full[2 * h], 128);
+      mbar_init(&p_full[2 * h + 1], 128);
       mbar_init(&pv_done[h], 1);
       mbar_init(&m_ready[h], 128);
     }
@@ -223,18 +231,35 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
   if (threadIdx.x == 0) griddep_launch_dependents();
   if (warp == 0) {
     // ---------------------------------------------------- TMA producer
+    // K of a tile is released once its S MMAs are done and V only after its
+    // P V MMAs, so K runs one tile ahead: K(0), K(1), V(0), K(2), V(1), ...
     griddep_wait();                               // q, k and V^T come from the preceding kernel
     int dummy = 0;
-    long long issued = 0;                         // kv stages issued (for the drain)
+    int nk = 0, nv = 0;                           // K and V tiles issued (for the drain)
     bool ok = true;
     if (lane == 0) {
       mbar_arrive_expect_tx(q_full, GH * C::Q_BYTES);
       for (int h = 0; h < GH; ++h)
         tma_load_2d(sQ + h * C::Q_BYTES, &tmQ, q_full, 0, ((b * p.H) + h_first + h) * T + q0);
     }
-    for (int it = 0; it < ntiles; ++it) {
+    for (int it = -1; it < ntiles && ok; ++it) {
+      const int ik = it + 1;                      // K tile issued in this step
+      if (ik < ntiles) {
+        const int st = ik % kNST;
+        if (lane == 0) {
+          ok = mbar_wait_bounded(&k_empty[st], ((ik / kNST) & 1) ^ 1, abort_flag);
+          if (ok) {
+            mbar_arrive_expect_tx(&k_full[st], C::K_BYTES);
+            tma_load_2d(sK + st * C::K_BYTES, &tmK, &k_full[st], 0, (b * p.KV + kvh) * Tk + (j_lo + ik) * kBK);
+            ++nk;
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+      }
+      if (it < 0) continue;
       const int j = j_lo + it, st = it % kNST;
-      if (lane == 0) ok = mbar_wait_bounded(&kv_empty[st], ((it / kNST) & 1) ^ 1, abort_flag);
+      if (lane == 0) ok = mbar_wait_bounded(&v_empty[st], ((it / kNST) & 1) ^ 1, abort_flag);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       if constexpr (KM) {
@@ -249,14 +274,13 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
         __syncwarp();
       }
       if (lane == 0) {
-        // the arrive below releases the mask words to the softmax warps
-        mbar_arrive_expect_tx(&kv_full[st], C::K_BYTES + 2 * C::VT_TMA);
-        tma_load_2d(sK + st * C::K_BYTES, &tmK, &kv_full[st], 0, (b * p.KV + kvh) * Tk + j * kBK);
-        tma_load_2d(sVt + st * C::VT_BYTES, &tmVt, &kv_full[st], j * kBK, (b * p.KV + kvh) * kHD);
-        tma_load_2d(sVt + st * C::VT_BYTES + C::VT_SUB, &tmVt, &kv_full[st], j * kBK + 64,
+        // the arrive below also releases the mask words to the softmax warps
+        mbar_arrive_expect_tx(&v_full[st], 2 * C::VT_TMA);
+        tma_load_2d(sVt + st * C::VT_BYTES, &tmVt, &v_full[st], j * kBK, (b * p.KV + kvh) * kHD);
+        tma_load_2d(sVt + st * C::VT_BYTES + C::VT_SUB, &tmVt, &v_full[st], j * kBK + 64,
                     (b * p.KV + kvh) * kHD);
+        ++nv;
       }
-      ++issued;
     }
     if (lane == 0) {
       // wait (bounded) until every copy this thread issued has landed
@@ -265,9 +289,12 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
       if (!ok) {
         at_status(p.status, kAtTimeoutLoad);
         *abort_flag = 1;
-        const long long first = issued > kNST ? issued - kNST : 0;
-        for (long long i = first; i < issued; ++i)
-          if (!mbar_wait_bounded(&kv_full[i % kNST], (uint32_t)((i / kNST) & 1),
+        for (int i = nk > kNST ? nk - kNST : 0; i < nk; ++i)
+          if (!mbar_wait_bounded(&k_full[i % kNST], (uint32_t)((i / kNST) & 1),
+                                 reinterpret_cast<volatile int *>(&dummy)))
+            at_status(p.status, kAtTimeoutDrain);
+        for (int i = nv > kNST ? nv - kNST : 0; i < nv; ++i)
+          if (!mbar_wait_bounded(&v_full[i % kNST], (uint32_t)((i / kNST) & 1),
                                  reinterpret_cast<volatile int *>(&dummy)))
             at_status(p.status, kAtTimeoutDrain);
       }
@@ -280,7 +307,7 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
       for (int s = 0; s < nslots && ok; ++s) {
         const int it = s / GH, h = s - it * GH, sb = s & 1, st = it % kNST;
         if (!mbar_wait_bounded(&s_free[sb], ((s >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
-        if (h == 0 && !mbar_wait_bounded(&kv_full[st], (it / kNST) & 1, abort_flag)) { ok = false; break; }
+        if (h == 0 && !mbar_wait_bounded(&k_full[st], (it / kNST) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after_sync();
         const uint64_t a = sdesc_kmajor_sw128(smem_u32(sQ + h * C::Q_BYTES));
         const uint64_t bk = sdesc_kmajor_sw128(smem_u32(sK + st * C::K_BYTES));
@@ -289,6 +316,7 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
           umma_f16(tmem + kTmemS + sb * kBK, a + 2 * k, bk + 2 * k, kIdescS, k > 0);
         any = true;
         umma_commit(&s_full[sb]);
+        if (h == GH - 1) umma_commit(&k_empty[st]);   // every head's S of the tile issued
       }
       if (!ok) {
         at_status(p.status, kAtTimeoutMma);
@@ -304,14 +332,16 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
   } else if (warp < 4) {
     if (lane == 0) {
       // ---------------------------------------------------- O_h += P_h [V | 1] issuer
-      // warp 2 takes the even heads, warp 3 the odd ones, in slot order
+      // warp 2 takes the even slots, warp 3 the odd ones.  A head's P V MMAs of
+      // consecutive tiles never overlap even when issued from different warps:
+      // P of the next tile is written only after the previous P V is done.
       constexpr uint32_t kIdescO = idesc_f16_f32(kBQ, kNO);
       const int par = warp - 2;
       bool ok = true, any = false;
-      for (int s = 0; s < nslots && ok; ++s) {
+      for (int s = par; s < nslots && ok; s += 2) {
         const int it = s / GH, h = s - it * GH, st = it % kNST;
-        if ((h & 1) != par) continue;
-        if (!mbar_wait_bounded(&p_full[h], it & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait_bounded(&p_full[2 * h + (it & 1)], (it >> 1) & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait_bounded(&v_full[st], (it / kNST) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after_sync();
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb) {
@@ -323,7 +353,7 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
         }
         any = true;
         umma_commit(&pv_done[h]);
-        umma_commit(&kv_empty[st]);
+        umma_commit(&v_empty[st]);
       }
       if (!ok) {
         at_status(p.status, kAtTimeoutMma);
@@ -368,9 +398,8 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
       mbar_arrive(&s_free[sb]);                     // the S buffer may be overwritten now
       uint32_t vis[4] = {~0u, ~0u, ~0u, ~0u};
       if constexpr (KM) {
-        // the tile's mask words (already published: the S MMA of this tile
-        // waited for the same phase)
-        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&kv_full[st], (it / kNST) & 1, abort_flag))) {
+        // the tile's mask words, published with its V^T
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&v_full[st], (it / kNST) & 1, abort_flag))) {
           alive = false;
           break;
         }
@@ -413,8 +442,6 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
       } else if (m == -INFINITY) {
         m = mxa;                                    // first visible key(s) of this row
       }
-      m_state[h * 128 + r] = m;
-      mbar_arrive(&m_ready[h]);                     // releases the store to the head's next tile
       // P V of the previous tile must be done: it reads the P buffer, and a
       // rescale of O must not race its accumulation
       if (it > 0 &&
@@ -422,6 +449,11 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
         alive = false;
         break;
       }
+      // publish the max only now: whoever takes the head's next tile then
+      // knows this wait has passed, so its own pv_done wait is at most one
+      // phase ahead of the barrier (a parity wait two phases behind would pass)
+      m_state[h * 128 + r] = m;
+      mbar_arrive(&m_ready[h]);
       if (__any_sync(0xffffffffu, resc)) {
         // O_h (and its row-sum column) *= alpha, sixteen columns at a time
         tc_fence_after_sync();
@@ -458,7 +490,7 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
       }
       fence_proxy_async_smem();                     // P visible to the tensor core
       tc_fence_before_sync();                       // and the rescale's TMEM stores ordered before it
-      mbar_arrive(&p_full[h]);
+      mbar_arrive(&p_full[2 * h + (it & 1)]);
     }
     // ------------------------------------------------ normalise and store
     // each head is finished by the warpgroup that took its last tile
