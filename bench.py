@@ -458,6 +458,106 @@ def run_decode(S, args, rank, world, peaks, peaks_src):
     }
 
 
+# ----------------------------------------------------------------- the other workloads
+# The single SmolLM2-135M block, the four SmolLM3-shaped blocks and the
+# left-padded 125M-class block: each step runs every block of the workload
+# through smol_block_forward (bf16 residual stream between blocks).
+OTHER_CONFIGS = ("smollm2_block_b1_t128", "smollm3_4blocks_b4_t4096", "slm125m_block_leftpad_b16_t1024")
+
+
+def block_flops(wl, lengths=None):
+    """Algorithmic FLOPs of one step of a block workload: the projections on
+    valid tokens and causal-exact attention pairs over each sequence's valid
+    part (left padding excluded)."""
+    d, H, KV, hd, I = wl.hidden, wl.n_heads, wl.n_kv_heads, wl.head_dim, wl.intermediate
+    lin_per_token = 2 * ((H + 2 * KV) * hd * d + d * H * hd + 3 * I * d)
+    L = np.full(wl.B, wl.T, dtype=np.int64) if lengths is None else np.asarray(lengths, dtype=np.int64)
+    attn = int(np.sum(4 * hd * H * L * (L + 1) // 2))
+    return wl.n_layers * (lin_per_token * int(L.sum()) + attn), int(L.sum())
+
+
+def oracle_block_tokens_per_s(inp, n_tokens):
+    """The oracle on a bounded sample of a block workload: the first n_tokens
+    valid tokens of sequence 0 through every block (causal, so those rows are
+    exactly the workload's own); tokens per second through all blocks."""
+    from oracle import oracle as O
+    wl = inp.wl
+    f32 = lambda t: t.detach().float().cpu().numpy()
+    cfg_o = O.Config(wl.hidden, wl.n_heads, wl.n_kv_heads, wl.head_dim, wl.intermediate, wl.n_layers,
+                     0, wl.max_pos, wl.rms_eps, wl.rope_theta)
+    layers_o = [O.BlockWeights(**{k: f32(v) for k, v in lw.items()}) for lw in inp.layers]
+    vs0 = 0 if inp.valid_start is None else int(inp.valid_start[0])
+    x = f32(inp.x)[:1, vs0:vs0 + n_tokens]
+    t0 = time.perf_counter()
+    for l, w in enumerate(layers_o):
+        x = O.block_forward(cfg_o, w, x, layer=l)
+    dt = time.perf_counter() - t0
+    return x.shape[1] / dt, x.shape[1], dt
+
+
+def run_block_configs(S, args, rank, world, peaks, with_oracle):
+    out = {}
+    peak_tf = peaks["bf16_tflops"]
+    for name in OTHER_CONFIGS:
+        wl = synth.WORKLOADS[name]
+        cfg = S.config_of(wl)
+        inp = synth.generate(wl, seed=rank, device="cuda")
+        packed = S.prepare_weights(cfg, inp.layers)
+        ws = S.alloc_workspace(cfg, S.OP_BLOCK, wl.B, wl.T)
+        x = inp.x
+        bufs = [torch.empty_like(x), torch.empty_like(x)]
+        vs = inp.valid_start
+
+        def step():
+            cur = x
+            for l in range(wl.n_layers):
+                S.block_forward(cfg, packed, l, cur, bufs[l & 1], ws, valid_start=vs)
+                cur = bufs[l & 1]
+
+        for _ in range(args.warmup):
+            step()
+        if S.workspace_status(ws) != S.OK:
+            raise RuntimeError(f"a kernel reported a timeout during warm-up ({name})")
+        launches = S.last_launch_count() * wl.n_layers
+        tot, _ = kernel_breakdown(S, step)
+        graph = capture_graph(step)
+        ms = max_over_ranks(time_steps(graph.replay if graph else step, args.steps, world), world)
+        lengths = None if inp.lengths is None else inp.lengths.cpu().numpy()
+        flops, valid_tokens = block_flops(wl, lengths)
+        padded_flops, _ = block_flops(wl, None)
+        tf = flops / (ms / 1e3) / 1e12
+        ent = {
+            "workload": f"{name}: {wl.n_layers} block(s) d={wl.hidden} H={wl.n_heads} KV={wl.n_kv_heads} "
+                        f"hd={wl.head_dim} I={wl.intermediate}, batch {wl.B} x {wl.T}"
+                        + (", left-padded" if vs is not None else ""),
+            "ms_per_step": round(ms, 4), "tokens_per_s": round(valid_tokens * world / (ms / 1e3), 1),
+            "valid_tokens_per_step": valid_tokens,
+            "timing": "CUDA-graph replay of the step" if graph else "eager calls",
+            "algorithmic_flop_per_step": flops, "tflops": round(tf, 2),
+            "tensor_frac": round(tf / peak_tf, 4), "peak": peak_tf, "peak_unit": "TFLOP/s (measured bf16 burst)",
+            "gpu_launches": launches * args.steps,
+            "kernel_ms_per_step": {k: round(v, 4) for k, v in sorted(tot.items(), key=lambda kv: -kv[1])},
+        }
+        if vs is not None:
+            ent["padded_flop_per_step"] = padded_flops
+            ent["tensor_frac_padded_tokens"] = round(padded_flops / (ms / 1e3) / 1e12 / peak_tf, 4)
+        if with_oracle:
+            cpu_inp = synth.generate(wl, seed=rank, device="cpu")
+            n_valid = wl.T if lengths is None else int(lengths[0])
+            n = min(n_valid, 16)
+            _, _, t_probe = oracle_block_tokens_per_s(cpu_inp, n)
+            n = int(min(n_valid, max(n, n * 4.0 / max(t_probe, 1e-3))))   # about 4 s
+            v, n, dt = oracle_block_tokens_per_s(cpu_inp, n)
+            ent["cpu_baseline"] = {"value": round(v, 2), "unit": "tokens/s", "cores": cores_used(),
+                                   "kind": "oracle",
+                                   "sample": f"sequence 0, first {n} valid tokens through all {wl.n_layers} "
+                                             f"block(s), numpy fp64 ({dt:.1f} s)"}
+        out[name] = ent
+        del inp, packed, ws, x, bufs, graph
+        torch.cuda.empty_cache()
+    return out
+
+
 # ----------------------------------------------------------------- the oracle (CPU) arm
 def oracle_sample_seconds(inp_cpu, cfg_o, n_tokens, layers_o, E, fn):
     from oracle import oracle as O
@@ -566,6 +666,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode-step measurement")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="skip the single-block, SmolLM3-shaped and left-padded block workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the oracle")
     ap.add_argument("--profile-case", choices=["prefill", "decode"],
                     help="run one untimed step of the workload with --profile-layers blocks and exit "
@@ -587,6 +689,9 @@ def main():
     out, (inp, _) = run_prefill(S, args, rank, world, peaks, peaks_src)
     if not args.no_decode:
         out["decode"] = run_decode(S, args, rank, world, peaks, peaks_src)
+    if not args.no_other_configs:
+        out["other_configs"] = run_block_configs(S, args, rank, world, peaks,
+                                                 rank == 0 and world == 1 and not args.no_cpu_baseline)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(inp)
     if rank == 0:

@@ -28,6 +28,18 @@
  *   - Kernels never spin without a bound.  A bounded wait that gives up
  *     writes a nonzero code into the workspace's status word and the kernel
  *     returns; smol_workspace_status reads that word.
+ *   - Numeric range: the residual stream between and inside blocks and every
+ *     tensor-core operand are f16 (fp32 accumulation), so activations must
+ *     stay below 65504 in magnitude (SmolLM2-shaped activations are orders of
+ *     magnitude smaller).  A value that would round to infinity when the
+ *     input is converted or a residual sum is written, or a non-finite row,
+ *     is recorded in the status word (SMOL_ERR_RANGE); the outputs of that
+ *     call are then not defined.
+ *   - Input values that kernels clamp (a token id outside [0, V), a cache
+ *     length or left-padding start outside its stated range) are recorded in
+ *     the status word (SMOL_ERR_INPUT); the rows concerned are not defined.
+ *   - The status word keeps the first code written until
+ *     smol_workspace_status reads and clears it.
  *   - Supported shapes: head_dim in {64, 128}; hidden == n_heads * head_dim;
  *     n_heads % n_kv_heads == 0 with a group of at most 8; hidden, intermediate
  *     and vocab multiples of 64; T >= 1; rows (B*T) up to 2^31-1.
@@ -101,7 +113,9 @@ typedef enum smol_status {
   SMOL_ERR_WORKSPACE = -5,         /* workspace or packed buffer too small           */
   SMOL_ERR_CUDA = -6,              /* a CUDA runtime call or launch failed           */
   SMOL_ERR_DEVICE = -7,            /* current device is not a compute-capability 10.3 GPU */
-  SMOL_ERR_TIMEOUT = -8            /* a kernel's bounded wait gave up (status word)  */
+  SMOL_ERR_TIMEOUT = -8,           /* a kernel's bounded wait gave up (status word)  */
+  SMOL_ERR_RANGE = -9,             /* a value beyond the f16 range (status word)     */
+  SMOL_ERR_INPUT = -10             /* an input value out of range (status word)      */
 } smol_status;
 
 /* Operation selector for smol_workspace_bytes. */
@@ -109,7 +123,8 @@ enum { SMOL_OP_BLOCK = 1, SMOL_OP_MODEL = 2, SMOL_OP_DECODE = 3 };
 
 /* Element type of the residual stream (x and out) of smol_block_forward.
  * SMOL_ACT_F32 keeps the residual stream in fp32 across block calls (the
- * projections still read a bf16 copy as their tensor-core operand). */
+ * projections still read an f16 copy as their tensor-core operand, and the
+ * residual h inside the block is f16). */
 enum { SMOL_ACT_BF16 = 0, SMOL_ACT_F32 = 1 };
 
 /* ---------------------------------------------------------------------------
@@ -118,8 +133,9 @@ enum { SMOL_ACT_BF16 = 0, SMOL_ACT_F32 = 1 };
  * on `stream`:
  *   - the attention and MLP RMSNorm weights are folded into the columns of
  *     the projections that consume them (W'[j,k] = W[j,k] * w_norm[k],
- *     rounded to bf16), and the final-norm weight into a copy of the tied
- *     head, so each norm reduces to a per-row scale rsqrt(mean(x^2)+eps)
+ *     rounded to f16, the tensor-core operand type of every projection), and
+ *     the final-norm weight into an f16 copy of the tied head, so each norm
+ *     reduces to a per-row scale rsqrt(mean(x^2)+eps)
  *     ([M1] section 2; [M5] RMSNorm formula);
  *   - Wq, Wk, Wv are stacked into one [(H+2KV)*hd, d] matrix;
  *   - Wgate and Wup are interleaved in groups of 64 rows;
@@ -154,7 +170,8 @@ size_t smol_workspace_bytes(const smol_config *cfg, int op, int B, int T);
  *                section 4), and the position id of token t is
  *                t - valid_start[b] ([M4] position_ids).  Padding rows get an
  *                attention output of 0; their `out` rows are finite but are
- *                not defined by the method.  Each value must lie in [0, T].
+ *                not defined by the method.  Each value must lie in [0, T]
+ *                (a value outside is clamped and recorded as SMOL_ERR_INPUT).
  *   k_out,v_out  device [B, KV, T, hd] bf16 or NULL: post-RoPE keys and the
  *                values, the per-layer cache entries of [M1] section 4.
  *   ws           device workspace of at least
@@ -184,8 +201,9 @@ int smol_block_forward_masked(const smol_config *cfg, const void *packed, int la
 /* ---------------------------------------------------------------------------
  * smol_model_forward: embedding -> cfg->n_layers blocks -> final RMSNorm ->
  * tied lm_head ([M1] section 7 SmolLM2.forward; [M4] SmolLM2Model.forward).
- *   ids          device int32 [B, T], each in [0, V) (out-of-range ids are
- *                clamped into range by the gather).
+ *   ids          device int32 [B, T], each in [0, V) (an out-of-range id is
+ *                clamped into range by the gather and recorded as
+ *                SMOL_ERR_INPUT in the status word).
  *   valid_start  device int32 [B] or NULL (as in smol_block_forward).
  *   logits       device [B, T, V] bf16.
  *   ws           >= smol_workspace_bytes(cfg, SMOL_OP_MODEL, B, T) bytes.
@@ -211,7 +229,8 @@ int smol_model_forward_masked(const smol_config *cfg, const void *packed, const 
  * ones).  Per-block NoPE flags and windows apply as in the other calls.
  *   ids        device int32 [B, T].
  *   cache_len  device int32 [B], each in [0, min(S_max, max_pos - T)]
- *              (clamped into that range on the device).
+ *              (clamped into that range on the device; a value outside is
+ *              recorded as SMOL_ERR_INPUT in the status word).
  *   k_cache, v_cache  device [L, B, KV, S_max, hd] bf16, post-RoPE keys; read only.
  *   k_new, v_new      device [L, B, KV, T, hd] bf16 outputs: the new tokens'
  *              post-RoPE keys and values per layer, for the caller to append
@@ -235,7 +254,9 @@ int smol_prefill_with_cache(const smol_config *cfg, const void *packed, const in
  *              at position cache_len[b] and attends over those entries plus
  *              its own key/value, with no other mask.  Each value must lie in
  *              [0, S_max] and cache_len[b] < max_pos (not checked on the host:
- *              values are clamped to [0, min(S_max, max_pos-1)] on the device).
+ *              values are clamped to [0, min(S_max, max_pos-1)] on the device,
+ *              and a clamped value is recorded as SMOL_ERR_INPUT in the status
+ *              word).
  *   k_cache,v_cache device [L, B, KV, S_max, hd] bf16, post-RoPE keys (stored
  *              "after RoPE, before GQA expansion", [M1] section 4).  Read only.
  *   k_new,v_new device [L, B, KV, hd] bf16 outputs: this token's post-RoPE key
@@ -313,14 +334,25 @@ int smol_decode_noalloc_status(void *stream);
 int smol_sample(const void *logits, int B, int V, long long ld, float temperature, int top_k,
                 float top_p, int do_sample, const float *uniform, int32_t *next, void *stream);
 
-/* Reads (synchronising `stream`) and clears the workspace status word written
- * by kernels whose bounded waits gave up.  Returns SMOL_OK, SMOL_ERR_TIMEOUT
- * or SMOL_ERR_CUDA.  Not meant for the hot path. */
+/* Reads (synchronising `stream`) and clears the workspace status word.
+ * Returns SMOL_OK, SMOL_ERR_TIMEOUT (a bounded wait gave up), SMOL_ERR_RANGE
+ * (a value beyond the f16 range), SMOL_ERR_INPUT (an input value out of
+ * range) -- whichever a kernel recorded first since the last read -- or
+ * SMOL_ERR_CUDA.  Not meant for the hot path. */
 int smol_workspace_status(void *ws, void *stream);
 
 /* Number of kernels the most recent forward/decode call on this thread
  * launched (0 after an argument error). */
 int smol_last_launch_count(void);
+
+/* For tests of the failure path only (no counterpart on the pages): the limit,
+ * in nanoseconds, of the bounded waits of the prefill attention kernel in
+ * launches made from now on by any thread (0 restores the default of 1 s).  A
+ * limit shorter than the kernel's own latencies makes a wait give up: the
+ * kernel drains the copies and MMAs it issued (those drains keep the 1 s
+ * limit), records SMOL_ERR_TIMEOUT in the status word and returns, leaving its
+ * outputs undefined; the device stays usable. */
+void smol_set_wait_limit_ns(unsigned long long ns);
 
 /* ---------------------------------------------------------------------------
  * Per-launch timing, for measurement only (off unless started; not for use

@@ -74,7 +74,7 @@ struct AtCfg {
   static constexpr int OFF_MASK = OFF_P + GH * P_BYTES;   // [kNST][4] key-visibility words
   static constexpr int OFF_MST = OFF_MASK + kNST * 16;  // [GH][128] running row max per head
   static constexpr int OFF_BAR = OFF_MST + GH * 128 * 4;
-  static constexpr int NBAR = 1 + 4 * kNST + 4 + 4 * GH + 1;
+  static constexpr int NBAR = 1 + 4 * kNST + 4 + 4 * GH + 3;
   static constexpr int SMEM = 1024 + OFF_BAR + NBAR * 8 + 16;
   static_assert(GH >= 1 && GH * kNO <= kTmemS, "O accumulators must fit below the S buffers");
   static_assert(SMEM <= 232448, "shared memory per CTA");
@@ -88,6 +88,7 @@ struct AtParams {
   float scale_log2;
   int window;               // > 0: query t sees keys j > t - window only
   int Tk, q_off;            // keys per sequence; key index of query 0
+  unsigned long long wait_ns;   // limit of the bounded waits (drains keep 1 s)
   int *status;
 };
 
@@ -160,8 +161,8 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
   uint64_t *p_full = s_free + 2;
   uint64_t *pv_done = p_full + 2 * GH;        // [GH] P V of the head done
   uint64_t *m_ready = pv_done + GH;           // [GH] running max of the head's rows stored (128 arrivals)
-  uint64_t *drain = m_ready + GH;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  uint64_t *drain = m_ready + GH;             // [3] one per MMA-issuing warp (warps 1, 2, 3)
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 3);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -203,7 +204,7 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
       mbar_init(&pv_done[h], 1);
       mbar_init(&m_ready[h], 128);
     }
-    mbar_init(drain, 1);
+    for (int i = 0; i < 3; ++i) mbar_init(&drain[i], 1);
     *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tmQ);
@@ -234,7 +235,6 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
     // K of a tile is released once its S MMAs are done and V only after its
     // P V MMAs, so K runs one tile ahead: K(0), K(1), V(0), K(2), V(1), ...
     griddep_wait();                               // q, k and V^T come from the preceding kernel
-    int dummy = 0;
     int nk = 0, nv = 0;                           // K and V tiles issued (for the drain)
     bool ok = true;
     if (lane == 0) {
@@ -247,7 +247,7 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
       if (ik < ntiles) {
         const int st = ik % kNST;
         if (lane == 0) {
-          ok = mbar_wait_bounded(&k_empty[st], ((ik / kNST) & 1) ^ 1, abort_flag);
+          ok = mbar_wait_bounded(&k_empty[st], ((ik / kNST) & 1) ^ 1, abort_flag, p.wait_ns);
           if (ok) {
             mbar_arrive_expect_tx(&k_full[st], C::K_BYTES);
             tma_load_2d(sK + st * C::K_BYTES, &tmK, &k_full[st], 0, (b * p.KV + kvh) * Tk + (j_lo + ik) * kBK);
@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
       }
       if (it < 0) continue;
       const int j = j_lo + it, st = it % kNST;
-      if (lane == 0) ok = mbar_wait_bounded(&v_empty[st], ((it / kNST) & 1) ^ 1, abort_flag);
+      if (lane == 0) ok = mbar_wait_bounded(&v_empty[st], ((it / kNST) & 1) ^ 1, abort_flag, p.wait_ns);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       if constexpr (KM) {
@@ -284,18 +284,15 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
     }
     if (lane == 0) {
       // wait (bounded) until every copy this thread issued has landed
-      if (!mbar_wait_bounded(q_full, 0, reinterpret_cast<volatile int *>(&dummy)))
-        at_status(p.status, kAtTimeoutDrain);
+      if (!mbar_wait_drain(q_full, 0)) at_status(p.status, kAtTimeoutDrain);
       if (!ok) {
         at_status(p.status, kAtTimeoutLoad);
         *abort_flag = 1;
         for (int i = nk > kNST ? nk - kNST : 0; i < nk; ++i)
-          if (!mbar_wait_bounded(&k_full[i % kNST], (uint32_t)((i / kNST) & 1),
-                                 reinterpret_cast<volatile int *>(&dummy)))
+          if (!mbar_wait_drain(&k_full[i % kNST], (uint32_t)((i / kNST) & 1)))
             at_status(p.status, kAtTimeoutDrain);
         for (int i = nv > kNST ? nv - kNST : 0; i < nv; ++i)
-          if (!mbar_wait_bounded(&v_full[i % kNST], (uint32_t)((i / kNST) & 1),
-                                 reinterpret_cast<volatile int *>(&dummy)))
+          if (!mbar_wait_drain(&v_full[i % kNST], (uint32_t)((i / kNST) & 1)))
             at_status(p.status, kAtTimeoutDrain);
       }
     }
@@ -303,11 +300,11 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
     if (lane == 0) {
       // ---------------------------------------------------- S = Q_h K^T issuer
       constexpr uint32_t kIdescS = idesc_f16_f32(kBQ, kBK);
-      bool ok = mbar_wait_bounded(q_full, 0, abort_flag), any = false;
+      bool ok = mbar_wait_bounded(q_full, 0, abort_flag, p.wait_ns), any = false;
       for (int s = 0; s < nslots && ok; ++s) {
         const int it = s / GH, h = s - it * GH, sb = s & 1, st = it % kNST;
-        if (!mbar_wait_bounded(&s_free[sb], ((s >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
-        if (h == 0 && !mbar_wait_bounded(&k_full[st], (it / kNST) & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait_bounded(&s_free[sb], ((s >> 1) & 1) ^ 1, abort_flag, p.wait_ns)) { ok = false; break; }
+        if (h == 0 && !mbar_wait_bounded(&k_full[st], (it / kNST) & 1, abort_flag, p.wait_ns)) { ok = false; break; }
         tc_fence_after_sync();
         const uint64_t a = sdesc_kmajor_sw128(smem_u32(sQ + h * C::Q_BYTES));
         const uint64_t bk = sdesc_kmajor_sw128(smem_u32(sK + st * C::K_BYTES));
@@ -322,10 +319,9 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
         at_status(p.status, kAtTimeoutMma);
         *abort_flag = 1;
         if (any) {
-          umma_commit(drain);
-          int dummy = 0;
-          if (!mbar_wait_bounded(drain, 0, reinterpret_cast<volatile int *>(&dummy)))
-            at_status(p.status, kAtTimeoutDrain);
+          // wait for this warp's MMAs already issued before TMEM is freed
+          umma_commit(&drain[warp - 1]);
+          if (!mbar_wait_drain(&drain[warp - 1], 0)) at_status(p.status, kAtTimeoutDrain);
         }
       }
     }
@@ -340,8 +336,8 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
       bool ok = true, any = false;
       for (int s = par; s < nslots && ok; s += 2) {
         const int it = s / GH, h = s - it * GH, st = it % kNST;
-        if (!mbar_wait_bounded(&p_full[2 * h + (it & 1)], (it >> 1) & 1, abort_flag)) { ok = false; break; }
-        if (!mbar_wait_bounded(&v_full[st], (it / kNST) & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait_bounded(&p_full[2 * h + (it & 1)], (it >> 1) & 1, abort_flag, p.wait_ns)) { ok = false; break; }
+        if (!mbar_wait_bounded(&v_full[st], (it / kNST) & 1, abort_flag, p.wait_ns)) { ok = false; break; }
         tc_fence_after_sync();
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb) {
@@ -359,10 +355,9 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
         at_status(p.status, kAtTimeoutMma);
         *abort_flag = 1;
         if (any) {
-          umma_commit(drain);
-          int dummy = 0;
-          if (!mbar_wait_bounded(drain, 0, reinterpret_cast<volatile int *>(&dummy)))
-            at_status(p.status, kAtTimeoutDrain);
+          // wait for this warp's MMAs already issued before TMEM is freed
+          umma_commit(&drain[warp - 1]);
+          if (!mbar_wait_drain(&drain[warp - 1], 0)) at_status(p.status, kAtTimeoutDrain);
         }
       }
     }
@@ -384,7 +379,7 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
       const int k0 = (j_lo + it) * kBK;             // first key of the tile
       const bool need_mask =
           KM || (k0 + kBK - 1 > qo + q0) || (k0 < vs) || (p.window > 0 && k0 <= qo + last_q - p.window);
-      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&s_full[sb], (s >> 1) & 1, abort_flag))) {
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&s_full[sb], (s >> 1) & 1, abort_flag, p.wait_ns))) {
         alive = false;
         break;
       }
@@ -399,7 +394,7 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
       uint32_t vis[4] = {~0u, ~0u, ~0u, ~0u};
       if constexpr (KM) {
         // the tile's mask words, published with its V^T
-        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&v_full[st], (it / kNST) & 1, abort_flag))) {
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&v_full[st], (it / kNST) & 1, abort_flag, p.wait_ns))) {
           alive = false;
           break;
         }
@@ -428,7 +423,7 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
       // its previous tile
       float m = -INFINITY;
       if (it > 0) {
-        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&m_ready[h], (it - 1) & 1, abort_flag))) {
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&m_ready[h], (it - 1) & 1, abort_flag, p.wait_ns))) {
           alive = false;
           break;
         }
@@ -445,7 +440,7 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
       // P V of the previous tile must be done: it reads the P buffer, and a
       // rescale of O must not race its accumulation
       if (it > 0 &&
-          !__all_sync(0xffffffffu, mbar_wait_bounded(&pv_done[h], (it - 1) & 1, abort_flag))) {
+          !__all_sync(0xffffffffu, mbar_wait_bounded(&pv_done[h], (it - 1) & 1, abort_flag, p.wait_ns))) {
         alive = false;
         break;
       }
@@ -498,7 +493,7 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
     for (int h = 0; h < GH; ++h) {
       if (((ntiles - 1) * GH + h) % C::NG != g) continue;
       if (alive &&
-          !__all_sync(0xffffffffu, mbar_wait_bounded(&pv_done[h], (ntiles - 1) & 1, abort_flag)))
+          !__all_sync(0xffffffffu, mbar_wait_bounded(&pv_done[h], (ntiles - 1) & 1, abort_flag, p.wait_ns)))
         alive = false;
       if (!alive) break;
       tc_fence_after_sync();
@@ -574,6 +569,7 @@ cudaError_t launch_ghk(const AttnParams &a, const CUtensorMap &tq, const CUtenso
   p.window = a.window;
   p.Tk = a.Tk > 0 ? a.Tk : a.T;
   p.q_off = a.q_off;
+  p.wait_ns = a.wait_ns ? a.wait_ns : kWaitTimeoutNs;
   p.status = a.status;
   dim3 grid((unsigned)(a.B * a.KV * p.n_hsub), (unsigned)cdiv(a.T, kBQ), 1u);
   // as a programmatic dependent: CTAs set up barriers and TMEM while the

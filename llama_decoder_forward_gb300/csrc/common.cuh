@@ -141,6 +141,7 @@ struct AttnParams {
   int Tk;                 // keys per sequence (k: [B, KV, Tk, hd], v_t pitch T_pad >= Tk); 0: T
   int q_off;              // key index of query 0 (queries are the last T of Tk keys); 0 with Tk = T
   int pdl;                // tcgen05 kernel: launch as a programmatic dependent of the preceding kernel
+  unsigned long long wait_ns;   // tcgen05 kernel: bounded-wait limit, 0 = the default 1 s
 };
 cudaError_t launch_flash_attention(const AttnParams &p, cudaStream_t stream);
 // tcgen05 attention (head_dim 64, group of at most 4 query heads); needs v_t.
@@ -153,12 +154,24 @@ cudaError_t launch_sample(const void *logits, long long ld, int B, int V, float 
                           float top_p, int do_sample, const float *uniform, int *next, cudaStream_t st);
 
 // ------------------------------------------------------------------ small kernels
+// A per-sequence input value (left-padding start, cache length) that the
+// kernels clamp into [0, vmax]: the first kernel of a call checks it once per
+// sequence (the row with index a multiple of rows_per_seq) and records a value
+// outside the range in the status word.  vals == nullptr: nothing to check.
+struct SeqCheck {
+  const int *vals;
+  int rows_per_seq;
+  int vmax;
+};
+// The input conversions record out-of-range ids (embedding), values beyond
+// the f16 range and the SeqCheck in the status word.
 cudaError_t launch_embed_rows(const int *ids, const bf16 *embed, int vocab, int d, long long rows,
-                              f16 *x16, float *x_f32, float *ssq, cudaStream_t stream);
-cudaError_t launch_row_ssq(const bf16 *x, long long rows, int d, f16 *x16, float *ssq,
-                           cudaStream_t stream);
-cudaError_t launch_row_ssq_f32(const float *x, long long rows, int d, f16 *x16, float *ssq,
-                               cudaStream_t stream);
+                              f16 *x16, float *x_f32, float *ssq, int *status, SeqCheck chk,
+                              cudaStream_t stream);
+cudaError_t launch_row_ssq(const bf16 *x, long long rows, int d, f16 *x16, float *ssq, int *status,
+                           SeqCheck chk, cudaStream_t stream);
+cudaError_t launch_row_ssq_f32(const float *x, long long rows, int d, f16 *x16, float *ssq, int *status,
+                               SeqCheck chk, cudaStream_t stream);
 cudaError_t launch_scale_cols_copy(const bf16 *src, const bf16 *norm_w, long long rows, int cols,
                                    f16 *dst, cudaStream_t stream);
 cudaError_t launch_interleave_gate_up(const bf16 *wg, const bf16 *wu, const bf16 *norm_w, int I,

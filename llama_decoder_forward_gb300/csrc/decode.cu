@@ -1153,7 +1153,8 @@ cudaError_t run_decode(const DecodeArgs &a, void *ws, int sms, cudaStream_t st, 
 #define DEC_LAUNCH(expr) DEC_LAUNCH_K(SMOL_K_OTHER, expr)
 
   DEC_LAUNCH(launch_zero_ints(counters, B * KV, st));
-  DEC_LAUNCH_K(SMOL_K_EMBED, launch_embed_rows(a.ids, a.embed, V, d, B, x, nullptr, ssq_a, st));
+  DEC_LAUNCH_K(SMOL_K_EMBED, launch_embed_rows(a.ids, a.embed, V, d, B, x, nullptr, ssq_a, status,
+                                                SeqCheck{a.cache_len, 1, min(a.S_max, c.max_pos - 1)}, st));
 
   const float sl2 = 1.4426950408889634f / sqrtf((float)hd);
   for (int l = 0; l < L; ++l) {

@@ -231,6 +231,8 @@ __global__ void __launch_bounds__(kSkThreads, 1)
 #pragma unroll
     for (int o = 1; o < GPR; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
     if (row_ok && (t % GPR) == 0 && p.ssq_out) atomicAdd(p.ssq_out + row, part);
+    // the sum of squares of the rounded outputs is finite iff none overflowed
+    if (row_ok && (t % GPR) == 0 && !isfinite(part)) set_status(p.status, kDevRange);
   } else if constexpr (EPI == kEpiSwiglu) {
     // columns 0..15 gate, 16..31 up of act columns 16u .. 16u+15
     const int row = threadIdx.x >> 2, c = (threadIdx.x & 3) * 4;

@@ -306,8 +306,12 @@ __device__ __forceinline__ bool epi_residual_tma(const GemmParams &p, EpiCtx &e,
   const int nu = residual_units<BN>(p, e);
   if (nu == 0) return true;
   const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(e.rbar, e.rphase, abort_flag));
+  if (!ok) {
+    mbar_wait_drain(e.rbar, e.rphase);            // the residual boxes land before the CTA exits
+    e.rphase ^= 1u;
+    return false;
+  }
   e.rphase ^= 1u;
-  if (!ok) return false;
   const bool resid_f16 = p.resid_f16 != nullptr;
   float part = 0.f;
 #pragma unroll 1
@@ -334,6 +338,8 @@ __device__ __forceinline__ bool epi_residual_tma(const GemmParams &p, EpiCtx &e,
     stg_tma_store(&e.maps->out, tile, e.n0 + c, e.row0, e.lane, e.rows_valid);
   }
   if (e.lane < e.rows_valid && p.ssq_out) atomicAdd(p.ssq_out + e.row0 + e.lane, part);
+  // the sum of squares of the rounded outputs is finite iff none overflowed
+  if (e.lane < e.rows_valid && !isfinite(part)) set_status(p.status, kDevRange);
   return true;
 }
 
@@ -358,6 +364,7 @@ template <int BN>
 __device__ __forceinline__ void epi_residual_lane(const GemmParams &p, EpiCtx &e) {
   const bool row_ok = e.lane < e.rows_valid;
   float part = 0.f;
+  bool big = false;                               // an fp32 output whose f16 copy overflows
   uint8_t *buf = e.st, *st16 = e.st + kStgBytes;
   const long long row0_off = (long long)e.row0 * p.ldo;
   // unit 0's residual was prefetched by the caller into buf
@@ -377,7 +384,10 @@ __device__ __forceinline__ void epi_residual_lane(const GemmParams &p, EpiCtx &e
     for (int q = 0; q < 32; ++q) v[q] += __uint_as_float(r[q]);
     if (p.out_f32) {
 #pragma unroll
-      for (int q = 0; q < 32; ++q) part = fmaf(v[q], v[q], part);
+      for (int q = 0; q < 32; ++q) {
+        part = fmaf(v[q], v[q], part);
+        big |= p.out && p.out_is_f16 && !(fabsf(v[q]) < kF16Overflow);
+      }
       stg_put_f32(buf, e.lane, v);                // own row only: no hazard with other lanes
     } else {
 #pragma unroll
@@ -401,6 +411,7 @@ __device__ __forceinline__ void epi_residual_lane(const GemmParams &p, EpiCtx &e
   }
   cp_async_wait<0>();
   if (row_ok && p.ssq_out) atomicAdd(p.ssq_out + e.row0 + e.lane, part);
+  if (row_ok && (big || !isfinite(part))) set_status(p.status, kDevRange);
 }
 
 // Gate and up columns come in groups of 64 + 64 per 128 accumulator columns;
@@ -763,10 +774,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         *abort_flag = 1;
         // wait (bounded) for the copies still in flight before the CTA exits
         const long long first = issued > C::STAGES ? issued - C::STAGES : 0;
-        int dummy = 0;
         for (long long j = first; j < issued; ++j) {
-          if (!mbar_wait_bounded(&full[j % C::STAGES], (uint32_t)((j / C::STAGES) & 1),
-                                 reinterpret_cast<volatile int *>(&dummy)))
+          if (!mbar_wait_drain(&full[j % C::STAGES], (uint32_t)((j / C::STAGES) & 1)))
             record_status(p.status, kDevTimeoutDrain);
         }
       }
@@ -821,9 +830,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           // wait (bounded) for the MMAs already issued before TMEM is freed
           if constexpr (PAIR == 1) umma_commit(drain);
           else umma_commit_pair(drain, 0x1);
-          int dummy = 0;
-          if (!mbar_wait_bounded(drain, 0, reinterpret_cast<volatile int *>(&dummy)))
-            record_status(p.status, kDevTimeoutDrain);
+          if (!mbar_wait_drain(drain, 0)) record_status(p.status, kDevTimeoutDrain);
         }
       }
     }
@@ -877,10 +884,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (lane == 0) record_status(p.status, kDevTimeoutEpilogue);
         *abort_flag = 1;
         cp_async_wait<0>();                       // no copy in flight when the CTA exits
-        if (resid_tma && residual_units<BN>(p, e) > 0) {
-          int dummy = 0;
-          mbar_wait_bounded(e.rbar, e.rphase, reinterpret_cast<volatile int *>(&dummy));
-        }
+        if (resid_tma && residual_units<BN>(p, e) > 0) mbar_wait_drain(e.rbar, e.rphase);
         break;
       }
       tc_fence_after_sync();

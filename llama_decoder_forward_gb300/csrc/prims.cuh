@@ -21,7 +21,22 @@ enum DeviceStatus : int {
   kDevTimeoutMma = 0x102,
   kDevTimeoutEpilogue = 0x103,
   kDevTimeoutDrain = 0x104,
+  // a value went beyond the f16 range of the residual stream or of a
+  // tensor-core operand (|x| >= 65520 rounds to infinity), or a row's sum of
+  // squares is not finite
+  kDevRange = 0x301,
+  // an input value was outside its range (a token id outside [0, V), a cache
+  // length outside [0, min(S_max, max_pos - 1)]) and was clamped
+  kDevBadInput = 0x401,
 };
+
+// Largest |x| that rounds to a finite f16 (65504 + half an ulp).
+constexpr float kF16Overflow = 65520.f;
+
+// Records a device status code (the first one written stays).
+__device__ __forceinline__ void set_status(int *status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -82,18 +97,29 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
 
 // Wait for the phase with the given parity to complete.  Gives up (returns
 // false) when `abort_flag` (shared memory, set by another role that gave up)
-// becomes nonzero or after kWaitTimeoutNs.
+// becomes nonzero or after limit_ns nanoseconds (kWaitTimeoutNs unless a
+// launch passes its own limit).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
-                                                  volatile int *abort_flag) {
+                                                  volatile int *abort_flag,
+                                                  uint64_t limit_ns = kWaitTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
+  const uint32_t hint = limit_ns < 20000u ? static_cast<uint32_t>(limit_ns) : 20000u;
   const uint64_t t0 = global_timer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 8; ++i)
-      if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+      if (mbar_try_wait_sleep(bar, parity, hint)) return true;
     if (*abort_flag) return false;
-    if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
   }
+}
+
+// The wait of a drain after a role gave up: for copies or MMAs that were
+// issued and will complete, so it ignores the abort flag and keeps the full
+// kWaitTimeoutNs limit whatever limit the launch's other waits have.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity) {
+  int never = 0;
+  return mbar_wait_bounded(bar, parity, reinterpret_cast<volatile int *>(&never), kWaitTimeoutNs);
 }
 
 // Non-blocking test for the completion of the phase with the given parity.

@@ -7,18 +7,33 @@
 
 namespace smol {
 
+__device__ __forceinline__ void seq_check(const SeqCheck &chk, long long r, int lane, int *status) {
+  if (chk.vals && lane == 0 && r % chk.rows_per_seq == 0) {
+    const int v = chk.vals[r / chk.rows_per_seq];
+    if (v < 0 || v > chk.vmax) set_status(status, kDevBadInput);
+  }
+}
+
 // x[r, :] = E[ids[r], :] as an f16 operand copy (x16) and in fp32 (x_f32,
 // optional), and ssq[r] = sum_k x[r,k]^2 (feeds the first RMSNorm).
 // "model.py" (SmolLM2-135M) section 7: embed_tokens(input_ids).  One warp per
-// row, 16-byte loads.  d must be a multiple of 8.
+// row, 16-byte loads.  d must be a multiple of 8.  An id outside [0, V) is
+// clamped into range and recorded in the status word (kDevBadInput); a value
+// beyond the f16 range is recorded too (kDevRange).
 __global__ void embed_rows_kernel(const int *__restrict__ ids, const bf16 *__restrict__ E, int V,
                                   int d, long long rows, f16 *__restrict__ x16,
-                                  float *__restrict__ x_f32, float *__restrict__ ssq) {
+                                  float *__restrict__ x_f32, float *__restrict__ ssq, int *status,
+                                  const SeqCheck chk) {
   const long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= rows) return;
+  seq_check(chk, r, lane, status);
   int id = ids[r];
-  id = id < 0 ? 0 : (id >= V ? V - 1 : id);
+  if (id < 0 || id >= V) {
+    if (lane == 0) set_status(status, kDevBadInput);
+    id = id < 0 ? 0 : V - 1;
+  }
+  bool in_range = true;
   const uint4 *src = reinterpret_cast<const uint4 *>(E + (long long)id * d);
   uint4 *dst = reinterpret_cast<uint4 *>(x16 + r * d);
   float acc = 0.f;
@@ -32,6 +47,7 @@ __global__ void embed_rows_kernel(const int *__restrict__ ids, const bf16 *__res
       f[2 * e] = t.x;
       f[2 * e + 1] = t.y;
       acc += t.x * t.x + t.y * t.y;
+      in_range &= fabsf(t.x) < kF16Overflow && fabsf(t.y) < kF16Overflow;
     }
     dst[c] = make_uint4(pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]), pack_f16x2(f[4], f[5]),
                         pack_f16x2(f[6], f[7]));
@@ -44,38 +60,49 @@ __global__ void embed_rows_kernel(const int *__restrict__ ids, const bf16 *__res
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
   if (lane == 0) ssq[r] = acc;
+  if (!__all_sync(0xffffffffu, in_range) && lane == 0) set_status(status, kDevRange);
 }
 
 // ssq[r] = sum_k x[r,k]^2 for an fp32 row, plus its f16 copy (the tensor-core
-// operand of the next projection).
+// operand of the next projection); values beyond the f16 range (or not finite)
+// are recorded in the status word (kDevRange).
 __global__ void row_ssq_f32_kernel(const float *__restrict__ x, long long rows, int d,
-                                   f16 *__restrict__ x16, float *__restrict__ ssq) {
+                                   f16 *__restrict__ x16, float *__restrict__ ssq, int *status,
+                                   const SeqCheck chk) {
   const long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= rows) return;
+  seq_check(chk, r, lane, status);
   const float4 *src = reinterpret_cast<const float4 *>(x + r * d);
   uint4 *dst = reinterpret_cast<uint4 *>(x16 + r * d);
-  float acc = 0.f;
+  float acc = 0.f, amax = 0.f;
   for (int c = lane; c < d / 8; c += 32) {
     const float4 a = src[2 * c], b = src[2 * c + 1];
     acc += a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w + b.x * b.x + b.y * b.y + b.z * b.z + b.w * b.w;
+    amax = fmaxf(amax, fmaxf(fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))),
+                             fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w)))));
     dst[c] = make_uint4(pack_f16x2(a.x, a.y), pack_f16x2(a.z, a.w), pack_f16x2(b.x, b.y),
                         pack_f16x2(b.z, b.w));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
   if (lane == 0) ssq[r] = acc;
+  // fmaxf ignores NaN: a NaN row shows in the non-finite sum of squares
+  if (!__all_sync(0xffffffffu, amax < kF16Overflow && isfinite(acc)) && lane == 0) set_status(status, kDevRange);
 }
 
 // The same for a bf16 row.
 __global__ void row_ssq_kernel(const bf16 *__restrict__ x, long long rows, int d,
-                               f16 *__restrict__ x16, float *__restrict__ ssq) {
+                               f16 *__restrict__ x16, float *__restrict__ ssq, int *status,
+                               const SeqCheck chk) {
   const long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= rows) return;
+  seq_check(chk, r, lane, status);
   const uint4 *src = reinterpret_cast<const uint4 *>(x + r * d);
   uint4 *dst = reinterpret_cast<uint4 *>(x16 + r * d);
   float acc = 0.f;
+  bool in_range = true;
   for (int c = lane; c < d / 8; c += 32) {
     const uint4 v = src[c];
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -84,6 +111,7 @@ __global__ void row_ssq_kernel(const bf16 *__restrict__ x, long long rows, int d
     for (int e = 0; e < 4; ++e) {
       const float2 f = unpack_bf16x2(w[e]);
       acc += f.x * f.x + f.y * f.y;
+      in_range &= fabsf(f.x) < kF16Overflow && fabsf(f.y) < kF16Overflow;
       o[e] = pack_f16x2(f.x, f.y);
     }
     dst[c] = make_uint4(o[0], o[1], o[2], o[3]);
@@ -91,6 +119,7 @@ __global__ void row_ssq_kernel(const bf16 *__restrict__ x, long long rows, int d
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
   if (lane == 0) ssq[r] = acc;
+  if (!__all_sync(0xffffffffu, in_range) && lane == 0) set_status(status, kDevRange);
 }
 
 // dst[r, c] = f16(src[r, c] * w[c]) (w == nullptr: plain conversion).  Folds
@@ -160,24 +189,25 @@ static int grid_for(long long n, int threads) {
 }
 
 cudaError_t launch_embed_rows(const int *ids, const bf16 *embed, int vocab, int d, long long rows,
-                              f16 *x16, float *x_f32, float *ssq, cudaStream_t stream) {
+                              f16 *x16, float *x_f32, float *ssq, int *status, SeqCheck chk,
+                              cudaStream_t stream) {
   const int wpb = 8;
   embed_rows_kernel<<<(unsigned)cdiv(rows, wpb), wpb * 32, 0, stream>>>(ids, embed, vocab, d, rows,
-                                                                          x16, x_f32, ssq);
+                                                                          x16, x_f32, ssq, status, chk);
   return cudaGetLastError();
 }
 
-cudaError_t launch_row_ssq(const bf16 *x, long long rows, int d, f16 *x16, float *ssq,
-                           cudaStream_t stream) {
+cudaError_t launch_row_ssq(const bf16 *x, long long rows, int d, f16 *x16, float *ssq, int *status,
+                           SeqCheck chk, cudaStream_t stream) {
   const int wpb = 8;
-  row_ssq_kernel<<<(unsigned)cdiv(rows, wpb), wpb * 32, 0, stream>>>(x, rows, d, x16, ssq);
+  row_ssq_kernel<<<(unsigned)cdiv(rows, wpb), wpb * 32, 0, stream>>>(x, rows, d, x16, ssq, status, chk);
   return cudaGetLastError();
 }
 
-cudaError_t launch_row_ssq_f32(const float *x, long long rows, int d, f16 *x16, float *ssq,
-                               cudaStream_t stream) {
+cudaError_t launch_row_ssq_f32(const float *x, long long rows, int d, f16 *x16, float *ssq, int *status,
+                               SeqCheck chk, cudaStream_t stream) {
   const int wpb = 8;
-  row_ssq_f32_kernel<<<(unsigned)cdiv(rows, wpb), wpb * 32, 0, stream>>>(x, rows, d, x16, ssq);
+  row_ssq_f32_kernel<<<(unsigned)cdiv(rows, wpb), wpb * 32, 0, stream>>>(x, rows, d, x16, ssq, status, chk);
   return cudaGetLastError();
 }
 

@@ -16,6 +16,9 @@ using namespace smol;
 namespace {
 
 thread_local char g_cuda_err[256] = "";
+// Bounded-wait limit passed to the attention kernel (0: its default of 1 s);
+// see smol_set_wait_limit_ns.
+std::atomic<unsigned long long> g_attn_wait_ns{0};
 thread_local int g_launches = 0;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -247,6 +250,7 @@ int run_block(const smol_config *c, const void *packed, int layer, const BlockIO
   ap.window = layer_window(c, layer);
   ap.key_mask = key_mask;
   ap.status = status;
+  ap.wait_ns = g_attn_wait_ns.load(std::memory_order_relaxed);
   ap.pdl = 1;
   if (cc) {
     // the cached slice and the new keys as one left-padded sequence of Tk keys;
@@ -402,11 +406,13 @@ int block_forward_impl(const smol_config *cfg, const void *packed, int layer, co
   io.k_bf = static_cast<bf16 *>(k_out);
   io.v_bf = static_cast<bf16 *>(v_out);
   if (act_dtype == SMOL_ACT_F32) {
-    LAUNCH_K(SMOL_K_ROWSTATS, st, launch_row_ssq_f32(static_cast<const float *>(x), M, cfg->hidden, x16, ssq_a, st));
+    LAUNCH_K(SMOL_K_ROWSTATS, st, launch_row_ssq_f32(static_cast<const float *>(x), M, cfg->hidden, x16, ssq_a,
+                                                   reinterpret_cast<int *>(wsb + W.status), SeqCheck{valid_start, T, T}, st));
     io.resid_f32 = static_cast<const float *>(x);
     io.out_f32 = static_cast<float *>(out);
   } else {
-    LAUNCH_K(SMOL_K_ROWSTATS, st, launch_row_ssq(static_cast<const bf16 *>(x), M, cfg->hidden, x16, ssq_a, st));
+    LAUNCH_K(SMOL_K_ROWSTATS, st, launch_row_ssq(static_cast<const bf16 *>(x), M, cfg->hidden, x16, ssq_a,
+                                                   reinterpret_cast<int *>(wsb + W.status), SeqCheck{valid_start, T, T}, st));
     io.resid_bf = static_cast<const bf16 *>(x);
     io.out16 = out;
     io.out16_is_f16 = 0;
@@ -440,7 +446,8 @@ int model_forward_impl(const smol_config *cfg, const void *packed, const int32_t
   f16 *x = reinterpret_cast<f16 *>(wsb + W.x);
   float *ssq_a = reinterpret_cast<float *>(wsb + W.ssq_a);
   LAUNCH_K(SMOL_K_EMBED, st, launch_embed_rows(ids, reinterpret_cast<const bf16 *>(pk + L.embed_off), cfg->vocab,
-                           cfg->hidden, M, x, nullptr, ssq_a, st));
+                           cfg->hidden, M, x, nullptr, ssq_a, reinterpret_cast<int *>(wsb + W.status),
+                           SeqCheck{valid_start, T, T}, st));
   // the residual stream is f16: each block reads x and writes its output over it
   BlockIO io{};
   io.x16 = x;
@@ -579,7 +586,8 @@ SMOL_API int smol_prefill_with_cache(const smol_config *cfg, const void *packed,
   f16 *x = reinterpret_cast<f16 *>(wsb + W.x);
   float *ssq_a = reinterpret_cast<float *>(wsb + W.ssq_a);
   LAUNCH_K(SMOL_K_EMBED, st, launch_embed_rows(ids, reinterpret_cast<const bf16 *>(pk + L.embed_off), cfg->vocab,
-                           cfg->hidden, M, x, nullptr, ssq_a, st));
+                           cfg->hidden, M, x, nullptr, ssq_a, reinterpret_cast<int *>(wsb + W.status),
+                           SeqCheck{cache_len, T, cache_lmax(cfg, T, S_max)}, st));
   const size_t layer_cache = (size_t)B * cfg->n_kv_heads * S_max * cfg->head_dim;
   const size_t layer_new = (size_t)B * cfg->n_kv_heads * T * cfg->head_dim;
   for (int l = 0; l < cfg->n_layers; ++l) {
@@ -625,6 +633,16 @@ SMOL_API int smol_sample(const void *logits, int B, int V, long long ld, float t
   return SMOL_OK;
 }
 
+// The host status of a device status word: the first code any kernel wrote
+// (range 0x3xx: a value beyond f16; 0x4xx: a clamped input; the rest: a bounded
+// wait that gave up).
+int status_of_word(int h) {
+  if (h == 0) return SMOL_OK;
+  if ((h & 0xf00) == 0x300) return SMOL_ERR_RANGE;
+  if ((h & 0xf00) == 0x400) return SMOL_ERR_INPUT;
+  return SMOL_ERR_TIMEOUT;
+}
+
 SMOL_API int smol_workspace_status(void *ws, void *stream) {
   if (!ws) return SMOL_ERR_INVALID_ARG;
   int h = 0;
@@ -634,10 +652,14 @@ SMOL_API int smol_workspace_status(void *ws, void *stream) {
   if (e == cudaSuccess) e = cudaMemsetAsync(ws, 0, sizeof(int), st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return cuda_fail(e);
-  return h == 0 ? SMOL_OK : SMOL_ERR_TIMEOUT;
+  return status_of_word(h);
 }
 
 SMOL_API int smol_last_launch_count(void) { return g_launches; }
+
+SMOL_API void smol_set_wait_limit_ns(unsigned long long ns) {
+  g_attn_wait_ns.store(ns, std::memory_order_relaxed);
+}
 
 SMOL_API const char *smol_status_string(int status) {
   switch (status) {
@@ -650,6 +672,8 @@ SMOL_API const char *smol_status_string(int status) {
     case SMOL_ERR_CUDA: return g_cuda_err[0] ? g_cuda_err : "CUDA error";
     case SMOL_ERR_DEVICE: return "current device is not compute capability 10.3 (GB300)";
     case SMOL_ERR_TIMEOUT: return "a kernel's bounded wait gave up";
+    case SMOL_ERR_RANGE: return "a value went beyond the f16 range of the residual stream or an operand";
+    case SMOL_ERR_INPUT: return "an input value (token id, cache length, left-padding start) was out of range";
     default: return "unknown status";
   }
 }

@@ -26,6 +26,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 OK = 0
 ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_MISALIGNED, ERR_TOO_LONG = -1, -2, -3, -4
 ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE, ERR_TIMEOUT = -5, -6, -7, -8
+ERR_RANGE, ERR_INPUT = -9, -10
 OP_BLOCK, OP_MODEL, OP_DECODE = 1, 2, 3
 ACT_BF16, ACT_F32 = 0, 1
 
@@ -69,6 +70,7 @@ _SIGS = {
     "smol_decode_step_noalloc": (c_int, [_CFG, c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p,
                                          c_int, c_void_p, c_void_p, c_void_p, c_void_p]),
     "smol_decode_noalloc_status": (c_int, [c_void_p]),
+    "smol_set_wait_limit_ns": (None, [ctypes.c_ulonglong]),
     "smol_prefill_cache_workspace_bytes": (c_size_t, [_CFG, c_int, c_int, c_int]),
     "smol_prefill_with_cache": (c_int, [_CFG, c_void_p, c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p,
                                         c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
@@ -321,6 +323,12 @@ def sample(logits: torch.Tensor, next_ids: torch.Tensor, uniform: Optional[torch
     _check(_lib.smol_sample(_p(logits), B, V, logits.stride(0), float(temperature), int(top_k),
                             float(top_p), int(bool(do_sample)), _p(uniform), _p(next_ids),
                             _stream(stream)), "smol_sample")
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    """Failure-path tests only: bounded-wait limit of the prefill attention
+    kernel for later launches (0 restores the default of 1 s)."""
+    _lib.smol_set_wait_limit_ns(int(ns))
 
 
 def decode_noalloc_status(stream=None) -> int:

@@ -61,3 +61,24 @@ def test_decode_bytes_follow_the_parameter_total():
     assert step - step0 == int(lengths.sum()) * wl.n_layers * 768
     # one attention launch reads one layer's prefix plus the new key/value of each sequence
     assert attn == int((lengths + 1).sum()) * 768 and attn0 == wl.B * 768
+
+
+def test_block_workload_flops():
+    # one unpadded SmolLM2 block step costs exactly one layer of the prefill count
+    wl = synth.WORKLOADS["smollm2_block_b1_t128"]
+    per = bench.prefill_flops_per_launch(wl)
+    layer = sum(v for k, v in per.items() if k != "lm_head_gemm")
+    flops, tokens = bench.block_flops(wl)
+    assert (flops, tokens) == (layer, wl.B * wl.T)
+    # left padding: only valid tokens count, each sequence's attention over its own length
+    wl3 = synth.WORKLOADS["slm125m_block_leftpad_b16_t1024"]
+    lengths = np.array([128, 1024] + [500] * (wl3.B - 2))
+    f3, n3 = bench.block_flops(wl3, lengths)
+    assert n3 == lengths.sum()
+    lin = 2 * ((wl3.n_heads + 2 * wl3.n_kv_heads) * wl3.head_dim * wl3.hidden
+               + wl3.hidden * wl3.n_heads * wl3.head_dim + 3 * wl3.intermediate * wl3.hidden)
+    assert lin == 12_582_912                          # the per-token figure quoted with the workload
+    attn = sum(4 * wl3.head_dim * wl3.n_heads * L * (L + 1) // 2 for L in lengths)
+    assert f3 == lin * n3 + attn
+    full, _ = bench.block_flops(wl3)
+    assert full > f3

@@ -129,3 +129,35 @@ def test_full_decode_smollm2_b64_cache4096(S):
     print(f"decode seqs {picks} (lengths {lens[picks].tolist()}): cos {cos:.7f} max abs {mabs:.3e} k {ek:.3e} v {ev:.3e}")
     assert cos >= LOGITS_COS_MIN and mabs <= LOGITS_MAX_ABS, (cos, mabs)
     assert ek <= BLOCK_REL_TOL and ev <= BLOCK_REL_TOL, (ek, ev)
+
+
+def test_full_prefill_with_cache_smollm2_b64_cache4096(S):
+    # a 64-token chunk on top of the decode workload's caches (B = 64, 30
+    # layers, lengths uniform in [1024, 4096] in 4096-slot caches)
+    wl = W["smollm2_decode_b64_cache4096"]
+    inp = synth.generate(wl, seed=1, device="cuda")
+    cfg = S.config_of(wl)
+    packed = S.prepare_weights(cfg, inp.layers, inp.embed, inp.final_norm)
+    L, B, KV, hd, T = wl.n_layers, wl.B, wl.n_kv_heads, wl.head_dim, 64
+    g = torch.Generator(device="cuda").manual_seed(2)
+    ids = torch.randint(0, wl.vocab, (B, T), generator=g, device="cuda", dtype=torch.int32)
+    ws = S.prefill_cache_workspace(cfg, B, T, wl.s_max)
+    k_new = torch.empty(L, B, KV, T, hd, dtype=torch.bfloat16, device="cuda")
+    v_new = torch.empty_like(k_new)
+    logits = torch.empty(B, T, wl.vocab, dtype=torch.bfloat16, device="cuda")
+    S.prefill_with_cache(cfg, packed, ids, inp.lengths, inp.k_cache, inp.v_cache, k_new, v_new, logits, ws)
+    assert S.workspace_status(ws) == S.OK
+    assert bool(torch.isfinite(logits).all())
+    lens = inp.lengths.cpu().numpy()
+    picks = sorted({int(np.argmin(lens)), int(np.argmax(lens)), 40})
+    ref, kr, vr = O.prefill_with_cache(oracle_config(wl), oracle_layers(inp), np32(inp.embed),
+                                       np32(inp.final_norm), ids[picks].cpu().numpy().astype(np.int64),
+                                       lens[picks], np32(inp.k_cache[:, picks]), np32(inp.v_cache[:, picks]))
+    got = np32(logits[picks])
+    cos, mabs = cosine(got, ref), max_abs(got, ref)
+    ek = rel_max_err_bf16_out(np32(k_new[:, picks]), kr)
+    ev = rel_max_err_bf16_out(np32(v_new[:, picks]), vr)
+    print(f"prefill on cache seqs {picks} (lengths {lens[picks].tolist()}): cos {cos:.7f} max abs {mabs:.3e} "
+          f"k {ek:.3e} v {ev:.3e}")
+    assert cos >= LOGITS_COS_MIN and mabs <= LOGITS_MAX_ABS, (cos, mabs)
+    assert ek <= BLOCK_REL_TOL and ev <= BLOCK_REL_TOL, (ek, ev)

@@ -485,3 +485,54 @@ def test_prefill_with_cache_long_chunk_nope_window(S):
     wl = W["smollm2_decode_b64_cache4096"].scaled(n_layers=2, s_max=200, vocab=512, no_rope_layers=(1, 0),
                                                   sliding_window=(0, 150))
     run_prefill_cache_case(S, wl, [5, 200], T=260, seed=71)
+
+
+def test_prefill_append_decode_chain(S):
+    # prefill a chunk on top of the caches, append its keys and values, then
+    # decode the next token: the GPU chain against the oracle's own chain
+    wl = W["smollm2_decode_b64_cache4096"].scaled(B=3, n_layers=2, s_max=300, vocab=512,
+                                                  sliding_window=(0, 40))
+    inp = synth.generate(wl, seed=72)
+    lengths = [0, 37, 250]
+    T = 20
+    g = torch.Generator().manual_seed(73)
+    ids = torch.randint(0, wl.vocab, (wl.B, T), generator=g).to(torch.int32)
+    nxt = torch.randint(0, wl.vocab, (wl.B,), generator=g).to(torch.int32)
+    dev = to_device(inp)
+    cfg = S.config_of(wl)
+    packed = S.prepare_weights(cfg, dev.layers, dev.embed, dev.final_norm)
+    L, B, KV, hd = wl.n_layers, wl.B, wl.n_kv_heads, wl.head_dim
+    lens = torch.tensor(lengths, dtype=torch.int32)
+    # GPU: prefill, append, decode
+    ws = S.prefill_cache_workspace(cfg, B, T, wl.s_max)
+    k_new = torch.empty(L, B, KV, T, hd, dtype=torch.bfloat16, device="cuda")
+    v_new = torch.empty_like(k_new)
+    logits_p = torch.empty(B, T, wl.vocab, dtype=torch.bfloat16, device="cuda")
+    S.prefill_with_cache(cfg, packed, ids.cuda(), lens.cuda(), dev.k_cache, dev.v_cache, k_new, v_new,
+                         logits_p, ws)
+    assert S.workspace_status(ws) == S.OK
+    kc, vc = dev.k_cache.clone(), dev.v_cache.clone()
+    for b, Lb in enumerate(lengths):
+        kc[:, b, :, Lb:Lb + T] = k_new[:, b]
+        vc[:, b, :, Lb:Lb + T] = v_new[:, b]
+    wsd = S.alloc_workspace(cfg, S.OP_DECODE, B, 1)
+    k1 = torch.empty(L, B, KV, hd, dtype=torch.bfloat16, device="cuda")
+    v1 = torch.empty_like(k1)
+    logits_d = torch.empty(B, wl.vocab, dtype=torch.bfloat16, device="cuda")
+    S.decode_step(cfg, packed, nxt.cuda(), (lens + T).cuda(), kc, vc, k1, v1, logits_d, wsd)
+    assert S.workspace_status(wsd) == S.OK
+    # oracle: the same chain on its own values
+    oc, ol = oracle_config(wl), oracle_layers(inp)
+    E, fn = np32(inp.embed), np32(inp.final_norm)
+    ref_p, kr, vr = O.prefill_with_cache(oc, ol, E, fn, ids.numpy().astype(np.int64), np.asarray(lengths),
+                                         np32(inp.k_cache), np32(inp.v_cache))
+    okc = np32(inp.k_cache).astype(np.float64)
+    ovc = np32(inp.v_cache).astype(np.float64)
+    for b, Lb in enumerate(lengths):
+        okc[:, b, :, Lb:Lb + T] = kr[:, b]
+        ovc[:, b, :, Lb:Lb + T] = vr[:, b]
+    ref_d, _, _ = O.decode_step(oc, ol, E, fn, nxt.numpy().astype(np.int64), np.asarray(lengths) + T, okc, ovc)
+    for got, ref, what in ((np32(logits_p), ref_p, "prefill"), (np32(logits_d), ref_d, "decode")):
+        cos, mabs = cosine(got, ref), max_abs(got, ref)
+        print(f"chain {what}: cos {cos:.7f} max abs {mabs:.3e}")
+        assert cos >= LOGITS_COS_MIN and mabs <= LOGITS_MAX_ABS, (what, cos, mabs)
