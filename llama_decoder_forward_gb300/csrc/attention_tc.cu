@@ -51,19 +51,21 @@ namespace {
 
 constexpr int kBQ = 128;      // query rows per tile (UMMA M)
 constexpr int kBK = 128;      // keys per KV tile
-constexpr int kHD = 64;
-constexpr int kNO = 80;       // accumulator columns per head: 64 value dims, the row sum, 15 zero
 constexpr int kNST = 2;       // K/V stages
 constexpr int kTmemS = 256;   // S buffers at TMEM columns 256 and 384
 
-template <int GH>
+// HD = head dim (64 or 128).  Q and K tiles are HD/64 swizzled sub-tiles of
+// 64 columns; a V^T half tile holds the HD value rows and 16 constant rows.
+template <int HD, int GH>
 struct AtCfg {
-  static constexpr int NG = GH == 1 ? 1 : 2;            // softmax warpgroups, taking the slots in turn
+  static constexpr int NO = HD + 16;                    // accumulator columns per head: HD values, the row sum, 15 zero
+  static constexpr int NSUB = HD / 64;                  // 64-column sub-tiles of a Q or K tile
+  static constexpr int NG = (GH == 1 && HD == 64) ? 1 : 2;   // softmax warpgroups, taking the slots in turn
   static constexpr int THREADS = 128 * (1 + NG);        // one control warpgroup + NG softmax warpgroups
-  static constexpr int Q_BYTES = kBQ * kHD * 2;         // one head: [128 rows][64] f16
-  static constexpr int K_BYTES = kBK * kHD * 2;         // [128 keys][64]
-  static constexpr int VT_TMA = kHD * 128;              // [64 dims][64 keys], written by TMA
-  static constexpr int VT_SUB = kNO * 128;              // + [16 rows][64 keys]: a row of ones, 15 of zeros
+  static constexpr int Q_BYTES = kBQ * HD * 2;          // one head: NSUB x [128 rows][64] f16
+  static constexpr int K_BYTES = kBK * HD * 2;          // NSUB x [128 keys][64]
+  static constexpr int VT_TMA = HD * 128;               // [HD dims][64 keys], written by TMA
+  static constexpr int VT_SUB = NO * 128;               // + [16 rows][64 keys]: a row of ones, 15 of zeros
   static constexpr int VT_BYTES = 2 * VT_SUB;           // keys 0..63 and 64..127 of the tile
   static constexpr int P_SUB = kBQ * 128;               // [128 rows][64 keys] f16
   static constexpr int P_BYTES = 2 * P_SUB;             // one head's P, also its output staging
@@ -76,7 +78,7 @@ struct AtCfg {
   static constexpr int OFF_BAR = OFF_MST + GH * 128 * 4;
   static constexpr int NBAR = 1 + 4 * kNST + 4 + 4 * GH + 3;
   static constexpr int SMEM = 1024 + OFF_BAR + NBAR * 8 + 16;
-  static_assert(GH >= 1 && GH * kNO <= kTmemS, "O accumulators must fit below the S buffers");
+  static_assert(GH >= 1 && GH * NO <= kTmemS, "O accumulators must fit below the S buffers");
   static_assert(SMEM <= 232448, "shared memory per CTA");
 };
 
@@ -132,12 +134,13 @@ __device__ __forceinline__ void at_status(int *status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
 
-template <int GH, bool KM>
-__global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
+template <int HD, int GH, bool KM>
+__global__ void __launch_bounds__(AtCfg<HD, GH>::THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmVt, const __grid_constant__ CUtensorMap tmO,
                    const AtParams p) {
-  using C = AtCfg<GH>;
+  using C = AtCfg<HD, GH>;
+  constexpr int NO = C::NO;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -240,7 +243,9 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
     if (lane == 0) {
       mbar_arrive_expect_tx(q_full, GH * C::Q_BYTES);
       for (int h = 0; h < GH; ++h)
-        tma_load_2d(sQ + h * C::Q_BYTES, &tmQ, q_full, 0, ((b * p.H) + h_first + h) * T + q0);
+        for (int qs = 0; qs < C::NSUB; ++qs)
+          tma_load_2d(sQ + h * C::Q_BYTES + qs * (kBQ * 128), &tmQ, q_full, qs * 64,
+                      ((b * p.H) + h_first + h) * T + q0);
     }
     for (int it = -1; it < ntiles && ok; ++it) {
       const int ik = it + 1;                      // K tile issued in this step
@@ -250,7 +255,9 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
           ok = mbar_wait_bounded(&k_empty[st], ((ik / kNST) & 1) ^ 1, abort_flag, p.wait_ns);
           if (ok) {
             mbar_arrive_expect_tx(&k_full[st], C::K_BYTES);
-            tma_load_2d(sK + st * C::K_BYTES, &tmK, &k_full[st], 0, (b * p.KV + kvh) * Tk + (j_lo + ik) * kBK);
+            for (int ks = 0; ks < C::NSUB; ++ks)
+              tma_load_2d(sK + st * C::K_BYTES + ks * (kBK * 128), &tmK, &k_full[st], ks * 64,
+                          (b * p.KV + kvh) * Tk + (j_lo + ik) * kBK);
             ++nk;
           }
         }
@@ -276,9 +283,9 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
       if (lane == 0) {
         // the arrive below also releases the mask words to the softmax warps
         mbar_arrive_expect_tx(&v_full[st], 2 * C::VT_TMA);
-        tma_load_2d(sVt + st * C::VT_BYTES, &tmVt, &v_full[st], j * kBK, (b * p.KV + kvh) * kHD);
+        tma_load_2d(sVt + st * C::VT_BYTES, &tmVt, &v_full[st], j * kBK, (b * p.KV + kvh) * HD);
         tma_load_2d(sVt + st * C::VT_BYTES + C::VT_SUB, &tmVt, &v_full[st], j * kBK + 64,
-                    (b * p.KV + kvh) * kHD);
+                    (b * p.KV + kvh) * HD);
         ++nv;
       }
     }
@@ -306,11 +313,13 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
         if (!mbar_wait_bounded(&s_free[sb], ((s >> 1) & 1) ^ 1, abort_flag, p.wait_ns)) { ok = false; break; }
         if (h == 0 && !mbar_wait_bounded(&k_full[st], (it / kNST) & 1, abort_flag, p.wait_ns)) { ok = false; break; }
         tc_fence_after_sync();
-        const uint64_t a = sdesc_kmajor_sw128(smem_u32(sQ + h * C::Q_BYTES));
-        const uint64_t bk = sdesc_kmajor_sw128(smem_u32(sK + st * C::K_BYTES));
 #pragma unroll
-        for (int k = 0; k < kHD / 16; ++k)
-          umma_f16(tmem + kTmemS + sb * kBK, a + 2 * k, bk + 2 * k, kIdescS, k > 0);
+        for (int k = 0; k < HD / 16; ++k) {
+          // k step k: sub-tile k / 4, +32 bytes per 16 columns inside it
+          const uint64_t a = sdesc_kmajor_sw128(smem_u32(sQ + h * C::Q_BYTES + (k >> 2) * (kBQ * 128)));
+          const uint64_t bk = sdesc_kmajor_sw128(smem_u32(sK + st * C::K_BYTES + (k >> 2) * (kBK * 128)));
+          umma_f16(tmem + kTmemS + sb * kBK, a + 2 * (k & 3), bk + 2 * (k & 3), kIdescS, k > 0);
+        }
         any = true;
         umma_commit(&s_full[sb]);
         if (h == GH - 1) umma_commit(&k_empty[st]);   // every head's S of the tile issued
@@ -331,7 +340,7 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
       // warp 2 takes the even slots, warp 3 the odd ones.  A head's P V MMAs of
       // consecutive tiles never overlap even when issued from different warps:
       // P of the next tile is written only after the previous P V is done.
-      constexpr uint32_t kIdescO = idesc_f16_f32(kBQ, kNO);
+      constexpr uint32_t kIdescO = idesc_f16_f32(kBQ, NO);
       const int par = warp - 2;
       bool ok = true, any = false;
       for (int s = par; s < nslots && ok; s += 2) {
@@ -345,7 +354,7 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
           const uint64_t bv = sdesc_kmajor_sw128(smem_u32(sVt + st * C::VT_BYTES + kb * C::VT_SUB));
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            umma_f16(tmem + h * kNO, ap + 2 * k, bv + 2 * k, kIdescO, (it | kb | k) != 0);
+            umma_f16(tmem + h * NO, ap + 2 * k, bv + 2 * k, kIdescO, (it | kb | k) != 0);
         }
         any = true;
         umma_commit(&pv_done[h]);
@@ -452,9 +461,9 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
       if (__any_sync(0xffffffffu, resc)) {
         // O_h (and its row-sum column) *= alpha, sixteen columns at a time
         tc_fence_after_sync();
-        const uint32_t o_col = lane_base + h * kNO;
+        const uint32_t o_col = lane_base + h * NO;
 #pragma unroll 1
-        for (int c = 0; c < kNO; c += 16) {
+        for (int c = 0; c < NO; c += 16) {
           uint32_t ov[16];
           tmem_ld16(o_col + c, ov);
           tmem_ld_wait();
@@ -498,40 +507,44 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
       if (!alive) break;
       tc_fence_after_sync();
       uint32_t ov[32], os[16];
-      const uint32_t o_col = lane_base + h * kNO;
-      tmem_ld16(o_col + 64, os);
+      const uint32_t o_col = lane_base + h * NO;
+      tmem_ld16(o_col + HD, os);
       tmem_ld_wait();
       const float lt = __uint_as_float(os[0]);
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
       const bool row_ok = t < T;
       const bool warp_rows_ok = q0 + quarter * 32 + 31 < T;   // all 32 rows of this warp exist
-      // the warp's 32 rows x 64 columns staged in the head's (now free) P buffer, swizzled
-      uint8_t *stg = sP + h * C::P_BYTES + quarter * 32 * 128;
-      f16 *dst = p.o + ((long long)b * T + t) * ((long long)p.H * kHD) + (long long)(h_first + h) * kHD;
+      f16 *dst = p.o + ((long long)b * T + t) * ((long long)p.H * HD) + (long long)(h_first + h) * HD;
+#pragma unroll 1
+      for (int j = 0; j < C::NSUB; ++j) {
+        // the warp's 32 rows x 64 columns j*64.. staged in sub-tile j of the
+        // head's (now free) P buffer, swizzled
+        uint8_t *stg = sP + h * C::P_BYTES + j * C::P_SUB + quarter * 32 * 128;
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        tmem_ld32(o_col + 32 * half, ov);
-        tmem_ld_wait();
+        for (int half = 0; half < 2; ++half) {
+          tmem_ld32(o_col + j * 64 + 32 * half, ov);
+          tmem_ld_wait();
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float *f = reinterpret_cast<const float *>(&ov[8 * q]);
-          const uint4 w = make_uint4(pack_f16x2(f[0] * inv, f[1] * inv), pack_f16x2(f[2] * inv, f[3] * inv),
-                                     pack_f16x2(f[4] * inv, f[5] * inv), pack_f16x2(f[6] * inv, f[7] * inv));
-          const int c = half * 4 + q;
-          if (warp_rows_ok)
-            *reinterpret_cast<uint4 *>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) = w;
-          else if (row_ok)
-            *reinterpret_cast<uint4 *>(dst + 8 * c) = w;
+          for (int q = 0; q < 4; ++q) {
+            const float *f = reinterpret_cast<const float *>(&ov[8 * q]);
+            const uint4 w = make_uint4(pack_f16x2(f[0] * inv, f[1] * inv), pack_f16x2(f[2] * inv, f[3] * inv),
+                                       pack_f16x2(f[4] * inv, f[5] * inv), pack_f16x2(f[6] * inv, f[7] * inv));
+            const int c = half * 4 + q;
+            if (warp_rows_ok)
+              *reinterpret_cast<uint4 *>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) = w;
+            else if (row_ok)
+              *reinterpret_cast<uint4 *>(dst + j * 64 + 8 * c) = w;
+          }
         }
-      }
-      if (warp_rows_ok) {
-        // one TMA box per warp (a lane per row would make every store
-        // instruction 32 separate row segments)
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_2d(&tmO, stg, (h_first + h) * kHD, b * T + q0 + quarter * 32);
-          bulk_commit_group();
+        if (warp_rows_ok) {
+          // one TMA box per warp and 64 columns (a lane per row would make
+          // every store instruction 32 separate row segments)
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmO, stg, (h_first + h) * HD + j * 64, b * T + q0 + quarter * 32);
+            bulk_commit_group();
+          }
         }
       }
     }
@@ -550,12 +563,12 @@ __global__ void __launch_bounds__(AtCfg<GH>::THREADS, 1)
   }
 }
 
-template <int GH, bool KM>
+template <int HD, int GH, bool KM>
 cudaError_t launch_ghk(const AttnParams &a, const CUtensorMap &tq, const CUtensorMap &tk,
                        const CUtensorMap &tv, const CUtensorMap &to, cudaStream_t st) {
-  using C = AtCfg<GH>;
-  auto kern = attn_tc_kernel<GH, KM>;
-  cudaError_t e = ensure_smem_attr<attn_tc_kernel<GH, KM>>(C::SMEM);
+  using C = AtCfg<HD, GH>;
+  auto kern = attn_tc_kernel<HD, GH, KM>;
+  cudaError_t e = ensure_smem_attr<attn_tc_kernel<HD, GH, KM>>(C::SMEM);
   if (e != cudaSuccess) return e;
   AtParams p{};
   p.o = a.o;
@@ -587,40 +600,43 @@ cudaError_t launch_ghk(const AttnParams &a, const CUtensorMap &tq, const CUtenso
   return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, to, p);
 }
 
-template <int GH>
+template <int HD, int GH>
 cudaError_t launch_gh(const AttnParams &a, const CUtensorMap &tq, const CUtensorMap &tk,
                       const CUtensorMap &tv, const CUtensorMap &to, cudaStream_t st) {
-  return a.key_mask ? launch_ghk<GH, true>(a, tq, tk, tv, to, st) : launch_ghk<GH, false>(a, tq, tk, tv, to, st);
+  return a.key_mask ? launch_ghk<HD, GH, true>(a, tq, tk, tv, to, st)
+                    : launch_ghk<HD, GH, false>(a, tq, tk, tv, to, st);
 }
 
 }  // namespace
 
 bool attention_tc_supported(int hd, int H, int KV) {
   const int G = H / KV;
-  return hd == kHD && (G == 1 || G == 2 || G == 3 || G == 4 || G == 6 || G == 8);
+  return (hd == 64 || hd == 128) && (G == 1 || G == 2 || G == 3 || G == 4 || G == 6 || G == 8);
 }
 
 cudaError_t launch_attention_tc(const AttnParams &a, cudaStream_t st) {
   if (!attention_tc_supported(a.hd, a.H, a.KV) || a.v_t == nullptr) return cudaErrorInvalidConfiguration;
+  const int HDv = a.hd;
   CUtensorMap tq, tk, tv, to;
-  if (!get_tmap_f16(&tq, a.q, (uint64_t)a.B * a.H * a.T, kHD, kHD, kBQ)) return cudaErrorInvalidValue;
+  if (!get_tmap_f16(&tq, a.q, (uint64_t)a.B * a.H * a.T, HDv, HDv, kBQ)) return cudaErrorInvalidValue;
   const int Tk = a.Tk > 0 ? a.Tk : a.T;
   if (Tk < a.T || a.q_off < 0 || a.q_off + a.T > Tk) return cudaErrorInvalidValue;
   if (a.key_mask && Tk != a.T) return cudaErrorInvalidValue;
-  if (!get_tmap_f16(&tk, a.k, (uint64_t)a.B * a.KV * Tk, kHD, kHD, kBK)) return cudaErrorInvalidValue;
+  if (!get_tmap_f16(&tk, a.k, (uint64_t)a.B * a.KV * Tk, HDv, HDv, kBK)) return cudaErrorInvalidValue;
   // V^T: rows are (b, kv head, dim), columns are keys; columns >= Tk read as zero
-  if (!get_tmap_f16(&tv, a.v_t, (uint64_t)a.B * a.KV * kHD, Tk, a.T_pad, kHD)) return cudaErrorInvalidValue;
+  if (!get_tmap_f16(&tv, a.v_t, (uint64_t)a.B * a.KV * HDv, Tk, a.T_pad, HDv)) return cudaErrorInvalidValue;
   // output rows [B*T, H*hd]: a softmax warp's 32 rows x 64 columns per box, swizzled
-  if (!get_tmap_2d(&to, a.o, (uint64_t)a.B * a.T, (uint64_t)a.H * kHD, (uint64_t)a.H * kHD, 64, 32, true))
+  if (!get_tmap_2d(&to, a.o, (uint64_t)a.B * a.T, (uint64_t)a.H * HDv, (uint64_t)a.H * HDv, 64, 32, true))
     return cudaErrorInvalidValue;
   const int G = a.H / a.KV;
+  if (HDv == 128) return launch_gh<128, 1>(a, tq, tk, tv, to, st);   // one query head per CTA
   switch (G) {
-    case 1: return launch_gh<1>(a, tq, tk, tv, to, st);
-    case 2: return launch_gh<2>(a, tq, tk, tv, to, st);
-    case 3: return launch_gh<3>(a, tq, tk, tv, to, st);
-    case 4: return launch_gh<2>(a, tq, tk, tv, to, st);   // two CTAs per group of four
-    case 6: return launch_gh<3>(a, tq, tk, tv, to, st);   // two CTAs per group of six
-    case 8: return launch_gh<2>(a, tq, tk, tv, to, st);   // four CTAs per group of eight
+    case 1: return launch_gh<64, 1>(a, tq, tk, tv, to, st);
+    case 2: return launch_gh<64, 2>(a, tq, tk, tv, to, st);
+    case 3: return launch_gh<64, 3>(a, tq, tk, tv, to, st);
+    case 4: return launch_gh<64, 2>(a, tq, tk, tv, to, st);   // two CTAs per group of four
+    case 6: return launch_gh<64, 3>(a, tq, tk, tv, to, st);   // two CTAs per group of six
+    case 8: return launch_gh<64, 2>(a, tq, tk, tv, to, st);   // four CTAs per group of eight
   }
   return cudaErrorInvalidConfiguration;
 }

@@ -553,7 +553,8 @@ SMOL_API int smol_decode_step(const smol_config *cfg, const void *packed, const 
 
 SMOL_API size_t smol_prefill_cache_workspace_bytes(const smol_config *cfg, int B, int T, int S_max) {
   if (check_cfg(cfg) != SMOL_OK || B <= 0 || T <= 0 || S_max <= 0 || T >= cfg->max_pos) return 0;
-  if (!attention_tc_supported(cfg->head_dim, cfg->n_heads, cfg->n_kv_heads)) return 0;
+  // the gather of cached keys into the attention's layout is written for head_dim 64
+  if (cfg->head_dim != 64 || !attention_tc_supported(cfg->head_dim, cfg->n_heads, cfg->n_kv_heads)) return 0;
   return ws_layout_cache(cfg, B, T, S_max).total;
 }
 
@@ -567,7 +568,8 @@ SMOL_API int smol_prefill_with_cache(const smol_config *cfg, const void *packed,
   if (!packed || !ids || !cache_len || !k_cache || !v_cache || !k_new || !v_new || !logits || !ws || B <= 0 ||
       T <= 0 || S_max <= 0 || cfg->vocab <= 0)
     return SMOL_ERR_INVALID_ARG;
-  if (!attention_tc_supported(cfg->head_dim, cfg->n_heads, cfg->n_kv_heads)) return SMOL_ERR_UNSUPPORTED_SHAPE;
+  if (cfg->head_dim != 64 || !attention_tc_supported(cfg->head_dim, cfg->n_heads, cfg->n_kv_heads))
+    return SMOL_ERR_UNSUPPORTED_SHAPE;
   if ((long long)B * T > 0x7fffffffLL) return SMOL_ERR_UNSUPPORTED_SHAPE;
   if (T >= cfg->max_pos) return SMOL_ERR_TOO_LONG;
   if (!aligned16(packed) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) ||
