@@ -436,6 +436,7 @@ def run_decode(S, args, rank, world, peaks, peaks_src):
     for _ in range(3):
         choose()
     smp_ms = max_over_ranks(time_steps(choose, args.steps, world), world)
+    gen = run_generate_loop(S, cfg, inp, packed, ws, wl, args, world, rank)
     return {
         "workload": f"{wl.name}: SmolLM2-135M decode step, {L} blocks, batch {B}, cache lengths uniform "
                     f"in [{wl.len_range[0]}, {wl.len_range[1]}], cache [{L},{B},{KV},{wl.s_max},{hd}] bf16",
@@ -455,7 +456,64 @@ def run_decode(S, args, rank, world, peaks, peaks_src):
         "next_token_choice": {"ms_per_call": round(smp_ms, 4), "rows": B, "vocab": wl.vocab,
                               "config": "temperature 0.8, top_k 50, top_p 0.9, uniform from the caller",
                               "launches": 1, "logits_bytes": B * wl.vocab * 2},
+        "generate": gen,
     }
+
+
+GEN_TOKENS = 16
+
+
+def run_generate_loop(S, cfg, inp, packed, ws, wl, args, world, rank):
+    """The generate loop of the pages (model.py (Sualeh77) section 7 generate):
+    GEN_TOKENS steps of decode step + next-token choice + append of the new
+    keys/values, the chosen ids fed back, the whole loop replayed as one CUDA
+    graph.  The decode workload's caches, with lengths capped at S_max -
+    GEN_TOKENS so that every appended token has a slot."""
+    L, B, KV, hd, G = wl.n_layers, wl.B, wl.n_kv_heads, wl.head_dim, GEN_TOKENS
+    lens0 = torch.clamp(inp.lengths, max=wl.s_max - G).to(torch.int32)
+    ids0 = inp.ids.clone()
+    lens = lens0.clone()
+    ids = ids0.clone()
+    k_new = torch.empty(L, B, KV, hd, dtype=torch.bfloat16, device="cuda")
+    v_new = torch.empty_like(k_new)
+    logits = torch.empty(B, wl.vocab, dtype=torch.bfloat16, device="cuda")
+    g = torch.Generator(device="cuda")
+    g.manual_seed(300 + rank)
+    us = torch.rand(G, B, generator=g, device="cuda")
+    out = {"tokens_per_sequence": G, "rows": B,
+           "workload": f"decode workload caches, lengths capped at {wl.s_max - G}; each step: decode step, "
+                       "next-token choice, append of the new keys and values, ids fed back"}
+    for mode, kw in (("greedy", dict(do_sample=False)),
+                     ("sampled", dict(do_sample=True, temperature=0.8, top_k=50, top_p=0.9))):
+        def loop():
+            for s in range(G):
+                S.decode_next(cfg, packed, ids, lens, inp.k_cache, inp.v_cache, k_new, v_new, ids, ws,
+                              logits=logits if kw["do_sample"] else None,
+                              uniform=us[s] if kw["do_sample"] else None, **kw)
+                S.append_kv(cfg, k_new, v_new, inp.k_cache, inp.v_cache, lens)
+
+        def reset():
+            lens.copy_(lens0)
+            ids.copy_(ids0)
+
+        reset()
+        loop()
+        if S.workspace_status(ws) != S.OK:
+            raise RuntimeError("a kernel reported a problem in the generate loop")
+        reset()
+        graph = capture_graph(loop)
+        times = []
+        for _ in range(max(3, min(args.steps, 5))):
+            reset()
+            torch.cuda.synchronize()
+            times.append(time_steps(graph.replay if graph else loop, 1, world))
+        ms = max_over_ranks(statistics.median(times), world)
+        out[mode] = {"ms_per_loop": round(ms, 4), "ms_per_token_step": round(ms / G, 4),
+                     "tokens_per_s": round(B * G * world / (ms / 1e3), 1),
+                     "timing": "CUDA-graph replay of the whole loop" if graph else "eager calls",
+                     "config": {k: v for k, v in kw.items()}}
+    reset()
+    return out
 
 
 # ----------------------------------------------------------------- the other workloads

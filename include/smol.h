@@ -311,6 +311,47 @@ int smol_decode_step_noalloc(const smol_config *cfg, const void *packed, const i
 int smol_decode_noalloc_status(void *stream);
 
 /* ---------------------------------------------------------------------------
+ * smol_decode_next: smol_decode_step followed by the next-token choice of
+ * smol_sample ([M1] section 7 generate: logits of the last position, then
+ * argmax or a draw).  Arguments as in smol_decode_step and smol_sample:
+ *   logits     device [B, V] bf16; may be NULL for a greedy choice.
+ *   temperature, top_k, top_p, do_sample, uniform: as in smol_sample (uniform,
+ *              device fp32 [B], is needed only when sampling).
+ *   next       device int32 [B] output.  It may be the same buffer as `ids`
+ *              (ids are read by the step's first kernel, next written by its
+ *              last), so a generate loop can feed it back.
+ * Greedy (do_sample == 0 or temperature <= 0): the choice is taken inside the
+ * tied head's GEMM epilogue -- every output tile keeps each row's largest
+ * bf16-rounded logit and its first column, combined across tiles by a 64-bit
+ * atomic maximum -- so the logits need not be written or read again.
+ * Sampling: the step writes the logits and the choice kernel of smol_sample
+ * reads them.  Errors as smol_decode_step; SMOL_ERR_INVALID_ARG also for a
+ * NULL `next`, a NaN temperature or top_p, or, when sampling, a NULL logits
+ * or uniform.
+ * ------------------------------------------------------------------------- */
+int smol_decode_next(const smol_config *cfg, const void *packed, const int32_t *ids,
+                     const int32_t *cache_len, int B, const void *k_cache, const void *v_cache,
+                     int S_max, void *k_new, void *v_new, void *logits, float temperature, int top_k,
+                     float top_p, int do_sample, const float *uniform, int32_t *next,
+                     void *ws, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * smol_append_kv: appends a decode step's new keys and values to the caches,
+ * the caller's part of [M1] section 4 (the cache grows by the new token's
+ * post-RoPE key and its value):
+ *   k_cache[l, b, kv, cache_len[b], :] = k_new[l, b, kv, :] (and v alike) for
+ *   every layer l and kv head, then cache_len[b] += 1.
+ *   k_new, v_new      device [L, B, KV, hd] bf16 (smol_decode_step's outputs).
+ *   k_cache, v_cache  device [L, B, KV, S_max, hd] bf16.
+ *   cache_len         device int32 [B], read and incremented.  A row whose
+ *                     length is outside [0, S_max) (a full cache) is left as
+ *                     it is, its length unchanged.
+ * Two kernel launches on `stream`, no workspace.
+ * ------------------------------------------------------------------------- */
+int smol_append_kv(const smol_config *cfg, int B, const void *k_new, const void *v_new, void *k_cache,
+                   void *v_cache, int S_max, int32_t *cache_len, void *stream);
+
+/* ---------------------------------------------------------------------------
  * smol_sample: the next token of each row of logits, chosen the way the pages'
  * generate loop chooses it ([M1] section 7 generate; [M4] generate).
  *   Greedy when do_sample == 0 or temperature <= 0: the first index of the row

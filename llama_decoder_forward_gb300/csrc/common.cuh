@@ -75,6 +75,10 @@ struct GemmParams {
   int pos_limit;
   int max_pos;
   int *status;            // device status word
+  // kEpiScale with bf16 output: per-row maximum of the rounded outputs and its
+  // first column (argmax_pack), combined by atomicMax; zero before the launch.
+  // `out` may be nullptr then (only the maxima are wanted).
+  unsigned long long *argmax;
   int raster_m;           // set by launch_gemm: 1 = consecutive tiles walk down M (B tile reused)
   int epi_tma;            // set by launch_gemm: which epilogue tensor maps are valid
   int pdl;                // launch as a programmatic dependent of the preceding kernel
@@ -177,6 +181,11 @@ cudaError_t launch_scale_cols_copy(const bf16 *src, const bf16 *norm_w, long lon
 cudaError_t launch_interleave_gate_up(const bf16 *wg, const bf16 *wu, const bf16 *norm_w, int I,
                                       int d, f16 *dst, cudaStream_t stream);
 cudaError_t launch_rope_table(int max_pos, int hd, float theta, float2 *table, cudaStream_t stream);
+// Appends one decode step's keys and values to the caches: cache[l, b, kv,
+// cache_len[b], :] = new[l, b, kv, :], then cache_len[b] += 1; rows whose
+// length is outside [0, S_max) are left as they are (two launches).
+cudaError_t launch_append_kv(const bf16 *k_new, const bf16 *v_new, bf16 *k_cache, bf16 *v_cache, int *cache_len,
+                             int L, int B, int KV, int S_max, int hd, cudaStream_t stream);
 // One layer's cached keys/values plus the T new ones as left-padded f16 sequences of Tk
 // keys (hd 64): K [B, KV, Tk, 64], V^T [B, KV, 64, Tk_pad]; vs[b] = first visible slot.
 cudaError_t launch_gather_cache_kv(const bf16 *kc, const bf16 *vc, int S_max, const int *cache_len, int lmax,

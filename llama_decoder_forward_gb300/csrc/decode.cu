@@ -40,7 +40,7 @@ constexpr int kChunk = 256;        // keys per CTA
 constexpr int kDecWarps = 4;       // warps per CTA
 
 struct DecWs {
-  size_t status, x, h, q, o, a, ssq_a, ssq_b, part_m, part_l, part_o, counters, total;
+  size_t status, x, h, q, o, a, ssq_a, ssq_b, part_m, part_l, part_o, counters, argmax, total;
   int max_splits;
 };
 
@@ -63,7 +63,11 @@ static DecWs dec_ws(const smol_config *c, int B) {
   W.part_m = o; o = align_up(o + (size_t)B * H * W.max_splits * 4, 1024);
   W.part_l = o; o = align_up(o + (size_t)B * H * W.max_splits * 4, 1024);
   W.part_o = o; o = align_up(o + (size_t)B * H * W.max_splits * hd * 4, 1024);
-  W.counters = o; o = align_up(o + (size_t)B * KV * 4, 1024);
+  // B x KV arrival counters, then B packed row maxima of the logits (one
+  // contiguous range, cleared by one kernel at the start of the step)
+  W.counters = o; o += (size_t)B * KV * 4;
+  o = align_up(o, 8);
+  W.argmax = o; o = align_up(o + (size_t)B * 8, 1024);
   W.total = o;
   return W;
 }
@@ -1108,6 +1112,12 @@ static cudaError_t launch_decode_attn(const DecAttnParams &ap, int hd, dim3 grid
   return launch_decode_attn_hd<128>(ap, grid, st);
 }
 
+// next[b] = the column of row b's packed maximum (argmax_pack).
+__global__ void argmax_finish_kernel(const unsigned long long *argmax, int B, int *next) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b < B) next[b] = argmax_index(argmax[b]);
+}
+
 __global__ void zero_ints_kernel(int *p, int n) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) p[i] = 0;
@@ -1152,7 +1162,8 @@ cudaError_t run_decode(const DecodeArgs &a, void *ws, int sms, cudaStream_t st, 
   } while (0)
 #define DEC_LAUNCH(expr) DEC_LAUNCH_K(SMOL_K_OTHER, expr)
 
-  DEC_LAUNCH(launch_zero_ints(counters, B * KV, st));
+  unsigned long long *argmax = reinterpret_cast<unsigned long long *>(wb + W.argmax);
+  DEC_LAUNCH(launch_zero_ints(counters, static_cast<int>((W.argmax + (size_t)B * 8 - W.counters) / 4), st));
   DEC_LAUNCH_K(SMOL_K_EMBED, launch_embed_rows(a.ids, a.embed, V, d, B, x, nullptr, ssq_a, status,
                                                 SeqCheck{a.cache_len, 1, min(a.S_max, c.max_pos - 1)}, st));
 
@@ -1208,7 +1219,14 @@ cudaError_t run_decode(const DecodeArgs &a, void *ws, int sms, cudaStream_t st, 
   GemmParams ph{};
   ph.M = B; ph.N = V; ph.K = d; ph.out = a.logits; ph.out_is_f16 = 0; ph.ldo = V; ph.ssq_in = ssq_a;
   ph.inv_dim = 1.0f / d; ph.eps = c.rms_eps; ph.status = status; ph.pdl = 1;
+  ph.argmax = a.next ? argmax : nullptr;         // the greedy choice, in the head's epilogue
   DEC_LAUNCH_K(SMOL_K_HEAD, launch_gemm(kEpiScale, gemm_pick_bn(kEpiScale, V, hd), x, a.head, ph, sms, st));
+  if (a.next) {
+    argmax_finish_kernel<<<(unsigned)cdiv(B, 128), 128, 0, st>>>(argmax, B, a.next);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    ++n;
+  }
 #undef DEC_LAUNCH
   *launches = n;
   return cudaSuccess;

@@ -18,6 +18,9 @@ struct DecodeArgs {
   const f16 *head;         // f16 norm-folded tied head
   const uint8_t *layer0;   // first packed layer
   size_t layer_bytes, off_qkv, off_o, off_gu, off_down;
+  int *next;               // [B] or nullptr: the greedy next token of each row (first maximum
+                           // of the bf16 logits), taken in the head GEMM's epilogue; logits
+                           // may then be nullptr
 };
 
 size_t decode_ws_bytes(const smol_config *cfg, int B);

@@ -243,7 +243,8 @@ __device__ __forceinline__ void epi_scale(const GemmParams &p, EpiCtx &e) {
   const float rs = e.rs;
   const bool tma = p.epi_tma & kTmaOut;
   const long long ld = p.ldo * 2;
-  uint8_t *gbase = static_cast<uint8_t *>(p.out) + ((long long)e.row0 * p.ldo) * 2;
+  uint8_t *gbase = p.out ? static_cast<uint8_t *>(p.out) + ((long long)e.row0 * p.ldo) * 2 : nullptr;
+  unsigned long long best = 0;                    // this row's largest rounded output (argmax_pack)
 #pragma unroll 1
   for (int c = e.split * 64; c < BN; c += 64 * kSplit) {
     if (e.n0 + c >= p.N) break;                   // uniform across the warp
@@ -253,12 +254,23 @@ __device__ __forceinline__ void epi_scale(const GemmParams &p, EpiCtx &e) {
     tmem_ld_wait();
     float v[32];
 #pragma unroll
-    for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r0[k]) * rs;
-    stg_reuse_wait<0>(e.lane);
-    stg_put_16(e.st, e.lane, 0, v, p.out_is_f16);
+    for (int h = 0; h < 2; ++h) {
 #pragma unroll
-    for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r1[k]) * rs;
-    stg_put_16(e.st, e.lane, 4, v, p.out_is_f16);
+      for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(h ? r1[k] : r0[k]) * rs;
+      if (p.argmax) {
+        // the same bf16 rounding as the stored logits
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const uint16_t bits = __bfloat16_as_ushort(__float2bfloat16_rn(v[k]));
+          best = max(best, argmax_pack(bf16_order_key(bits), static_cast<uint32_t>(e.n0 + c + 32 * h + k)));
+        }
+      }
+      if (p.out) {
+        if (h == 0) stg_reuse_wait<0>(e.lane);
+        stg_put_16(e.st, e.lane, 4 * h, v, p.out_is_f16);
+      }
+    }
+    if (!p.out) continue;                         // uniform: only the row maxima are wanted
     if (tma) {
       stg_tma_store(&e.maps->out, e.st, e.n0 + c, e.row0, e.lane, e.rows_valid);
     } else {
@@ -267,6 +279,7 @@ __device__ __forceinline__ void epi_scale(const GemmParams &p, EpiCtx &e) {
                        [&](int rr) { return rr * ld; }, e.rows_valid, e.lane);
     }
   }
+  if (p.argmax && e.lane < e.rows_valid && best) atomicMax(p.argmax + e.row0 + e.lane, best);
 }
 
 // ---- residual: out = resid + D.

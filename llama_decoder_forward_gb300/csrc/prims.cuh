@@ -440,6 +440,23 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n) {
 }
 
 // ---------------------------------------------------------------- misc
+// 16-bit key ordering bf16 values numerically (a larger value has a larger
+// key; -0 and +0 share one key).
+__device__ __forceinline__ uint32_t bf16_order_key(uint16_t bits) {
+  if (bits == 0x8000u) bits = 0;
+  return (bits & 0x8000u) ? (~static_cast<uint32_t>(bits) & 0xFFFFu) : (static_cast<uint32_t>(bits) | 0x8000u);
+}
+
+// A row maximum and its first index as one 64-bit value that atomicMax and
+// max() combine: the value's key above, the complement of the index below
+// (among equal values the smaller index wins).
+__device__ __forceinline__ unsigned long long argmax_pack(uint32_t key, uint32_t index) {
+  return (static_cast<unsigned long long>(key) << 32) | (0xFFFFFFFFu - index);
+}
+__device__ __forceinline__ int argmax_index(unsigned long long packed) {
+  return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(packed));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&v);

@@ -23,6 +23,7 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "prims.cuh"
 
 namespace smol {
 namespace {
@@ -31,10 +32,7 @@ constexpr int kSmpThreads = 1024;
 constexpr float kMassScale = 17592186044416.f;   // 2^44
 
 // 16-bit key ordering bf16 values numerically (larger value, larger key).
-__device__ __forceinline__ uint32_t bf16_key(uint16_t bits) {
-  if (bits == 0x8000u) bits = 0;                 // -0 is the same number as +0
-  return (bits & 0x8000u) ? (~static_cast<uint32_t>(bits) & 0xFFFFu) : (static_cast<uint32_t>(bits) | 0x8000u);
-}
+__device__ __forceinline__ uint32_t bf16_key(uint16_t bits) { return bf16_order_key(bits); }
 
 __device__ __forceinline__ float key_value(uint32_t key) {
   const uint16_t bits = (key & 0x8000u) ? static_cast<uint16_t>(key & 0x7FFFu)
@@ -161,6 +159,7 @@ __global__ void __launch_bounds__(kSmpThreads, 1) sample_kernel(const SamplePara
   const bool greedy = !p.do_sample || !(p.temperature > 0.f);
   const bool use_k = !greedy && p.top_k > 0 && p.top_k < V;
   const bool use_p = !greedy && p.top_p < 1.f;
+  auto key_at = [&](int i) -> uint32_t { return bf16_key(row[i]); };
 
   for (int i = tid; i < 256; i += kSmpThreads) {
     cnt_hi[i] = cnt_lo[i] = cnt_p[i] = 0u;
@@ -172,14 +171,14 @@ __global__ void __launch_bounds__(kSmpThreads, 1) sample_kernel(const SamplePara
   // ---- pass 1: row maximum (its first index) and high-byte counts for top-k
   unsigned long long best = 0;
   for (int i = i0; i < i1; ++i) {
-    const uint32_t k = bf16_key(row[i]);
-    best = max(best, (static_cast<unsigned long long>(k) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(i)));
+    const uint32_t k = key_at(i);
+    best = max(best, argmax_pack(k, static_cast<uint32_t>(i)));
     if (use_k) atomicAdd(&cnt_hi[k >> 8], 1u);
   }
   best = block_max_u64(best, red);               // also orders the count atomics before their reads
   const uint32_t kmax = static_cast<uint32_t>(best >> 32);
   if (greedy) {
-    if (tid == 0) p.next[blockIdx.x] = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best));
+    if (tid == 0) p.next[blockIdx.x] = argmax_index(best);
     return;
   }
   const float T = p.temperature;
@@ -204,7 +203,7 @@ __global__ void __launch_bounds__(kSmpThreads, 1) sample_kernel(const SamplePara
     __syncthreads();
     const int h = s_h;                           // found: the V counts exceed top_k
     for (int i = i0; i < i1; ++i) {
-      const uint32_t k = bf16_key(row[i]);
+      const uint32_t k = key_at(i);
       if (static_cast<int>(k >> 8) == h) atomicAdd(&cnt_lo[k & 255u], 1u);
     }
     __syncthreads();
@@ -224,7 +223,7 @@ __global__ void __launch_bounds__(kSmpThreads, 1) sample_kernel(const SamplePara
   unsigned long long tcut = 0;                   // members of v with rank <= tcut survive
   if (use_p) {
     for (int i = i0; i < i1; ++i) {
-      const uint32_t k = bf16_key(row[i]);
+      const uint32_t k = key_at(i);
       if (k >= tau) atomicAdd(&mass_hi[k >> 8], mass_of(k));
     }
     __syncthreads();
@@ -246,7 +245,7 @@ __global__ void __launch_bounds__(kSmpThreads, 1) sample_kernel(const SamplePara
     const int h = s_h;
     if (h >= 0) {
       for (int i = i0; i < i1; ++i) {
-        const uint32_t k = bf16_key(row[i]);
+        const uint32_t k = key_at(i);
         if (k >= tau && static_cast<int>(k >> 8) == h) {
           atomicAdd(&mass_lo[k & 255u], mass_of(k));
           atomicAdd(&cnt_p[k & 255u], 1u);
@@ -281,7 +280,7 @@ __global__ void __launch_bounds__(kSmpThreads, 1) sample_kernel(const SamplePara
   // block scan, and the first index whose running mass exceeds u * total
   unsigned long long my_v = 0;
   if (cut)
-    for (int i = i0; i < i1; ++i) my_v += bf16_key(row[i]) == vcut ? 1ull : 0ull;
+    for (int i = i0; i < i1; ++i) my_v += key_at(i) == vcut ? 1ull : 0ull;
   unsigned long long nv_total = 0;
   const unsigned long long vbase = block_excl_scan_u64(my_v, red, &nv_total);
   auto survives = [&](uint32_t k, unsigned long long &r) {
@@ -295,7 +294,7 @@ __global__ void __launch_bounds__(kSmpThreads, 1) sample_kernel(const SamplePara
   {
     unsigned long long r = vbase;
     for (int i = i0; i < i1; ++i) {
-      const uint32_t k = bf16_key(row[i]);
+      const uint32_t k = key_at(i);
       if (survives(k, r)) {
         const unsigned long long m = mass_of(k);
         if (m) {
@@ -312,7 +311,7 @@ __global__ void __launch_bounds__(kSmpThreads, 1) sample_kernel(const SamplePara
   if (my_mass && !crosses(pre) && crosses(pre + my_mass)) {   // exactly one thread
     unsigned long long r = vbase, run = pre;
     for (int i = i0; i < i1; ++i) {
-      const uint32_t k = bf16_key(row[i]);
+      const uint32_t k = key_at(i);
       if (survives(k, r)) {
         run += mass_of(k);
         if (crosses(run)) {

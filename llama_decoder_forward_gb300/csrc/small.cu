@@ -273,6 +273,50 @@ cudaError_t launch_gather_cache_kv(const bf16 *kc, const bf16 *vc, int S_max, co
   return cudaGetLastError();
 }
 
+// Appends one decode step's new keys and values ("model.py" (SmolLM2-135M)
+// section 4: the cache grows by the new token's post-RoPE key and its value);
+// one thread per 16 bytes of a row, K and V alike.
+__global__ void append_kv_kernel(const bf16 *__restrict__ k_new, const bf16 *__restrict__ v_new,
+                                 bf16 *__restrict__ k_cache, bf16 *__restrict__ v_cache,
+                                 const int *__restrict__ cache_len, int L, int B, int KV, int S_max, int hd) {
+  const int cpr = hd / 8;                                   // 16-byte chunks per row
+  const long long items = 2LL * L * B * KV * cpr;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < items;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int ch = static_cast<int>(i % cpr);
+    long long r = i / cpr;                                  // ((which * L + l) * B + b) * KV + kv
+    const int kv = static_cast<int>(r % KV);
+    r /= KV;
+    const int b = static_cast<int>(r % B);
+    r /= B;
+    const int l = static_cast<int>(r % L);
+    const int which = static_cast<int>(r / L);
+    const int pos = cache_len[b];
+    if (pos < 0 || pos >= S_max) continue;
+    const long long src = (((long long)l * B + b) * KV + kv) * hd + ch * 8;
+    const long long dst = ((((long long)l * B + b) * KV + kv) * S_max + pos) * hd + ch * 8;
+    const bf16 *s = which ? v_new : k_new;
+    bf16 *d = which ? v_cache : k_cache;
+    *reinterpret_cast<uint4 *>(d + dst) = *reinterpret_cast<const uint4 *>(s + src);
+  }
+}
+
+__global__ void bump_lengths_kernel(int *cache_len, int B, int S_max) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b < B && cache_len[b] >= 0 && cache_len[b] < S_max) cache_len[b] += 1;
+}
+
+cudaError_t launch_append_kv(const bf16 *k_new, const bf16 *v_new, bf16 *k_cache, bf16 *v_cache, int *cache_len,
+                             int L, int B, int KV, int S_max, int hd, cudaStream_t stream) {
+  const long long items = 2LL * L * B * KV * (hd / 8);
+  append_kv_kernel<<<grid_for(items, 256), 256, 0, stream>>>(k_new, v_new, k_cache, v_cache, cache_len, L, B, KV,
+                                                             S_max, hd);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  bump_lengths_kernel<<<static_cast<unsigned>(cdiv(B, 128)), 128, 0, stream>>>(cache_len, B, S_max);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_rope_table(int max_pos, int hd, float theta, float2 *table, cudaStream_t stream) {
   rope_table_kernel<<<grid_for(rope_table_rows(max_pos) * (hd / 4), 256), 256, 0, stream>>>(
       max_pos, hd, static_cast<double>(theta), reinterpret_cast<float4 *>(table));

@@ -505,19 +505,23 @@ SMOL_API int smol_model_forward_masked(const smol_config *cfg, const void *packe
   return model_forward_impl(cfg, packed, ids, B, T, nullptr, key_mask, logits, ws, ws_bytes, stream);
 }
 
-SMOL_API int smol_decode_step(const smol_config *cfg, const void *packed, const int32_t *ids,
-                              const int32_t *cache_len, int B, const void *k_cache,
-                              const void *v_cache, int S_max, void *k_new, void *v_new,
-                              void *logits, void *ws, size_t ws_bytes, void *stream) {
+namespace {
+
+// The decode step; with `next` the greedy choice is taken in the head GEMM's
+// epilogue (logits may then be nullptr).
+int decode_impl(const smol_config *cfg, const void *packed, const int32_t *ids, const int32_t *cache_len, int B,
+                const void *k_cache, const void *v_cache, int S_max, void *k_new, void *v_new, void *logits,
+                int32_t *next, void *ws, size_t ws_bytes, void *stream) {
   g_launches = 0;
   int rc = check_cfg(cfg);
   if (rc) return rc;
-  if (!packed || !ids || !cache_len || !k_cache || !v_cache || !k_new || !v_new || !logits || !ws ||
+  if (!packed || !ids || !cache_len || !k_cache || !v_cache || !k_new || !v_new || (!logits && !next) || !ws ||
       B <= 0 || S_max <= 0 || cfg->vocab <= 0)
     return SMOL_ERR_INVALID_ARG;
   if (!aligned16(packed) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) ||
-      !aligned16(v_new) || !aligned16(logits) || !aligned16(ws) ||
-      (reinterpret_cast<uintptr_t>(ids) & 3u) || (reinterpret_cast<uintptr_t>(cache_len) & 3u))
+      !aligned16(v_new) || (logits && !aligned16(logits)) || !aligned16(ws) ||
+      (reinterpret_cast<uintptr_t>(ids) & 3u) || (reinterpret_cast<uintptr_t>(cache_len) & 3u) ||
+      (reinterpret_cast<uintptr_t>(next) & 3u))
     return SMOL_ERR_MISALIGNED;
   if (ws_bytes < decode_ws_bytes(cfg, B)) return SMOL_ERR_WORKSPACE;
   int sms;
@@ -534,6 +538,7 @@ SMOL_API int smol_decode_step(const smol_config *cfg, const void *packed, const 
   a.k_new = static_cast<bf16 *>(k_new);
   a.v_new = static_cast<bf16 *>(v_new);
   a.logits = static_cast<bf16 *>(logits);
+  a.next = next;
   const uint8_t *pk = static_cast<const uint8_t *>(packed);
   a.rope = reinterpret_cast<const float2 *>(pk + L.rope_off);
   a.embed = reinterpret_cast<const bf16 *>(pk + L.embed_off);
@@ -548,6 +553,58 @@ SMOL_API int smol_decode_step(const smol_config *cfg, const void *packed, const 
   cudaError_t e = run_decode(a, ws, sms, static_cast<cudaStream_t>(stream), &n);
   g_launches = n;
   if (e != cudaSuccess) return cuda_fail(e);
+  return SMOL_OK;
+}
+
+}  // namespace
+
+SMOL_API int smol_decode_step(const smol_config *cfg, const void *packed, const int32_t *ids,
+                              const int32_t *cache_len, int B, const void *k_cache,
+                              const void *v_cache, int S_max, void *k_new, void *v_new,
+                              void *logits, void *ws, size_t ws_bytes, void *stream) {
+  if (!logits) {
+    g_launches = 0;
+    return SMOL_ERR_INVALID_ARG;
+  }
+  return decode_impl(cfg, packed, ids, cache_len, B, k_cache, v_cache, S_max, k_new, v_new, logits, nullptr,
+                     ws, ws_bytes, stream);
+}
+
+SMOL_API int smol_decode_next(const smol_config *cfg, const void *packed, const int32_t *ids,
+                              const int32_t *cache_len, int B, const void *k_cache, const void *v_cache,
+                              int S_max, void *k_new, void *v_new, void *logits, float temperature,
+                              int top_k, float top_p, int do_sample, const float *uniform, int32_t *next,
+                              void *ws, size_t ws_bytes, void *stream) {
+  g_launches = 0;
+  if (!next || temperature != temperature || top_p != top_p) return SMOL_ERR_INVALID_ARG;
+  const bool greedy = !do_sample || !(temperature > 0.f);
+  if (greedy)
+    return decode_impl(cfg, packed, ids, cache_len, B, k_cache, v_cache, S_max, k_new, v_new, logits, next,
+                       ws, ws_bytes, stream);
+  if (!logits || !uniform || (reinterpret_cast<uintptr_t>(uniform) & 3u)) return SMOL_ERR_INVALID_ARG;
+  int rc = decode_impl(cfg, packed, ids, cache_len, B, k_cache, v_cache, S_max, k_new, v_new, logits, nullptr,
+                       ws, ws_bytes, stream);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);   // g_launches holds the decode step's launches
+  LAUNCH_K(SMOL_K_SAMPLE, st, launch_sample(logits, cfg->vocab, B, cfg->vocab, temperature, top_k, top_p, 1,
+                                            uniform, next, st));
+  return SMOL_OK;
+}
+
+SMOL_API int smol_append_kv(const smol_config *cfg, int B, const void *k_new, const void *v_new, void *k_cache,
+                            void *v_cache, int S_max, int32_t *cache_len, void *stream) {
+  g_launches = 0;
+  int rc = check_cfg(cfg);
+  if (rc) return rc;
+  if (!k_new || !v_new || !k_cache || !v_cache || !cache_len || B <= 0 || S_max <= 0) return SMOL_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(cache_len) & 3u))
+    return SMOL_ERR_MISALIGNED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  LAUNCH(launch_append_kv(static_cast<const bf16 *>(k_new), static_cast<const bf16 *>(v_new),
+                          static_cast<bf16 *>(k_cache), static_cast<bf16 *>(v_cache), cache_len, cfg->n_layers,
+                          B, cfg->n_kv_heads, S_max, cfg->head_dim, st));
+  ++g_launches;                                   // the copy and the length update
   return SMOL_OK;
 }
 

@@ -71,6 +71,11 @@ _SIGS = {
                                          c_int, c_void_p, c_void_p, c_void_p, c_void_p]),
     "smol_decode_noalloc_status": (c_int, [c_void_p]),
     "smol_set_wait_limit_ns": (None, [ctypes.c_ulonglong]),
+    "smol_decode_next": (c_int, [_CFG, c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_int,
+                                 c_void_p, c_void_p, c_void_p, c_float, c_int, c_float, c_int, c_void_p,
+                                 c_void_p, c_void_p, c_size_t, c_void_p]),
+    "smol_append_kv": (c_int, [_CFG, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p,
+                               c_void_p]),
     "smol_prefill_cache_workspace_bytes": (c_size_t, [_CFG, c_int, c_int, c_int]),
     "smol_prefill_with_cache": (c_int, [_CFG, c_void_p, c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p,
                                         c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
@@ -307,6 +312,42 @@ def decode_step_noalloc(cfg: Config, packed: torch.Tensor, ids: torch.Tensor, ca
     _check(_lib.smol_decode_step_noalloc(ctypes.byref(cfg), _p(packed), _p(ids), _p(cache_len), B,
                                          _p(k_cache), _p(v_cache), S_max, _p(k_new), _p(v_new),
                                          _p(logits), _stream(stream)), "smol_decode_step_noalloc")
+
+
+def decode_next(cfg: Config, packed: torch.Tensor, ids: torch.Tensor, cache_len: torch.Tensor,
+                k_cache: torch.Tensor, v_cache: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                next_ids: torch.Tensor, ws: torch.Tensor, logits: Optional[torch.Tensor] = None,
+                uniform: Optional[torch.Tensor] = None, temperature: float = 1.0, top_k: int = 0,
+                top_p: float = 1.0, do_sample: bool = False, stream=None) -> None:
+    """The decode step and the next-token choice (greedy inside the head GEMM's
+    epilogue; sampling through the choice kernel over `logits`)."""
+    B = ids.shape[0]
+    S_max = k_cache.shape[3]
+    _dev(ids, torch.int32, "ids")
+    _dev(cache_len, torch.int32, "cache_len")
+    _dev(next_ids, torch.int32, "next_ids")
+    for name, t in (("k_cache", k_cache), ("v_cache", v_cache), ("k_new", k_new), ("v_new", v_new)):
+        _dev(t, torch.bfloat16, name)
+    if logits is not None:
+        _dev(logits, torch.bfloat16, "logits")
+    if uniform is not None:
+        _dev(uniform, torch.float32, "uniform")
+    _check(_lib.smol_decode_next(ctypes.byref(cfg), _p(packed), _p(ids), _p(cache_len), B, _p(k_cache),
+                                 _p(v_cache), S_max, _p(k_new), _p(v_new), _p(logits), float(temperature),
+                                 int(top_k), float(top_p), int(bool(do_sample)), _p(uniform), _p(next_ids),
+                                 _p(ws), ws.numel(), _stream(stream)), "smol_decode_next")
+
+
+def append_kv(cfg: Config, k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+              v_cache: torch.Tensor, cache_len: torch.Tensor, stream=None) -> None:
+    """Appends a decode step's new keys/values at slot cache_len[b] and increments cache_len."""
+    B = cache_len.shape[0]
+    S_max = k_cache.shape[3]
+    for name, t in (("k_new", k_new), ("v_new", v_new), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _dev(t, torch.bfloat16, name)
+    _dev(cache_len, torch.int32, "cache_len")
+    _check(_lib.smol_append_kv(ctypes.byref(cfg), B, _p(k_new), _p(v_new), _p(k_cache), _p(v_cache), S_max,
+                               _p(cache_len), _stream(stream)), "smol_append_kv")
 
 
 def sample(logits: torch.Tensor, next_ids: torch.Tensor, uniform: Optional[torch.Tensor] = None,

@@ -198,3 +198,28 @@ def test_status_strings(smol):
     for code in range(-8, 1):
         assert smol.status_string(code)
     assert "unknown" in smol.status_string(-99)
+
+
+def test_decode_next_and_append_argument_errors(smol):
+    cfg = _cfg(smol)
+    f = ctypes.c_void_p(0x10000)
+    big = 1 << 40
+    nxt = smol.raw.smol_decode_next
+    nan = float("nan")
+    # no `next`
+    assert nxt(ctypes.byref(cfg), f, f, f, 4, f, f, 64, f, f, f, 1.0, 0, 1.0, 0, None, None, f, big, None) == -1
+    # NaN temperature / top_p
+    assert nxt(ctypes.byref(cfg), f, f, f, 4, f, f, 64, f, f, f, nan, 0, 1.0, 1, f, f, f, big, None) == -1
+    assert nxt(ctypes.byref(cfg), f, f, f, 4, f, f, 64, f, f, f, 1.0, 0, nan, 1, f, f, f, big, None) == -1
+    # sampling needs logits and uniform
+    assert nxt(ctypes.byref(cfg), f, f, f, 4, f, f, 64, f, f, None, 1.0, 0, 1.0, 1, f, f, f, big, None) == -1
+    assert nxt(ctypes.byref(cfg), f, f, f, 4, f, f, 64, f, f, f, 1.0, 0, 1.0, 1, None, f, f, big, None) == -1
+    # greedy without logits is accepted up to the workspace check
+    assert nxt(ctypes.byref(cfg), f, f, f, 4, f, f, 64, f, f, None, 1.0, 0, 1.0, 0, None, f, f, 16, None) == -5
+    # smol_decode_step still needs its logits
+    assert smol.raw.smol_decode_step(ctypes.byref(cfg), f, f, f, 4, f, f, 64, f, f, None, f, big, None) == -1
+    app = smol.raw.smol_append_kv
+    assert app(ctypes.byref(cfg), 4, None, f, f, f, 64, f, None) == -1
+    assert app(ctypes.byref(cfg), 0, f, f, f, f, 64, f, None) == -1
+    assert app(ctypes.byref(cfg), 4, f, f, f, f, 64, ctypes.c_void_p(0x10002), None) == -3
+    assert smol.last_launch_count() == 0

@@ -15,6 +15,20 @@ from oracle import oracle as O
 from parity_util import (BLOCK_REL_TOL, LOGITS_COS_MIN, LOGITS_MAX_ABS, cosine, max_abs, np32,
                          oracle_config, oracle_layers, rel_max_err, rel_max_err_bf16_out)
 
+
+def check_cache_entries(got_k, got_v, ref_k, ref_v, what):
+    """New cache entries of a whole-model pass [L, ...]: layer 0's come from a
+    block whose input is the oracle's own (the embedding), held to the block
+    bar; every layer's are intermediate outputs deep in the model, held to the
+    model bar (cosine >= 0.999 and max |err| <= 5e-2 x RMS of the entries)."""
+    for got, ref, name in ((got_k, ref_k, "k"), (got_v, ref_v, "v")):
+        e0 = rel_max_err_bf16_out(got[0], ref[0])
+        cos = cosine(got, ref)
+        rel = max_abs(got, ref) / float(np.sqrt(np.mean(np.asarray(ref, np.float64) ** 2)))
+        print(f"{what} {name}: layer 0 {e0:.3e}, all layers cos {cos:.7f} max/rms {rel:.3e}")
+        assert e0 <= BLOCK_REL_TOL, (what, name, e0)
+        assert cos >= LOGITS_COS_MIN and rel <= LOGITS_MAX_ABS, (what, name, cos, rel)
+
 pytestmark = pytest.mark.gpu
 
 W = synth.WORKLOADS
@@ -124,11 +138,9 @@ def test_full_decode_smollm2_b64_cache4096(S):
     ref, kr, vr = O.decode_step(oc, ol, E, fn, ids[picks], lens[picks], kc, vc)
     got = np32(logits[picks])
     cos, mabs = cosine(got, ref), max_abs(got, ref)
-    ek = rel_max_err_bf16_out(np32(k_new[:, picks]), kr)
-    ev = rel_max_err_bf16_out(np32(v_new[:, picks]), vr)
-    print(f"decode seqs {picks} (lengths {lens[picks].tolist()}): cos {cos:.7f} max abs {mabs:.3e} k {ek:.3e} v {ev:.3e}")
+    print(f"decode seqs {picks} (lengths {lens[picks].tolist()}): cos {cos:.7f} max abs {mabs:.3e}")
     assert cos >= LOGITS_COS_MIN and mabs <= LOGITS_MAX_ABS, (cos, mabs)
-    assert ek <= BLOCK_REL_TOL and ev <= BLOCK_REL_TOL, (ek, ev)
+    check_cache_entries(np32(k_new[:, picks]), np32(v_new[:, picks]), kr, vr, "decode")
 
 
 def test_full_prefill_with_cache_smollm2_b64_cache4096(S):
@@ -155,9 +167,6 @@ def test_full_prefill_with_cache_smollm2_b64_cache4096(S):
                                        lens[picks], np32(inp.k_cache[:, picks]), np32(inp.v_cache[:, picks]))
     got = np32(logits[picks])
     cos, mabs = cosine(got, ref), max_abs(got, ref)
-    ek = rel_max_err_bf16_out(np32(k_new[:, picks]), kr)
-    ev = rel_max_err_bf16_out(np32(v_new[:, picks]), vr)
-    print(f"prefill on cache seqs {picks} (lengths {lens[picks].tolist()}): cos {cos:.7f} max abs {mabs:.3e} "
-          f"k {ek:.3e} v {ev:.3e}")
+    print(f"prefill on cache seqs {picks} (lengths {lens[picks].tolist()}): cos {cos:.7f} max abs {mabs:.3e}")
     assert cos >= LOGITS_COS_MIN and mabs <= LOGITS_MAX_ABS, (cos, mabs)
-    assert ek <= BLOCK_REL_TOL and ev <= BLOCK_REL_TOL, (ek, ev)
+    check_cache_entries(np32(k_new[:, picks]), np32(v_new[:, picks]), kr, vr, "prefill on cache")
