@@ -304,8 +304,10 @@ int smol_decode_step_noalloc(const smol_config *cfg, const void *packed, const i
 
 /* Reads (synchronising `stream`) and clears the status word that
  * smol_decode_step_noalloc's kernels write into the library's scratch array on
- * the current device: SMOL_OK, SMOL_ERR_TIMEOUT (a bounded wait gave up since
- * the last read; the outputs of that call are not valid) or SMOL_ERR_CUDA.
+ * the current device, with the codes of smol_workspace_status: SMOL_OK,
+ * SMOL_ERR_TIMEOUT, SMOL_ERR_RANGE or SMOL_ERR_INPUT (the first one recorded
+ * since the last read; the outputs of that call are not valid), or
+ * SMOL_ERR_CUDA.
  * No counterpart on the pages.  Not meant for the hot path, nor for use while
  * `stream` is capturing. */
 int smol_decode_noalloc_status(void *stream);

@@ -1,4 +1,4 @@
-// attention_tc.cu - causal grouped-query attention on tcgen05 (sm_103a), hd = 64.
+// attention_tc.cu - causal grouped-query attention on tcgen05 (sm_103a), hd 64 or 128.
 //
 // o[b,t,h,:] = sum_{j visible} softmax_j(q[b,h,t].k[b,h/g,j] / sqrt(hd)) v[b,h/g,j]
 // with j visible iff valid_start[b] <= j <= t ("model.py" (SmolLM2-135M)
@@ -14,18 +14,18 @@
 // key sequence.
 //
 // One CTA owns (sequence b, kv head, a tile of 128 query tokens) and GH query
-// heads of that kv head.  Each K tile [128 keys x 64] and V^T tile [64 x 128
+// heads of that kv head.  Each K tile [128 keys x hd] and V^T tile [hd x 128
 // keys] is loaded once by TMA into shared memory and serves all GH heads: K/V
 // are never expanded per query head.  Per (kv tile, head):
-//   S = Q_h K^T        tcgen05.mma, M=128 N=128 K=64, fp32 in TMEM (two S buffers
+//   S = Q_h K^T        tcgen05.mma, M=128 N=128 K=hd, fp32 in TMEM (two S buffers
 //                      taken in turn by the heads)
 //   P = exp2(S*c - m)  a softmax warpgroup, one query row per thread,
 //                      all 128 keys of the tile (no exchange between warps); P is
 //                      written as f16 into the head's shared-memory P buffer, in the
 //                      swizzled K-major layout of an MMA operand, and the S buffer is
 //                      released as soon as it has been read
-//   O_h += P [V | 1]   tcgen05.mma, M=128 N=80 K=128: the 64 value columns plus a
-//                      constant row of ones appended to V^T, so column 64 of the
+//   O_h += P [V | 1]   tcgen05.mma, M=128 N=hd+16 K=128: the hd value columns plus a
+//                      constant row of ones appended to V^T, so column hd of the
 //                      accumulator is the row sum of the very f16 P that weights V
 // The tensor pipe is fed by three issuing warps: an issue of tcgen05.mma takes
 // a fixed ~110 cycles of its issuing thread whatever N is (measured), so one
@@ -610,8 +610,7 @@ cudaError_t launch_gh(const AttnParams &a, const CUtensorMap &tq, const CUtensor
 }  // namespace
 
 bool attention_tc_supported(int hd, int H, int KV) {
-  const int G = H / KV;
-  return (hd == 64 || hd == 128) && (G == 1 || G == 2 || G == 3 || G == 4 || G == 6 || G == 8);
+  return (hd == 64 || hd == 128) && KV > 0 && H >= KV && H % KV == 0;
 }
 
 cudaError_t launch_attention_tc(const AttnParams &a, cudaStream_t st) {
@@ -630,15 +629,11 @@ cudaError_t launch_attention_tc(const AttnParams &a, cudaStream_t st) {
     return cudaErrorInvalidValue;
   const int G = a.H / a.KV;
   if (HDv == 128) return launch_gh<128, 1>(a, tq, tk, tv, to, st);   // one query head per CTA
-  switch (G) {
-    case 1: return launch_gh<64, 1>(a, tq, tk, tv, to, st);
-    case 2: return launch_gh<64, 2>(a, tq, tk, tv, to, st);
-    case 3: return launch_gh<64, 3>(a, tq, tk, tv, to, st);
-    case 4: return launch_gh<64, 2>(a, tq, tk, tv, to, st);   // two CTAs per group of four
-    case 6: return launch_gh<64, 3>(a, tq, tk, tv, to, st);   // two CTAs per group of six
-    case 8: return launch_gh<64, 2>(a, tq, tk, tv, to, st);   // four CTAs per group of eight
-  }
-  return cudaErrorInvalidConfiguration;
+  // the group's heads split over G / GH CTAs: three heads per CTA where G is
+  // a multiple of 3, two where it is even, else one (groups of 5 and 7)
+  if (G % 3 == 0) return launch_gh<64, 3>(a, tq, tk, tv, to, st);
+  if (G % 2 == 0) return launch_gh<64, 2>(a, tq, tk, tv, to, st);
+  return launch_gh<64, 1>(a, tq, tk, tv, to, st);
 }
 
 }  // namespace smol

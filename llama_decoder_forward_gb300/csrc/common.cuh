@@ -131,8 +131,8 @@ cudaError_t launch_skinny_gemm(int epi, const void *A, const void *W, const Gemm
 // ------------------------------------------------------------------ attention
 struct AttnParams {
   const f16 *q;           // [B, H, T, hd]
-  const f16 *k, *v;       // [B, KV, T, hd]
-  const f16 *v_t;         // [B, KV, hd, T_pad] (tcgen05 kernel) or nullptr
+  const f16 *k, *v;       // k: [B, KV, Tk, hd]; v unused (nullptr)
+  const f16 *v_t;         // [B, KV, hd, T_pad], required
   int T_pad;
   int *status;            // device status word (bounded waits)
   int num_sms;
@@ -144,11 +144,10 @@ struct AttnParams {
   const uint8_t *key_mask; // [B, T] or nullptr: key j of sequence b hidden where 0
   int Tk;                 // keys per sequence (k: [B, KV, Tk, hd], v_t pitch T_pad >= Tk); 0: T
   int q_off;              // key index of query 0 (queries are the last T of Tk keys); 0 with Tk = T
-  int pdl;                // tcgen05 kernel: launch as a programmatic dependent of the preceding kernel
-  unsigned long long wait_ns;   // tcgen05 kernel: bounded-wait limit, 0 = the default 1 s
+  int pdl;                // launch as a programmatic dependent of the preceding kernel
+  unsigned long long wait_ns;   // bounded-wait limit, 0 = the default 1 s
 };
-cudaError_t launch_flash_attention(const AttnParams &p, cudaStream_t stream);
-// tcgen05 attention (head_dim 64, group of at most 4 query heads); needs v_t.
+// tcgen05 attention: head_dim 64 or 128, any query group; needs v_t.
 bool attention_tc_supported(int hd, int H, int KV);
 cudaError_t launch_attention_tc(const AttnParams &p, cudaStream_t stream);
 

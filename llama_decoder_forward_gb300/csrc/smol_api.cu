@@ -219,14 +219,9 @@ int run_block(const smol_config *c, const void *packed, int layer, const BlockIO
   GemmParams p{};
   p.M = (int)M; p.N = (H + 2 * KV) * hd; p.K = d;
   p.ssq_in = ssq_a; p.inv_dim = 1.0f / d; p.eps = c->rms_eps; p.ssq_zero = ssq_b;
-  const bool tc_attn = attention_tc_supported(hd, H, KV);
   p.q = q; p.k = k; p.k_bf = io.k_bf; p.v_bf = io.v_bf;
-  if (tc_attn) {
-    p.v_t = v;
-    p.T_pad = (int)t_pad(T);
-  } else {
-    p.v = v;
-  }
+  p.v_t = v;
+  p.T_pad = (int)t_pad(T);
   p.T = T; p.H = H; p.KV = KV; p.hd = hd;
   // a NoPE block passes no table: the epilogue then leaves q and k unrotated
   p.rope = layer_rotary(c, layer)
@@ -270,13 +265,11 @@ int run_block(const smol_config *c, const void *packed, int layer, const BlockIO
     ap.valid_start = vsb;
     ap.pdl = 0;                    // the gather kernel in between is not a programmatic launch
     LAUNCH_K(SMOL_K_ATTN, st, launch_attention_tc(ap, st));
-  } else if (tc_attn) {
+  } else {
     ap.v = nullptr;
     ap.v_t = v;
     ap.T_pad = (int)t_pad(T);
     LAUNCH_K(SMOL_K_ATTN, st, launch_attention_tc(ap, st));
-  } else {
-    LAUNCH_K(SMOL_K_ATTN, st, launch_flash_attention(ap, st));
   }
 
   // 3. O projection + residual: h = x + o Wo^T (f16), ssq_b += rowsum(h^2)

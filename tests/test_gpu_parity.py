@@ -81,11 +81,11 @@ def test_block_smollm2_ragged(S, B, T):
     run_block_case(S, W["smollm2_block_b1_t128"].scaled(B=B, T=T), seed=B * 1000 + T)
 
 
-@pytest.mark.parametrize("H,KV", [(4, 4), (4, 2), (4, 1), (6, 1)])
+@pytest.mark.parametrize("H,KV", [(4, 4), (4, 2), (4, 1), (6, 1), (5, 1), (7, 1), (8, 1)])
 def test_block_group_sizes(S, H, KV):
-    # query heads per kv head 1, 2, 4 and 6: one CTA per group of 1 or 2 heads
-    # (one softmax warpgroup, or two taking the slots in turn) and groups split
-    # over several CTAs
+    # query heads per kv head 1, 2, 4, 6, 5, 7 and 8: one CTA per group of 1 or
+    # 2 heads (one softmax warpgroup, or two taking the slots in turn) and groups
+    # split over several CTAs (two or three heads each, or one for 5 and 7)
     wl = W["smollm2_block_b1_t128"].scaled(B=2, T=300, hidden=64 * H, n_heads=H, n_kv_heads=KV,
                                            intermediate=512)
     run_block_case(S, wl, seed=40 + H * 10 + KV)
@@ -250,7 +250,7 @@ def test_block_window_left_padded(S):
 
 
 def test_block_smollm3_nope_window_head_dim_128(S):
-    # head dim 128: the mma.sync flash attention
+    # head dim 128: the tcgen05 attention with one query head per CTA
     wl = W["smollm3_4blocks_b4_t4096"].scaled(B=2, T=150, n_layers=2, no_rope_layers=(1, 0),
                                               sliding_window=(0, 37))
     run_block_case(S, wl, seed=42, layer=1)
@@ -402,7 +402,7 @@ def _key_mask(B, T, seed, keep=0.6):
 @pytest.mark.parametrize("wl_name,B,T,layer_kw", [
     ("smollm2_block_b1_t128", 2, 300, dict()),                                   # tcgen05, G = 3
     ("smollm2_block_b1_t128", 1, 257, dict(sliding_window=(90,))),               # mask + window
-    ("smollm3_4blocks_b4_t4096", 2, 130, dict()),                                # hd 128 flash path
+    ("smollm3_4blocks_b4_t4096", 2, 130, dict()),                                # tcgen05, hd 128
 ])
 def test_block_key_mask(S, wl_name, B, T, layer_kw):
     wl = W[wl_name].scaled(B=B, T=T, n_layers=1, **layer_kw)
