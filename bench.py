@@ -700,6 +700,17 @@ def profile_case(args):
         ws = S.alloc_workspace(cfg, S.OP_MODEL, wl.B, wl.T)
         logits = torch.empty(wl.B, wl.T, wl.vocab, dtype=torch.bfloat16, device="cuda")
         S.model_forward(cfg, packed, inp.ids, logits, ws)
+    elif args.profile_case == "smollm3":
+        wl = synth.WORKLOADS["smollm3_4blocks_b4_t4096"].scaled(n_layers=args.profile_layers)
+        cfg = S.config_of(wl)
+        inp = synth.generate(wl, seed=0, device="cuda")
+        packed = S.prepare_weights(cfg, inp.layers)
+        ws = S.alloc_workspace(cfg, S.OP_BLOCK, wl.B, wl.T)
+        bufs = [torch.empty_like(inp.x), torch.empty_like(inp.x)]
+        cur = inp.x
+        for l in range(wl.n_layers):
+            S.block_forward(cfg, packed, l, cur, bufs[l & 1], ws)
+            cur = bufs[l & 1]
     else:
         wl = DECODE.scaled(n_layers=args.profile_layers)
         cfg = S.config_of(wl)
@@ -727,7 +738,7 @@ def main():
     ap.add_argument("--no-other-configs", action="store_true",
                     help="skip the single-block, SmolLM3-shaped and left-padded block workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the oracle")
-    ap.add_argument("--profile-case", choices=["prefill", "decode"],
+    ap.add_argument("--profile-case", choices=["prefill", "decode", "smollm3"],
                     help="run one untimed step of the workload with --profile-layers blocks and exit "
                          "(the per-launch shapes equal the full workload's; a small case for ncu)")
     ap.add_argument("--profile-layers", type=int, default=2)
