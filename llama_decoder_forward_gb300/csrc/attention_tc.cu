@@ -92,6 +92,7 @@ struct AtParams {
   int Tk, q_off;            // keys per sequence; key index of query 0
   unsigned long long wait_ns;   // limit of the bounded waits (drains keep 1 s)
   int *status;
+  int *done_out;            // or nullptr: +1 at done_out[b * T / 128 + query tile] when written
 };
 
 enum : int {
@@ -552,11 +553,21 @@ __global__ void __launch_bounds__(AtCfg<HD, GH>::THREADS, 1)
       if (lane == 0) at_status(p.status, kAtTimeoutSoftmax);
       *abort_flag = 1;
     }
-    if (lane == 0) bulk_wait_group_read<0>();     // the staging is read before the CTA exits
+    // the staging is read before the CTA exits; with a completion flag the
+    // stores must also be complete
+    if (lane == 0) {
+      if (p.done_out) bulk_wait_group<0>();
+      else bulk_wait_group_read<0>();
+    }
   }
 
+  if (p.done_out) __threadfence();                // every lane's direct row stores
   tc_fence_before_sync();
   __syncthreads();
+  if (p.done_out && threadIdx.x == 0) {
+    fence_proxy_async_global();
+    flag_add_release(p.done_out + b * (T / kBQ) + q0 / kBQ, 1);
+  }
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, 512);
@@ -584,6 +595,7 @@ cudaError_t launch_ghk(const AttnParams &a, const CUtensorMap &tq, const CUtenso
   p.q_off = a.q_off;
   p.wait_ns = a.wait_ns ? a.wait_ns : kWaitTimeoutNs;
   p.status = a.status;
+  p.done_out = (a.done_out && a.T % kBQ == 0 && (a.Tk <= 0 || a.Tk == a.T)) ? a.done_out : nullptr;
   dim3 grid((unsigned)(a.B * a.KV * p.n_hsub), (unsigned)cdiv(a.T, kBQ), 1u);
   // as a programmatic dependent: CTAs set up barriers and TMEM while the
   // preceding kernel drains, and wait for it before touching its outputs
@@ -608,6 +620,13 @@ cudaError_t launch_gh(const AttnParams &a, const CUtensorMap &tq, const CUtensor
 }
 
 }  // namespace
+
+int attention_tc_ctas_per_tile(int hd, int H, int KV) {
+  if (!attention_tc_supported(hd, H, KV)) return 0;
+  const int G = H / KV;
+  const int GH = hd == 128 ? 1 : (G % 3 == 0 ? 3 : (G % 2 == 0 ? 2 : 1));
+  return KV * (G / GH);
+}
 
 bool attention_tc_supported(int hd, int H, int KV) {
   return (hd == 64 || hd == 128) && KV > 0 && H >= KV && H % KV == 0;

@@ -82,6 +82,13 @@ struct GemmParams {
   int raster_m;           // set by launch_gemm: 1 = consecutive tiles walk down M (B tile reused)
   int epi_tma;            // set by launch_gemm: which epilogue tensor maps are valid
   int pdl;                // launch as a programmatic dependent of the preceding kernel
+  // Row-block completion flags (one int per 128 rows of M), or nullptr: the
+  // producer waits for done_in[row block] >= done_need before loading A rows
+  // (instead of waiting for the whole preceding kernel); every epilogue warp
+  // adds 1 to done_out[row block] once a tile's outputs are written.
+  int *done_out;
+  const int *done_in;
+  int done_need;
 };
 
 // Raises the dynamic shared-memory limit of kernel `Kern` to `bytes`, once per
@@ -146,9 +153,13 @@ struct AttnParams {
   int q_off;              // key index of query 0 (queries are the last T of Tk keys); 0 with Tk = T
   int pdl;                // launch as a programmatic dependent of the preceding kernel
   unsigned long long wait_ns;   // bounded-wait limit, 0 = the default 1 s
+  int *done_out;          // or nullptr: each CTA adds 1 to done_out[b * T / 128 + query tile]
+                          // once its outputs are written (T a multiple of 128)
 };
 // tcgen05 attention: head_dim 64 or 128, any query group; needs v_t.
 bool attention_tc_supported(int hd, int H, int KV);
+// CTAs that write one (sequence, query tile): the kv heads times the CTAs per group.
+int attention_tc_ctas_per_tile(int hd, int H, int KV);
 cudaError_t launch_attention_tc(const AttnParams &p, cudaStream_t stream);
 
 // ------------------------------------------------------------------ next-token choice

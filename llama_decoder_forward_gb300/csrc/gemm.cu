@@ -757,11 +757,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           load_b(kb, kb, n_blk);
         }
       }
-      griddep_wait();
+      // with row-block flags only the rows a tile reads must be complete;
+      // otherwise the whole preceding kernel
+      if (!p.done_in) griddep_wait();
       for (int tile = first_tile; tile < num_tiles && ok; tile += tile_step) {
         int m_grp, n_blk;
         decode_tile(tile, m_grp, n_blk);
         const int m_blk = m_grp * PAIR + rank;
+        // (a pair's second row block may lie past M: no rows, no flag)
+        if (p.done_in && m_blk * C::BM < p.M) {
+          if (!flag_wait_geq(p.done_in + m_blk, p.done_need, abort_flag)) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async_global();             // the A rows are read by TMA
+        }
         for (int kb = 0; kb < num_kb; ++kb) {
           const bool preloaded = issued < pre;     // stage armed and its B requested above
           if (!preloaded && !mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag)) {
@@ -849,7 +859,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else {
     // -------------------------------------------------- epilogue (warps 2 .. 1+kEpiWarps)
-    griddep_wait();                               // reads and writes activations
+    // reads and writes activations: with row-block flags each tile waits for
+    // its own rows below (the buffers it writes are not read by the preceding
+    // kernel); otherwise the whole preceding kernel
+    if (!p.done_in) griddep_wait();
     const int quarter = warp & 3;                 // TMEM lanes 32*quarter .. +31
     EpiCtx e;
     e.lane = lane;
@@ -880,6 +893,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       e.rows_valid = min(32, max(0, p.M - e.row0));
       e.n0 = n_blk * BN;
       e.n_blk = n_blk;
+      if (p.done_in && m_blk * C::BM < p.M) {
+        // the row statistics and the residual rows come from the preceding kernel
+        if (!__all_sync(0xffffffffu, flag_wait_geq(p.done_in + m_blk, p.done_need, abort_flag))) {
+          if (lane == 0) record_status(p.status, kDevTimeoutEpilogue);
+          *abort_flag = 1;
+          break;
+        }
+        fence_proxy_async_global();
+      }
       if constexpr (EPI != kEpiResidual) e.rs = row_rstd(p, e.row0 + lane);
       if constexpr (EPI == kEpiResidual) {
         // start fetching this warp's residual while the MMAs run
@@ -926,6 +948,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // even CTA's barrier for a pair
       if (lane == 0)
         mbar_arrive_relaxed_cluster((PAIR == 1 ? smem_u32(tempty) : tempty0_leader) + 8u * acc);
+      if (p.done_out && m_blk * C::BM < p.M) {
+        // this warp's part of the tile is written (its TMA stores complete,
+        // its lanes' stores and row-sum atomics fenced): one arrival on the
+        // row block's flag
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) {
+          bulk_wait_group<0>();
+          fence_proxy_async_global();
+          flag_add_release(p.done_out + m_blk, 1);
+        }
+        __syncwarp();
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }

@@ -412,6 +412,46 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Orders this thread's generic-proxy accesses to global memory with its
+// async-proxy (TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- completion flags
+// Row-block completion counters between kernels of one step: a producer adds 1
+// (release, GPU scope) once its writes to a block are complete; a consumer
+// waits (acquire) until the count reaches what every producer of the block
+// adds.  The consumer kernel is launched as a programmatic dependent, so it
+// starts only after every CTA of the producer kernel has started: a wait
+// never holds an SM that a producer CTA still needs.
+__device__ __forceinline__ int flag_load_acquire(const int *flag) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void flag_add_release(int *flag, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(flag), "r"(v) : "memory");
+}
+
+// Waits until *flag >= need.  Gives up (false) when `abort_flag` becomes
+// nonzero or after limit_ns nanoseconds.
+__device__ __forceinline__ bool flag_wait_geq(const int *flag, int need, volatile int *abort_flag,
+                                              uint64_t limit_ns = kWaitTimeoutNs) {
+  if (flag_load_acquire(flag) >= need) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i) {
+      __nanosleep(64);
+      if (flag_load_acquire(flag) >= need) return true;
+    }
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }

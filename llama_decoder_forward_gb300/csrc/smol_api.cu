@@ -57,6 +57,7 @@ PackLayout pack_layout(const smol_config *c, int n_layers, int with_embed) {
 struct WsLayout {
   size_t status, x, h, q, k, v, o, a, ssq_a, ssq_b;
   size_t kc, vtc, vs;        // prefill on top of a cache only
+  size_t flags;              // the model forward only: row-block completion flags
   size_t total;
 };
 
@@ -64,7 +65,12 @@ struct WsLayout {
 // kernel is used; T_pad = T rounded up to a multiple of 8.
 long long t_pad(int T) { return (T + 7) / 8 * 8; }
 
-WsLayout ws_layout(const smol_config *c, int B, int T) {
+// Row blocks of 128 rows of M = B*T (the tile GEMMs' row tiles).
+long long row_blocks(int B, int T) { return ((long long)B * T + 127) / 128; }
+
+// `chain`: the model forward, whose kernels hand some row blocks to one
+// another through completion flags.
+WsLayout ws_layout(const smol_config *c, int B, int T, bool chain = false) {
   WsLayout W{};
   const long long M = (long long)B * T;
   const size_t d = c->hidden, hd = c->head_dim, H = c->n_heads, KV = c->n_kv_heads, I = c->intermediate;
@@ -80,6 +86,9 @@ WsLayout ws_layout(const smol_config *c, int B, int T) {
   W.a = o; o = align_up(o + M * I * 2, 1024);
   W.ssq_a = o; o = align_up(o + M * 4, 1024);
   W.ssq_b = o; o = align_up(o + M * 4, 1024);
+  if (chain) {
+    W.flags = o; o = align_up(o + (size_t)c->n_layers * 2 * row_blocks(B, T) * 4, 1024);
+  }
   W.total = o;
   return W;
 }
@@ -198,9 +207,26 @@ struct CacheCtx {
   int S_max, lmax;
 };
 
+// Row-block completion flags of the model forward, zeroed before its first
+// kernel: per layer two arrays of row_blocks ints, written by the attention
+// (read by the O projection) and by the down projection (read by the next
+// layer's QKV projection or the head).  These two hand-offs follow a kernel
+// whose last CTAs run well after the others; between the other kernels the
+// whole-kernel wait measured faster (the flag's stores-complete wait in every
+// epilogue warp cost more than the overlap gained).
+struct FlagCtx {
+  int *flags;
+  long long mblocks;
+  int *at(int layer, int stage) const { return flags + ((long long)layer * 2 + stage) * mblocks; }
+};
+
+// Arrivals per row block from a tile GEMM of N columns and tile width bn: one
+// per epilogue warp (eight per CTA) and column tile.
+int gemm_arrivals(int N, int bn) { return 8 * static_cast<int>((N + bn - 1) / bn); }
+
 int run_block(const smol_config *c, const void *packed, int layer, const BlockIO &io, int B, int T,
               const int32_t *valid_start, const uint8_t *key_mask, const WsLayout &W, uint8_t *ws, int sms,
-              cudaStream_t st, const CacheCtx *cc = nullptr) {
+              cudaStream_t st, const CacheCtx *cc = nullptr, const FlagCtx *fc = nullptr) {
   const long long M = (long long)B * T;
   const int d = c->hidden, H = c->n_heads, KV = c->n_kv_heads, hd = c->head_dim, I = c->intermediate;
   const LayerPtrs lp = layer_ptrs(c, packed, layer);
@@ -212,6 +238,13 @@ int run_block(const smol_config *c, const void *packed, int layer, const BlockIO
   f16 *k = reinterpret_cast<f16 *>(ws + W.k);
   f16 *v = reinterpret_cast<f16 *>(ws + W.v);
   f16 *o = reinterpret_cast<f16 *>(ws + W.o);
+  const int bn_qkv = gemm_pick_bn(kEpiQkvRope, (H + 2 * KV) * hd, hd);
+  const int bn_o = gemm_pick_bn(kEpiResidual, d, hd);
+  const int bn_gu = gemm_pick_bn(kEpiSwiglu, 2 * I, hd);
+  const int bn_down = bn_o;
+  // the attention's per-(sequence, query tile) flags coincide with row blocks
+  // of 128 rows when T is a multiple of 128
+  const bool attn_flags = fc && T % 128 == 0 && !key_mask && !cc;
   f16 *h = reinterpret_cast<f16 *>(ws + W.h);
   f16 *a = reinterpret_cast<f16 *>(ws + W.a);
 
@@ -233,9 +266,17 @@ int run_block(const smol_config *c, const void *packed, int layer, const BlockIO
     p.pos_limit = cc->lmax;
   }
   // every kernel of the block is a programmatic dependent of the one before
-  // (each waits for it with griddepcontrol.wait before touching its data)
+  // (each waits for it with griddepcontrol.wait before touching its data, or,
+  // in the model forward, for the flags of the row blocks it reads)
   p.pdl = 1;
-  LAUNCH_K(SMOL_K_QKV, st, launch_gemm(kEpiQkvRope, gemm_pick_bn(kEpiQkvRope, p.N, hd), io.x16, lp.qkv, p, sms, st));
+  if (fc && layer > 0) {
+    // the rows of x this tile reads, from the previous layer's down projection
+    // (whose tiles complete only after the whole previous attention has, so
+    // q, k and V^T are no longer read when they are overwritten here)
+    p.done_in = fc->at(layer - 1, 1);
+    p.done_need = gemm_arrivals(d, bn_down);
+  }
+  LAUNCH_K(SMOL_K_QKV, st, launch_gemm(kEpiQkvRope, bn_qkv, io.x16, lp.qkv, p, sms, st));
 
   // 2. causal GQA attention
   AttnParams ap{};
@@ -247,6 +288,7 @@ int run_block(const smol_config *c, const void *packed, int layer, const BlockIO
   ap.status = status;
   ap.wait_ns = g_attn_wait_ns.load(std::memory_order_relaxed);
   ap.pdl = 1;
+  if (attn_flags) ap.done_out = fc->at(layer, 0);
   if (cc) {
     // the cached slice and the new keys as one left-padded sequence of Tk keys;
     // the queries are its last T
@@ -277,21 +319,26 @@ int run_block(const smol_config *c, const void *packed, int layer, const BlockIO
   po.M = (int)M; po.N = d; po.K = H * hd;
   po.out = h; po.out_is_f16 = 1; po.ldo = d; po.ssq_out = ssq_b; po.status = status;
   po.resid = io.resid_bf; po.resid_f16 = io.resid_f16; po.resid_f32 = io.resid_f32; po.pdl = 1;
-  LAUNCH_K(SMOL_K_OPROJ, st, launch_gemm(kEpiResidual, gemm_pick_bn(kEpiResidual, d, hd), o, lp.o, po, sms, st));
+  if (attn_flags) {
+    po.done_in = fc->at(layer, 0);
+    po.done_need = attention_tc_ctas_per_tile(hd, H, KV);
+  }
+  LAUNCH_K(SMOL_K_OPROJ, st, launch_gemm(kEpiResidual, bn_o, o, lp.o, po, sms, st));
 
   // 4. RMSNorm2 + gate/up + SwiGLU: a = silu(g) * u ; clears ssq_a for step 5
   GemmParams pg{};
   pg.M = (int)M; pg.N = 2 * I; pg.K = d;
   pg.out = a; pg.out_is_f16 = 1; pg.ldo = I; pg.ssq_in = ssq_b; pg.inv_dim = 1.0f / d;
   pg.eps = c->rms_eps; pg.ssq_zero = ssq_a; pg.status = status; pg.pdl = 1;
-  LAUNCH_K(SMOL_K_GATEUP, st, launch_gemm(kEpiSwiglu, gemm_pick_bn(kEpiSwiglu, 2 * I, hd), h, lp.gu, pg, sms, st));
+  LAUNCH_K(SMOL_K_GATEUP, st, launch_gemm(kEpiSwiglu, bn_gu, h, lp.gu, pg, sms, st));
 
   // 5. down projection + residual: out = h + a Wd^T, ssq_a += rowsum(out^2)
   GemmParams pd{};
   pd.M = (int)M; pd.N = d; pd.K = I;
   pd.out = io.out16; pd.out_is_f16 = io.out16_is_f16; pd.out_f32 = io.out_f32; pd.ldo = d;
   pd.resid_f16 = h; pd.ssq_out = ssq_a; pd.status = status; pd.pdl = 1;
-  LAUNCH_K(SMOL_K_DOWN, st, launch_gemm(kEpiResidual, gemm_pick_bn(kEpiResidual, d, hd), a, lp.down, pd, sms, st));
+  if (fc) pd.done_out = fc->at(layer, 1);
+  LAUNCH_K(SMOL_K_DOWN, st, launch_gemm(kEpiResidual, bn_down, a, lp.down, pd, sms, st));
   return SMOL_OK;
 }
 
@@ -365,7 +412,7 @@ SMOL_API size_t smol_workspace_bytes(const smol_config *cfg, int op, int B, int 
   if (op == SMOL_OP_DECODE) return decode_ws_bytes(cfg, B);
   if (T <= 0) return 0;
   if (op != SMOL_OP_BLOCK && op != SMOL_OP_MODEL) return 0;
-  return ws_layout(cfg, B, T).total;
+  return ws_layout(cfg, B, T, op == SMOL_OP_MODEL).total;
 }
 
 namespace {
@@ -427,7 +474,7 @@ int model_forward_impl(const smol_config *cfg, const void *packed, const int32_t
       (reinterpret_cast<uintptr_t>(ids) & 3u) ||
       (valid_start && (reinterpret_cast<uintptr_t>(valid_start) & 3u)))
     return SMOL_ERR_MISALIGNED;
-  const WsLayout W = ws_layout(cfg, B, T);
+  const WsLayout W = ws_layout(cfg, B, T, true);
   if (ws_bytes < W.total) return SMOL_ERR_WORKSPACE;
   int sms;
   if ((rc = device_sms(&sms))) return rc;
@@ -435,6 +482,11 @@ int model_forward_impl(const smol_config *cfg, const void *packed, const int32_t
   uint8_t *wsb = static_cast<uint8_t *>(ws);
   const long long M = (long long)B * T;
   const PackLayout L = pack_layout(cfg, cfg->n_layers, 1);
+  FlagCtx fc{reinterpret_cast<int *>(wsb + W.flags), row_blocks(B, T)};
+  {
+    const cudaError_t e = cudaMemsetAsync(fc.flags, 0, (size_t)cfg->n_layers * 2 * fc.mblocks * 4, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
   const uint8_t *pk = static_cast<const uint8_t *>(packed);
   f16 *x = reinterpret_cast<f16 *>(wsb + W.x);
   float *ssq_a = reinterpret_cast<float *>(wsb + W.ssq_a);
@@ -448,11 +500,13 @@ int model_forward_impl(const smol_config *cfg, const void *packed, const int32_t
   io.out16 = x;
   io.out16_is_f16 = 1;
   for (int l = 0; l < cfg->n_layers; ++l) {
-    rc = run_block(cfg, packed, l, io, B, T, valid_start, key_mask, W, wsb, sms, st);
+    rc = run_block(cfg, packed, l, io, B, T, valid_start, key_mask, W, wsb, sms, st, nullptr, &fc);
     if (rc) return rc;
   }
   GemmParams p{};
   p.M = (int)M; p.N = cfg->vocab; p.K = cfg->hidden;
+  p.done_in = fc.at(cfg->n_layers - 1, 1);
+  p.done_need = gemm_arrivals(cfg->hidden, gemm_pick_bn(kEpiResidual, cfg->hidden, cfg->head_dim));
   p.out = logits; p.out_is_f16 = 0; p.ldo = cfg->vocab;
   p.ssq_in = ssq_a; p.inv_dim = 1.0f / cfg->hidden; p.eps = cfg->rms_eps;
   p.status = reinterpret_cast<int *>(wsb + W.status);
