@@ -766,7 +766,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int m_blk = m_grp * PAIR + rank;
         // (a pair's second row block may lie past M: no rows, no flag)
         if (p.done_in && m_blk * C::BM < p.M) {
-          if (!flag_wait_geq(p.done_in + m_blk, p.done_need, abort_flag)) {
+          if (!flag_wait_geq(p.done_in + m_blk, p.done_need, abort_flag, p.status)) {
             ok = false;
             break;
           }
@@ -895,7 +895,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       e.n_blk = n_blk;
       if (p.done_in && m_blk * C::BM < p.M) {
         // the row statistics and the residual rows come from the preceding kernel
-        if (!__all_sync(0xffffffffu, flag_wait_geq(p.done_in + m_blk, p.done_need, abort_flag))) {
+        if (!__all_sync(0xffffffffu, flag_wait_geq(p.done_in + m_blk, p.done_need, abort_flag, p.status))) {
           if (lane == 0) record_status(p.status, kDevTimeoutEpilogue);
           *abort_flag = 1;
           break;

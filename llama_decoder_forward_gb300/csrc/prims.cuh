@@ -436,8 +436,12 @@ __device__ __forceinline__ void flag_add_release(int *flag, int v) {
 }
 
 // Waits until *flag >= need.  Gives up (false) when `abort_flag` becomes
-// nonzero or after limit_ns nanoseconds.
+// nonzero, when the workspace status word `status` (may be nullptr) records a
+// bounded wait of any kernel of the step that gave up (codes 0x1xx and
+// 0x2xx: such a producer never raises its flags, and its consumers should not
+// each wait out their own limit), or after limit_ns nanoseconds.
 __device__ __forceinline__ bool flag_wait_geq(const int *flag, int need, volatile int *abort_flag,
+                                              const int *status = nullptr,
                                               uint64_t limit_ns = kWaitTimeoutNs) {
   if (flag_load_acquire(flag) >= need) return true;
   const uint64_t t0 = global_timer_ns();
@@ -448,6 +452,10 @@ __device__ __forceinline__ bool flag_wait_geq(const int *flag, int need, volatil
       if (flag_load_acquire(flag) >= need) return true;
     }
     if (*abort_flag) return false;
+    if (status) {
+      const int st = *reinterpret_cast<const volatile int *>(status);
+      if (st != 0 && (st >> 8) <= 2) return false;
+    }
     if (global_timer_ns() - t0 > limit_ns) return false;
   }
 }
