@@ -142,3 +142,31 @@ def test_attention_wait_gives_up(S):
     finally:
         S.set_wait_limit_ns(0)
     _normal_block_call(S, wl, inp, dev, cfg, packed, ws)
+
+
+def test_model_attention_wait_gives_up(S):
+    # the model forward hands row blocks from the attention to the O projection
+    # and from each down projection to the next QKV projection through
+    # completion flags: an attention whose waits give up still raises its
+    # flags, the step ends (no kernel waits out its limit on a flag), the
+    # status word reports the timeout, and the next call is correct
+    wl = W["smollm2_model_b8_t2048"].scaled(B=2, T=256, n_layers=2, vocab=512)
+    inp = synth.generate(wl, seed=35)
+    dev = to_device(inp)
+    cfg = S.config_of(wl)
+    packed = S.prepare_weights(cfg, dev.layers, dev.embed, dev.final_norm)
+    ws = S.alloc_workspace(cfg, S.OP_MODEL, wl.B, wl.T)
+    logits = torch.empty(wl.B, wl.T, wl.vocab, dtype=torch.bfloat16, device="cuda")
+    try:
+        S.set_wait_limit_ns(1)
+        S.model_forward(cfg, packed, dev.ids, logits, ws)
+        torch.cuda.synchronize()
+        assert S.workspace_status(ws) == S.ERR_TIMEOUT
+    finally:
+        S.set_wait_limit_ns(0)
+    S.model_forward(cfg, packed, dev.ids, logits, ws)
+    assert S.workspace_status(ws) == S.OK
+    ref = O.model_forward(oracle_config(wl), oracle_layers(inp), np32(inp.embed), np32(inp.final_norm),
+                          inp.ids.numpy().astype(np.int64))
+    got = np32(logits)
+    assert cosine(got, ref) >= LOGITS_COS_MIN and max_abs(got, ref) <= LOGITS_MAX_ABS
