@@ -165,6 +165,15 @@ def test_model_ragged_small_vocab(S):
     run_model_case(S, W["smollm2_model_b8_t2048"].scaled(B=3, T=37, n_layers=3, vocab=1024), seed=4)
 
 
+@pytest.mark.parametrize("B,T", [(1, 1100), (1, 1152), (3, 384)])
+def test_model_row_block_flags(S, B, T):
+    # the model forward hands row blocks over through completion flags: CTA
+    # pairs over an odd number of 128-row blocks (the last pair's second block
+    # lies past M), with the attention's flags (T a multiple of 128) and
+    # without them
+    run_model_case(S, W["smollm2_model_b8_t2048"].scaled(B=B, T=T, n_layers=2, vocab=512), seed=5)
+
+
 def run_decode_case(S, wl, lengths, seed=0):
     wl = wl.scaled(B=len(lengths))
     inp = synth.generate(wl, seed=seed)
