@@ -165,6 +165,28 @@ def test_model_ragged_small_vocab(S):
     run_model_case(S, W["smollm2_model_b8_t2048"].scaled(B=3, T=37, n_layers=3, vocab=1024), seed=4)
 
 
+def test_model_left_padded(S):
+    # left padding in the model forward (the attention's completion flags on:
+    # T is a multiple of 128); rows before each sequence's start are not compared
+    wl = W["smollm2_model_b8_t2048"].scaled(B=3, T=256, n_layers=2, vocab=512)
+    inp = synth.generate(wl, seed=6)
+    vs = torch.tensor([0, 37, 200], dtype=torch.int32)
+    dev = to_device(inp)
+    cfg = S.config_of(wl)
+    packed = S.prepare_weights(cfg, dev.layers, dev.embed, dev.final_norm)
+    ws = S.alloc_workspace(cfg, S.OP_MODEL, wl.B, wl.T)
+    logits = torch.empty(wl.B, wl.T, wl.vocab, dtype=torch.bfloat16, device="cuda")
+    S.model_forward(cfg, packed, dev.ids, logits, ws, valid_start=vs.cuda())
+    assert S.workspace_status(ws) == S.OK
+    ref = O.model_forward(oracle_config(wl), oracle_layers(inp), np32(inp.embed), np32(inp.final_norm),
+                          inp.ids.numpy().astype(np.int64), valid_start=vs.numpy())
+    got = np32(logits)
+    for b in range(wl.B):
+        g, r = got[b, int(vs[b]):], ref[b, int(vs[b]):]
+        cos, mabs = cosine(g, r), max_abs(g, r)
+        assert cos >= LOGITS_COS_MIN and mabs <= LOGITS_MAX_ABS, (b, cos, mabs)
+
+
 @pytest.mark.parametrize("B,T", [(1, 1100), (1, 1152), (3, 384)])
 def test_model_row_block_flags(S, B, T):
     # the model forward hands row blocks over through completion flags: CTA
