@@ -255,6 +255,15 @@ def test_decode_single_sequence_long_cache(S):
     run_decode_case(S, wl, [4095], seed=8)
 
 
+@pytest.mark.parametrize("H,KV", [(4, 4), (4, 2), (8, 2), (6, 1), (8, 1)])
+def test_decode_group_sizes(S, H, KV):
+    # query heads per kv head 1, 2, 4, 6 and 8 in the persistent decode
+    # attention (groups above 4 take its eight-row fragment layout)
+    wl = W["smollm2_decode_b64_cache4096"].scaled(hidden=64 * H, n_heads=H, n_kv_heads=KV, intermediate=512,
+                                                  n_layers=2, s_max=600, vocab=512)
+    run_decode_case(S, wl, [0, 1, 255, 256, 257, 600, 413], seed=50 + H * 10 + KV)
+
+
 def test_decode_empty_caches(S):
     # no cached keys: attention over the new token alone
     wl = W["smollm2_decode_b64_cache4096"].scaled(n_layers=2, s_max=64, vocab=512)
