@@ -237,7 +237,7 @@ int smol_model_forward_masked(const smol_config *cfg, const void *packed, const 
  *              at slots cache_len[b] .. cache_len[b] + T - 1.
  *   logits     device [B, T, V] bf16.
  *   ws         >= smol_prefill_cache_workspace_bytes(cfg, B, T, S_max) bytes.
- * Supported: head_dim 64 (SMOL_ERR_UNSUPPORTED_SHAPE otherwise); T < max_pos.
+ * Supported: head_dim 64 and 128, as the other calls; T < max_pos (SMOL_ERR_TOO_LONG).
  * ------------------------------------------------------------------------- */
 size_t smol_prefill_cache_workspace_bytes(const smol_config *cfg, int B, int T, int S_max);
 int smol_prefill_with_cache(const smol_config *cfg, const void *packed, const int32_t *ids, int B,

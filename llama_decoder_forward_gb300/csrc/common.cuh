@@ -200,6 +200,6 @@ cudaError_t launch_append_kv(const bf16 *k_new, const bf16 *v_new, bf16 *k_cache
 // keys (hd 64): K [B, KV, Tk, 64], V^T [B, KV, 64, Tk_pad]; vs[b] = first visible slot.
 cudaError_t launch_gather_cache_kv(const bf16 *kc, const bf16 *vc, int S_max, const int *cache_len, int lmax,
                                    const f16 *kn, const f16 *vtn, int T_pad, int B, int KV, int T, int Tk,
-                                   int Tk_pad, f16 *Kc, f16 *Vtc, int *vs, cudaStream_t stream);
+                                   int Tk_pad, int hd, f16 *Kc, f16 *Vtc, int *vs, cudaStream_t stream);
 
 }  // namespace smol

@@ -227,13 +227,13 @@ cudaError_t launch_interleave_gate_up(const bf16 *wg, const bf16 *wu, const bf16
 // tokens, laid out as one left-padded sequence of Tk keys per (sequence b,
 // kv head): slots [Tk - T - L_b, Tk - T) hold the L_b cached rows (bf16 ->
 // f16, exact for values in f16 range), slots [Tk - T, Tk) the new rows, the
-// slots before are zero.  K: [B, KV, Tk, 64]; V^T: [B, KV, 64, Tk_pad].
+// slots before are zero.  K: [B, KV, Tk, hd]; V^T: [B, KV, hd, Tk_pad].
 // vs[b] = Tk - T - L_b is the first visible slot (the padding start).
 __global__ void gather_cache_kv_kernel(const bf16 *__restrict__ kc, const bf16 *__restrict__ vc, int S_max,
                                        const int *__restrict__ cache_len, int lmax,
                                        const f16 *__restrict__ kn, const f16 *__restrict__ vtn, int T_pad,
-                                       int B, int KV, int T, int Tk, int Tk_pad, f16 *__restrict__ Kc,
-                                       f16 *__restrict__ Vtc, int *__restrict__ vs) {
+                                       int B, int KV, int T, int Tk, int Tk_pad, int hd,
+                                       f16 *__restrict__ Kc, f16 *__restrict__ Vtc, int *__restrict__ vs) {
   const long long rows = static_cast<long long>(B) * KV * Tk;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < rows;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -244,32 +244,33 @@ __global__ void gather_cache_kv_kernel(const bf16 *__restrict__ kc, const bf16 *
     L = L < 0 ? 0 : (L > lmax ? lmax : L);
     const int start = Tk - T - L;
     if (r == 0 && bk % KV == 0) vs[b] = start;
-    f16 *krow = Kc + i * 64;
-    f16 *vcol = Vtc + bk * 64 * Tk_pad + r;       // column r of the 64 dims
+    f16 *krow = Kc + i * hd;
+    f16 *vcol = Vtc + bk * hd * Tk_pad + r;       // column r of the hd dimensions
     if (r < start) {
-      for (int c = 0; c < 8; ++c) reinterpret_cast<uint4 *>(krow)[c] = make_uint4(0u, 0u, 0u, 0u);
-      for (int d = 0; d < 64; ++d) vcol[static_cast<long long>(d) * Tk_pad] = __float2half_rn(0.f);
+      for (int c = 0; c < hd / 8; ++c) reinterpret_cast<uint4 *>(krow)[c] = make_uint4(0u, 0u, 0u, 0u);
+      for (int d = 0; d < hd; ++d) vcol[static_cast<long long>(d) * Tk_pad] = __float2half_rn(0.f);
     } else if (r < Tk - T) {
-      const long long src = (bk * S_max + (r - start)) * 64;
-      for (int d = 0; d < 64; ++d) {
+      const long long src = (bk * S_max + (r - start)) * hd;
+      for (int d = 0; d < hd; ++d) {
         krow[d] = __float2half_rn(__bfloat162float(kc[src + d]));
         vcol[static_cast<long long>(d) * Tk_pad] = __float2half_rn(__bfloat162float(vc[src + d]));
       }
     } else {
       const int n = r - (Tk - T);
-      const f16 *ks = kn + (bk * T + n) * 64;
-      for (int c = 0; c < 8; ++c) reinterpret_cast<uint4 *>(krow)[c] = reinterpret_cast<const uint4 *>(ks)[c];
-      for (int d = 0; d < 64; ++d)
-        vcol[static_cast<long long>(d) * Tk_pad] = vtn[(bk * 64 + d) * T_pad + n];
+      const f16 *ks = kn + (bk * T + n) * hd;
+      for (int c = 0; c < hd / 8; ++c) reinterpret_cast<uint4 *>(krow)[c] = reinterpret_cast<const uint4 *>(ks)[c];
+      for (int d = 0; d < hd; ++d)
+        vcol[static_cast<long long>(d) * Tk_pad] = vtn[(bk * hd + d) * T_pad + n];
     }
   }
 }
 
 cudaError_t launch_gather_cache_kv(const bf16 *kc, const bf16 *vc, int S_max, const int *cache_len, int lmax,
                                    const f16 *kn, const f16 *vtn, int T_pad, int B, int KV, int T, int Tk,
-                                   int Tk_pad, f16 *Kc, f16 *Vtc, int *vs, cudaStream_t stream) {
+                                   int Tk_pad, int hd, f16 *Kc, f16 *Vtc, int *vs, cudaStream_t stream) {
+  if (hd % 8) return cudaErrorInvalidValue;
   gather_cache_kv_kernel<<<grid_for(static_cast<long long>(B) * KV * Tk, 256), 256, 0, stream>>>(
-      kc, vc, S_max, cache_len, lmax, kn, vtn, T_pad, B, KV, T, Tk, Tk_pad, Kc, Vtc, vs);
+      kc, vc, S_max, cache_len, lmax, kn, vtn, T_pad, B, KV, T, Tk, Tk_pad, hd, Kc, Vtc, vs);
   return cudaGetLastError();
 }
 

@@ -297,7 +297,7 @@ int run_block(const smol_config *c, const void *packed, int layer, const BlockIO
     f16 *vtc = reinterpret_cast<f16 *>(ws + W.vtc);
     int *vsb = reinterpret_cast<int *>(ws + W.vs);
     LAUNCH(launch_gather_cache_kv(cc->k_cache, cc->v_cache, cc->S_max, cc->cache_len, cc->lmax, k, v,
-                                  (int)t_pad(T), B, KV, T, Tk, (int)t_pad(Tk), kc, vtc, vsb, st));
+                                  (int)t_pad(T), B, KV, T, Tk, (int)t_pad(Tk), hd, kc, vtc, vsb, st));
     ap.k = kc;
     ap.v = nullptr;
     ap.v_t = vtc;
@@ -657,8 +657,7 @@ SMOL_API int smol_append_kv(const smol_config *cfg, int B, const void *k_new, co
 
 SMOL_API size_t smol_prefill_cache_workspace_bytes(const smol_config *cfg, int B, int T, int S_max) {
   if (check_cfg(cfg) != SMOL_OK || B <= 0 || T <= 0 || S_max <= 0 || T >= cfg->max_pos) return 0;
-  // the gather of cached keys into the attention's layout is written for head_dim 64
-  if (cfg->head_dim != 64 || !attention_tc_supported(cfg->head_dim, cfg->n_heads, cfg->n_kv_heads)) return 0;
+  if (!attention_tc_supported(cfg->head_dim, cfg->n_heads, cfg->n_kv_heads)) return 0;
   return ws_layout_cache(cfg, B, T, S_max).total;
 }
 
@@ -672,8 +671,7 @@ SMOL_API int smol_prefill_with_cache(const smol_config *cfg, const void *packed,
   if (!packed || !ids || !cache_len || !k_cache || !v_cache || !k_new || !v_new || !logits || !ws || B <= 0 ||
       T <= 0 || S_max <= 0 || cfg->vocab <= 0)
     return SMOL_ERR_INVALID_ARG;
-  if (cfg->head_dim != 64 || !attention_tc_supported(cfg->head_dim, cfg->n_heads, cfg->n_kv_heads))
-    return SMOL_ERR_UNSUPPORTED_SHAPE;
+  if (!attention_tc_supported(cfg->head_dim, cfg->n_heads, cfg->n_kv_heads)) return SMOL_ERR_UNSUPPORTED_SHAPE;
   if ((long long)B * T > 0x7fffffffLL) return SMOL_ERR_UNSUPPORTED_SHAPE;
   if (T >= cfg->max_pos) return SMOL_ERR_TOO_LONG;
   if (!aligned16(packed) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) ||

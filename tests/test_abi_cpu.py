@@ -148,8 +148,8 @@ def test_prefill_with_cache_argument_errors(smol):
     assert pwc(ctypes.byref(cfg), f, f, 2, 8, f, f, f, 0, f, f, f, f, big, None) == -1        # S_max
     assert pwc(ctypes.byref(cfg), f, f, 2, 8192, f, f, f, 64, f, f, f, f, big, None) == -4    # T >= max_pos
     assert pwc(ctypes.byref(cfg), f, f, 2, 8, f, f, f, 64, f, f, f, f, 16, None) == -5        # workspace
-    hd128 = _cfg(smol, hidden=1152, head_dim=128)
-    assert pwc(ctypes.byref(hd128), f, f, 2, 8, f, f, f, 64, f, f, f, f, big, None) == -2
+    hd96 = _cfg(smol, hidden=864, head_dim=96)
+    assert pwc(ctypes.byref(hd96), f, f, 2, 8, f, f, f, 64, f, f, f, f, big, None) == -2    # head_dim
     assert smol.raw.smol_prefill_cache_workspace_bytes(ctypes.byref(cfg), 2, 8, 64) > \
         smol.workspace_bytes(cfg, smol.OP_MODEL, 2, 8)
     assert smol.last_launch_count() == 0

@@ -527,6 +527,14 @@ def test_prefill_with_cache_long_chunk_nope_window(S):
     run_prefill_cache_case(S, wl, [5, 200], T=260, seed=71)
 
 
+def test_prefill_with_cache_head_dim_128(S):
+    # SmolLM3-shaped layer (hd 128, groups of 4)
+    wl = W["smollm2_decode_b64_cache4096"].scaled(
+        hidden=2048, n_heads=16, n_kv_heads=4, head_dim=128, intermediate=11008, n_layers=1,
+        vocab=512, s_max=300, rms_eps=1e-6, rope_theta=1e6, w_std=0.02)
+    run_prefill_cache_case(S, wl, [0, 129, 300], T=45, seed=74)
+
+
 def test_prefill_append_decode_chain(S):
     # prefill a chunk on top of the caches, append its keys and values, then
     # decode the next token: the GPU chain against the oracle's own chain
