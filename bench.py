@@ -437,6 +437,7 @@ def run_decode(S, args, rank, world, peaks, peaks_src):
         choose()
     smp_ms = max_over_ranks(time_steps(choose, args.steps, world), world)
     gen = run_generate_loop(S, cfg, inp, packed, ws, wl, args, world, rank)
+    pwc = run_prefill_cache(S, cfg, inp, packed, wl, args, world)
     return {
         "workload": f"{wl.name}: SmolLM2-135M decode step, {L} blocks, batch {B}, cache lengths uniform "
                     f"in [{wl.len_range[0]}, {wl.len_range[1]}], cache [{L},{B},{KV},{wl.s_max},{hd}] bf16",
@@ -457,7 +458,41 @@ def run_decode(S, args, rank, world, peaks, peaks_src):
                               "config": "temperature 0.8, top_k 50, top_p 0.9, uniform from the caller",
                               "launches": 1, "logits_bytes": B * wl.vocab * 2},
         "generate": gen,
+        "prefill_with_cache": pwc,
     }
+
+
+PWC_TOKENS = 128
+
+
+def run_prefill_cache(S, cfg, inp, packed, wl, args, world):
+    """Prefill on top of a cache (model.py (Sualeh77) section 4 with a past):
+    PWC_TOKENS new tokens per sequence over the decode workload's caches, all
+    30 blocks and the head, the call replayed as one CUDA graph."""
+    L, B, KV, hd, T = wl.n_layers, wl.B, wl.n_kv_heads, wl.head_dim, PWC_TOKENS
+    g = torch.Generator(device="cuda")
+    g.manual_seed(400)
+    ids = torch.randint(0, wl.vocab, (B, T), generator=g, device="cuda", dtype=torch.int32)
+    ws = S.prefill_cache_workspace(cfg, B, T, wl.s_max)
+    k_new = torch.empty(L, B, KV, T, hd, dtype=torch.bfloat16, device="cuda")
+    v_new = torch.empty_like(k_new)
+    logits = torch.empty(B, T, wl.vocab, dtype=torch.bfloat16, device="cuda")
+
+    def call():
+        S.prefill_with_cache(cfg, packed, ids, inp.lengths, inp.k_cache, inp.v_cache, k_new, v_new, logits, ws)
+
+    for _ in range(3):
+        call()
+    if S.workspace_status(ws) != S.OK:
+        raise RuntimeError("a kernel reported a timeout during warm-up (prefill with cache)")
+    tot, _ = kernel_breakdown(S, call)
+    graph = capture_graph(call)
+    ms = max_over_ranks(time_steps(graph.replay if graph else call, max(3, args.steps // 2), world), world)
+    return {"workload": f"{T} new tokens per sequence on the decode workload's caches (batch {B}, cache "
+                        f"lengths {wl.len_range[0]}..{wl.len_range[1]}), {L} blocks and the tied head",
+            "ms_per_call": round(ms, 4), "tokens_per_s": round(B * T * world / (ms / 1e3), 1),
+            "timing": "CUDA-graph replay of the call" if graph else "eager calls",
+            "kernel_ms_per_call": {k: round(v, 4) for k, v in sorted(tot.items(), key=lambda kv: -kv[1])}}
 
 
 GEN_TOKENS = 16

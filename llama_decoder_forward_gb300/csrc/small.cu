@@ -229,48 +229,81 @@ cudaError_t launch_interleave_gate_up(const bf16 *wg, const bf16 *wu, const bf16
 // f16, exact for values in f16 range), slots [Tk - T, Tk) the new rows, the
 // slots before are zero.  K: [B, KV, Tk, hd]; V^T: [B, KV, hd, Tk_pad].
 // vs[b] = Tk - T - L_b is the first visible slot (the padding start).
-__global__ void gather_cache_kv_kernel(const bf16 *__restrict__ kc, const bf16 *__restrict__ vc, int S_max,
-                                       const int *__restrict__ cache_len, int lmax,
-                                       const f16 *__restrict__ kn, const f16 *__restrict__ vtn, int T_pad,
-                                       int B, int KV, int T, int Tk, int Tk_pad, int hd,
-                                       f16 *__restrict__ Kc, f16 *__restrict__ Vtc, int *__restrict__ vs) {
-  const long long rows = static_cast<long long>(B) * KV * Tk;
-  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < rows;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int r = static_cast<int>(i % Tk);
-    const long long bk = i / Tk;                   // b * KV + kv head
-    const int b = static_cast<int>(bk / KV);
-    int L = cache_len[b];
-    L = L < 0 ? 0 : (L > lmax ? lmax : L);
-    const int start = Tk - T - L;
-    if (r == 0 && bk % KV == 0) vs[b] = start;
-    f16 *krow = Kc + i * hd;
-    f16 *vcol = Vtc + bk * hd * Tk_pad + r;       // column r of the hd dimensions
-    if (r < start) {
-      for (int c = 0; c < hd / 8; ++c) reinterpret_cast<uint4 *>(krow)[c] = make_uint4(0u, 0u, 0u, 0u);
-      for (int d = 0; d < hd; ++d) vcol[static_cast<long long>(d) * Tk_pad] = __float2half_rn(0.f);
-    } else if (r < Tk - T) {
-      const long long src = (bk * S_max + (r - start)) * hd;
-      for (int d = 0; d < hd; ++d) {
-        krow[d] = __float2half_rn(__bfloat162float(kc[src + d]));
-        vcol[static_cast<long long>(d) * Tk_pad] = __float2half_rn(__bfloat162float(vc[src + d]));
+// One CTA per (b, kv head) and 64 slots: K rows are converted 16 bytes per
+// thread; V goes through shared memory and leaves as 64-key rows of V^T, so
+// every global access is a contiguous run.  Slots in 128-key tiles wholly
+// before the padding start are never read by the attention and are skipped.
+constexpr int kGatherSlots = 64;
+
+__global__ void __launch_bounds__(256) gather_cache_kv_kernel(
+    const bf16 *__restrict__ kc, const bf16 *__restrict__ vc, int S_max, const int *__restrict__ cache_len,
+    int lmax, const f16 *__restrict__ kn, const f16 *__restrict__ vtn, int T_pad, int KV, int T, int Tk, int Tk_pad,
+    int hd, f16 *__restrict__ Kc, f16 *__restrict__ Vtc, int *__restrict__ vs) {
+  extern __shared__ uint4 gather_smem[];
+  // [64 slots][hd + 2]: the odd word stride keeps the column reads below at
+  // two lanes per bank
+  uint32_t *sV = reinterpret_cast<uint32_t *>(gather_smem);
+  const int ldw = hd / 2 + 1;
+  const long long bk = blockIdx.y;                   // b * KV + kv head
+  const int b = static_cast<int>(bk / KV);
+  const int r0 = blockIdx.x * kGatherSlots;
+  int L = cache_len[b];
+  L = L < 0 ? 0 : (L > lmax ? lmax : L);
+  const int start = Tk - T - L;
+  if (blockIdx.x == 0 && bk % KV == 0 && threadIdx.x == 0) vs[b] = start;
+  if (r0 + kGatherSlots <= start / 128 * 128) return;   // before the first key tile the attention reads
+  const int cpr = hd / 8;                             // 16-byte chunks per row
+  for (int i = threadIdx.x; i < kGatherSlots * cpr; i += blockDim.x) {
+    const int sl = i / cpr, c = i - sl * cpr, r = r0 + sl;
+    uint4 kw = make_uint4(0u, 0u, 0u, 0u), vw = make_uint4(0u, 0u, 0u, 0u);
+    if (r >= start && r < Tk - T) {                   // cached row: bf16 -> f16
+      const long long src = (bk * S_max + (r - start)) * hd + c * 8;
+      const uint4 ku = *reinterpret_cast<const uint4 *>(kc + src);
+      const uint4 vu = *reinterpret_cast<const uint4 *>(vc + src);
+      const uint32_t *kp = reinterpret_cast<const uint32_t *>(&ku), *vp = reinterpret_cast<const uint32_t *>(&vu);
+      uint32_t *ko = reinterpret_cast<uint32_t *>(&kw), *vo = reinterpret_cast<uint32_t *>(&vw);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 kf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kp[q]));
+        const float2 vf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&vp[q]));
+        const __half2 kh = __floats2half2_rn(kf.x, kf.y), vh = __floats2half2_rn(vf.x, vf.y);
+        ko[q] = *reinterpret_cast<const uint32_t *>(&kh);
+        vo[q] = *reinterpret_cast<const uint32_t *>(&vh);
       }
-    } else {
+    } else if (r >= Tk - T && r < Tk) {              // new row: k as is, v from its transposed copy
       const int n = r - (Tk - T);
-      const f16 *ks = kn + (bk * T + n) * hd;
-      for (int c = 0; c < hd / 8; ++c) reinterpret_cast<uint4 *>(krow)[c] = reinterpret_cast<const uint4 *>(ks)[c];
-      for (int d = 0; d < hd; ++d)
-        vcol[static_cast<long long>(d) * Tk_pad] = vtn[(bk * hd + d) * T_pad + n];
+      kw = *reinterpret_cast<const uint4 *>(kn + (bk * T + n) * hd + c * 8);
+      f16 *vh = reinterpret_cast<f16 *>(&vw);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) vh[e] = vtn[(bk * hd + c * 8 + e) * T_pad + n];
     }
+    if (r < Tk) *reinterpret_cast<uint4 *>(Kc + (bk * Tk + r) * hd + c * 8) = kw;
+    const uint32_t *vq = reinterpret_cast<const uint32_t *>(&vw);   // zeros past Tk as well
+#pragma unroll
+    for (int q = 0; q < 4; ++q) sV[sl * ldw + c * 4 + q] = vq[q];
+  }
+  __syncthreads();
+  // V^T rows: dimension d, eight keys per thread and step
+  for (int i = threadIdx.x; i < hd * (kGatherSlots / 8); i += blockDim.x) {
+    const int d = i / (kGatherSlots / 8), k8 = i - d * (kGatherSlots / 8);
+    const int r = r0 + k8 * 8;
+    if (r >= Tk_pad) continue;
+    uint4 w;
+    f16 *wh = reinterpret_cast<f16 *>(&w);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) wh[e] = reinterpret_cast<const f16 *>(sV + (k8 * 8 + e) * ldw)[d];
+    *reinterpret_cast<uint4 *>(Vtc + (bk * hd + d) * Tk_pad + r) = w;
   }
 }
 
 cudaError_t launch_gather_cache_kv(const bf16 *kc, const bf16 *vc, int S_max, const int *cache_len, int lmax,
                                    const f16 *kn, const f16 *vtn, int T_pad, int B, int KV, int T, int Tk,
                                    int Tk_pad, int hd, f16 *Kc, f16 *Vtc, int *vs, cudaStream_t stream) {
-  if (hd % 8) return cudaErrorInvalidValue;
-  gather_cache_kv_kernel<<<grid_for(static_cast<long long>(B) * KV * Tk, 256), 256, 0, stream>>>(
-      kc, vc, S_max, cache_len, lmax, kn, vtn, T_pad, B, KV, T, Tk, Tk_pad, hd, Kc, Vtc, vs);
+  if (hd % 8 || Tk_pad % 8 || B * KV > 65535) return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>((Tk + kGatherSlots - 1) / kGatherSlots), static_cast<unsigned>(B * KV));
+  const int smem = kGatherSlots * (hd + 2) * 2;
+  gather_cache_kv_kernel<<<grid, 256, smem, stream>>>(kc, vc, S_max, cache_len, lmax, kn, vtn, T_pad, KV, T, Tk,
+                                                      Tk_pad, hd, Kc, Vtc, vs);
   return cudaGetLastError();
 }
 
