@@ -76,7 +76,7 @@ struct AtCfg {
   static constexpr int OFF_MASK = OFF_P + GH * P_BYTES;   // [kNST][4] key-visibility words
   static constexpr int OFF_MST = OFF_MASK + kNST * 16;  // [GH][128] running row max per head
   static constexpr int OFF_BAR = OFF_MST + GH * 128 * 4;
-  static constexpr int NBAR = 1 + 4 * kNST + 4 + 4 * GH + 3;
+  static constexpr int NBAR = 1 + 4 * kNST + 4 + 5 * GH + 3;
   static constexpr int SMEM = 1024 + OFF_BAR + NBAR * 8 + 16;
   static_assert(GH >= 1 && GH * NO <= kTmemS, "O accumulators must fit below the S buffers");
   static_assert(SMEM <= 232448, "shared memory per CTA");
@@ -163,8 +163,8 @@ __global__ void __launch_bounds__(AtCfg<HD, GH>::THREADS, 1)
   // phase: a P V warp takes a given head only every other tile, and a parity
   // wait two phases behind would pass early.
   uint64_t *p_full = s_free + 2;
-  uint64_t *pv_done = p_full + 2 * GH;        // [GH] P V of the head done
-  uint64_t *m_ready = pv_done + GH;           // [GH] running max of the head's rows stored (128 arrivals)
+  uint64_t *pv_done = p_full + 2 * GH;        // [GH][2] P V of the head done, per tile parity
+  uint64_t *m_ready = pv_done + 2 * GH;       // [GH] running max of the head's rows stored (128 arrivals)
   uint64_t *drain = m_ready + GH;             // [3] one per MMA-issuing warp (warps 1, 2, 3)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 3);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -205,7 +205,8 @@ __global__ void __launch_bounds__(AtCfg<HD, GH>::THREADS, 1)
     for (int h = 0; h < GH; ++h) {
       mbar_init(&p_full[2 * h], 128);
       mbar_init(&p_full[2 * h + 1], 128);
-      mbar_init(&pv_done[h], 1);
+      mbar_init(&pv_done[2 * h], 1);
+      mbar_init(&pv_done[2 * h + 1], 1);
       mbar_init(&m_ready[h], 128);
     }
     for (int i = 0; i < 3; ++i) mbar_init(&drain[i], 1);
@@ -358,7 +359,7 @@ __global__ void __launch_bounds__(AtCfg<HD, GH>::THREADS, 1)
             umma_f16(tmem + h * NO, ap + 2 * k, bv + 2 * k, kIdescO, (it | kb | k) != 0);
         }
         any = true;
-        umma_commit(&pv_done[h]);
+        umma_commit(&pv_done[2 * h + (it & 1)]);
         umma_commit(&v_empty[st]);
       }
       if (!ok) {
@@ -447,18 +448,20 @@ __global__ void __launch_bounds__(AtCfg<HD, GH>::THREADS, 1)
       } else if (m == -INFINITY) {
         m = mxa;                                    // first visible key(s) of this row
       }
-      // P V of the previous tile must be done: it reads the P buffer, and a
-      // rescale of O must not race its accumulation
-      if (it > 0 &&
-          !__all_sync(0xffffffffu, mbar_wait_bounded(&pv_done[h], (it - 1) & 1, abort_flag, p.wait_ns))) {
+      // publish the max at once, so that the group taking the head's next tile
+      // can start its exponents.  pv_done is one barrier per (head, tile
+      // parity), and whoever waits for tile i's P V below has itself waited
+      // for tile i - 2's (a head's tiles alternate between the two groups, or
+      // all go to one), so no parity wait runs two phases behind its barrier.
+      m_state[h * 128 + r] = m;
+      mbar_arrive(&m_ready[h]);
+      // P V of the head's previous tile must be done: it reads the P buffer,
+      // and a rescale of O must not race its accumulation
+      if (it > 0 && !__all_sync(0xffffffffu, mbar_wait_bounded(&pv_done[2 * h + ((it - 1) & 1)], ((it - 1) >> 1) & 1,
+                                                              abort_flag, p.wait_ns))) {
         alive = false;
         break;
       }
-      // publish the max only now: whoever takes the head's next tile then
-      // knows this wait has passed, so its own pv_done wait is at most one
-      // phase ahead of the barrier (a parity wait two phases behind would pass)
-      m_state[h * 128 + r] = m;
-      mbar_arrive(&m_ready[h]);
       if (__any_sync(0xffffffffu, resc)) {
         // O_h (and its row-sum column) *= alpha, sixteen columns at a time
         tc_fence_after_sync();
@@ -503,7 +506,8 @@ __global__ void __launch_bounds__(AtCfg<HD, GH>::THREADS, 1)
     for (int h = 0; h < GH; ++h) {
       if (((ntiles - 1) * GH + h) % C::NG != g) continue;
       if (alive &&
-          !__all_sync(0xffffffffu, mbar_wait_bounded(&pv_done[h], (ntiles - 1) & 1, abort_flag, p.wait_ns)))
+          !__all_sync(0xffffffffu, mbar_wait_bounded(&pv_done[2 * h + ((ntiles - 1) & 1)], ((ntiles - 1) >> 1) & 1,
+                                                     abort_flag, p.wait_ns)))
         alive = false;
       if (!alive) break;
       tc_fence_after_sync();
