@@ -342,6 +342,8 @@ def run_prefill(S, args, rank, world, peaks, peaks_src):
     e2e_steps = max(2, min(args.steps, 10))
     e2e_ms = max_over_ranks(e2e_run(e2e_steps), world)
 
+    key_mask = run_prefill_key_mask(S, cfg, packed, ids, logits, ws, wl, args, world, rank, ms)
+
     flops = prefill_flops_per_launch(wl)
     # the forward is timed in a region of a fraction of a second, at full clocks: the
     # burst figure is its denominator; the seconds-long sustained one is shown beside it
@@ -387,8 +389,39 @@ def run_prefill(S, args, rank, world, peaks, peaks_src):
         "step_tensor_frac_of_sustained": round(step_tf / peak_sus, 4) if peak_sus else None,
         "step_tflops": round(step_tf, 2),
         "kernel_ms_per_step": {k: round(v, 4) for k, v in sorted(tot.items(), key=lambda kv: -kv[1])},
+        "key_mask": key_mask,
     }
     return out, (inp, cfg)
+
+
+KEY_MASK_HIDDEN = 0.10
+
+
+def run_prefill_key_mask(S, cfg, packed, ids, logits, ws, wl, args, world, rank, ms_plain):
+    """The same forward with an additive key mask: a uint8 [B, T] mask hiding
+    KEY_MASK_HIDDEN of the keys at random (seeded), through the masked entry
+    point (the attention's mask path, no left padding).  The attention still
+    computes every causal score, so the algorithmic work is the unmasked one."""
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(4321 + rank)
+    km = (torch.rand(wl.B, wl.T, generator=gen, device="cuda") >= KEY_MASK_HIDDEN).to(torch.uint8)
+
+    def step():
+        S.model_forward_masked(cfg, packed, ids, logits, ws, km)
+
+    for _ in range(args.warmup):
+        step()
+    if S.workspace_status(ws) != S.OK:
+        raise RuntimeError("a kernel reported a timeout during the masked warm-up")
+    tot, _ = kernel_breakdown(S, step)
+    graph = capture_graph(step)
+    ms = max_over_ranks(time_steps(graph.replay if graph else step, args.steps, world), world)
+    return {"workload": f"{wl.name} with a uint8 key mask hiding {KEY_MASK_HIDDEN:.0%} of the keys at random "
+                        f"(smol_model_forward_masked)",
+            "ms_per_step": round(ms, 4), "tokens_per_s": round(wl.B * wl.T * world / (ms / 1e3), 1),
+            "vs_unmasked": round(ms / ms_plain, 4),
+            "timing": "CUDA-graph replay of the step" if graph else "eager calls",
+            "kernel_ms_per_step": {k: round(v, 4) for k, v in sorted(tot.items(), key=lambda kv: -kv[1])}}
 
 
 def run_decode(S, args, rank, world, peaks, peaks_src):

@@ -9,7 +9,8 @@
 // 3B checkpoints leave off") also hides keys j <= t - w: the CTA starts at the
 // tile of its first query's window and masks per row.  An optional key mask
 // (the additive 0 / -inf attention_mask of "model.py" section 4, as bytes)
-// hides further keys; every tile then takes the masked path.  With a KV cache
+// hides further keys: each key tile gets the mask as one additive row of 0 and
+// -inf, the same for every query row, added to S.  With a KV cache
 // in front (prefill on top of a cache), query t is key q_off + t of a longer
 // key sequence.
 //
@@ -36,7 +37,7 @@
 // max grows by more than 2^8 (otherwise P may exceed 1 by up to 256, exact in
 // the fp32 sums and within f16 range), the FlashAttention-4 idea.
 // Warp 0 issues TMA (and, with a key mask, turns the tile's mask bytes into
-// bit words).  Warps 4.. form two softmax warpgroups (one when GH = 1) that
+// its additive row).  Warps 4.. form two softmax warpgroups (one when GH = 1) that
 // take the (tile, head) slots in turn; a head's running row max passes from
 // one to the other through shared memory.  All waits are bounded (status
 // word + abort flag, copies and MMAs drained before exit).
@@ -73,8 +74,9 @@ struct AtCfg {
   static constexpr int OFF_K = OFF_Q + GH * Q_BYTES;
   static constexpr int OFF_VT = OFF_K + kNST * K_BYTES;
   static constexpr int OFF_P = OFF_VT + kNST * VT_BYTES;
-  static constexpr int OFF_MASK = OFF_P + GH * P_BYTES;   // [kNST][4] key-visibility words
-  static constexpr int OFF_MST = OFF_MASK + kNST * 16;  // [GH][128] running row max per head
+  static constexpr int OFF_MASK = OFF_P + GH * P_BYTES;   // [kNST][128] key-mask bias (0 or -inf) per key
+  static constexpr int OFF_MANY = OFF_MASK + kNST * kBK * 4;  // [kNST] the tile hides some key (int)
+  static constexpr int OFF_MST = OFF_MANY + 16;         // [GH][128] running row max per head
   static constexpr int OFF_BAR = OFF_MST + GH * 128 * 4;
   static constexpr int NBAR = 1 + 4 * kNST + 4 + 5 * GH + 3;
   static constexpr int SMEM = 1024 + OFF_BAR + NBAR * 8 + 16;
@@ -124,6 +126,19 @@ __device__ __forceinline__ float2 ffma2(float a0, float a1, float b, float c) {
   return d;
 }
 
+// (a0 + b0, a1 + b1) on the packed two-lane fp32 path (one instruction).
+__device__ __forceinline__ float2 fadd2(float a0, float a1, float b0, float b1) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+  return d;
+}
+
 // max(a, b, c) in one instruction (three-input max of sm_100 and later).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
@@ -149,12 +164,13 @@ __global__ void __launch_bounds__(AtCfg<HD, GH>::THREADS, 1)
   uint8_t *sK = smem + C::OFF_K;
   uint8_t *sVt = smem + C::OFF_VT;
   uint8_t *sP = smem + C::OFF_P;
-  uint32_t *sMask = reinterpret_cast<uint32_t *>(smem + C::OFF_MASK);
+  float *sBias = reinterpret_cast<float *>(smem + C::OFF_MASK);
+  int *sBiasAny = reinterpret_cast<int *>(smem + C::OFF_MANY);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
   uint64_t *q_full = bars;
   uint64_t *k_full = bars + 1;                // [kNST] K of a tile landed
   uint64_t *k_empty = k_full + kNST;          // [kNST] every head's S of the tile done
-  uint64_t *v_full = k_empty + kNST;          // [kNST] V^T of a tile (and its key-mask words) landed
+  uint64_t *v_full = k_empty + kNST;          // [kNST] V^T of a tile (and its key-mask row) landed
   uint64_t *v_empty = v_full + kNST;          // [kNST] every head's P V of the tile done (GH commits)
   uint64_t *s_full = v_empty + kNST;          // [2] S computed
   uint64_t *s_free = s_full + 2;              // [2] S read by its softmax warpgroup (128 arrivals)
@@ -242,6 +258,17 @@ __global__ void __launch_bounds__(AtCfg<HD, GH>::THREADS, 1)
     griddep_wait();                               // q, k and V^T come from the preceding kernel
     int nk = 0, nv = 0;                           // K and V tiles issued (for the drain)
     bool ok = true;
+    // with a key mask: this lane's bytes of the next V tile's keys, loaded a
+    // tile ahead so that their latency stays off the V loads
+    const uint8_t *km = KM ? p.key_mask + (long long)b * T : nullptr;
+    uint32_t mb[4] = {0u, 0u, 0u, 0u};
+    if constexpr (KM) {
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const int key = j_lo * kBK + 32 * w + lane;
+        mb[w] = key < T ? km[key] : 0u;
+      }
+    }
     if (lane == 0) {
       mbar_arrive_expect_tx(q_full, GH * C::Q_BYTES);
       for (int h = 0; h < GH; ++h)
@@ -272,18 +299,35 @@ __global__ void __launch_bounds__(AtCfg<HD, GH>::THREADS, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       if constexpr (KM) {
-        // visibility words of the tile's 128 keys (bit e of word w: key j*128 + 32w + e)
-        const uint8_t *km = p.key_mask + (long long)b * T;
+        // the tile's key mask as one additive row (0 visible, -inf hidden; the
+        // same for every query row): key j*128 + 32w + e is bit e of word w,
+        // and lane 0 writes the row (or only marks a tile that hides no key)
+        uint32_t bits[4];
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const int key = j * kBK + 32 * w + lane;
-          const uint32_t bits = __ballot_sync(0xffffffffu, key < T && km[key] != 0);
-          if (lane == 0) sMask[st * 4 + w] = bits;
+        for (int w = 0; w < 4; ++w) bits[w] = __ballot_sync(0xffffffffu, mb[w] != 0u);
+        if (it + 1 < ntiles) {
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const int key = (j + 1) * kBK + 32 * w + lane;
+            mb[w] = key < T ? km[key] : 0u;
+          }
         }
-        __syncwarp();
+        if (lane == 0) {
+          const int any = (bits[0] & bits[1] & bits[2] & bits[3]) != ~0u;
+          sBiasAny[st] = any;
+          if (any) {
+            float4 *row = reinterpret_cast<float4 *>(sBias + st * kBK);
+#pragma unroll
+            for (int e4 = 0; e4 < kBK / 4; ++e4) {
+              const uint32_t nib = bits[e4 >> 3] >> ((e4 & 7) * 4);
+              row[e4] = make_float4((nib & 1u) ? 0.f : -INFINITY, (nib & 2u) ? 0.f : -INFINITY,
+                                    (nib & 4u) ? 0.f : -INFINITY, (nib & 8u) ? 0.f : -INFINITY);
+            }
+          }
+        }
       }
       if (lane == 0) {
-        // the arrive below also releases the mask words to the softmax warps
+        // the arrive below also releases the mask row to the softmax warps
         mbar_arrive_expect_tx(&v_full[st], 2 * C::VT_TMA);
         tma_load_2d(sVt + st * C::VT_BYTES, &tmVt, &v_full[st], j * kBK, (b * p.KV + kvh) * HD);
         tma_load_2d(sVt + st * C::VT_BYTES + C::VT_SUB, &tmVt, &v_full[st], j * kBK + 64,
@@ -389,7 +433,7 @@ __global__ void __launch_bounds__(AtCfg<HD, GH>::THREADS, 1)
       const int it = s / GH, h = s - it * GH, sb = s & 1, st = it % kNST;
       const int k0 = (j_lo + it) * kBK;             // first key of the tile
       const bool need_mask =
-          KM || (k0 + kBK - 1 > qo + q0) || (k0 < vs) || (p.window > 0 && k0 <= qo + last_q - p.window);
+          (k0 + kBK - 1 > qo + q0) || (k0 < vs) || (p.window > 0 && k0 <= qo + last_q - p.window);
       if (!__all_sync(0xffffffffu, mbar_wait_bounded(&s_full[sb], (s >> 1) & 1, abort_flag, p.wait_ns))) {
         alive = false;
         break;
@@ -402,23 +446,33 @@ __global__ void __launch_bounds__(AtCfg<HD, GH>::THREADS, 1)
       tmem_ld_wait();
       tc_fence_before_sync();
       mbar_arrive(&s_free[sb]);                     // the S buffer may be overwritten now
-      uint32_t vis[4] = {~0u, ~0u, ~0u, ~0u};
       if constexpr (KM) {
-        // the tile's mask words, published with its V^T
+        // the tile's key-mask row, published with its V^T: s + (-inf) = -inf
+        // hides a key, s + 0 leaves it (every row reads the same 128 values)
         if (!__all_sync(0xffffffffu, mbar_wait_bounded(&v_full[st], (it / kNST) & 1, abort_flag, p.wait_ns))) {
           alive = false;
           break;
         }
+        const float4 *row = reinterpret_cast<const float4 *>(sBias + st * kBK);
+        if (sBiasAny[st])
 #pragma unroll
-        for (int w = 0; w < 4; ++w) vis[w] = sMask[st * 4 + w];
+        for (int e4 = 0; e4 < kBK / 4; ++e4) {
+          const float4 bb = row[e4];
+          const float2 x = fadd2(__uint_as_float(sv[4 * e4]), __uint_as_float(sv[4 * e4 + 1]), bb.x, bb.y);
+          const float2 y = fadd2(__uint_as_float(sv[4 * e4 + 2]), __uint_as_float(sv[4 * e4 + 3]), bb.z, bb.w);
+          sv[4 * e4] = __float_as_uint(x.x);
+          sv[4 * e4 + 1] = __float_as_uint(x.y);
+          sv[4 * e4 + 2] = __float_as_uint(y.x);
+          sv[4 * e4 + 3] = __float_as_uint(y.y);
+        }
       }
-      // hidden keys (causal, padding, window and key-mask limits) become -inf
-      // in place, so one code path serves masked and unmasked tiles
+      // keys hidden by the causal, padding and window limits become -inf in
+      // place, so one code path serves masked and unmasked tiles
       if (need_mask) {
         const int hi = tk - k0, lo = row_lo - k0;   // keys k0+e visible iff lo <= e <= hi
 #pragma unroll
         for (int e = 0; e < kBK; ++e)
-          if (!(e <= hi && e >= lo && ((vis[e >> 5] >> (e & 31)) & 1u))) sv[e] = 0xff800000u;
+          if (!(e <= hi && e >= lo)) sv[e] = 0xff800000u;
       }
       // row max; eight independent chains
       float mc[8];

@@ -244,7 +244,7 @@ int run_block(const smol_config *c, const void *packed, int layer, const BlockIO
   const int bn_down = bn_o;
   // the attention's per-(sequence, query tile) flags coincide with row blocks
   // of 128 rows when T is a multiple of 128
-  const bool attn_flags = fc && T % 128 == 0 && !key_mask && !cc;
+  const bool attn_flags = fc && T % 128 == 0 && !cc;
   f16 *h = reinterpret_cast<f16 *>(ws + W.h);
   f16 *a = reinterpret_cast<f16 *>(ws + W.a);
 

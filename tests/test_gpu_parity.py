@@ -466,16 +466,26 @@ def test_block_key_mask(S, wl_name, B, T, layer_kw):
     assert err <= BLOCK_REL_TOL
 
 
-def test_model_key_mask(S):
-    wl = W["smollm2_model_b8_t2048"].scaled(B=2, T=150, n_layers=2, vocab=1024)
+@pytest.mark.parametrize("B,T,kind", [(2, 150, "random"), (2, 384, "random"), (2, 384, "prefix")])
+def test_model_key_mask(S, B, T, kind):
+    # T = 384: whole 128-row blocks, so the O projection waits on the attention's
+    # row-block flags instead of its completion.  "prefix": a padding-shaped mask
+    # (each sequence hides a leading run of keys), so whole key tiles hide
+    # nothing and take the attention's unmasked branch
+    wl = W["smollm2_model_b8_t2048"].scaled(B=B, T=T, n_layers=2, vocab=1024)
     inp = synth.generate(wl, seed=62)
-    mask = _key_mask(2, 150, 63)
-    mask[:, 0] = 1
+    if kind == "random":
+        mask = _key_mask(B, T, 63)
+        mask[:, 0] = 1
+    else:
+        mask = torch.ones(B, T, dtype=torch.uint8)
+        mask[0, :5] = 0                               # rows 0..4 of sequence 0 see no key
+        mask[1, :200] = 0
     dev = to_device(inp)
     cfg = S.config_of(wl)
     packed = S.prepare_weights(cfg, dev.layers, dev.embed, dev.final_norm)
-    ws = S.alloc_workspace(cfg, S.OP_MODEL, 2, 150)
-    logits = torch.empty(2, 150, 1024, dtype=torch.bfloat16, device="cuda")
+    ws = S.alloc_workspace(cfg, S.OP_MODEL, B, T)
+    logits = torch.empty(B, T, 1024, dtype=torch.bfloat16, device="cuda")
     S.model_forward_masked(cfg, packed, dev.ids, logits, ws, mask.cuda())
     assert S.workspace_status(ws) == S.OK
     ref = O.model_forward(oracle_config(wl), oracle_layers(inp), np32(inp.embed), np32(inp.final_norm),
