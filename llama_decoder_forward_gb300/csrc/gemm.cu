@@ -1085,7 +1085,10 @@ int gemm_pick_bn(int epi, int N, int hd) {
     if (N % 128) return 0;
     return N % 256 == 0 ? 256 : 128;
   }
-  if (epi == kEpiResidual) {                       // its staging leaves room for BN <= 192
+  if (epi == kEpiResidual) {
+    // 256 columns where they divide N and N is wide (fewer A re-reads and MMA
+    // issues per flop); for N = 576 (SmolLM2) 192 divides it
+    if (N >= 1024 && N % 256 == 0) return 256;
     const int cands[3] = {192, 128, 64};
     for (int c : cands)
       if (N % c == 0) return c;
@@ -1208,6 +1211,7 @@ cudaError_t launch_gemm(int epi, int bn, const void *A, const void *B, const Gem
       if (bn == 64) return launch_impl<64, kEpiScale, 64>(ta, tb, maps, p, num_sms, stream);
       break;
     case kEpiResidual:
+      if (bn == 256) return launch_impl<256, kEpiResidual, 64>(ta, tb, maps, p, num_sms, stream);
       if (bn == 192) return launch_impl<192, kEpiResidual, 64>(ta, tb, maps, p, num_sms, stream);
       if (bn == 128) return launch_impl<128, kEpiResidual, 64>(ta, tb, maps, p, num_sms, stream);
       if (bn == 64) return launch_impl<64, kEpiResidual, 64>(ta, tb, maps, p, num_sms, stream);

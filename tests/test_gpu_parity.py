@@ -196,6 +196,13 @@ def test_model_row_block_flags(S, B, T):
     run_model_case(S, W["smollm2_model_b8_t2048"].scaled(B=B, T=T, n_layers=2, vocab=512), seed=5)
 
 
+def test_model_at_max_positions(S):
+    # the longest sequence a configuration takes: T = max_pos, so the last row
+    # rotates at position max_pos - 1, the table's last entry
+    run_model_case(S, W["smollm2_model_b8_t2048"].scaled(B=1, T=1024, n_layers=2, vocab=512, max_pos=1024),
+                   seed=8)
+
+
 def run_decode_case(S, wl, lengths, seed=0):
     wl = wl.scaled(B=len(lengths))
     inp = synth.generate(wl, seed=seed)
