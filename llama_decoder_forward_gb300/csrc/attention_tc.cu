@@ -87,6 +87,7 @@ struct AtCfg {
 struct AtParams {
   f16 *o;                   // [B, T, H*hd]
   const int *valid_start;
+  const int *seq_order;     // [B] or nullptr: sequence of the CTAs' sequence slot
   const uint8_t *key_mask;  // [B, T] or nullptr: key j of sequence b hidden where 0
   int B, T, H, KV, G, GH, n_hsub;
   float scale_log2;
@@ -192,9 +193,10 @@ __global__ void __launch_bounds__(AtCfg<HD, GH>::THREADS, 1)
   // first and the short ones fill the tail (longest-processing-time order)
   const int q0 = (gridDim.y - 1 - blockIdx.y) * kBQ;
   const int groups = p.KV * p.n_hsub;
-  const int b = blockIdx.x / groups;
-  const int kvh = (blockIdx.x - b * groups) / p.n_hsub;
-  const int hsub = blockIdx.x - b * groups - kvh * p.n_hsub;
+  const int bslot = blockIdx.x / groups;
+  const int b = p.seq_order ? p.seq_order[bslot] : bslot;   // the sequence (longest first with an order)
+  const int kvh = (blockIdx.x - bslot * groups) / p.n_hsub;
+  const int hsub = blockIdx.x - bslot * groups - kvh * p.n_hsub;
   const int h_first = kvh * p.G + hsub * GH;
   const int Tk = p.Tk, qo = p.q_off;              // query t is key qo + t
   const int vs = p.valid_start ? min(max(p.valid_start[b], 0), Tk) : 0;
@@ -642,6 +644,7 @@ cudaError_t launch_ghk(const AttnParams &a, const CUtensorMap &tq, const CUtenso
   AtParams p{};
   p.o = a.o;
   p.valid_start = a.valid_start;
+  p.seq_order = a.seq_order;
   p.key_mask = a.key_mask;
   p.B = a.B; p.T = a.T; p.H = a.H; p.KV = a.KV;
   p.G = a.H / a.KV;

@@ -145,6 +145,7 @@ struct AttnParams {
   int num_sms;
   f16 *o;                 // [B, T, H * hd]
   const int *valid_start; // [B] or nullptr
+  const int *seq_order;   // [B] or nullptr: the CTAs take the sequences in this order (a permutation)
   int B, T, H, KV, hd;
   float scale_log2;       // log2(e) / sqrt(hd)
   int window;             // > 0: query t sees keys j > t - window only (sliding window)
@@ -197,9 +198,11 @@ cudaError_t launch_rope_table(int max_pos, int hd, float theta, float2 *table, c
 cudaError_t launch_append_kv(const bf16 *k_new, const bf16 *v_new, bf16 *k_cache, bf16 *v_cache, int *cache_len,
                              int L, int B, int KV, int S_max, int hd, cudaStream_t stream);
 // One layer's cached keys/values plus the T new ones as left-padded f16 sequences of Tk
-// keys (hd 64): K [B, KV, Tk, 64], V^T [B, KV, 64, Tk_pad]; vs[b] = first visible slot.
+// keys (hd 64 or 128): K [B, KV, Tk, hd], V^T [B, KV, hd, Tk_pad]; vs[b] = first visible
+// slot; order[] = the sequences by descending cache length (ties by index).
 cudaError_t launch_gather_cache_kv(const bf16 *kc, const bf16 *vc, int S_max, const int *cache_len, int lmax,
                                    const f16 *kn, const f16 *vtn, int T_pad, int B, int KV, int T, int Tk,
-                                   int Tk_pad, int hd, f16 *Kc, f16 *Vtc, int *vs, cudaStream_t stream);
+                                   int Tk_pad, int hd, f16 *Kc, f16 *Vtc, int *vs, int *order,
+                                   cudaStream_t stream);
 
 }  // namespace smol

@@ -228,7 +228,10 @@ cudaError_t launch_interleave_gate_up(const bf16 *wg, const bf16 *wu, const bf16
 // kv head): slots [Tk - T - L_b, Tk - T) hold the L_b cached rows (bf16 ->
 // f16, exact for values in f16 range), slots [Tk - T, Tk) the new rows, the
 // slots before are zero.  K: [B, KV, Tk, hd]; V^T: [B, KV, hd, Tk_pad].
-// vs[b] = Tk - T - L_b is the first visible slot (the padding start).
+// vs[b] = Tk - T - L_b is the first visible slot (the padding start), and
+// order[] lists the sequences by descending L_b (ties by index): the attention
+// takes them in that order, the longest first, so that the short ones fill the
+// tail of its launch.
 // One CTA per (b, kv head) and 64 slots: K rows are converted 16 bytes per
 // thread; V goes through shared memory and leaves as 64-key rows of V^T, so
 // every global access is a contiguous run.  Slots in 128-key tiles wholly
@@ -238,7 +241,7 @@ constexpr int kGatherSlots = 64;
 __global__ void __launch_bounds__(256) gather_cache_kv_kernel(
     const bf16 *__restrict__ kc, const bf16 *__restrict__ vc, int S_max, const int *__restrict__ cache_len,
     int lmax, const f16 *__restrict__ kn, const f16 *__restrict__ vtn, int T_pad, int KV, int T, int Tk, int Tk_pad,
-    int hd, f16 *__restrict__ Kc, f16 *__restrict__ Vtc, int *__restrict__ vs) {
+    int hd, f16 *__restrict__ Kc, f16 *__restrict__ Vtc, int *__restrict__ vs, int *__restrict__ order) {
   extern __shared__ uint4 gather_smem[];
   // [64 slots][hd + 2]: the odd word stride keeps the column reads below at
   // two lanes per bank
@@ -250,7 +253,26 @@ __global__ void __launch_bounds__(256) gather_cache_kv_kernel(
   int L = cache_len[b];
   L = L < 0 ? 0 : (L > lmax ? lmax : L);
   const int start = Tk - T - L;
-  if (blockIdx.x == 0 && bk % KV == 0 && threadIdx.x == 0) vs[b] = start;
+  if (blockIdx.x == 0 && bk % KV == 0) {
+    // this sequence's place in the order: the longer sequences, and the equal
+    // ones of lower index, come before it
+    __shared__ int s_rank;
+    if (threadIdx.x == 0) s_rank = 0;
+    __syncthreads();
+    const int B = static_cast<int>(gridDim.y) / KV;
+    int n = 0;
+    for (int i = threadIdx.x; i < B; i += blockDim.x) {
+      int Li = cache_len[i];
+      Li = Li < 0 ? 0 : (Li > lmax ? lmax : Li);
+      n += (Li > L || (Li == L && i < b)) ? 1 : 0;
+    }
+    if (n) atomicAdd(&s_rank, n);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      vs[b] = start;
+      order[s_rank] = b;
+    }
+  }
   if (r0 + kGatherSlots <= start / 128 * 128) return;   // before the first key tile the attention reads
   const int cpr = hd / 8;                             // 16-byte chunks per row
   for (int i = threadIdx.x; i < kGatherSlots * cpr; i += blockDim.x) {
@@ -298,12 +320,13 @@ __global__ void __launch_bounds__(256) gather_cache_kv_kernel(
 
 cudaError_t launch_gather_cache_kv(const bf16 *kc, const bf16 *vc, int S_max, const int *cache_len, int lmax,
                                    const f16 *kn, const f16 *vtn, int T_pad, int B, int KV, int T, int Tk,
-                                   int Tk_pad, int hd, f16 *Kc, f16 *Vtc, int *vs, cudaStream_t stream) {
+                                   int Tk_pad, int hd, f16 *Kc, f16 *Vtc, int *vs, int *order,
+                                   cudaStream_t stream) {
   if (hd % 8 || Tk_pad % 8 || B * KV > 65535) return cudaErrorInvalidValue;
   const dim3 grid(static_cast<unsigned>((Tk + kGatherSlots - 1) / kGatherSlots), static_cast<unsigned>(B * KV));
   const int smem = kGatherSlots * (hd + 2) * 2;
   gather_cache_kv_kernel<<<grid, 256, smem, stream>>>(kc, vc, S_max, cache_len, lmax, kn, vtn, T_pad, KV, T, Tk,
-                                                      Tk_pad, hd, Kc, Vtc, vs);
+                                                      Tk_pad, hd, Kc, Vtc, vs, order);
   return cudaGetLastError();
 }
 

@@ -105,7 +105,7 @@ WsLayout ws_layout_cache(const smol_config *c, int B, int T, int S_max) {
   size_t o = W.total;
   W.kc = o; o = align_up(o + (size_t)B * KV * Tk * hd * 2, 1024);
   W.vtc = o; o = align_up(o + (size_t)B * KV * hd * t_pad((int)Tk) * 2, 1024);
-  W.vs = o; o = align_up(o + (size_t)B * 4, 1024);
+  W.vs = o; o = align_up(o + (size_t)B * 8, 1024);   // vs[B], then the sequence order[B]
   W.total = o;
   return W;
 }
@@ -297,7 +297,7 @@ int run_block(const smol_config *c, const void *packed, int layer, const BlockIO
     f16 *vtc = reinterpret_cast<f16 *>(ws + W.vtc);
     int *vsb = reinterpret_cast<int *>(ws + W.vs);
     LAUNCH(launch_gather_cache_kv(cc->k_cache, cc->v_cache, cc->S_max, cc->cache_len, cc->lmax, k, v,
-                                  (int)t_pad(T), B, KV, T, Tk, (int)t_pad(Tk), hd, kc, vtc, vsb, st));
+                                  (int)t_pad(T), B, KV, T, Tk, (int)t_pad(Tk), hd, kc, vtc, vsb, vsb + B, st));
     ap.k = kc;
     ap.v = nullptr;
     ap.v_t = vtc;
@@ -305,6 +305,7 @@ int run_block(const smol_config *c, const void *packed, int layer, const BlockIO
     ap.Tk = Tk;
     ap.q_off = Tk - T;
     ap.valid_start = vsb;
+    ap.seq_order = vsb + B;        // longest caches first
     ap.pdl = 0;                    // the gather kernel in between is not a programmatic launch
     LAUNCH_K(SMOL_K_ATTN, st, launch_attention_tc(ap, st));
   } else {
