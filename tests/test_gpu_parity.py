@@ -538,6 +538,13 @@ def test_prefill_with_cache_ragged(S):
     run_prefill_cache_case(S, wl, [0, 1, 130, 300], T=37, seed=70)
 
 
+def test_prefill_with_cache_equal_lengths(S):
+    # the attention takes the sequences longest cache first; equal lengths keep
+    # their index order, and the order must still cover every sequence once
+    wl = W["smollm2_decode_b64_cache4096"].scaled(n_layers=2, s_max=300, vocab=512)
+    run_prefill_cache_case(S, wl, [130, 7, 130, 130, 0, 7, 300, 0], T=20, seed=72)
+
+
 def test_prefill_with_cache_long_chunk_nope_window(S):
     wl = W["smollm2_decode_b64_cache4096"].scaled(n_layers=2, s_max=200, vocab=512, no_rope_layers=(1, 0),
                                                   sliding_window=(0, 150))
