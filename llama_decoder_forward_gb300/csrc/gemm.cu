@@ -1074,7 +1074,8 @@ int gemm_pick_bn(int epi, int N, int hd) {
     // 256 columns (four 64-wide head units, two per epilogue warp) even when
     // the last tile is ragged: the RoPE units cost about twice the MMAs of a
     // tile, so an even split between the warps matters more than the columns
-    // the last tile computes in vain
+    // the last tile computes in vain (for N = 960, five 192-column tiles ran
+    // the SmolLM2 forward in 5.50 ms against 5.40 with four of 256)
     if (N >= 256) return 256;
     const int cands[2] = {192, 128};
     for (int c : cands)
