@@ -127,6 +127,36 @@ def test_decode_cache_length_out_of_range(S):
     assert cosine(got, ref) >= LOGITS_COS_MIN and max_abs(got, ref) <= LOGITS_MAX_ABS
 
 
+def test_prefill_with_cache_length_out_of_range(S):
+    # a cache length beyond what the call can hold (S_max, and max_pos - T for
+    # the new tokens' positions) or below 0 is clamped on the device and reported
+    wl = W["smollm2_decode_b64_cache4096"].scaled(B=2, n_layers=1, s_max=96, vocab=512)
+    inp = synth.generate(wl, seed=33)
+    T = 12
+    g = torch.Generator().manual_seed(34)
+    ids = torch.randint(0, wl.vocab, (wl.B, T), generator=g).to(torch.int32)
+    dev = to_device(inp)
+    cfg = S.config_of(wl)
+    packed = S.prepare_weights(cfg, dev.layers, dev.embed, dev.final_norm)
+    ws = S.prefill_cache_workspace(cfg, wl.B, T, wl.s_max)
+    k_new = torch.empty(1, wl.B, wl.n_kv_heads, T, wl.head_dim, dtype=torch.bfloat16, device="cuda")
+    v_new = torch.empty_like(k_new)
+    logits = torch.empty(wl.B, T, wl.vocab, dtype=torch.bfloat16, device="cuda")
+    for bad in ([97, 10], [-1, 10]):
+        S.prefill_with_cache(cfg, packed, ids.cuda(), torch.tensor(bad, dtype=torch.int32, device="cuda"),
+                             dev.k_cache, dev.v_cache, k_new, v_new, logits, ws)
+        assert S.workspace_status(ws) == S.ERR_INPUT, bad
+    lens = [96, 10]
+    S.prefill_with_cache(cfg, packed, ids.cuda(), torch.tensor(lens, dtype=torch.int32, device="cuda"),
+                         dev.k_cache, dev.v_cache, k_new, v_new, logits, ws)
+    assert S.workspace_status(ws) == S.OK
+    ref, _, _ = O.prefill_with_cache(oracle_config(wl), oracle_layers(inp), np32(inp.embed), np32(inp.final_norm),
+                                     ids.numpy().astype(np.int64), np.asarray(lens), np32(inp.k_cache),
+                                     np32(inp.v_cache))
+    got = np32(logits)
+    assert cosine(got, ref) >= LOGITS_COS_MIN and max_abs(got, ref) <= LOGITS_MAX_ABS
+
+
 def test_attention_wait_gives_up(S):
     # a wait limit far below the attention kernel's own latencies: a wait gives
     # up, the kernel drains what it issued and reports a timeout; the device
