@@ -126,8 +126,10 @@ class ClockSampler:
             for name, v in zip(names[1:], r[5:9]):
                 if v.lower() in ("active", "1", "0x1"):
                     reasons.add(name)
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(rows)}
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(pw) if pw else None}
 
 
 # Translation units that hold none of the kernels whose DRAM traffic is recorded
@@ -649,7 +651,10 @@ def run_block_configs(S, args, rank, world, peaks, with_oracle):
         launches = S.last_launch_count() * wl.n_layers
         tot, _ = kernel_breakdown(S, step)
         graph = capture_graph(step)
+        sampler = ClockSampler()
+        sampler.start()
         ms = max_over_ranks(time_steps(graph.replay if graph else step, args.steps, world), world)
+        clocks = sampler.stop()
         lengths = None if inp.lengths is None else inp.lengths.cpu().numpy()
         flops, valid_tokens = block_flops(wl, lengths)
         padded_flops, _ = block_flops(wl, None)
@@ -663,8 +668,11 @@ def run_block_configs(S, args, rank, world, peaks, with_oracle):
             "timing": "CUDA-graph replay of the step" if graph else "eager calls",
             "algorithmic_flop_per_step": flops, "tflops": round(tf, 2),
             "tensor_frac": round(tf / peak_tf, 4), "peak": peak_tf, "peak_unit": "TFLOP/s (measured bf16 burst)",
+            "tensor_frac_of_sustained": round(tf / peaks["bf16_tflops_sustained"], 4)
+            if peaks.get("bf16_tflops_sustained") else None,
             "gpu_launches": launches * args.steps,
             "kernel_ms_per_step": {k: round(v, 4) for k, v in sorted(tot.items(), key=lambda kv: -kv[1])},
+            "clocks": clocks,
         }
         if vs is not None:
             ent["padded_flop_per_step"] = padded_flops
