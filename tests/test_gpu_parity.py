@@ -473,13 +473,18 @@ def test_block_key_mask(S, wl_name, B, T, layer_kw):
     assert err <= BLOCK_REL_TOL
 
 
-@pytest.mark.parametrize("B,T,kind", [(2, 150, "random"), (2, 384, "random"), (2, 384, "prefix")])
-def test_model_key_mask(S, B, T, kind):
+@pytest.mark.parametrize("B,T,kind,shape", [(2, 150, "random", "smollm2"), (2, 384, "random", "smollm2"),
+                                           (2, 384, "prefix", "smollm2"), (1, 256, "random", "smollm3")])
+def test_model_key_mask(S, B, T, kind, shape):
     # T = 384: whole 128-row blocks, so the O projection waits on the attention's
     # row-block flags instead of its completion.  "prefix": a padding-shaped mask
     # (each sequence hides a leading run of keys), so whole key tiles hide
-    # nothing and take the attention's unmasked branch
-    wl = W["smollm2_model_b8_t2048"].scaled(B=B, T=T, n_layers=2, vocab=1024)
+    # nothing and take the attention's unmasked branch.  "smollm3": head_dim 128,
+    # groups of 4, with the flags
+    if shape == "smollm2":
+        wl = W["smollm2_model_b8_t2048"].scaled(B=B, T=T, n_layers=2, vocab=1024)
+    else:
+        wl = W["smollm3_4blocks_b4_t4096"].scaled(kind="model", B=B, T=T, n_layers=2, vocab=1024)
     inp = synth.generate(wl, seed=62)
     if kind == "random":
         mask = _key_mask(B, T, 63)
